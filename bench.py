@@ -1,0 +1,589 @@
+#!/usr/bin/env python3
+"""Benchmark of the ternary-g128 product on one GB300 (or N replicas).
+
+Headline (one "step"): a decode sweep at M = 1 over a 64-layer synthetic
+backbone, each layer's three MLP projections (gate and up 5120 -> 17408,
+down 17408 -> 5120), every projection with its own weights (4.55 GB of packed
+codes and scales, far above the 129 MB L2, so every step streams from HBM).
+The sweep is captured once in a CUDA graph and replayed; value = weight bytes
+(codes + scales) streamed per second.
+
+Also reported (separate timed loops, same process): the small-batch / verify
+shapes (M in {1,2,4,5,8,16}), the rotation and the rotation-fused product at
+K = 4096, N = 12288, and the pp512 prefill over the 64-layer backbone
+(gate, up, qkv-like 5120 -> 6144, down) on the tensor cores.
+
+`--impl reference` times the CPU oracle on the same workload and metric.
+Under torchrun each rank runs its own replica (weak scaling, no collective on
+the data path); rank 0 prints the one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ternary GEMV M=1 weight GB/s (% HBM peak); pp512 GEMM TFLOP/s (% bf16 peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "_source": "fallback"}
+DECODE_LAYERS = 64
+GEMV_SRC = os.path.join(ROOT, "bit_gemv_gemm_gb300", "csrc", "tern_gemv.cu")
+GEMM_SRC = os.path.join(ROOT, "bit_gemv_gemm_gb300", "csrc", "tern_gemm.cu")
+
+
+def weight_bytes(N: int, K: int) -> int:
+    return N * K // 4 + N * K // 64
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["_source"] = "measured"
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+def src_hash(path: str) -> str:
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def load_traffic(kernel: str, src: str):
+    """Per-launch DRAM bytes of `kernel` from a committed ncu summary, or None if
+    the kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("source_sha256_16") != src_hash(src):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.file.seek(0)
+        sms, mx, pw, reasons = [], [], [], set()
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sms.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                pw.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(mx), "power_w_max": max(pw),
+                "samples": len(sms), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# multi-rank plumbing (replicas; the only collectives time the ranks)
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, ws: int) -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# timing helpers
+# ---------------------------------------------------------------------------
+
+def graph_of(fn):
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, steps: int, warmup: int) -> float:
+    """Average ms per replay, CUDA events on the launching stream."""
+    import torch
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(steps):
+        g.replay()
+    b.record(st)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+class DecodeSweep:
+    """64 layers x (gate, up, down) at M tokens; each projection its own weights."""
+
+    def __init__(self, tern, layers: int, seed: int = 2):
+        import torch
+        import synth
+        self.tern = tern
+        self.layers = []
+        self.shapes = [("gate", 5120, 17408), ("up", 5120, 17408), ("down", 17408, 5120)]
+        for l in range(layers):
+            projs = []
+            for name, K, N in self.shapes:
+                t = synth.device_trits(seed, f"L{l}.{name}.t", (N, K))
+                codes = tern.pack(t)
+                del t
+                s = synth.device_scales(seed, f"L{l}.{name}.s", (N, K // 128))
+                projs.append((name, K, N, codes, s))
+            self.layers.append(projs)
+        torch.cuda.synchronize()
+
+    def weight_bytes(self) -> int:
+        return sum(weight_bytes(N, K) for projs in self.layers for (_, K, N, _, _) in projs)
+
+    def buffers(self, M: int, seed: int = 2):
+        """Per-projection x, y and one shared workspace for M tokens."""
+        import torch
+        import synth
+        xs, ys = [], []
+        for l, projs in enumerate(self.layers):
+            for (name, K, N, _, _) in projs:
+                xs.append(synth.device_activations(seed, f"L{l}.{name}.x{M}", (M, K)))
+                ys.append(torch.empty((M, N), dtype=torch.float32, device="cuda"))
+        ws = self.tern.workspace(max(self.tern.gemv_workspace_bytes(M, N, K) for (_, K, N) in self.shapes))
+        return xs, ys, ws
+
+    def run(self, xs, ys, ws):
+        i = 0
+        for projs in self.layers:
+            for (_, K, N, codes, s) in projs:
+                self.tern.gemv(xs[i], codes, s, y=ys[i], ws=ws)
+                i += 1
+
+    def alg_bytes(self, M: int) -> int:
+        return sum(weight_bytes(N, K) + 2 * M * K + 4 * M * N
+                   for projs in self.layers for (_, K, N, _, _) in projs)
+
+
+def bench_decode(tern, sweep: DecodeSweep, steps: int, warmup: int, ws_count: int, dev_index: int):
+    import torch
+    M = 1
+    xs, ys, ws = sweep.buffers(M)
+    g = graph_of(lambda: sweep.run(xs, ys, ws))
+    time_graph(g, 2, warmup)                       # warm
+    with ClockSampler(dev_index) as clk:
+        barrier(ws_count)
+        torch.cuda.synchronize()
+        ms = time_graph(g, steps, 0)
+        torch.cuda.synchronize()
+        barrier(ws_count)
+    ms = max_over_ranks(ms, ws_count)
+    launches = 2 * sum(len(p) for p in sweep.layers)
+
+    # end to end through the same API: H2D of every projection's x, the sweep,
+    # D2H of every y; pinned host buffers, copies inside the timed region.
+    xh = [x.cpu().pin_memory() for x in xs]
+    yh = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys]
+    xin = torch.cat([x.flatten() for x in xs])
+    xhost = torch.cat([x.flatten() for x in xh]).pin_memory()
+    yout = torch.cat([y.flatten() for y in ys])
+    yhost = torch.empty_like(yout, device="cpu").pin_memory()
+    views, off = [], 0
+    for x in xs:
+        views.append(xin[off:off + x.numel()].view(x.shape))
+        off += x.numel()
+    yviews, off = [], 0
+    for y in ys:
+        yviews.append(yout[off:off + y.numel()].view(y.shape))
+        off += y.numel()
+    g2 = graph_of(lambda: sweep.run(views, yviews, ws))
+    st = torch.cuda.current_stream()
+
+    def e2e_step():
+        xin.copy_(xhost, non_blocking=True)
+        g2.replay()
+        yhost.copy_(yout, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(10, steps // 4)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws_count)
+    a.record(st)
+    for _ in range(e_steps):
+        e2e_step()
+    b.record(st)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / e_steps, ws_count)
+    del xh, yh
+    return {
+        "ms": ms, "clocks": clk.summary(), "launches_per_step": launches,
+        "weight_bytes": sweep.weight_bytes(), "alg_bytes": sweep.alg_bytes(M),
+        "e2e_ms": e2e_ms, "h2d": xhost.numel() * 2, "d2h": yhost.numel() * 4,
+    }
+
+
+def bench_verify(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int):
+    """M in {1,2,4,5,8,16} at K=5120, N=17408 (gate weights of all layers) and
+    N=6144 (qkv-like weights of all layers)."""
+    import torch
+    import synth
+    out = []
+    layers = len(sweep.layers)
+    gate = [(p[0][3], p[0][4]) for p in sweep.layers]
+    for N, mats in ((17408, gate), (6144, qkv)):
+        for M in synth.VERIFY_M:
+            K = 5120
+            xs = [synth.device_activations(3, f"V{l}.x{M}.{N}", (M, K)) for l in range(layers)]
+            ys = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in range(layers)]
+            ws = tern.workspace(tern.gemv_workspace_bytes(M, N, K))
+
+            def run():
+                for l in range(layers):
+                    tern.gemv(xs[l], mats[l][0], mats[l][1], y=ys[l], ws=ws)
+
+            g = graph_of(run)
+            ms = time_graph(g, max(3, steps // 4), warmup)
+            per = ms / layers * 1e-3
+            wb = weight_bytes(N, K)
+            out.append({"M": M, "K": K, "N": N, "us": per * 1e6, "weight_GBps": wb / per / 1e9,
+                        "TFLOPs": 2.0 * M * N * K / per / 1e12})
+    return out
+
+
+def bench_rotated(tern, steps: int, warmup: int, copies: int = 40):
+    import torch
+    import synth
+    K, N = synth.ROTATED["K"], synth.ROTATED["N"]
+    mats = []
+    for c in range(copies):
+        t = synth.device_trits(4, f"R{c}.t", (N, K))
+        mats.append((tern.pack(t), synth.device_scales(4, f"R{c}.s", (N, K // 128))))
+        del t
+    signs = synth.device_signs(4, "R.signs", K)
+    out = []
+    for M in synth.ROTATED["M"]:
+        xs = [synth.device_activations(4, f"R{c}.x{M}", (M, K)) for c in range(copies)]
+        xr = [torch.empty_like(x) for x in xs]
+        ys = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in range(copies)]
+        ws = tern.workspace(tern.gemv_workspace_bytes(M, N, K))
+
+        def fused():
+            for c in range(copies):
+                tern.fwht_gemm(xs[c], signs, mats[c][0], mats[c][1], y=ys[c], ws=ws)
+
+        def separate():
+            for c in range(copies):
+                tern.fwht(xs[c], signs, y=xr[c])
+                tern.gemv(xr[c], mats[c][0], mats[c][1], y=ys[c], ws=ws)
+
+        def rot_only():
+            for c in range(copies):
+                tern.fwht(xs[c], signs, y=xr[c])
+
+        res = {"M": M, "K": K, "N": N}
+        for name, fn in (("fused", fused), ("separate", separate), ("fwht_only", rot_only)):
+            g = graph_of(fn)
+            ms = time_graph(g, max(3, steps // 4), warmup)
+            res[f"{name}_us"] = ms / copies * 1e3
+        wb = weight_bytes(N, K)
+        res["fused_weight_GBps"] = wb / (res["fused_us"] * 1e-6) / 1e9
+        res["fwht_GBps"] = 4.0 * M * K / (res["fwht_only_us"] * 1e-6) / 1e9
+        out.append(res)
+    del mats
+    return out
+
+
+def bench_prefill(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int, peaks: dict, dev_index: int):
+    """pp512: 64 layers x (gate, up, qkv, down) at M=512, bf16 in, bf16 out."""
+    import torch
+    import synth
+    M = synth.PREFILL_M
+    layers = len(sweep.layers)
+    x5 = synth.device_activations(5, "P.x5120", (M, 5120))
+    x17 = synth.device_activations(5, "P.x17408", (M, 17408))
+    outs = {N: torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for N in (17408, 6144, 5120)}
+    ws = tern.workspace(max(tern.gemm_workspace_bytes(M, N, K) for (_, K, N) in synth.PREFILL_LAYER))
+    try:
+        tern.gemm(x5, sweep.layers[0][0][3], sweep.layers[0][0][4], y=outs[17408], ws=ws)
+        torch.cuda.synchronize()
+    except tern.TernError as e:
+        return {"unavailable": f"tern_gemm: {e}"}
+    mats = {"gate": [(p[0][3], p[0][4]) for p in sweep.layers],
+            "up": [(p[1][3], p[1][4]) for p in sweep.layers],
+            "qkv": qkv,
+            "down": [(p[2][3], p[2][4]) for p in sweep.layers]}
+    per_gemm = {}
+    for (name, K, N) in synth.PREFILL_LAYER:
+        x = x5 if K == 5120 else x17
+
+        def run(name=name, x=x, N=N):
+            for l in range(layers):
+                tern.gemm(x, mats[name][l][0], mats[name][l][1], y=outs[N], ws=ws)
+
+        g = graph_of(run)
+        ms = time_graph(g, max(2, steps // 20), max(1, warmup // 2))
+        per = ms / layers * 1e-3
+        per_gemm[name] = {"K": K, "N": N, "us": per * 1e6, "TFLOPs": 2.0 * M * N * K / per / 1e12}
+
+    def full():
+        for l in range(layers):
+            for (name, K, N) in synth.PREFILL_LAYER:
+                tern.gemm(x5 if K == 5120 else x17, mats[name][l][0], mats[name][l][1], y=outs[N], ws=ws)
+
+    g = graph_of(full)
+    with ClockSampler(dev_index) as clk:
+        ms = time_graph(g, max(2, steps // 20), max(1, warmup // 2))
+    flops = layers * sum(2.0 * M * N * K for (_, K, N) in synth.PREFILL_LAYER)
+    tf = flops / (ms * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    dom = max(per_gemm.items(), key=lambda kv: kv[1]["us"])
+    return {
+        "M": M, "layers": layers, "ms_per_pass": ms, "TFLOPs": tf, "tokens_per_s": M / (ms * 1e-3),
+        "per_gemm": per_gemm, "clocks": clk.summary(),
+        "roofline": {"bound": "tensor", "kernel": "tern_gemm (tcgen05)", "achieved": tf, "peak": peak,
+                     "unit": "TFLOP/s", "frac": tf / peak,
+                     "peak_source": f"{peaks['_source']} bf16_tflops_sustained (pass of {ms:.1f} ms)",
+                     "traffic": load_traffic("gemm_kernel", GEMM_SRC)},
+        "dominant": dom[0],
+    }
+
+
+def cpu_baseline(budget_s: float = 12.0) -> dict:
+    """The oracle, as it stands, on a bounded sample of the decode workload:
+    repeated full M=1 products of one gate-shaped (5120 -> 17408) matrix."""
+    import oracle
+    import synth
+    oracle.build()
+    K, N = 5120, 17408
+    p = synth.problem(2, 1, N, K, tag="cpu")
+    codes, _ = oracle.pack(p.t)
+    oracle.matmul(p.x[:, :], codes[:64], p.s[:64])              # warm the library
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        oracle.matmul(p.x, codes, p.s)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or calls >= 200:
+            break
+    gbps = calls * weight_bytes(N, K) / el / 1e9
+    return {"value": gbps, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{calls} full M=1 products of one 5120->17408 matrix (23.7 MB packed) in {el:.1f} s "
+                      f"with the C oracle (fp64, OpenMP over outputs)"}
+
+
+def run_reference(args) -> None:
+    """The reference arm: the CPU oracle on the decode workload's metric."""
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import synth
+    oracle.build()
+    K, N = 5120, 17408
+    p = synth.problem(2, 1, N, K, tag="cpu")
+    codes, _ = oracle.pack(p.t)
+    # size each step's sample so the whole run stays within about a minute
+    t0 = time.perf_counter()
+    oracle.matmul(p.x, codes[:1024], p.s[:1024])
+    rate = 1024 / max(time.perf_counter() - t0, 1e-6)                 # rows per second
+    total_steps = args.steps + args.warmup
+    rows = int(max(64, min(N, rate * 60.0 / max(total_steps, 1))))
+    for _ in range(args.warmup):
+        oracle.matmul(p.x, codes[:rows], p.s[:rows])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.matmul(p.x, codes[:rows], p.s[:rows])
+    el = time.perf_counter() - t0
+    gbps = args.steps * weight_bytes(rows, K) / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbps, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "decode GEMV M=1, 5120->17408 rows sample (CPU oracle)", "M": 1, "K": K,
+                   "N_sampled": rows},
+        "cpu_baseline": {"value": gbps, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": f"{rows} rows x K={K} per step, {args.steps} steps"},
+        "e2e": {"value": gbps, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=DECODE_LAYERS)
+    ap.add_argument("--skip", default="", help="comma list of parts to skip: verify,rotated,prefill,cpu")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    ws_count, rank, local = dist_setup()
+    import __graft_entry__
+    __graft_entry__.build()
+    import bit_gemv_gemm_gb300 as tern
+    import synth
+    peaks = load_peaks()
+    skip = set(filter(None, args.skip.split(",")))
+    dev_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local
+
+    sweep = DecodeSweep(tern, args.layers)
+    qkv = []
+    for l in range(args.layers):
+        t = synth.device_trits(2, f"L{l}.qkv.t", (6144, 5120))
+        qkv.append((tern.pack(t), synth.device_scales(2, f"L{l}.qkv.s", (6144, 40))))
+        del t
+    torch.cuda.synchronize()
+
+    dec = bench_decode(tern, sweep, args.steps, args.warmup, ws_count, dev_index)
+    value = ws_count * dec["weight_bytes"] / (dec["ms"] * 1e-3) / 1e9
+    achieved = dec["alg_bytes"] / (dec["ms"] * 1e-3) / 1e9
+    hbm = peaks["hbm_gbs"]
+    rows = {}
+    if "verify" not in skip:
+        rows["verify"] = bench_verify(tern, sweep, qkv, args.steps, args.warmup)
+    if "rotated" not in skip:
+        rows["rotated"] = bench_rotated(tern, args.steps, args.warmup)
+    if "prefill" not in skip:
+        rows["pp512"] = bench_prefill(tern, sweep, qkv, args.steps, args.warmup, peaks, dev_index)
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": ws_count,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dec["ms"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"decode GEMV M=1 sweep, {args.layers} layers x (gate 5120->17408, "
+                               f"up 5120->17408, down 17408->5120), distinct weights",
+                   "M": 1, "layers": args.layers, "weight_bytes_per_step": dec["weight_bytes"],
+                   "l2": "inputs larger than L2 (4.55 GB of weights per step vs 129 MB L2)",
+                   "parallelism": f"replicas x{ws_count}", "cuda_graph": True},
+        "hbm_frac": value / ws_count / hbm,
+        "roofline": {"bound": "hbm", "kernel": "gemv_kernel + prologue (per tern_gemv call)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_source": f"{peaks['_source']} hbm_gbs",
+                     "traffic": load_traffic("gemv_kernel", GEMV_SRC)},
+        "clocks": dec["clocks"],
+        "e2e": {"value": ws_count * dec["weight_bytes"] / (dec["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": dec["h2d"], "d2h_bytes_per_step": dec["d2h"]},
+        "gpu_launches": dec["launches_per_step"] * args.steps,
+        "rows": rows,
+    }
+    if rank == 0 and "cpu" not in skip:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws_count > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,232 @@
+"""bit_gemv_gemm_gb300 -- Python binding of libtern (GB300 ternary-g128 product).
+
+A thin ctypes layer over the C ABI in ``include/tern.h``: it checks tensor
+types, passes ``data_ptr()`` and the current CUDA stream, and turns status codes
+into exceptions.  Every step of the computation runs in the library's CUDA
+kernels; PyTorch only allocates device memory and supplies streams.  There is
+no fallback: if the library is not built, or the device is not an sm_103 GPU,
+the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libtern.so")
+
+TERN_OK = 0
+_STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "misaligned pointer", 4: "workspace too small",
+           5: "CUDA error", 6: "device is not sm_103", 7: "device-side error"}
+
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+_LL = ctypes.c_longlong
+
+EXPORTS = {
+    "tern_status_str": (ctypes.c_char_p, [_I]),
+    "tern_packed_bytes": (_SZ, [_I, _I]),
+    "tern_pack": (_I, [_P, _I, _I, _P, _P, _P]),
+    "tern_pack_host": (_I, [_P, _I, _I, _P, _P]),
+    "tern_unpack_host": (_I, [_P, _I, _I, _P, _P]),
+    "tern_validate_host": (_I, [_P, _I, _I, _P]),
+    "tern_gemv_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "tern_gemv": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
+    "tern_fwht": (_I, [_P, _P, _P, _I, _I, _P]),
+    "tern_fwht_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
+    "tern_gemm_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "tern_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
+    "tern_device_error": (_I, [_P]),
+    "tern_last_launch_count": (_I, []),
+}
+
+
+class TernError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {_STATUS.get(status, 'unknown')} (status {status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libtern.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libtern.so is not built ({LIB_PATH}); run "
+                                   "`python -m bit_gemv_gemm_gb300.build` or __graft_entry__.build()")
+            l = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in EXPORTS.items():
+                fn = getattr(l, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = l
+    return _lib
+
+
+def _check(fn: str, st: int) -> None:
+    if st != TERN_OK:
+        raise TernError(fn, st)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+# ---------------------------------------------------------------------------
+# sizes
+# ---------------------------------------------------------------------------
+
+def packed_bytes(N: int, K: int) -> int:
+    return int(lib().tern_packed_bytes(N, K))
+
+
+def gemv_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().tern_gemv_workspace_bytes(M, N, K))
+
+
+def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().tern_gemm_workspace_bytes(M, N, K))
+
+
+def workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A device byte buffer usable as a libtern workspace (256-byte aligned)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+# ---------------------------------------------------------------------------
+# packing
+# ---------------------------------------------------------------------------
+
+def pack(t: torch.Tensor, codes: torch.Tensor | None = None, bad_count: torch.Tensor | None = None,
+         stream=None) -> torch.Tensor:
+    """Device packer: int8 trits [N, K] -> uint32 codes [N, K/16] (as int32 storage).
+
+    If ``bad_count`` (int32 CUDA tensor of one element) is given, the number of
+    entries outside {-1, 0, +1} is added to it."""
+    N, K = t.shape
+    if codes is None:
+        codes = torch.empty((N, K // 16), dtype=torch.int32, device=t.device)
+    bp = _dev(bad_count, torch.int32, "bad_count") if bad_count is not None else None
+    _check("tern_pack", lib().tern_pack(_dev(t, torch.int8, "t"), N, K, _dev(codes, torch.int32, "codes"),
+                                        bp, _stream(stream)))
+    return codes
+
+
+def pack_host(t: np.ndarray) -> tuple[np.ndarray, int]:
+    t = np.ascontiguousarray(t, dtype=np.int8)
+    N, K = t.shape
+    codes = np.empty((N, K // 16), dtype=np.uint32)
+    bad = ctypes.c_longlong(0)
+    _check("tern_pack_host", lib().tern_pack_host(t.ctypes.data, N, K, codes.ctypes.data, ctypes.byref(bad)))
+    return codes, int(bad.value)
+
+
+def unpack_host(codes: np.ndarray, K: int) -> tuple[np.ndarray, int]:
+    codes = np.ascontiguousarray(codes, dtype=np.uint32)
+    N = codes.shape[0]
+    t = np.empty((N, K), dtype=np.int8)
+    bad = ctypes.c_longlong(0)
+    _check("tern_unpack_host", lib().tern_unpack_host(codes.ctypes.data, N, K, t.ctypes.data, ctypes.byref(bad)))
+    return t, int(bad.value)
+
+
+def validate_host(codes: np.ndarray, K: int) -> int:
+    codes = np.ascontiguousarray(codes, dtype=np.uint32)
+    bad = ctypes.c_longlong(0)
+    _check("tern_validate_host", lib().tern_validate_host(codes.ctypes.data, codes.shape[0], K, ctypes.byref(bad)))
+    return int(bad.value)
+
+
+# ---------------------------------------------------------------------------
+# products and rotation
+# ---------------------------------------------------------------------------
+
+def gemv(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor | None = None,
+         ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y (fp32 [M, N]) = x W^T for M = 1..16; x bf16 [M, K], codes int32 [N, K/16], scales fp16 [N, K/128]."""
+    M, K = x.shape
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(gemv_workspace_bytes(M, N, K), x.device)
+    _check("tern_gemv", lib().tern_gemv(
+        _dev(x, torch.bfloat16, "x"), _dev(codes, torch.int32, "codes"), _dev(scales, torch.float16, "scales"),
+        _dev(y, torch.float32, "y"), M, N, K, _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return y
+
+
+def fwht(x: torch.Tensor, signs: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y (bf16 [M, K]) = H_4096 (signs * x) / 64 per 4096-block of the last dimension."""
+    M, K = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    _check("tern_fwht", lib().tern_fwht(_dev(x, torch.bfloat16, "x"), _dev(signs, torch.int8, "signs"),
+                                        _dev(y, torch.bfloat16, "y"), M, K, _stream(stream)))
+    return y
+
+
+def fwht_gemm(x: torch.Tensor, signs: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
+              y: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y (fp32 [M, N]) = rotate(x) W^T with the rotation fused into the product's prologue."""
+    M, K = x.shape
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(gemv_workspace_bytes(M, N, K), x.device)
+    _check("tern_fwht_gemm", lib().tern_fwht_gemm(
+        _dev(x, torch.bfloat16, "x"), _dev(signs, torch.int8, "signs"), _dev(codes, torch.int32, "codes"),
+        _dev(scales, torch.float16, "scales"), _dev(y, torch.float32, "y"), M, N, K,
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return y
+
+
+def gemm(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor | None = None,
+         out_dtype=torch.float32, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y ([M, N], fp32 or bf16) = x W^T on the tcgen05 tensor cores, any M >= 1."""
+    M, K = x.shape
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    if y.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("y must be float32 or bfloat16")
+    if ws is None:
+        ws = workspace(gemm_workspace_bytes(M, N, K), x.device)
+    _check("tern_gemm", lib().tern_gemm(
+        _dev(x, torch.bfloat16, "x"), _dev(codes, torch.int32, "codes"), _dev(scales, torch.float16, "scales"),
+        _dev(y, y.dtype, "y"), 1 if y.dtype == torch.bfloat16 else 0, M, N, K,
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return y
+
+
+def device_error() -> int:
+    """Reads and clears the device-side error word (synchronizes the device)."""
+    code = ctypes.c_int(0)
+    _check("tern_device_error", lib().tern_device_error(ctypes.byref(code)))
+    return int(code.value)
+
+
+def last_launch_count() -> int:
+    return int(lib().tern_last_launch_count())

@@ -1,0 +1,137 @@
+// tern_api.cu -- status strings, device checks, host packer/unpacker/validator.
+//
+// Storage format: each trit t in {-1, 0, +1} in a 2-bit slot, code q = t + 1,
+// sixteen slots per little-endian uint32 ("prism-ml/Ternary-Bonsai-27B-mlx-2bit"
+// model card, "Memory requirement": each ternary value is stored in a 2-bit slot,
+// 2.125 bits per weight with the FP16 scale of each 128-weight group).
+#include <atomic>
+#include <mutex>
+
+#include "tern_common.cuh"
+
+namespace tern {
+
+namespace {
+std::atomic<int> g_last_launches{0};
+std::mutex g_dev_mu;
+int g_dev_checked[64] = {0};   // 0 = unknown, 1 = ok, -1 = unsupported
+int g_dev_sms[64] = {0};
+}  // namespace
+
+void set_launch_count(int n) { g_last_launches.store(n, std::memory_order_relaxed); }
+
+tern_status check_device(int* sm_count) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TERN_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return TERN_ERR_ARCH;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_dev_checked[dev] == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return TERN_ERR_CUDA;
+        g_dev_checked[dev] = (major == 10 && minor == 3) ? 1 : -1;
+        g_dev_sms[dev] = sms;
+    }
+    if (g_dev_checked[dev] != 1) return TERN_ERR_ARCH;
+    if (sm_count) *sm_count = g_dev_sms[dev];
+    return TERN_OK;
+}
+
+}  // namespace tern
+
+using namespace tern;
+
+extern "C" {
+
+const char* tern_status_str(tern_status s) {
+    switch (s) {
+        case TERN_OK: return "ok";
+        case TERN_ERR_NULL: return "a required pointer is NULL";
+        case TERN_ERR_SHAPE: return "shape out of range or not a required multiple";
+        case TERN_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        case TERN_ERR_WORKSPACE: return "workspace missing or too small";
+        case TERN_ERR_CUDA: return "a CUDA call or kernel launch failed";
+        case TERN_ERR_ARCH: return "the current device is not sm_103 (GB300)";
+        case TERN_ERR_DEVICE: return "a kernel reported a device-side error";
+    }
+    return "unknown status";
+}
+
+size_t tern_packed_bytes(int N, int K) {
+    if (N < 0 || K < 0 || K % 128 != 0) return 0;
+    return (size_t)N * (size_t)K / 4 + (size_t)N * (size_t)K / 64;
+}
+
+int tern_last_launch_count(void) { return g_last_launches.load(std::memory_order_relaxed); }
+
+tern_status tern_device_error(int* code) {
+    if (!code) return TERN_ERR_NULL;
+    *code = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return TERN_ERR_CUDA;
+    if (read_gemm_device_error(code) != cudaSuccess) return TERN_ERR_CUDA;
+    return TERN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Host packer / unpacker / validator.  Word-at-a-time: a 16-entry slice of a
+// row becomes one uint32 through a code table indexed by the trit's byte.
+// ---------------------------------------------------------------------------
+
+tern_status tern_pack_host(const int8_t* t, int N, int K, uint32_t* codes, long long* bad_count) {
+    if (N < 0 || K < 0 || K % 16 != 0) return TERN_ERR_SHAPE;
+    if ((N > 0 && K > 0) && (!t || !codes)) return TERN_ERR_NULL;
+    long long bad = 0;
+    const size_t words = (size_t)N * (size_t)(K / 16);
+    for (size_t w = 0; w < words; ++w) {
+        const int8_t* src = t + w * 16;
+        uint32_t word = 0;
+        for (int i = 15; i >= 0; --i) {
+            const uint8_t b = (uint8_t)src[i];
+            // -1 (0xFF) -> 0, 0 -> 1, +1 -> 2, anything else -> 3 (invalid)
+            uint32_t q = (b == 0xFFu) ? 0u : (b == 0u) ? 1u : (b == 1u) ? 2u : 3u;
+            bad += (q == 3u);
+            word = (word << 2) | q;
+        }
+        codes[w] = word;
+    }
+    if (bad_count) *bad_count = bad;
+    return TERN_OK;
+}
+
+tern_status tern_unpack_host(const uint32_t* codes, int N, int K, int8_t* t, long long* bad_count) {
+    if (N < 0 || K < 0 || K % 16 != 0) return TERN_ERR_SHAPE;
+    if ((N > 0 && K > 0) && (!t || !codes)) return TERN_ERR_NULL;
+    static const int8_t kTrit[4] = {-1, 0, 1, 0};
+    long long bad = 0;
+    const size_t words = (size_t)N * (size_t)(K / 16);
+    for (size_t w = 0; w < words; ++w) {
+        uint32_t word = codes[w];
+        for (int i = 0; i < 16; ++i, word >>= 2) {
+            const uint32_t q = word & 3u;
+            bad += (q == 3u);
+            t[w * 16 + i] = kTrit[q];
+        }
+    }
+    if (bad_count) *bad_count = bad;
+    return TERN_OK;
+}
+
+tern_status tern_validate_host(const uint32_t* codes, int N, int K, long long* bad_count) {
+    if (N < 0 || K < 0 || K % 16 != 0) return TERN_ERR_SHAPE;
+    if ((N > 0 && K > 0) && !codes) return TERN_ERR_NULL;
+    if (!bad_count) return TERN_ERR_NULL;
+    long long bad = 0;
+    const size_t words = (size_t)N * (size_t)(K / 16);
+    for (size_t w = 0; w < words; ++w) {
+        const uint32_t v = codes[w];
+        // a slot is 3 iff both of its bits are set
+        const uint32_t both = v & (v >> 1) & 0x55555555u;
+        bad += __builtin_popcount(both);
+    }
+    *bad_count = bad;
+    return TERN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,90 @@
+// tern_fwht.cuh -- 4096-point Walsh-Hadamard transform of one block in shared
+// memory by one 256-thread CTA (internal).
+//
+// The rotation is the normalized Sylvester-Walsh-Hadamard transform of block
+// 4096 along the activation's last dimension with an explicit +-1 sign pattern
+// ("Ternary-Bonsai-2-9B-2bit" article, section 3): x' = H_4096 (s (.) x) / 64,
+// H[i][j] = (-1)^popcount(i & j) (natural order).
+//
+// Because H_4096 = H_16 (x) H_16 (x) H_16 in natural order, the transform is
+// three passes of 16-point transforms, one per 4-bit digit of the index.  Each
+// thread owns 16 elements per pass (registers); the passes exchange through a
+// padded fp32 shared buffer (one pad word per 16 keeps every pass's accesses
+// on distinct banks).
+#pragma once
+
+#include "tern_common.cuh"
+
+namespace tern {
+
+constexpr int kFwhtN = 4096;
+constexpr int kFwhtThreads = 256;
+constexpr int kFwhtSmemFloats = kFwhtN + kFwhtN / 16;
+
+__device__ __forceinline__ int fwht_pos(int idx) { return idx + (idx >> 4); }
+
+// In-register 16-point transform, natural order.
+__device__ __forceinline__ void fwht16(float (&v)[16]) {
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if ((i & h) == 0) {
+                const float a = v[i], b = v[i + h];
+                v[i] = a + b;
+                v[i + h] = a - b;
+            }
+        }
+    }
+}
+
+// Rotates one 4096 block: x (bf16, 16-byte aligned), signs (int8, 16-byte
+// aligned), result (scaled by 1/64) left in `sm` at fwht_pos(idx).  Must be
+// called by all 256 threads; ends with a __syncthreads().
+__device__ __forceinline__ void fwht4096_block(const __nv_bfloat16* __restrict__ x,
+                                               const int8_t* __restrict__ signs,
+                                               float* __restrict__ sm) {
+    const int i = threadIdx.x;
+    float v[16];
+    // pass 1: index digit 0 (bits 0..3); thread i owns [16 i, 16 i + 16)
+    {
+        const int4* xp = reinterpret_cast<const int4*>(x + 16 * i);
+        const int4 x0 = __ldg(xp), x1 = __ldg(xp + 1);
+        const int4 sg = __ldg(reinterpret_cast<const int4*>(signs + 16 * i));
+        const uint32_t xw[8] = {(uint32_t)x0.x, (uint32_t)x0.y, (uint32_t)x0.z, (uint32_t)x0.w,
+                                (uint32_t)x1.x, (uint32_t)x1.y, (uint32_t)x1.z, (uint32_t)x1.w};
+        const uint32_t sw[4] = {(uint32_t)sg.x, (uint32_t)sg.y, (uint32_t)sg.z, (uint32_t)sg.w};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const uint32_t bits = (xw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+            const float xv = __uint_as_float(bits << 16);
+            const int s = (int)(int8_t)((sw[e >> 2] >> (8 * (e & 3))) & 0xFFu);
+            v[e] = s < 0 ? -xv : xv;
+        }
+        fwht16(v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sm[fwht_pos(16 * i + e)] = v[e];
+    }
+    __syncthreads();
+    // pass 2: digit 1 (bits 4..7)
+    {
+        const int base = (i & 15) | ((i >> 4) << 8);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = sm[fwht_pos(base | (e << 4))];
+        fwht16(v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sm[fwht_pos(base | (e << 4))] = v[e];
+    }
+    __syncthreads();
+    // pass 3: digit 2 (bits 8..11), then the 1/sqrt(4096) normalization
+    {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = sm[fwht_pos(i | (e << 8))];
+        fwht16(v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sm[fwht_pos(i | (e << 8))] = v[e] * (1.0f / 64.0f);
+    }
+    __syncthreads();
+}
+
+}  // namespace tern

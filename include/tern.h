@@ -1,0 +1,175 @@
+/*
+ * tern.h -- C ABI of libtern, the GB300 (sm_103a) ternary-g128 matrix product
+ * and Walsh-Hadamard rotation library.
+ *
+ * The method (from the "prism-ml/Ternary-Bonsai-27B-mlx-2bit" Hugging Face
+ * model card and the "Ternary-Bonsai-2-9B-2bit" article):
+ *   - every weight is t * s_g, t in {-1, 0, +1}, with one FP16 scale s_g per
+ *     128 consecutive weights along K (card, "Weight representation: ternary
+ *     g128");
+ *   - each t is stored in a 2-bit slot, 2.125 bits per weight with the scales
+ *     (card, "Memory requirement");
+ *   - the packed weights are used directly: codes are unpacked and scaled
+ *     inside the matrix product, never expanded to a dense FP16 tensor (card,
+ *     "CUDA (NVIDIA GPUs)");
+ *   - where a layer uses it, the activation's last dimension is first rotated
+ *     by the normalized Sylvester-Walsh-Hadamard transform, block 4096, with an
+ *     explicit sign pattern (article, section 3 "Ternary weights and Hadamard
+ *     rotation").
+ *
+ * Data layout (shared by every entry point):
+ *   x       bf16 [M][K] row-major activations.
+ *   codes   uint32 [N][K/16] row-major.  Weight (n, k) has code
+ *           q = t + 1 in {0, 1, 2} in bits 2*(k%16) .. 2*(k%16)+1 of word
+ *           codes[n][k/16] (little-endian uint32).  q = 3 is invalid.
+ *   scales  fp16 [N][K/128] row-major: s[n][g] scales k in [128 g, 128 g + 128).
+ *   y       [M][N] row-major, y[m][n] = sum_k x[m][k] * (q[n][k] - 1) * s[n][k/128].
+ *   signs   int8 [K], each +1 or -1.
+ *   Packed size: N*K/4 bytes of codes + N*K/64 bytes of scales.
+ *
+ * Conventions:
+ *   - Device entry points take device pointers owned by the caller, launch
+ *     asynchronously on `stream` (NULL = the legacy default stream) and
+ *     allocate nothing.  Where a kernel needs scratch memory the caller passes
+ *     a device workspace of at least the size the matching *_workspace_bytes
+ *     query returns (256-byte aligned).
+ *   - The return value reports host-side argument validation and launch
+ *     errors only; on any error nothing is launched.  Device-side problems
+ *     (a bounded wait that gave up) set a sticky device flag that
+ *     tern_device_error() reads.
+ *   - Pointers must be 16-byte aligned (TERN_ERR_ALIGN otherwise).
+ *   - The kernels of tern_gemv, tern_fwht_gemm and tern_fwht use programmatic
+ *     dependent launch: a tern_* kernel may begin reading `codes` and `scales`
+ *     while the previous tern_* kernel on the stream is still running, so
+ *     codes/scales must not be outputs of the immediately preceding tern_*
+ *     call (tern_pack excepted: it never releases its dependents early).
+ *     Activations, outputs and workspaces are always ordered.
+ *   - Only sm_103 devices (GB300) are supported (TERN_ERR_ARCH otherwise).
+ */
+#ifndef TERN_H
+#define TERN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *tern_stream_t;
+
+typedef enum {
+    TERN_OK = 0,
+    TERN_ERR_NULL = 1,      /* a required pointer is NULL */
+    TERN_ERR_SHAPE = 2,     /* M, N or K out of range or not a required multiple */
+    TERN_ERR_ALIGN = 3,     /* a pointer is not 16-byte aligned */
+    TERN_ERR_WORKSPACE = 4, /* workspace NULL or smaller than required */
+    TERN_ERR_CUDA = 5,      /* a CUDA runtime/driver call or a launch failed */
+    TERN_ERR_ARCH = 6,      /* the current device is not sm_103 */
+    TERN_ERR_DEVICE = 7     /* a kernel reported a device-side error (bounded wait gave up) */
+} tern_status;
+
+/* A short English description of a status code (static storage). */
+const char *tern_status_str(tern_status s);
+
+/* Packed bytes of an N x K ternary-g128 matrix: N*K/4 + N*K/64. */
+size_t tern_packed_bytes(int N, int K);
+
+/* ---------------------------------------------------------------------- */
+/* Packing and validation (card, "Memory requirement": 2-bit slots)        */
+/* ---------------------------------------------------------------------- */
+
+/* Device packer.  t: int8 [N][K] in {-1,0,+1}; codes: uint32 [N][K/16].
+ * An entry outside {-1,0,+1} is written as the invalid code 3 and counted:
+ * if bad_count (device int, nullable) is given, the number of invalid entries
+ * is atomically ADDED to it (the caller zeroes it first).
+ * K % 16 == 0 and N >= 0, K >= 0 (TERN_ERR_SHAPE otherwise); t 16-byte aligned. */
+tern_status tern_pack(const int8_t *t, int N, int K, uint32_t *codes, int *bad_count,
+                      tern_stream_t stream);
+
+/* Host packer (loaders, tests): same layout and rules as tern_pack; the
+ * number of invalid entries is stored in *bad_count (nullable). */
+tern_status tern_pack_host(const int8_t *t, int N, int K, uint32_t *codes,
+                           long long *bad_count);
+
+/* Host unpacker: t[n][k] = q - 1; code 3 is written as 0 and counted. */
+tern_status tern_unpack_host(const uint32_t *codes, int N, int K, int8_t *t,
+                             long long *bad_count);
+
+/* Host validator: counts code-3 slots in codes [N][K/16] into *bad_count. */
+tern_status tern_validate_host(const uint32_t *codes, int N, int K, long long *bad_count);
+
+/* ---------------------------------------------------------------------- */
+/* Decode / small-batch product, M = 1..16 (card, "Cross-platform          */
+/* throughput": tg128 is the memory-bandwidth-bound phase; "Speculative    */
+/* decoding: DSpark": verify runs k + 1 tokens)                            */
+/* ---------------------------------------------------------------------- */
+
+/* Workspace bytes tern_gemv / tern_fwht_gemm need for (M, K); 0 on bad input. */
+size_t tern_gemv_workspace_bytes(int M, int N, int K);
+
+/* y (fp32 [M][N]) = x W^T with W given by (codes, scales).
+ * 1 <= M <= 16, N >= 1, K >= 128 with K % 128 == 0.  The workspace holds
+ * the activation staged for the tensor-core adder (see the library's design
+ * notes); it is fully rewritten by every call.  y is overwritten (the call
+ * zeroes it before accumulating).  Results agree with the exact product to
+ * within 1e-3 * sum_k |x w| + 1e-6 per element; the split-K summation order
+ * varies between runs, so results are not bitwise reproducible. */
+tern_status tern_gemv(const void *x, const uint32_t *codes, const void *scales, float *y,
+                      int M, int N, int K, void *workspace, size_t workspace_bytes,
+                      tern_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Rotation (article, section 3: normalized Sylvester-Walsh-Hadamard,      */
+/* block 4096, last dimension, explicit signs)                             */
+/* ---------------------------------------------------------------------- */
+
+/* y (bf16 [M][K]) = H_4096 (signs (.) x) / 64 for each 4096-block of each row,
+ * H in natural (Sylvester) order, computed in fp32 and rounded to nearest
+ * even.  M >= 1, K >= 4096 with K % 4096 == 0.  x and y may not alias. */
+tern_status tern_fwht(const void *x, const int8_t *signs, void *y, int M, int K,
+                      tern_stream_t stream);
+
+/* Rotation fused into the product: y (fp32 [M][N]) = rot(x) W^T with the
+ * rotated activation kept in fp32 on chip (never rounded to bf16).
+ * 1 <= M <= 16, K % 4096 == 0; workspace as for tern_gemv. */
+tern_status tern_fwht_gemm(const void *x, const int8_t *signs, const uint32_t *codes,
+                           const void *scales, float *y, int M, int N, int K,
+                           void *workspace, size_t workspace_bytes, tern_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Prefill product (card, "Cross-platform throughput": pp512 is the        */
+/* compute-bound phase)                                                    */
+/* ---------------------------------------------------------------------- */
+
+/* Workspace bytes tern_gemm needs; 0 on bad input. */
+size_t tern_gemm_workspace_bytes(int M, int N, int K);
+
+/* y = x W^T on the tcgen05 tensor cores: each weight is unpacked on chip to
+ * bf16 t * bf16(s_g) (the group scale rounded to bf16 and folded in), the
+ * product accumulates in fp32 in tensor memory, and y is written as fp32
+ * (y_is_bf16 == 0) or bf16 rounded to nearest even (y_is_bf16 != 0).
+ * M >= 1, N >= 1 with N % 16 == 0, K >= 128 with K % 128 == 0. */
+tern_status tern_gemm(const void *x, const uint32_t *codes, const void *scales, void *y,
+                      int y_is_bf16, int M, int N, int K, void *workspace,
+                      size_t workspace_bytes, tern_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Diagnostics                                                             */
+/* ---------------------------------------------------------------------- */
+
+/* Reads and clears the sticky device-side error word of the current device
+ * (synchronizes the device).  *code = 0 when no kernel reported an error;
+ * otherwise a nonzero code naming the wait that gave up.  Returns TERN_OK or
+ * TERN_ERR_CUDA. */
+tern_status tern_device_error(int *code);
+
+/* The number of kernels the last entry point call launched (for launch
+ * accounting in benchmarks); host-side, per process. */
+int tern_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TERN_H */

@@ -119,3 +119,49 @@ PREFILL_M = 512
 PREFILL_LAYER = [("gate", 5120, 17408), ("up", 5120, 17408), ("qkv", 5120, 6144),
                  ("down", 17408, 5120)]                   # (name, K, N)
 PREFILL_LAYERS = 64
+
+
+# ---------------------------------------------------------------------------
+# Device-side draws for the benchmark's multi-gigabyte weight sets (torch's
+# seeded CUDA generator; same distributions as above, not the same values).
+# ---------------------------------------------------------------------------
+
+def device_generator(seed: int, name: str, device="cuda"):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed((int(seed) << 32) ^ zlib.crc32(name.encode("utf-8")))
+    return g
+
+
+def device_trits(seed: int, name: str, shape, dist: str = SPARSE40, device="cuda"):
+    """int8 CUDA tensor of iid trits."""
+    import torch
+    g = device_generator(seed, name, device)
+    u = torch.rand(shape, generator=g, device=device)
+    lo, hi = (1.0 / 3.0, 2.0 / 3.0) if dist == UNIFORM else (0.3, 0.7)
+    t = (u >= lo).to(torch.int8)
+    t += (u >= hi).to(torch.int8)
+    t -= 1
+    return t
+
+
+def device_scales(seed: int, name: str, shape, dist: str = SCALE_HALFNORMAL, device="cuda"):
+    import torch
+    g = device_generator(seed, name, device)
+    if dist == SCALE_UNIFORM:
+        v = torch.rand(shape, generator=g, device=device) * 0.045 + 0.005
+    else:
+        v = torch.randn(shape, generator=g, device=device).abs_() * 0.02 + 1e-3
+    return v.to(torch.float16)
+
+
+def device_activations(seed: int, name: str, shape, device="cuda"):
+    import torch
+    g = device_generator(seed, name, device)
+    return torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
+
+
+def device_signs(seed: int, name: str, n: int, device="cuda"):
+    import torch
+    g = device_generator(seed, name, device)
+    return torch.where(torch.rand(n, generator=g, device=device) < 0.5, -1, 1).to(torch.int8)

@@ -1,0 +1,124 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, validates arguments before touching the device, and its host packer,
+unpacker and validator agree bit for bit with the oracle's."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def tern():
+    from bit_gemv_gemm_gb300 import build
+    build.build()
+    import bit_gemv_gemm_gb300 as t
+    return t
+
+
+def declared_entry_points():
+    src = open(os.path.join(ROOT, "include", "tern.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tern_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_entry_points()
+    for n in ("tern_pack", "tern_gemv", "tern_gemm", "tern_fwht", "tern_fwht_gemm"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(tern):
+    lib = tern.lib()
+    names = declared_entry_points()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), n
+    # and the binding knows every one of them
+    assert set(names) <= set(tern.EXPORTS)
+
+
+def test_status_strings(tern):
+    lib = tern.lib()
+    for s in range(8):
+        assert lib.tern_status_str(s)
+    assert lib.tern_status_str(99) == b"unknown status"
+
+
+def test_packed_bytes(tern):
+    assert tern.packed_bytes(17408, 5120) == 17408 * 5120 // 4 + 17408 * 5120 // 64 == 23674880
+    assert tern.packed_bytes(5120, 6144 // 6144 * 6144) == 5120 * 6144 * 17 // 64
+    assert tern.packed_bytes(12288, 4096) == 13369344
+    assert tern.packed_bytes(256, 512) == 34816
+    assert tern.packed_bytes(3, 100) == 0
+
+
+def test_host_pack_matches_oracle(tern, orc):
+    for seed, (N, K) in enumerate([(1, 16), (7, 128), (33, 1024), (64, 4096)]):
+        t = synth.trits(seed, "t", (N, K), synth.UNIFORM)
+        c_lib, bad = tern.pack_host(t)
+        c_orc, bad_o = orc.pack(t)
+        assert bad == bad_o == 0
+        assert np.array_equal(c_lib, c_orc)
+        back, bad2 = tern.unpack_host(c_lib, K)
+        assert bad2 == 0 and np.array_equal(back, t)
+        assert tern.validate_host(c_lib, K) == 0
+
+
+def test_host_pack_invalid_entries(tern, orc):
+    t = synth.trits(5, "t", (4, 64), synth.UNIFORM)
+    t[0, 3] = 2
+    t[1, 63] = -128
+    t[3, 17] = 5
+    c_lib, bad = tern.pack_host(t)
+    c_orc, bad_o = orc.pack(t)
+    assert bad == bad_o == 3
+    assert np.array_equal(c_lib, c_orc)
+    assert tern.validate_host(c_lib, 64) == 3
+    _, bad_u = tern.unpack_host(c_lib, 64)
+    assert bad_u == 3
+
+
+def test_validate_counts_every_code3_slot(tern):
+    words = np.array([[0xFFFFFFFF, 0x55555555, 0xC0000003, 0x00000000]], dtype=np.uint32)
+    assert tern.validate_host(words, 64) == 16 + 0 + 2 + 0
+
+
+def test_argument_errors_never_launch(tern):
+    """Shape, NULL, alignment and workspace errors are reported before any
+    device call, so they can be checked without a GPU."""
+    lib = tern.lib()
+    P = 4096  # a fake, 16-byte aligned "device" address; nothing dereferences it
+    # shapes
+    assert lib.tern_gemv(P, P, P, P, 0, 16, 128, P, 1 << 20, None) == 2
+    assert lib.tern_gemv(P, P, P, P, 17, 16, 128, P, 1 << 20, None) == 2
+    assert lib.tern_gemv(P, P, P, P, 1, 16, 100, P, 1 << 20, None) == 2
+    assert lib.tern_gemv(P, P, P, P, 1, 0, 128, P, 1 << 20, None) == 2
+    assert lib.tern_fwht(P, P, P, 1, 4000, None) == 2
+    assert lib.tern_fwht_gemm(P, P, P, P, P, 1, 16, 5120, P, 1 << 20, None) == 2
+    assert lib.tern_pack(P, 4, 17, P, None, None) == 2
+    assert lib.tern_gemm(P, P, P, P, 0, 0, 16, 128, P, 1 << 20, None) == 2
+    # NULL
+    assert lib.tern_gemv(None, P, P, P, 1, 16, 128, P, 1 << 20, None) == 1
+    assert lib.tern_fwht(P, None, P, 1, 4096, None) == 1
+    assert lib.tern_fwht_gemm(P, None, P, P, P, 1, 16, 4096, P, 1 << 20, None) == 1
+    # alignment
+    assert lib.tern_gemv(P + 2, P, P, P, 1, 16, 128, P, 1 << 20, None) == 3
+    assert lib.tern_fwht(P, P + 8, P, 1, 4096, None) == 3
+    # workspace
+    need = tern.gemv_workspace_bytes(1, 16, 128)
+    assert need > 0
+    assert lib.tern_gemv(P, P, P, P, 1, 16, 128, P, need - 1, None) == 4
+    assert lib.tern_gemv(P, P, P, P, 1, 16, 128, None, need, None) == 4
+    assert tern.gemv_workspace_bytes(17, 16, 128) == 0
+
+
+def test_workspace_sizes(tern):
+    # staged activation: 256 bytes per (token, group), fs: 8 bytes per (padded token, group)
+    assert tern.gemv_workspace_bytes(1, 17408, 5120) == 40 * 256 + 40 * 8 * 8
+    assert tern.gemv_workspace_bytes(16, 10, 17408) == 16 * 136 * 256 + 136 * 16 * 8
