@@ -110,8 +110,9 @@ def gemm_workspace_bytes(M: int, N: int, K: int) -> int:
 
 
 def workspace(nbytes: int, device=None) -> torch.Tensor:
-    """A device byte buffer usable as a libtern workspace (256-byte aligned)."""
-    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+    """A zero-filled device byte buffer usable as a libtern workspace (torch's
+    allocations are 256-byte aligned)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
 
 
 # ---------------------------------------------------------------------------

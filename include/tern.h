@@ -32,7 +32,9 @@
  *     asynchronously on `stream` (NULL = the legacy default stream) and
  *     allocate nothing.  Where a kernel needs scratch memory the caller passes
  *     a device workspace of at least the size the matching *_workspace_bytes
- *     query returns (256-byte aligned).
+ *     query returns, 256-byte aligned and zero-filled once before its first
+ *     use (cudaMemset); every completed call leaves it ready for the next.
+ *     Calls that share a workspace must be ordered (one stream, or events).
  *   - The return value reports host-side argument validation and launch
  *     errors only; on any error nothing is launched.  Device-side problems
  *     (a bounded wait that gave up) set a sticky device flag that
@@ -106,16 +108,20 @@ tern_status tern_validate_host(const uint32_t *codes, int N, int K, long long *b
 /* decoding: DSpark": verify runs k + 1 tokens)                            */
 /* ---------------------------------------------------------------------- */
 
-/* Workspace bytes tern_gemv / tern_fwht_gemm need for (M, K); 0 on bad input. */
+/* Workspace bytes tern_gemv and tern_fwht_gemm need for (M, N, K); 0 on bad
+ * input.  The size covers both calls.  It holds the per-K-slice partial row
+ * sums and one arrival counter per 16-row tile (and, for tern_fwht_gemm, the
+ * fp32 rotated activation). */
 size_t tern_gemv_workspace_bytes(int M, int N, int K);
 
 /* y (fp32 [M][N]) = x W^T with W given by (codes, scales).
- * 1 <= M <= 16, N >= 1, K >= 128 with K % 128 == 0.  The workspace holds
- * the activation staged for the tensor-core adder (see the library's design
- * notes); it is fully rewritten by every call.  y is overwritten (the call
- * zeroes it before accumulating).  Results agree with the exact product to
- * within 1e-3 * sum_k |x w| + 1e-6 per element; the split-K summation order
- * varies between runs, so results are not bitwise reproducible. */
+ * 1 <= M <= 16, N >= 1, K >= 128 with K % 128 == 0.  One kernel launch.
+ * For K <= 1024 the workspace may be NULL.  y is written once per element
+ * (no pre-zeroing needed).  Results agree with the exact product to within
+ * 1e-3 * sum_k |x w| + 1e-6 per element, and a row of zero weights gives
+ * exactly 0.  The fp32 sums within a K-slice are combined with shared-memory
+ * atomics, so the last bits may vary from run to run.  |x| must stay below
+ * 2^100 (larger values overflow the fp16 staging). */
 tern_status tern_gemv(const void *x, const uint32_t *codes, const void *scales, float *y,
                       int M, int N, int K, void *workspace, size_t workspace_bytes,
                       tern_stream_t stream);
@@ -131,9 +137,10 @@ tern_status tern_gemv(const void *x, const uint32_t *codes, const void *scales, 
 tern_status tern_fwht(const void *x, const int8_t *signs, void *y, int M, int K,
                       tern_stream_t stream);
 
-/* Rotation fused into the product: y (fp32 [M][N]) = rot(x) W^T with the
- * rotated activation kept in fp32 on chip (never rounded to bf16).
- * 1 <= M <= 16, K % 4096 == 0; workspace as for tern_gemv. */
+/* Rotation fused into the product: y (fp32 [M][N]) = rot(x) W^T.  A rotation
+ * prologue kernel leaves the rotated activation in fp32 in the workspace
+ * (L2-resident, never rounded to bf16) and the product stages it from there.
+ * 1 <= M <= 16, K % 4096 == 0; workspace as for tern_gemv (required). */
 tern_status tern_fwht_gemm(const void *x, const int8_t *signs, const uint32_t *codes,
                            const void *scales, float *y, int M, int N, int K,
                            void *workspace, size_t workspace_bytes, tern_stream_t stream);
