@@ -22,15 +22,18 @@ enum DeviceError : int {
     kDevErrGemmMmaWait = 0x103,        // MMA issuer gave up waiting for operands / TMEM
     kDevErrGemmEpilogueWait = 0x104,   // epilogue gave up waiting for an accumulator
     kDevErrGemmTeardownWait = 0x105,   // teardown gave up waiting for in-flight work
+    kDevErrGemvProducerWait = 0x201,   // decode producer gave up waiting for a free ring slot
+    kDevErrGemvConsumerWait = 0x202,   // decode warps gave up waiting for a code tile
 };
 
-// The translation unit whose kernels can report an error (the tcgen05 GEMM,
-// the only kernel with waits) defines its own word, so no relocatable device
-// code is needed, and exports a host reader that reads and clears it.
+// Each translation unit whose kernels wait on barriers (the prefill and the
+// decode products) defines its own word, so no relocatable device code is
+// needed, and exports a host reader that reads and clears it.
 __device__ __forceinline__ void report_device_error(int* word, int code) {
     atomicCAS(word, 0, code);
 }
 cudaError_t read_gemm_device_error(int* code);
+cudaError_t read_gemv_device_error(int* code);
 
 // ----------------------------------------------------------------------------
 // Programmatic dependent launch (PDL).

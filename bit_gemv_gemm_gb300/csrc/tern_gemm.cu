@@ -1,9 +1,369 @@
-// tern_gemm.cu -- prefill product on the tcgen05 tensor cores (in progress).
-#include "tern_common.cuh"
+// tern_gemm.cu -- prefill ternary-g128 product on the tcgen05 tensor cores.
+//
+//   y[m][n] = sum_k x[m][k] * t[n][k] * s[n][k/128]
+//
+// ("prism-ml/Ternary-Bonsai-27B-mlx-2bit" model card: ternary g128 weights,
+// "Weight representation"; the packed codes are unpacked and scaled inside the
+// matrix product and never expanded to a dense tensor in memory, "CUDA (NVIDIA
+// GPUs)"; pp512 prompt processing is the compute-bound phase, "Cross-platform
+// throughput".)
+//
+// Design.  The product is computed as y^T = W x^T so that the unpacked weights
+// are the MMA's A operand and can live in tensor memory:
+//   * a TMA producer warp streams, per 64-wide K stage, the x tile (256 tokens
+//     x 64, bf16, 128-byte swizzle: the MMA's B operand, K-major) and the
+//     packed code tile (128 weight rows x 4 words) into a shared-memory ring;
+//   * eight unpack warps turn each code into bf16 t * bf16(s_g) in registers
+//     (shift + mask puts two codes into bf16 exponent bits, one bf16x2 FMA gives
+//     q - 1 exactly, one bf16x2 multiply applies the scale, one byte permute
+//     pairs neighbouring k) and store them with tcgen05.st straight into a
+//     tensor-memory slot: the weights never touch shared or global memory in
+//     unpacked form;
+//   * one thread issues tcgen05.mma kind::f16 (M = 128 weight rows, N = 256
+//     tokens, K = 16) with A from tensor memory and B from shared memory,
+//     accumulating fp32 in tensor memory;
+//   * four epilogue warps read the accumulator with tcgen05.ld and store y
+//     (fp32 or bf16) with coalesced stores along n.
+// Stage hand-offs use mbarriers (TMA transaction counts, thread arrivals and
+// tcgen05.commit).  Every wait is bounded: after a second it raises a CTA abort
+// flag and the device error word, every role drains what it issued, tensor
+// memory is freed and the kernel returns.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "tern_sm100.cuh"
 
 namespace tern {
 namespace {
+
 __device__ int g_gemm_error;
+
+constexpr int kBM = 128;                    // weight rows per tile (tensor-memory lanes)
+constexpr int kBN = 256;                    // tokens per tile (MMA N)
+constexpr int kBK = 64;                     // K per stage
+constexpr int kStages = 4;
+constexpr int kXStageBytes = kBN * kBK * 2; // 32 KB
+constexpr int kCStageBytes = kBM * kBK / 4; // 2 KB of codes
+constexpr int kNumWarps = 14;               // 0 TMA, 1 MMA, 2-5 epilogue, 6-13 unpack
+constexpr int kThreads = kNumWarps * 32;
+constexpr int kTmemCols = 512;
+constexpr int kTmemD = 0;                   // accumulator: columns [0, 256)
+constexpr int kTmemA = 256;                 // weight slots: 32 columns per stage
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
+constexpr uint32_t kIdesc = sm100::idesc_bf16_f32(kBM, kBN);
+
+constexpr size_t kSmemX = 0;
+constexpr size_t kSmemC = kSmemX + (size_t)kStages * kXStageBytes;
+constexpr size_t kSmemBar = kSmemC + (size_t)kStages * kCStageBytes;
+// barriers: full[S], afull[S], empty[S], dfull, dempty, drain; then tmem base and abort flag
+constexpr size_t kSmemMisc = kSmemBar + (size_t)(3 * kStages + 3) * 8;
+constexpr size_t kSmemBytes = kSmemMisc + 16 + 1024;   // + alignment slack
+
+struct GemmArgs {
+    const __half* scales;
+    void* y;
+    int y_is_bf16;
+    int M, N, K;
+};
+
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// 16 codes of one word -> 8 bf16 pairs (k, k+1) of t * s.
+// Codes j and j + 8 sit 16 bits apart, so one shift puts both into bit 7 of
+// their halves (the bf16 exponent's low bits): the halves read as q * 2^-126,
+// and fma(., 2^126, -1) = q - 1 exactly.
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t s2, uint32_t (&o)[8]) {
+    constexpr uint32_t kTwo126 = 0x7E807E80u;   // bf16 2^126, both halves
+    constexpr uint32_t kMinus1 = 0xBF80BF80u;   // bf16 -1, both halves
+    uint32_t v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t m = (j <= 3 ? (w << (7 - 2 * j)) : (w >> (2 * j - 7))) & 0x01800180u;
+        v[j] = bf16x2_mul(bf16x2_fma(m, kTwo126, kMinus1), s2);   // (w_j, w_{j+8})
+    }
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        o[p] = prmt(v[2 * p], v[2 * p + 1], 0x5410u);       // (w_{2p},   w_{2p+1})
+        o[p + 4] = prmt(v[2 * p], v[2 * p + 1], 0x7632u);   // (w_{2p+8}, w_{2p+9})
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_c,
+            const GemmArgs a) {
+    using namespace sm100;
+    extern __shared__ __align__(1024) unsigned char smem_dyn[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + (uint32_t)kSmemBar;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto afull_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
+    const uint32_t dfull_bar = bar0 + 8u * (3 * kStages);
+    const uint32_t dempty_bar = dfull_bar + 8u;
+    const uint32_t drain_bar = dfull_bar + 16u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int M = a.M, N = a.N, K = a.K;
+    const int G = K / 128;
+    const int KS = K / kBK;
+    const int m_tiles = (M + kBN - 1) / kBN;
+    const int n_tiles = (N + kBM - 1) / kBM;
+    const int total = m_tiles * n_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(afull_bar(s), 8);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(dfull_bar, 1);
+        mbar_init(dempty_bar, 4);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmap_x);
+        tma_prefetch_desc(&tmap_c);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // x may be the previous kernel's output
+    pdl_wait();
+
+    auto fail = [&](int code) {
+        if (!*abort_flag) {
+            *abort_flag = 1;
+            report_device_error(&g_gemm_error, code);
+        }
+    };
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const int nt = tile / m_tiles, mt = tile - nt * m_tiles;
+                for (int ks = 0; ks < KS; ++ks, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                        fail(kDevErrGemmProducerWait);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(s), kXStageBytes + kCStageBytes);
+                    tma_load_2d(sbase + (uint32_t)(kSmemX + (size_t)s * kXStageBytes), &tmap_x, ks * kBK, mt * kBN,
+                                full_bar(s));
+                    tma_load_2d(sbase + (uint32_t)(kSmemC + (size_t)s * kCStageBytes), &tmap_c, ks * (kBK / 16),
+                                nt * kBM, full_bar(s));
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA goes away
+                const uint32_t n = it < (uint32_t)kStages ? it : (uint32_t)kStages;
+                for (uint32_t i = 0; i < n; ++i) {
+                    const uint32_t k = it - 1 - i;
+                    (void)mbar_wait_drain(full_bar(k % kStages), (k / kStages) & 1u, 100000000ull);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            uint32_t it = 0, tc = 0;
+            bool ok = true, issued = false;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tc) {
+                if (!mbar_wait_bounded(dempty_bar, (tc & 1u) ^ 1u, abort_flag, kWaitLimitNs)) {
+                    fail(kDevErrGemmMmaWait);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int ks = 0; ks < KS; ++ks, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (!mbar_wait_bounded(full_bar(s), ph, abort_flag, kWaitLimitNs) ||
+                        !mbar_wait_bounded(afull_bar(s), ph, abort_flag, kWaitLimitNs)) {
+                        fail(kDevErrGemmMmaWait);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t bdesc = smem_desc_k_sw128(sbase + (uint32_t)(kSmemX + (size_t)s * kXStageBytes));
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        // A: 8 columns (16 bf16) per K=16 step; B: advance 32 bytes inside the swizzle atom
+                        mma_f16_ts(tmem + kTmemD, tmem + kTmemA + 32u * s + 8u * kk, bdesc + (uint64_t)(2 * kk),
+                                   kIdesc, (ks | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    mma_commit(empty_bar(s));
+                }
+                if (!ok) break;
+                mma_commit(dfull_bar);
+            }
+            if (!ok && issued) {
+                // wait for every MMA issued so far before tensor memory is freed
+                mma_commit(drain_bar);
+                (void)mbar_wait_drain(drain_bar, 0u, 100000000ull);
+            }
+        }
+    } else if (warp < 6) {
+        // ------------------------------ epilogue ------------------------------
+        const int q = warp & 3;
+        const int rl = q * 32 + lane;
+        uint32_t tc = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tc) {
+            const int nt = tile / m_tiles, mt = tile - nt * m_tiles;
+            const int row = nt * kBM + rl;
+            if (!mbar_wait_bounded(dfull_bar, tc & 1u, abort_flag, kWaitLimitNs)) {
+                fail(kDevErrGemmEpilogueWait);
+                break;
+            }
+            tc_fence_after();
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_x32(tmem + ((uint32_t)(q * 32) << 16) + kTmemD + 32u * c, v);
+                tmem_ld_wait();
+                if (c == kBN / 32 - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(dempty_bar);
+                }
+                if (row < N) {
+                    const int m0 = mt * kBN + 32 * c;
+                    if (a.y_is_bf16) {
+                        __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(a.y);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (m0 + i < M) y[(size_t)(m0 + i) * N + row] = __float2bfloat16_rn(__uint_as_float(v[i]));
+                    } else {
+                        float* y = reinterpret_cast<float*>(a.y);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (m0 + i < M) y[(size_t)(m0 + i) * N + row] = __uint_as_float(v[i]);
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------ unpack ------------------------------
+        const int q = warp & 3;             // tensor-memory lane quadrant
+        const int h = (warp - 6) >> 2;      // K half of the stage: 0 -> k 0..31, 1 -> k 32..63
+        const int rl = q * 32 + lane;
+        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + kTmemA + 16u * h;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            const int nt = tile / m_tiles;
+            const int row = nt * kBM + rl;
+            const __half* srow = a.scales + (size_t)(row < N ? row : 0) * G;
+            uint32_t s2 = 0;
+            unsigned short s_next = row < N ? __half_as_ushort(__ldg(srow)) : (unsigned short)0;
+            for (int ks = 0; ks < KS; ++ks, ++it) {
+                if ((ks & 1) == 0) {
+                    // this group's scale as a bf16 pair; fetch the next group's
+                    const float sf = __half2float(__ushort_as_half(s_next));
+                    const __nv_bfloat16 sb = __float2bfloat16_rn(sf);
+                    const uint32_t sbits = __bfloat16_as_ushort(sb);
+                    s2 = sbits | (sbits << 16);
+                    const int gn = (ks >> 1) + 1;
+                    if (gn < G && row < N) s_next = __half_as_ushort(__ldg(srow + gn));
+                }
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1u;
+                // the MMAs of this slot's previous round are done (tensor-memory slot free)
+                // and this round's codes have landed
+                if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kWaitLimitNs) ||
+                    !mbar_wait_bounded(full_bar(s), ph, abort_flag, kWaitLimitNs)) {
+                    fail(kDevErrGemmUnpackWait);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint2 w = *reinterpret_cast<const uint2*>(smem + kSmemC + (size_t)s * kCStageBytes +
+                                                                 (size_t)rl * 16 + 8 * h);
+                uint32_t o[16];
+                uint32_t o0[8], o1[8];
+                unpack_word(w.x, s2, o0);
+                unpack_word(w.y, s2, o1);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    o[i] = o0[i];
+                    o[8 + i] = o1[i];
+                }
+                tmem_st_x16(tbase + 32u * s, o);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(afull_bar(s));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps through the driver entry point (no libcuda link).
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t gdim[2] = {inner, outer};
+    cuuint64_t gstride[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, dt, 2, const_cast<void*>(base), gdim, gstride, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t read_gemm_device_error(int* code) {
@@ -12,20 +372,58 @@ cudaError_t read_gemm_device_error(int* code) {
     if (e != cudaSuccess) return e;
     return cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(int));
 }
+
 }  // namespace tern
 
 using namespace tern;
 
 extern "C" size_t tern_gemm_workspace_bytes(int M, int N, int K) {
     if (M < 1 || N < 1 || K < 128 || K % 128 != 0) return 0;
-    return 256;
+    return 0;   // the prefill kernel needs no scratch memory
 }
 
 extern "C" tern_status tern_gemm(const void* x, const uint32_t* codes, const void* scales, void* y,
                                  int y_is_bf16, int M, int N, int K, void* workspace,
                                  size_t workspace_bytes, tern_stream_t stream) {
     set_launch_count(0);
-    (void)x; (void)codes; (void)scales; (void)y; (void)y_is_bf16; (void)M; (void)N; (void)K;
-    (void)workspace; (void)workspace_bytes; (void)stream;
-    return TERN_ERR_SHAPE;
+    (void)workspace;
+    (void)workspace_bytes;
+    if (M < 1 || N < 1 || K < 128 || K % 128 != 0) return TERN_ERR_SHAPE;
+    if ((long long)M * N >= (1LL << 40) || (long long)N * K >= (1LL << 40)) return TERN_ERR_SHAPE;
+    if (!x || !codes || !scales || !y) return TERN_ERR_NULL;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(y)) return TERN_ERR_ALIGN;
+    int sms = 0;
+    tern_status st = check_device(&sms);
+    if (st != TERN_OK) return st;
+
+    CUtensorMap mx, mc;
+    if (!make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kBK, kBN,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT32, codes, (uint64_t)(K / 16), (uint64_t)N,
+                     (uint64_t)(K / 16) * 4, kBK / 16, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return TERN_ERR_CUDA;
+
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TERN_ERR_CUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+            cudaSuccess)
+            return TERN_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    GemmArgs args;
+    args.scales = reinterpret_cast<const __half*>(scales);
+    args.y = y;
+    args.y_is_bf16 = y_is_bf16 ? 1 : 0;
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    const int total = ((M + kBN - 1) / kBN) * ((N + kBM - 1) / kBM);
+    const int grid = total < sms ? total : sms;
+    cudaError_t e = launch_pdl(gemm_kernel, dim3(grid), dim3(kThreads), kSmemBytes, (cudaStream_t)stream, true, mx,
+                               mc, args);
+    if (e != cudaSuccess) return TERN_ERR_CUDA;
+    set_launch_count(1);
+    return TERN_OK;
 }

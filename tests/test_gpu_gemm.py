@@ -1,0 +1,111 @@
+"""GPU parity of the tcgen05 prefill product against the CPU oracle.
+
+Tolerances.  The prefill kernel folds each group scale into the bf16 weight
+operand, so every weight is t * bf16(s_g): |bf16(s) - s| <= 2^-9 s.  Its fp32
+output is therefore held to |y - y_ref| <= 2^-8 * sum_k |x w| + 1e-6 (the
+scale rounding plus fp32 accumulation), and its bf16 output to
+|y - y_ref| <= 8e-3 * max(|y_ref|, sqrt(sum_k (x w)^2)).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests._util import assert_bf16_close, assert_fp32_close, dev_bf16, dev_scales, dev_trits, host_codes
+
+pytestmark = pytest.mark.gpu
+
+GEMM_REL = 2.0 ** -8
+
+
+@pytest.fixture(scope="module")
+def tern():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_gemv_gemm_gb300 import build
+    build.build()
+    import bit_gemv_gemm_gb300 as t
+    return t
+
+
+def l2_terms(orc, p, codes, ms=None, ns=None):
+    """sqrt(sum_k (x w)^2) per output, from the oracle's product of squares."""
+    # (x w)^2 = x^2 w^2: the product of x^2 with W^2; W^2 has t^2 in {0, 1} and s^2
+    xf = torch.from_numpy(p.x.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    w2 = (p.t.astype(np.float64) ** 2) * np.repeat(p.s.astype(np.float64) ** 2, 128, axis=1)
+    if ms is None:
+        return np.sqrt((xf ** 2) @ w2.T)
+    return np.sqrt(np.einsum("ik,ik->i", xf[ms] ** 2, w2[ns]))
+
+
+def run(tern, p, out_dtype=torch.float32):
+    codes = tern.pack(dev_trits(p.t))
+    y = tern.gemm(dev_bf16(p.x), codes, dev_scales(p.s), out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    return y, codes
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (5, 200, 256), (200, 256, 1024), (256, 384, 512),
+                                   (300, 130, 640), (512, 512, 2048), (17, 1000, 128)])
+def test_gemm_fp32_matches_oracle(tern, orc, M, N, K):
+    p = synth.problem(200 + M, M, N, K, tag=f"g{N}x{K}")
+    y, codes = run(tern, p)
+    y_ref, a_ref = orc.matmul(p.x, host_codes(codes), p.s)
+    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, rel=GEMM_REL, what=f"gemm M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 256, 512), (512, 384, 1024)])
+def test_gemm_bf16_matches_oracle(tern, orc, M, N, K):
+    p = synth.problem(300 + M, M, N, K, tag="b")
+    y, codes = run(tern, p, torch.bfloat16)
+    y_ref, _ = orc.matmul(p.x, host_codes(codes), p.s)
+    assert_bf16_close(y.to(torch.float64).cpu().numpy(), y_ref, l2_terms(orc, p, codes), what="gemm bf16")
+
+
+def test_gemm_exact_cases(tern):
+    """Zero weights give exactly 0; one-hot x picks t * bf16(s) exactly."""
+    M, N, K = 256, 128, 256
+    t = np.zeros((N, K), dtype=np.int8)
+    s = synth.scales(7, "s", (N, K // 128))
+    x = synth.activations(7, "x", (M, K))
+    y = tern.gemm(dev_bf16(x), tern.pack(dev_trits(t)), dev_scales(s))
+    torch.cuda.synchronize()
+    assert (y.cpu().numpy() == 0).all()
+    t = synth.trits(8, "t", (N, K), synth.UNIFORM)
+    x = np.zeros((M, K), dtype=np.uint16)
+    for m in range(M):
+        x[m, m % K] = 0x3F80
+    y = tern.gemm(dev_bf16(x), tern.pack(dev_trits(t)), dev_scales(s)).cpu().numpy()
+    sb = torch.from_numpy(s.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    W = t.astype(np.float64) * np.repeat(sb, 128, axis=1)
+    for m in range(M):
+        assert np.array_equal(y[m].astype(np.float64), W[:, m % K]), m
+
+
+@pytest.mark.parametrize("name,K,N", [(n, k, nn) for (n, k, nn) in synth.PREFILL_LAYER])
+def test_gemm_prefill_layer_sampled(tern, orc, name, K, N):
+    """One pp512 layer's projection at full size (M=512), sampled outputs."""
+    M = synth.PREFILL_M
+    p = synth.problem(5, M, N, K, tag=f"pp{name}")
+    y, codes = run(tern, p, torch.bfloat16)
+    rs = np.random.default_rng(K + N)
+    ms = rs.integers(0, M, 3000)
+    ns = rs.integers(0, N, 3000)
+    ms[:8], ns[:8] = M - 1, N - 1 - np.arange(8)
+    y_ref, a_ref = orc.matmul_sampled(p.x, host_codes(codes), p.s, ms, ns)
+    got = y.to(torch.float64).cpu().numpy()[ms, ns]
+    assert_bf16_close(got, y_ref, l2_terms(orc, p, codes, ms, ns), what=f"pp512 {name}")
+
+
+def test_gemm_back_to_back(tern, orc):
+    """Several products back to back on one stream (programmatic dependent
+    launch between them) stay correct."""
+    ps = [synth.problem(400 + i, 100 + 50 * i, 256, 512, tag=f"bb{i}") for i in range(4)]
+    ins = [(dev_bf16(p.x), tern.pack(dev_trits(p.t)), dev_scales(p.s)) for p in ps]
+    outs = [tern.gemm(*a) for a in ins for _ in range(2)]
+    torch.cuda.synchronize()
+    for i, p in enumerate(ps):
+        y_ref, a_ref = orc.matmul(p.x, host_codes(ins[i][1]), p.s)
+        for j in range(2):
+            assert_fp32_close(outs[2 * i + j].cpu().numpy(), y_ref, a_ref, rel=GEMM_REL, what=f"bb {i}")
