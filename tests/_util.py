@@ -39,15 +39,3 @@ def assert_fp32_close(y_gpu: np.ndarray, y_ref: np.ndarray, a_ref: np.ndarray, r
             f"{what}: {bad.sum()} of {bad.size} elements outside the bound; worst ratio "
             f"{np.max(err / bound):.3g}; first {i.tolist()}: got {y_gpu[bad][:5]}, want {y_ref[bad][:5]}")
     return float(np.max(err / bound)) if err.size else 0.0
-
-
-def assert_bf16_close(y_gpu: np.ndarray, y_ref: np.ndarray, l2_ref: np.ndarray, rel: float = 8e-3,
-                      what: str = ""):
-    """|y - y_ref| <= rel * max(|y_ref|, sqrt(sum_k (x w)^2)) per element (the bf16 bound)."""
-    err = np.abs(y_gpu.astype(np.float64) - y_ref)
-    bound = rel * np.maximum(np.abs(y_ref), l2_ref)
-    bad = ~(err <= bound)
-    if bad.any():
-        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements outside the bf16 bound; worst "
-                             f"ratio {np.max(err / np.maximum(bound, 1e-300)):.3g}")
-    return float(np.max(err / np.maximum(bound, 1e-300))) if err.size else 0.0

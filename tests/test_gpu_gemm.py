@@ -1,21 +1,24 @@
 """GPU parity of the tcgen05 prefill product against the CPU oracle.
 
 Tolerances.  The prefill kernel folds each group scale into the bf16 weight
-operand, so every weight is t * bf16(s_g): |bf16(s) - s| <= 2^-9 s.  Its fp32
-output is therefore held to |y - y_ref| <= 2^-8 * sum_k |x w| + 1e-6 (the
-scale rounding plus fp32 accumulation), and its bf16 output to
-|y - y_ref| <= 8e-3 * max(|y_ref|, sqrt(sum_k (x w)^2)).
+operand, so every weight is t * bf16(s_g) with |bf16(s) - s| <= 2^-9 s, and
+the error this adds to an output is at most 2^-9 * A, A = sum_k |x w|.  Its
+fp32 output is therefore held to |y - y_ref| <= 2^-8 * A + 1e-6 (the scale
+rounding plus fp32 accumulation).  Its bf16 output adds one rounding of y,
+at most 2^-9 |y| <= 2^-9 A, and is held to the bf16 tolerance read on the
+same error scale: |y - y_ref| <= 8e-3 * A + 1e-6.
 """
 import numpy as np
 import pytest
 import torch
 
 import synth
-from tests._util import assert_bf16_close, assert_fp32_close, dev_bf16, dev_scales, dev_trits, host_codes
+from tests._util import assert_fp32_close, dev_bf16, dev_scales, dev_trits, host_codes
 
 pytestmark = pytest.mark.gpu
 
 GEMM_REL = 2.0 ** -8
+BF16_REL = 8e-3
 
 
 @pytest.fixture(scope="module")
@@ -26,16 +29,6 @@ def tern():
     build.build()
     import bit_gemv_gemm_gb300 as t
     return t
-
-
-def l2_terms(orc, p, codes, ms=None, ns=None):
-    """sqrt(sum_k (x w)^2) per output, from the oracle's product of squares."""
-    # (x w)^2 = x^2 w^2: the product of x^2 with W^2; W^2 has t^2 in {0, 1} and s^2
-    xf = torch.from_numpy(p.x.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
-    w2 = (p.t.astype(np.float64) ** 2) * np.repeat(p.s.astype(np.float64) ** 2, 128, axis=1)
-    if ms is None:
-        return np.sqrt((xf ** 2) @ w2.T)
-    return np.sqrt(np.einsum("ik,ik->i", xf[ms] ** 2, w2[ns]))
 
 
 def run(tern, p, out_dtype=torch.float32):
@@ -59,8 +52,8 @@ def test_gemm_fp32_matches_oracle(tern, orc, M, N, K):
 def test_gemm_bf16_matches_oracle(tern, orc, M, N, K):
     p = synth.problem(300 + M, M, N, K, tag="b")
     y, codes = run(tern, p, torch.bfloat16)
-    y_ref, _ = orc.matmul(p.x, host_codes(codes), p.s)
-    assert_bf16_close(y.to(torch.float64).cpu().numpy(), y_ref, l2_terms(orc, p, codes), what="gemm bf16")
+    y_ref, a_ref = orc.matmul(p.x, host_codes(codes), p.s)
+    assert_fp32_close(y.to(torch.float64).cpu().numpy(), y_ref, a_ref, rel=BF16_REL, what="gemm bf16")
 
 
 def test_gemm_exact_cases(tern):
@@ -95,7 +88,7 @@ def test_gemm_prefill_layer_sampled(tern, orc, name, K, N):
     ms[:8], ns[:8] = M - 1, N - 1 - np.arange(8)
     y_ref, a_ref = orc.matmul_sampled(p.x, host_codes(codes), p.s, ms, ns)
     got = y.to(torch.float64).cpu().numpy()[ms, ns]
-    assert_bf16_close(got, y_ref, l2_terms(orc, p, codes, ms, ns), what=f"pp512 {name}")
+    assert_fp32_close(got, y_ref, a_ref, rel=BF16_REL, what=f"pp512 {name}")
 
 
 def test_gemm_back_to_back(tern, orc):
