@@ -47,6 +47,7 @@
 // written exactly once per element: no pre-zeroing, no global float atomics.
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "tern_fwht.cuh"
@@ -61,14 +62,14 @@ constexpr int kGroup = 128;            // weights per scale
 constexpr int kSliceGroups = 8;        // groups per K-slice = compute warps per CTA
 constexpr int kComputeWarps = 8;
 constexpr int kThreads = (kComputeWarps + 1) * 32;   // + the TMA producer warp
-constexpr int kRing = 8;               // code tiles in flight per CTA
 constexpr int kTileBytes = 16 * 128 * 2;   // 16 rows x 8 groups x 32 B, as two 128-B-wide halves
-constexpr int kMaxTilesPerCta = 64;
+constexpr int kTileScaleBytes = 16 * 8 * 2;   // 16 rows x 8 groups of fp16 scales
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr size_t kSmemPerSm = 227 * 1024;    // shared memory a GB300 SM offers its CTAs
 
 template <int MT> struct GemvCfg;
 template <> struct GemvCfg<1> { static constexpr int kCtasPerSm = 2; };
-template <> struct GemvCfg<2> { static constexpr int kCtasPerSm = 2; };
+template <> struct GemvCfg<2> { static constexpr int kCtasPerSm = 1; };
 
 struct GemvArgs {
     const void* x;              // bf16 [M][K], or fp32 [M][K] when the rotation prologue ran
@@ -77,21 +78,25 @@ struct GemvArgs {
     float* partial;             // [S][T][M][16]
     unsigned* counter;          // [T]
     int M, N, K, G, T, S, cps, rmax;
+    int ring;                   // ring slots (one per tile of the range whenever shared memory allows)
+    int scale_tma;              // scales stream through the ring (needs K % 1024 == 0)
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// dynamic shared memory: [code ring | barriers | activation fragments | (F, F*acc1) |
-//                         row accumulators | scales | finalize flags]
-__host__ __device__ inline size_t smem_bar() { return (size_t)kRing * kTileBytes; }
-__host__ __device__ inline size_t smem_b() { return smem_bar() + 2 * kRing * 8 + 16; }
-__host__ __device__ inline size_t smem_f(int MP) { return smem_b() + (size_t)kSliceGroups * MP * 64 * 4; }
-__host__ __device__ inline size_t smem_acc(int MP) { return smem_f(MP) + (size_t)kSliceGroups * MP * 8; }
-__host__ __device__ inline size_t smem_sc(int rmax, int MP) { return smem_acc(MP) + (size_t)rmax * 16 * MP * 4; }
-__host__ __device__ inline size_t smem_fin(int rmax, int MP) {
-    return smem_sc(rmax, MP) + align_up((size_t)kSliceGroups * rmax * 16 * 2, 16);
+// dynamic shared memory: [code ring | scale ring | barriers | activation fragments |
+//                         (F, F*acc1) | row accumulators | finalize flags]
+__host__ __device__ inline size_t smem_scl(int ring) { return (size_t)ring * kTileBytes; }
+__host__ __device__ inline size_t smem_bar(int ring) { return smem_scl(ring) + (size_t)ring * kTileScaleBytes; }
+__host__ __device__ inline size_t smem_b(int ring) { return align_up(smem_bar(ring) + (size_t)ring * 16 + 16, 16); }
+__host__ __device__ inline size_t smem_f(int ring, int MP) { return smem_b(ring) + (size_t)kSliceGroups * MP * 64 * 4; }
+__host__ __device__ inline size_t smem_acc(int ring, int MP) { return smem_f(ring, MP) + (size_t)kSliceGroups * MP * 8; }
+__host__ __device__ inline size_t smem_fin(int ring, int rmax, int MP) {
+    return smem_acc(ring, MP) + (size_t)rmax * 16 * MP * 4;
 }
-__host__ __device__ inline size_t smem_total(int rmax, int MP) { return smem_fin(rmax, MP) + (size_t)rmax * 4 + 1024; }
+__host__ __device__ inline size_t smem_total(int ring, int rmax, int MP) {
+    return smem_fin(ring, rmax, MP) + (size_t)rmax * 4 + 1024;
+}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1, bool accumulate) {
@@ -176,7 +181,8 @@ __device__ __forceinline__ void group_mmas(float (&acc)[NG][MT][4], const uint32
 
 template <int MT, bool XF32>
 __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kCtasPerSm)
-gemv_kernel(const __grid_constant__ CUtensorMap tmap_codes, const GemvArgs a) {
+gemv_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_constant__ CUtensorMap tmap_scales,
+            const GemvArgs a) {
     using namespace sm100;
     constexpr int MP = 8 * MT;
     constexpr int NG = MT == 1 ? 2 : 1;          // groups per step
@@ -184,16 +190,15 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_codes, const GemvArgs a) {
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
-    const int rmax = a.rmax;
-    const uint32_t bar0 = sbase + (uint32_t)smem_bar();
+    const int rmax = a.rmax, ring = a.ring;
+    const uint32_t bar0 = sbase + (uint32_t)smem_bar(ring);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kRing + s); };
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + smem_bar() + 2 * kRing * 8);
-    uint32_t* bsm = reinterpret_cast<uint32_t*>(smem + smem_b());                       // [8][MP][64]
-    float2* fcs = reinterpret_cast<float2*>(smem + smem_f(MP));                         // [8][MP]
-    float* accs = reinterpret_cast<float*>(smem + smem_acc(MP));                        // [rmax][16][MP]
-    unsigned short* scs = reinterpret_cast<unsigned short*>(smem + smem_sc(rmax, MP));  // [8][rmax][16]
-    int* fin = reinterpret_cast<int*>(smem + smem_fin(rmax, MP));                       // [rmax]
+    auto empty_bar = [&](int s) { return bar0 + 8u * (ring + s); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + smem_bar(ring) + 16 * ring);
+    uint32_t* bsm = reinterpret_cast<uint32_t*>(smem + smem_b(ring));                   // [8][MP][64]
+    float2* fcs = reinterpret_cast<float2*>(smem + smem_f(ring, MP));                   // [8][MP]
+    float* accs = reinterpret_cast<float*>(smem + smem_acc(ring, MP));                  // [rmax][16][MP]
+    int* fin = reinterpret_cast<int*>(smem + smem_fin(ring, rmax, MP));                 // [rmax]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, t = lane & 3;
@@ -206,13 +211,14 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_codes, const GemvArgs a) {
     const int R = tile_hi - tile_lo;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kRing; ++s) {
+        for (int s = 0; s < ring; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), kComputeWarps);
         }
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmap_codes);
+        if (a.scale_tma) tma_prefetch_desc(&tmap_scales);
     }
     __syncthreads();
     pdl_launch_dependents();
@@ -226,13 +232,15 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_codes, const GemvArgs a) {
 
     if (warp == kComputeWarps) {
         // ------------------------------ TMA producer ------------------------------
-        // codes are never the previous kernel's output: stream before the PDL wait
+        // codes and scales are never the previous kernel's output: stream them
+        // before the PDL wait; with one slot per tile every load goes out at once
         if (lane == 0) {
-            const uint32_t bytes = gs > 4 ? (uint32_t)kTileBytes : (uint32_t)kTileBytes / 2;
+            const uint32_t bytes = (gs > 4 ? (uint32_t)kTileBytes : (uint32_t)kTileBytes / 2) +
+                                   (a.scale_tma ? (uint32_t)kTileScaleBytes : 0u);
             int issued = 0;
             for (int i = 0; i < R; ++i, ++issued) {
-                const int s = i % kRing;
-                const uint32_t ph = (uint32_t)(i / kRing) & 1u;
+                const int s = i % ring;
+                const uint32_t ph = (uint32_t)(i / ring) & 1u;
                 if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kWaitLimitNs)) {
                     fail(kDevErrGemvProducerWait);
                     break;
@@ -242,25 +250,23 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_codes, const GemvArgs a) {
                 mbar_arrive_expect_tx(full_bar(s), bytes);
                 tma_load_2d(dst, &tmap_codes, g0 * 8, row, full_bar(s));
                 if (gs > 4) tma_load_2d(dst + kTileBytes / 2, &tmap_codes, g0 * 8 + 32, row, full_bar(s));
+                if (a.scale_tma)
+                    tma_load_2d(sbase + (uint32_t)(smem_scl(ring) + (size_t)s * kTileScaleBytes), &tmap_scales, g0,
+                                row, full_bar(s));
             }
             if (*abort_flag) {
-                const int n = issued < kRing ? issued : kRing;
+                const int n = issued < ring ? issued : ring;
                 for (int k = issued - n; k < issued; ++k)
-                    (void)mbar_wait_drain(full_bar(k % kRing), (uint32_t)(k / kRing) & 1u, 100000000ull);
+                    (void)mbar_wait_drain(full_bar(k % ring), (uint32_t)(k / ring) & 1u, 100000000ull);
             }
         }
         pdl_wait();
     } else {
         // ------------------------------ compute warps ------------------------------
         pdl_wait();
-        // warp w stages group g0 + w: its scales for the whole tile range, its
-        // activation B fragments and (F, F * acc1)
+        // warp w stages group g0 + w: its activation B fragments and (F, F * acc1)
         if (warp < gs) {
             const int g = g0 + warp;
-            for (int i = lane; i < R * 16; i += 32) {
-                const int row = tile_lo * 16 + i;
-                scs[(size_t)warp * rmax * 16 + i] = row < N ? __half_as_ushort(a.scales[(size_t)row * G + g]) : 0;
-            }
 #pragma unroll
             for (int nt = 0; nt < MT; ++nt) {
                 const int m = nt * 8 + gid;
@@ -339,14 +345,16 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_codes, const GemvArgs a) {
         const int U = R * gs;
         const int u0 = U * warp / kComputeWarps, u1 = U * (warp + 1) / kComputeWarps;
         for (int i = 0; i < R; ++i) {
-            const int s = i % kRing;
-            if (!mbar_wait_bounded(full_bar(s), (uint32_t)(i / kRing) & 1u, abort_flag, kWaitLimitNs)) {
+            const int s = i % ring;
+            if (!mbar_wait_bounded(full_bar(s), (uint32_t)(i / ring) & 1u, abort_flag, kWaitLimitNs)) {
                 fail(kDevErrGemvConsumerWait);
                 break;
             }
             const int ga = max(u0 - i * gs, 0), gb = min(u1 - i * gs, gs);
             if (ga < gb) {
                 const unsigned char* tile = smem + s * kTileBytes;
+                const unsigned char* tscale = smem + smem_scl(ring) + (size_t)s * kTileScaleBytes;
+                const int row0 = (tile_lo + i) * 16 + gid;
                 float ysum[MT][4];
 #pragma unroll
                 for (int nt = 0; nt < MT; ++nt)
@@ -384,9 +392,14 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_codes, const GemvArgs a) {
                     for (int q = 0; q < NG; ++q) {
                         if (g + q < gb) {
                             const int gq = g + q;
-                            const unsigned short* sc = scs + ((size_t)gq * rmax + i) * 16;
-                            const float s0 = __half2float(__ushort_as_half(sc[gid]));
-                            const float s1 = __half2float(__ushort_as_half(sc[gid + 8]));
+                            float s0, s1;
+                            if (a.scale_tma) {
+                                s0 = __half2float(*reinterpret_cast<const __half*>(tscale + gid * 16 + 2 * gq));
+                                s1 = __half2float(*reinterpret_cast<const __half*>(tscale + (gid + 8) * 16 + 2 * gq));
+                            } else {
+                                s0 = row0 < N ? __half2float(a.scales[(size_t)row0 * G + g0 + gq]) : 0.0f;
+                                s1 = row0 + 8 < N ? __half2float(a.scales[(size_t)(row0 + 8) * G + g0 + gq]) : 0.0f;
+                            }
 #pragma unroll
                             for (int nt = 0; nt < MT; ++nt) {
                                 // (F, F*acc1) of tokens 2t and 2t+1
@@ -494,7 +507,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 struct Plan {
-    int G, T, S, cps, ctas, rmax, MT;
+    int G, T, S, cps, ctas, rmax, ring, MT;
     size_t smem;
     size_t off_xr, off_partial, off_counter, bytes;
 };
@@ -505,14 +518,30 @@ Plan make_plan(int M, int N, int K, bool rot, int sms) {
     p.T = (N + 15) / 16;
     p.S = (p.G + kSliceGroups - 1) / kSliceGroups;
     p.MT = (M + 7) / 8;
-    const int cmax = sms * (p.MT == 1 ? GemvCfg<1>::kCtasPerSm : GemvCfg<2>::kCtasPerSm);
+    const int MP = 8 * p.MT;
+    const int per_sm = p.MT == 1 ? GemvCfg<1>::kCtasPerSm : GemvCfg<2>::kCtasPerSm;
+    const int cmax = sms * per_sm;
+    // ring slots that fit next to the fixed shared memory: one per tile of the
+    // CTA's range whenever possible, so every code load can be in flight at once
+    const size_t budget = kSmemPerSm / per_sm;
+    const size_t fixed = smem_total(0, 0, MP);
+    const size_t slot = (size_t)kTileBytes + kTileScaleBytes + 16;
+    const size_t acc_per_tile = (size_t)16 * MP * 4 + 4;
     p.cps = p.S >= cmax ? 1 : cmax / p.S;
     if (p.cps > p.T) p.cps = p.T;
-    const int need = (p.T + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
-    if (p.cps < need) p.cps = need;
+    for (;;) {
+        p.rmax = (p.T + p.cps - 1) / p.cps;
+        const size_t left = budget - fixed;
+        const long long fit = left > p.rmax * acc_per_tile
+                                  ? (long long)((left - p.rmax * acc_per_tile) / slot) : 0;
+        p.ring = (int)(fit < p.rmax ? fit : p.rmax);
+        if (p.ring >= p.rmax || (p.ring >= 8 && p.ring * 4 >= p.rmax * 3) || p.cps >= p.T) break;
+        p.cps = p.cps * 5 / 4 + 1;   // more, shorter ranges
+        if (p.cps > p.T) p.cps = p.T;
+    }
+    if (p.ring < 1) p.ring = 1;
     p.ctas = p.S * p.cps;
-    p.rmax = (p.T + p.cps - 1) / p.cps;
-    p.smem = smem_total(p.rmax, 8 * p.MT);
+    p.smem = smem_total(p.ring, p.rmax, MP);
     size_t off = 0;
     p.off_xr = off;
     if (rot) off = align_up(off + (size_t)M * K * 4, 256);
@@ -540,7 +569,8 @@ size_t workspace_bytes(int M, int N, int K, bool rot) {
 }
 
 template <int MT, bool XF32>
-cudaError_t launch_gemv(const CUtensorMap& tmap, const GemvArgs& args, const Plan& p, cudaStream_t stream) {
+cudaError_t launch_gemv(const CUtensorMap& tmap, const CUtensorMap& tmap_s, const GemvArgs& args, const Plan& p,
+                        cudaStream_t stream) {
     static int attr_bytes[64] = {};   // the attribute is per function and device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -551,7 +581,8 @@ cudaError_t launch_gemv(const CUtensorMap& tmap, const GemvArgs& args, const Pla
         if (e != cudaSuccess) return e;
         attr_bytes[dev] = (int)p.smem;
     }
-    return launch_pdl(gemv_kernel<MT, XF32>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, tmap, args);
+    return launch_pdl(gemv_kernel<MT, XF32>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, tmap, tmap_s,
+                      args);
 }
 
 tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const void* scales, float* y, int M,
@@ -566,7 +597,8 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
     }
     auto enc = get_encode();
     if (!enc) return TERN_ERR_CUDA;
-    CUtensorMap tmap;
+    CUtensorMap tmap, tmap_s;
+    memset(&tmap_s, 0, sizeof(tmap_s));
     {
         cuuint64_t gdim[2] = {(cuuint64_t)(K / 16), (cuuint64_t)N};
         cuuint64_t gstride[1] = {(cuuint64_t)(K / 16) * 4};
@@ -574,6 +606,18 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
         cuuint32_t es[2] = {1, 1};
         if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(codes), gdim, gstride, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return TERN_ERR_CUDA;
+    }
+    // scales ride along with the codes when a scale row is a multiple of 16 bytes
+    const bool scale_tma = (p.G % 8) == 0;
+    if (scale_tma) {
+        cuuint64_t gdim[2] = {(cuuint64_t)p.G, (cuuint64_t)N};
+        cuuint64_t gstride[1] = {(cuuint64_t)p.G * 2};
+        cuuint32_t box[2] = {8, 16};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(&tmap_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(scales), gdim, gstride, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return TERN_ERR_CUDA;
     }
@@ -592,6 +636,8 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
     args.S = p.S;
     args.cps = p.cps;
     args.rmax = p.rmax;
+    args.ring = p.ring;
+    args.scale_tma = scale_tma ? 1 : 0;
     int launches = 1;
     cudaError_t e;
     if (signs) {
@@ -601,9 +647,11 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
         if (e != cudaSuccess) return TERN_ERR_CUDA;
         args.x = xr;
         launches = 2;
-        e = p.MT == 1 ? launch_gemv<1, true>(tmap, args, p, stream) : launch_gemv<2, true>(tmap, args, p, stream);
+        e = p.MT == 1 ? launch_gemv<1, true>(tmap, tmap_s, args, p, stream)
+                      : launch_gemv<2, true>(tmap, tmap_s, args, p, stream);
     } else {
-        e = p.MT == 1 ? launch_gemv<1, false>(tmap, args, p, stream) : launch_gemv<2, false>(tmap, args, p, stream);
+        e = p.MT == 1 ? launch_gemv<1, false>(tmap, tmap_s, args, p, stream)
+                      : launch_gemv<2, false>(tmap, tmap_s, args, p, stream);
     }
     if (e != cudaSuccess) return TERN_ERR_CUDA;
     set_launch_count(launches);
