@@ -69,7 +69,7 @@ constexpr size_t kSmemPerSm = 227 * 1024;    // shared memory a GB300 SM offers 
 
 template <int MT> struct GemvCfg;
 template <> struct GemvCfg<1> { static constexpr int kCtasPerSm = 2; };
-template <> struct GemvCfg<2> { static constexpr int kCtasPerSm = 1; };
+template <> struct GemvCfg<2> { static constexpr int kCtasPerSm = 2; };
 
 struct GemvArgs {
     const void* x;              // bf16 [M][K], or fp32 [M][K] when the rotation prologue ran
@@ -84,15 +84,12 @@ struct GemvArgs {
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// dynamic shared memory: [code ring | scale ring | barriers | activation fragments |
-//                         (F, F*acc1) | row accumulators | finalize flags]
+// dynamic shared memory: [code ring | scale ring | barriers | row accumulators | finalize flags]
 __host__ __device__ inline size_t smem_scl(int ring) { return (size_t)ring * kTileBytes; }
 __host__ __device__ inline size_t smem_bar(int ring) { return smem_scl(ring) + (size_t)ring * kTileScaleBytes; }
-__host__ __device__ inline size_t smem_b(int ring) { return align_up(smem_bar(ring) + (size_t)ring * 16 + 16, 16); }
-__host__ __device__ inline size_t smem_f(int ring, int MP) { return smem_b(ring) + (size_t)kSliceGroups * MP * 64 * 4; }
-__host__ __device__ inline size_t smem_acc(int ring, int MP) { return smem_f(ring, MP) + (size_t)kSliceGroups * MP * 8; }
+__host__ __device__ inline size_t smem_acc(int ring) { return align_up(smem_bar(ring) + (size_t)ring * 16 + 16, 16); }
 __host__ __device__ inline size_t smem_fin(int ring, int rmax, int MP) {
-    return smem_acc(ring, MP) + (size_t)rmax * 16 * MP * 4;
+    return smem_acc(ring) + (size_t)rmax * 16 * MP * 4;
 }
 __host__ __device__ inline size_t smem_total(int ring, int rmax, int MP) {
     return smem_fin(ring, rmax, MP) + (size_t)rmax * 4 + 1024;
@@ -161,21 +158,22 @@ __device__ __forceinline__ void read_codes(const unsigned char* tile, int gl, in
     w[3] = v1.y;   // row gid + 8, word 2t + 1
 }
 
-// NG groups of one tile at once: NG x MT independent MMA chains, each in the
-// same slot order as mma_chain1 (so each keeps the ones-pass rounding).
-template <int MT, int NG>
-__device__ __forceinline__ void group_mmas(float (&acc)[NG][MT][4], const uint32_t (&w)[NG][4],
-                                           const uint32_t (&b)[NG][MT][16]) {
+// Two tiles of the warp's group at once: 2 x MT independent MMA chains sharing
+// the B fragments, each in the slot order of mma_chain1 (so each keeps the
+// ones-pass rounding).
+template <int MT>
+__device__ __forceinline__ void pair_mmas(float (&acc)[2][MT][4], const uint32_t (&w)[2][4],
+                                          const uint32_t (&b)[MT][16]) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        uint32_t r[NG][4];
+        uint32_t r[2][4];
 #pragma unroll
-        for (int q = 0; q < NG; ++q) slot_regs(j, w[q][0], w[q][1], w[q][2], w[q][3], r[q]);
+        for (int q = 0; q < 2; ++q) slot_regs(j, w[q][0], w[q][1], w[q][2], w[q][3], r[q]);
 #pragma unroll
-        for (int q = 0; q < NG; ++q)
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
             for (int nt = 0; nt < MT; ++nt)
-                mma16816(acc[q][nt], r[q][0], r[q][1], r[q][2], r[q][3], b[q][nt][2 * j], b[q][nt][2 * j + 1], j > 0);
+                mma16816(acc[q][nt], r[q][0], r[q][1], r[q][2], r[q][3], b[nt][2 * j], b[nt][2 * j + 1], j > 0);
     }
 }
 
@@ -185,7 +183,6 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_constan
             const GemvArgs a) {
     using namespace sm100;
     constexpr int MP = 8 * MT;
-    constexpr int NG = MT == 1 ? 2 : 1;          // groups per step
     extern __shared__ __align__(1024) unsigned char smem_dyn[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -195,9 +192,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_constan
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (ring + s); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + smem_bar(ring) + 16 * ring);
-    uint32_t* bsm = reinterpret_cast<uint32_t*>(smem + smem_b(ring));                   // [8][MP][64]
-    float2* fcs = reinterpret_cast<float2*>(smem + smem_f(ring, MP));                   // [8][MP]
-    float* accs = reinterpret_cast<float*>(smem + smem_acc(ring, MP));                  // [rmax][16][MP]
+    float* accs = reinterpret_cast<float*>(smem + smem_acc(ring));                      // [rmax][16][MP]
     int* fin = reinterpret_cast<int*>(smem + smem_fin(ring, rmax, MP));                 // [rmax]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -264,170 +259,145 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_constan
     } else {
         // ------------------------------ compute warps ------------------------------
         pdl_wait();
-        // warp w stages group g0 + w: its activation B fragments and (F, F * acc1)
-        if (warp < gs) {
-            const int g = g0 + warp;
+        // warp w owns group g0 + w of the slice for every tile of the range: it
+        // stages that group's activation B fragments and (F, F * acc1) into
+        // registers once
+        const bool active = warp < gs;
+        const int g = g0 + warp;
+        uint32_t b[MT][16];
+        float4 f[MT];   // (F, F*acc1) of tokens 2t and 2t+1 of each token tile
 #pragma unroll
-            for (int nt = 0; nt < MT; ++nt) {
-                const int m = nt * 8 + gid;
-                float v[32];
-                if (m < M) {
-                    const size_t off = (size_t)m * a.K + (size_t)g * kGroup + 32 * t;
-                    if (XF32) {
-                        const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) + off);
+        for (int nt = 0; nt < MT; ++nt) {
+            const int m = nt * 8 + gid;
+            float v[32];
+            if (active && m < M) {
+                const size_t off = (size_t)m * a.K + (size_t)g * kGroup + 32 * t;
+                if (XF32) {
+                    const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) + off);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const float4 u = src[q];
-                            v[4 * q] = u.x;
-                            v[4 * q + 1] = u.y;
-                            v[4 * q + 2] = u.z;
-                            v[4 * q + 3] = u.w;
-                        }
-                    } else {
-                        const uint4* src =
-                            reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) + off);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint4 u = src[q];
-                            const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                v[8 * q + 2 * e] = __uint_as_float(uw[e] << 16);
-                                v[8 * q + 2 * e + 1] = __uint_as_float(uw[e] & 0xFFFF0000u);
-                            }
-                        }
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 u = src[q];
+                        v[4 * q] = u.x;
+                        v[4 * q + 1] = u.y;
+                        v[4 * q + 2] = u.z;
+                        v[4 * q + 3] = u.w;
                     }
                 } else {
+                    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) + off);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 u = src[q];
+                        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            v[8 * q + 2 * e] = __uint_as_float(uw[e] << 16);
+                            v[8 * q + 2 * e + 1] = __uint_as_float(uw[e] & 0xFFFF0000u);
+                        }
+                    }
                 }
-                float mx = 0.0f;
+            } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(v[e]));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                int E = 0;
-                if (mx > 0.0f && mx <= 3.0e38f) {
-                    int ex;
-                    frexpf(mx, &ex);                       // mx < 2^ex
-                    E = max(-100, min(5 - ex, 150));       // mx * 2^(E + 10) < 2^15
-                }
-                uint32_t b[16];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float c = ldexpf(1.0f, E + 10 - 2 * (j < 6 ? j : j - 6));   // exact power of two
-                    const __half2 lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);       // k = 32t+j, +8
-                    const __half2 hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c); // k = 32t+16+j, +24
-                    b[2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
-                    b[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
-                }
-                uint4* dst = reinterpret_cast<uint4*>(bsm + ((size_t)warp * MP + m) * 64 + t * 16);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) dst[q] = make_uint4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
-                // the -1 correction: the same chain on the all-ones pattern; every
-                // row of the result is the same, lane (gid, t) holds tokens 2t, 2t+1
-                float acc1[4];
-                const uint32_t ones[4] = {0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u};
-                mma_chain1(acc1, ones, b);
-                const float F = (m < M) ? ldexpf(1.0f, 14 - E) : 0.0f;
-                const float F0 = __shfl_sync(0xffffffffu, F, (2 * t) * 4);
-                const float F1 = __shfl_sync(0xffffffffu, F, (2 * t + 1) * 4);
-                if (gid == 0)
-                    *reinterpret_cast<float4*>(fcs + warp * MP + nt * 8 + 2 * t) =
-                        make_float4(F0, F0 * acc1[0], F1, F1 * acc1[1]);
+                for (int e = 0; e < 32; ++e) v[e] = 0.0f;
             }
+            float mx = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(v[e]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            int E = 0;
+            if (mx > 0.0f && mx <= 3.0e38f) {
+                int ex;
+                frexpf(mx, &ex);                       // mx < 2^ex
+                E = max(-100, min(5 - ex, 150));       // mx * 2^(E + 10) < 2^15
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float c = ldexpf(1.0f, E + 10 - 2 * (j < 6 ? j : j - 6));   // exact power of two
+                const __half2 lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);       // k = 32t+j, +8
+                const __half2 hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c); // k = 32t+16+j, +24
+                b[nt][2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
+                b[nt][2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
+            // the -1 correction: the same chain on the all-ones pattern; every
+            // row of the result is the same, lane (gid, t) holds tokens 2t, 2t+1
+            float acc1[4];
+            const uint32_t ones[4] = {0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u};
+            mma_chain1(acc1, ones, b[nt]);
+            const float F = (m < M) ? ldexpf(1.0f, 14 - E) : 0.0f;
+            const float F0 = __shfl_sync(0xffffffffu, F, (2 * t) * 4);
+            const float F1 = __shfl_sync(0xffffffffu, F, (2 * t + 1) * 4);
+            f[nt] = make_float4(F0, F0 * acc1[0], F1, F1 * acc1[1]);
         }
         for (int i = threadIdx.x; i < R * 16 * MP; i += kComputeWarps * 32) accs[i] = 0.0f;
-        // staging and zeroed accumulators visible to every compute warp
+        // zeroed accumulators visible to every compute warp
         asm volatile("bar.sync 1, %0;" ::"r"(kComputeWarps * 32) : "memory");
 
-        // this warp's contiguous range of (tile, group) units
-        const int U = R * gs;
-        const int u0 = U * warp / kComputeWarps, u1 = U * (warp + 1) / kComputeWarps;
-        for (int i = 0; i < R; ++i) {
-            const int s = i % ring;
-            if (!mbar_wait_bounded(full_bar(s), (uint32_t)(i / ring) & 1u, abort_flag, kWaitLimitNs)) {
+        // every warp walks every tile in order (the ring is consumed in order)
+        auto epilogue = [&](int i, const float (&acc)[MT][4], float s0, float s1) {
+            float* row = accs + (size_t)i * 16 * MP;
+#pragma unroll
+            for (int nt = 0; nt < MT; ++nt) {
+                const int m0 = nt * 8 + 2 * t, m1 = m0 + 1;
+                if (nt * 8 < M) {
+                    if (m0 < M) {
+                        atomicAdd(row + gid * MP + m0, s0 * fmaf(f[nt].x, acc[nt][0], -f[nt].y));
+                        atomicAdd(row + (gid + 8) * MP + m0, s1 * fmaf(f[nt].x, acc[nt][2], -f[nt].y));
+                    }
+                    if (M > 1 && m1 < M) {
+                        atomicAdd(row + gid * MP + m1, s0 * fmaf(f[nt].z, acc[nt][1], -f[nt].w));
+                        atomicAdd(row + (gid + 8) * MP + m1, s1 * fmaf(f[nt].z, acc[nt][3], -f[nt].w));
+                    }
+                }
+            }
+        };
+        auto tile_scales = [&](int i, int s, float& s0, float& s1) {
+            if (a.scale_tma) {
+                const unsigned char* tscale = smem + smem_scl(ring) + (size_t)s * kTileScaleBytes;
+                s0 = __half2float(*reinterpret_cast<const __half*>(tscale + gid * 16 + 2 * warp));
+                s1 = __half2float(*reinterpret_cast<const __half*>(tscale + (gid + 8) * 16 + 2 * warp));
+            } else {
+                const int row0 = (tile_lo + i) * 16 + gid;
+                s0 = row0 < N ? __half2float(a.scales[(size_t)row0 * G + g]) : 0.0f;
+                s1 = row0 + 8 < N ? __half2float(a.scales[(size_t)(row0 + 8) * G + g]) : 0.0f;
+            }
+        };
+        for (int i = 0; i < R; i += 2) {
+            const bool two = i + 1 < R;
+            const int sA = i % ring, sB = (i + 1) % ring;
+            if (!mbar_wait_bounded(full_bar(sA), (uint32_t)(i / ring) & 1u, abort_flag, kWaitLimitNs) ||
+                (two && !mbar_wait_bounded(full_bar(sB), (uint32_t)((i + 1) / ring) & 1u, abort_flag, kWaitLimitNs))) {
                 fail(kDevErrGemvConsumerWait);
                 break;
             }
-            const int ga = max(u0 - i * gs, 0), gb = min(u1 - i * gs, gs);
-            if (ga < gb) {
-                const unsigned char* tile = smem + s * kTileBytes;
-                const unsigned char* tscale = smem + smem_scl(ring) + (size_t)s * kTileScaleBytes;
-                const int row0 = (tile_lo + i) * 16 + gid;
-                float ysum[MT][4];
+            if (active) {
+                uint32_t w2[2][4];
+                float sc[2][2];
+                read_codes(smem + sA * kTileBytes, warp, gid, t, w2[0]);
+                tile_scales(i, sA, sc[0][0], sc[0][1]);
+                if (two) {
+                    read_codes(smem + sB * kTileBytes, warp, gid, t, w2[1]);
+                    tile_scales(i + 1, sB, sc[1][0], sc[1][1]);
+                } else {
 #pragma unroll
-                for (int nt = 0; nt < MT; ++nt)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) ysum[nt][q] = 0.0f;
-                for (int g = ga; g < gb; g += NG) {
-                    uint32_t w[NG][4];
-                    uint32_t b[NG][MT][16];
-                    float acc[NG][MT][4];
-#pragma unroll
-                    for (int q = 0; q < NG; ++q) {
-                        const int gq = min(g + q, gb - 1);   // a repeated group's result is discarded
-                        read_codes(tile, gq, gid, t, w[q]);
-#pragma unroll
-                        for (int nt = 0; nt < MT; ++nt) {
-                            const int m = nt * 8 + gid;
-                            if (m < M) {
-                                const uint4* src = reinterpret_cast<const uint4*>(bsm + ((size_t)gq * MP + m) * 64 + t * 16);
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const uint4 v = src[e];
-                                    b[q][nt][4 * e] = v.x;
-                                    b[q][nt][4 * e + 1] = v.y;
-                                    b[q][nt][4 * e + 2] = v.z;
-                                    b[q][nt][4 * e + 3] = v.w;
-                                }
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) b[q][nt][e] = 0u;
-                            }
-                        }
-                    }
-                    group_mmas<MT, NG>(acc, w, b);
-#pragma unroll
-                    for (int q = 0; q < NG; ++q) {
-                        if (g + q < gb) {
-                            const int gq = g + q;
-                            float s0, s1;
-                            if (a.scale_tma) {
-                                s0 = __half2float(*reinterpret_cast<const __half*>(tscale + gid * 16 + 2 * gq));
-                                s1 = __half2float(*reinterpret_cast<const __half*>(tscale + (gid + 8) * 16 + 2 * gq));
-                            } else {
-                                s0 = row0 < N ? __half2float(a.scales[(size_t)row0 * G + g0 + gq]) : 0.0f;
-                                s1 = row0 + 8 < N ? __half2float(a.scales[(size_t)(row0 + 8) * G + g0 + gq]) : 0.0f;
-                            }
-#pragma unroll
-                            for (int nt = 0; nt < MT; ++nt) {
-                                // (F, F*acc1) of tokens 2t and 2t+1
-                                const float4 f = *reinterpret_cast<const float4*>(fcs + gq * MP + nt * 8 + 2 * t);
-                                ysum[nt][0] = fmaf(s0, fmaf(f.x, acc[q][nt][0], -f.y), ysum[nt][0]);
-                                ysum[nt][1] = fmaf(s0, fmaf(f.z, acc[q][nt][1], -f.w), ysum[nt][1]);
-                                ysum[nt][2] = fmaf(s1, fmaf(f.x, acc[q][nt][2], -f.y), ysum[nt][2]);
-                                ysum[nt][3] = fmaf(s1, fmaf(f.z, acc[q][nt][3], -f.w), ysum[nt][3]);
-                            }
-                        }
-                    }
+                    for (int e = 0; e < 4; ++e) w2[1][e] = 0x55555555u;
+                    sc[1][0] = sc[1][1] = 0.0f;
                 }
-                float* row = accs + (size_t)i * 16 * MP;
-#pragma unroll
-                for (int nt = 0; nt < MT; ++nt) {
-                    const int m0 = nt * 8 + 2 * t, m1 = m0 + 1;
-                    if (m0 < M) {
-                        atomicAdd(row + gid * MP + m0, ysum[nt][0]);
-                        atomicAdd(row + (gid + 8) * MP + m0, ysum[nt][2]);
-                    }
-                    if (m1 < M) {
-                        atomicAdd(row + gid * MP + m1, ysum[nt][1]);
-                        atomicAdd(row + (gid + 8) * MP + m1, ysum[nt][3]);
-                    }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(empty_bar(sA));
+                    if (two) mbar_arrive(empty_bar(sB));
+                }
+                float acc[2][MT][4];
+                pair_mmas<MT>(acc, w2, b);
+                epilogue(i, acc[0], sc[0][0], sc[0][1]);
+                if (two) epilogue(i + 1, acc[1], sc[1][0], sc[1][1]);
+            } else {
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(empty_bar(sA));
+                    if (two) mbar_arrive(empty_bar(sB));
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(s));
         }
     }
     __syncthreads();
