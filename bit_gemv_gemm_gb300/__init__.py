@@ -46,6 +46,7 @@ EXPORTS = {
     "tern_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
     "tern_device_error": (_I, [_P]),
     "tern_last_launch_count": (_I, []),
+    "tern_gemv_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
 }
 
 
@@ -175,6 +176,19 @@ def gemv(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y: torch.Te
     _check("tern_gemv", lib().tern_gemv(
         _dev(x, torch.bfloat16, "x"), _dev(codes, torch.int32, "codes"), _dev(scales, torch.float16, "scales"),
         _dev(y, torch.float32, "y"), M, N, K, _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return y
+
+
+def gemv_noalloc(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """tern_gemv without a workspace: the library's fixed scratch array is used."""
+    M, K = x.shape
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check("tern_gemv_noalloc", lib().tern_gemv_noalloc(
+        _dev(x, torch.bfloat16, "x"), _dev(codes, torch.int32, "codes"), _dev(scales, torch.float16, "scales"),
+        _dev(y, torch.float32, "y"), M, N, K, _stream(stream)))
     return y
 
 

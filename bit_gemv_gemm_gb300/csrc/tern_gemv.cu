@@ -573,3 +573,68 @@ extern "C" tern_status tern_fwht_gemm(const void* x, const int8_t* signs, const 
     if (!workspace || workspace_bytes_ < workspace_bytes(M, N, K, true)) return TERN_ERR_WORKSPACE;
     return run(x, signs, codes, scales, y, M, N, K, workspace, workspace_bytes_, (cudaStream_t)stream);
 }
+
+// ---------------------------------------------------------------------------
+// Decode product with no allocation anywhere.
+//
+// Some callers cannot allocate device memory for a workspace: code that runs
+// where an allocation may not happen (inside a custom allocator's own callback,
+// a caching allocator that must not recurse, an embedded runtime that owns all
+// device memory up front).  For them the product's scratch -- the per-slice
+// partial row sums and the per-tile arrival counters -- lives in one fixed
+// array in the library's own device memory.  Every GPU that loads the library
+// holds this array (TERN_NOALLOC_SCRATCH_BYTES) until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace tern {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = TERN_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};   // device address of the array, per device
+
+// The device address of the array on the current device.  In host code the
+// array's name is only a stand-in for the symbol, so the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+cudaError_t noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace tern
+
+extern "C" tern_status tern_gemv_noalloc(const void* x, const uint32_t* codes, const void* scales, float* y, int M,
+                                         int N, int K, tern_stream_t stream) {
+    set_launch_count(0);
+    const tern_status v = validate(x, codes, scales, y, M, N, K);
+    if (v != TERN_OK) return v;
+    if (tern::workspace_bytes(M, N, K, false) > kNoAllocScratchBytes) return TERN_ERR_WORKSPACE;
+    int sms = 0;
+    tern_status st = check_device(&sms);
+    if (st != TERN_OK) return st;
+    void* scratch = nullptr;
+    if (noalloc_scratch(&scratch) != cudaSuccess) return TERN_ERR_CUDA;
+    // the array keeps the previous call's contents: the arrival counters must
+    // start at zero, so clear them on the stream first (no allocation involved)
+    const Plan p = make_plan(M, N, K, false, sms);
+    if (p.S > 1 &&
+        cudaMemsetAsync(static_cast<char*>(scratch) + p.off_counter, 0, (size_t)p.T * 4, (cudaStream_t)stream) !=
+            cudaSuccess)
+        return TERN_ERR_CUDA;
+    return run(x, nullptr, codes, scales, y, M, N, K, scratch, kNoAllocScratchBytes, (cudaStream_t)stream);
+}

@@ -126,6 +126,30 @@ tern_status tern_gemv(const void *x, const uint32_t *codes, const void *scales, 
                       int M, int N, int K, void *workspace, size_t workspace_bytes,
                       tern_stream_t stream);
 
+/* Fixed size of the library-owned scratch array behind tern_gemv_noalloc. */
+#define TERN_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* The same product as tern_gemv, for callers that cannot allocate device
+ * memory (code running inside an allocator's own callback, a caching
+ * allocator that must not recurse into itself, a runtime that hands out all
+ * device memory up front): it takes no workspace and allocates nothing.  The
+ * pages describe no counterpart; this is a library convenience.
+ *   - Its scratch (per-slice partial sums, per-tile arrival counters) is one
+ *     file-scope device array of TERN_NOALLOC_SCRATCH_BYTES that every GPU
+ *     loading the library holds until the process exits.
+ *   - Shapes whose scratch, tern_gemv_workspace_bytes(M, N, K), exceeds that
+ *     size are rejected with TERN_ERR_WORKSPACE and nothing is launched.
+ *   - The first call on a device looks up the array's device address (once,
+ *     with that device current); make that first call before any stream
+ *     capture.
+ *   - Each call clears the arrival counters on `stream` before the product
+ *     kernel.  All calls share the one array, so calls whose kernels overlap
+ *     on the GPU (different streams, or devices sharing nothing else) race:
+ *     order them.
+ * Arguments, layout, results and tolerance as for tern_gemv. */
+tern_status tern_gemv_noalloc(const void *x, const uint32_t *codes, const void *scales, float *y,
+                              int M, int N, int K, tern_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* Rotation (article, section 3: normalized Sylvester-Walsh-Hadamard,      */
 /* block 4096, last dimension, explicit signs)                             */

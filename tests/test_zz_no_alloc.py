@@ -1,0 +1,69 @@
+"""The decode product for callers that cannot allocate device memory.
+
+tern_gemv_noalloc takes no workspace: its scratch (the partial row sums of each
+K-slice and the arrival counters of each row tile) is a fixed array inside the
+library.  It exists for code that must not call cudaMalloc -- for instance code
+running inside an allocator's own callback, or under a runtime that owns all
+device memory -- and so cannot provide the workspace tern_gemv asks for.
+
+These checks call it through the C ABI and compare it with tern_gemv on the
+same inputs, twice in a row (the second call starts from whatever the first
+left in the shared array), within the decode tolerance
+|y - y_ref| <= 1e-3 * sum_k |x w| + 1e-6.  This file sorts last so that a run
+stopping at the first failure has already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests._util import assert_fp32_close, dev_bf16, dev_scales, dev_trits, host_codes
+
+TERN_ERR_WORKSPACE = 4
+NOALLOC_BYTES = 8 << 20
+
+
+@pytest.fixture(scope="module")
+def tern():
+    from bit_gemv_gemm_gb300 import build
+    build.build()
+    import bit_gemv_gemm_gb300 as t
+    return t
+
+
+def _call_noalloc(tern, x, codes, s, y):
+    M, K = x.shape
+    N = codes.shape[0]
+    st = tern.lib().tern_gemv_noalloc(x.data_ptr(), codes.data_ptr(), s.data_ptr(), y.data_ptr(), M, N, K,
+                                      torch.cuda.current_stream().cuda_stream)
+    assert st == 0, f"tern_gemv_noalloc status {st}"
+
+
+def test_noalloc_rejects_oversized_shapes_without_launching(tern):
+    """A shape whose scratch exceeds the fixed array is refused up front."""
+    M, N, K = 16, 17408, 17408
+    assert tern.gemv_workspace_bytes(M, N, K) > NOALLOC_BYTES
+    P = 4096   # a fake aligned address: the size check comes before any device use
+    assert tern.lib().tern_gemv_noalloc(P, P, P, P, M, N, K, None) == TERN_ERR_WORKSPACE
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,N,K", [(1, 17408, 5120), (1, 5120, 17408), (3, 1000, 5120), (16, 600, 2048),
+                                   (5, 200, 512)])
+def test_noalloc_matches_gemv_twice(tern, orc, M, N, K):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    assert tern.gemv_workspace_bytes(M, N, K) <= NOALLOC_BYTES
+    p = synth.problem(500 + M, M, N, K, tag=f"na{N}x{K}")
+    x, codes, s = dev_bf16(p.x), tern.pack(dev_trits(p.t)), dev_scales(p.s)
+    y_ref_dev = tern.gemv(x, codes, s)
+    torch.cuda.synchronize()
+    y_ref = y_ref_dev.cpu().numpy().astype(np.float64)
+    _, a_ref = orc.matmul(p.x, host_codes(codes), p.s)
+    for call in range(2):
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        _call_noalloc(tern, x, codes, s, y)
+        torch.cuda.synchronize()
+        assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what=f"noalloc call {call} M={M} N={N} K={K}")
