@@ -54,13 +54,16 @@ constexpr int kGroup = 128;            // weights per scale
 constexpr int kSliceGroups = 8;        // groups per K-slice = warps per CTA
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kDepth = 8;              // tiles in flight per warp
+constexpr int kDepth = 12;             // tiles in flight per warp (even)
+constexpr int kEarly = 4;              // of which issued before the activation is staged
 constexpr int kSlotBytes = 16 * 32;    // one warp's share of a tile: 16 rows x 32 B
-constexpr int kMaxTiles = 48;          // tiles per CTA (shared partials)
+constexpr int kMaxTiles = 32;          // tiles per CTA (bounds the shared partials and scales)
 constexpr int kPrivateMaxM = 4;        // private per-warp partials up to this many tokens
+constexpr size_t kSmemPerSm = 228 * 1024;   // shared memory of one SM
+constexpr size_t kCtaSmemReserve = 1024;    // taken by the system from each resident CTA
 
 template <int MT> struct GemvCfg;
-template <> struct GemvCfg<1> { static constexpr int kCtasPerSm = 2; };
+template <> struct GemvCfg<1> { static constexpr int kCtasPerSm = 3; };
 template <> struct GemvCfg<2> { static constexpr int kCtasPerSm = 2; };
 
 struct GemvArgs {
@@ -75,7 +78,7 @@ struct GemvArgs {
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// dynamic shared memory: [code rings | scales | row partials | finalize flags]
+// dynamic shared memory: [code rings | scales [row][8] | row partials | finalize flags]
 __host__ __device__ inline size_t smem_sc() { return (size_t)kWarps * kDepth * kSlotBytes; }
 __host__ __device__ inline size_t smem_part(int rmax) {
     return smem_sc() + align_up((size_t)kWarps * rmax * 16 * 2, 16);
@@ -171,7 +174,7 @@ gemv_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int rmax = a.rmax;
     const int M = a.M;
-    unsigned short* scs = reinterpret_cast<unsigned short*>(smem + smem_sc());   // [8][rmax][16]
+    unsigned short* scs = reinterpret_cast<unsigned short*>(smem + smem_sc());   // [rmax * 16][8]
     float* part = reinterpret_cast<float*>(smem + smem_part(rmax));
     int* fin = reinterpret_cast<int*>(smem + smem_fin(rmax, M, MP));           // [rmax]
 
@@ -191,40 +194,44 @@ gemv_kernel(const GemvArgs a) {
     // this warp's ring; lane l copies row l/2, 16-byte half l%2 of its group's 32 bytes
     unsigned char* ring = smem + (size_t)warp * kDepth * kSlotBytes;
     const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
-    const int crow = lane >> 1, chalf = lane & 1;
-    auto issue = [&](int i) {
+    const int crow0 = tile_lo * 16 + (lane >> 1);
+    const uint32_t* csrc = a.codes + (size_t)crow0 * W + g * 8 + (lane & 1) * 4;
+    const size_t cstep = (size_t)16 * W;   // words per tile
+    // tile i into ring slot `slot` (= i mod kDepth)
+    auto issue = [&](int i, int slot) {
         if (active && i < R) {
-            const int row = (tile_lo + i) * 16 + crow;
-            const bool ok = row < N;
-            const uint32_t* src = a.codes + (size_t)(ok ? row : 0) * W + g * 8 + chalf * 4;
-            cp_async16(ring_s + (uint32_t)((i % kDepth) * kSlotBytes + lane * 16), src, ok);
+            const bool ok = crow0 + 16 * i < N;
+            cp_async16(ring_s + (uint32_t)(slot * kSlotBytes + lane * 16), ok ? csrc + (size_t)i * cstep : a.codes,
+                       ok);
         }
         cp_async_commit();   // one group per tile, empty past the end, so the waits count uniformly
     };
 
     pdl_launch_dependents();
-    // codes are never the previous kernel's output: start streaming before the PDL wait
-#pragma unroll
-    for (int i = 0; i < kDepth; ++i) issue(i);
-    pdl_wait();
-
-    // this warp's scales for the whole range (all loads in flight at once)
-    if (active) {
-        constexpr int kPer = (kMaxTiles * 16 + 31) / 32;
-        unsigned short sv[kPer];
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) {
-            const int i = lane + 32 * e;
+    // codes and scales are never the previous kernel's output: start streaming
+    // both before the PDL wait.  The scales of the whole range come first, as
+    // one commit group: a row's 8 slice scales are one 16-byte chunk when G is
+    // a multiple of 8 (one copy per row), else they are gathered one by one.
+    if (G % kSliceGroups == 0) {
+        const uint32_t scs_s = static_cast<uint32_t>(__cvta_generic_to_shared(scs));
+        for (int i = threadIdx.x; i < R * 16; i += kThreads) {
             const int row = tile_lo * 16 + i;
-            sv[e] = (i < R * 16 && row < N) ? __half_as_ushort(a.scales[(size_t)row * G + g]) : (unsigned short)0;
+            const bool ok = row < N;
+            cp_async16(scs_s + (uint32_t)i * 16u, a.scales + (size_t)(ok ? row : 0) * G + g0, ok);
         }
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) {
-            const int i = lane + 32 * e;
-            if (i < R * 16) scs[(size_t)warp * rmax * 16 + i] = sv[e];
+    } else {
+        for (int i = threadIdx.x; i < R * 16 * kSliceGroups; i += kThreads) {
+            const int row = tile_lo * 16 + (i >> 3), gg = i & 7;
+            scs[i] = (row < N && gg < gs) ? __half_as_ushort(a.scales[(size_t)row * G + g0 + gg])
+                                          : (unsigned short)0;
         }
     }
-    for (int i = threadIdx.x; i < (int)part_floats(rmax, M, MP); i += kThreads) part[i] = 0.0f;
+    cp_async_commit();
+#pragma unroll
+    for (int i = 0; i < kEarly; ++i) issue(i, i);
+    pdl_wait();
+    if (M > kPrivateMaxM)   // shared partials take atomics; private ones are written once each
+        for (int i = threadIdx.x; i < (int)part_floats(rmax, M, MP); i += kThreads) part[i] = 0.0f;
 
     // stage this warp's group: lane (gid, t) holds token nt*8+gid, k = 32t .. 32t+31
     uint32_t b[MT][16];
@@ -267,15 +274,14 @@ gemv_kernel(const GemvArgs a) {
         for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(v[e]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        // E with mx * 2^(E + 10) < 2^15: mx < 2^ex for ex = biased exponent - 126
+        const int be = (int)(__float_as_uint(mx) >> 23);   // mx >= 0
         int E = 0;
-        if (mx > 0.0f && mx <= 3.0e38f) {
-            int ex;
-            frexpf(mx, &ex);                       // mx < 2^ex
-            E = max(-100, min(5 - ex, 150));       // mx * 2^(E + 10) < 2^15
-        }
+        if (mx > 0.0f && be < 255) E = max(-100, min(5 - (max(be, 1) - 126), 110));
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float c = ldexpf(1.0f, E + 10 - 2 * (j < 6 ? j : j - 6));   // exact power of two
+            // exact power of two 2^(E + 10 - 2j'), exponent within [-100, 120]
+            const float c = __uint_as_float((uint32_t)(E + 10 - 2 * (j < 6 ? j : j - 6) + 127) << 23);
             const __half2 lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);       // k = 32t+j, +8
             const __half2 hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c); // k = 32t+16+j, +24
             b[nt][2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
@@ -286,18 +292,22 @@ gemv_kernel(const GemvArgs a) {
         float acc1[4];
         const uint32_t ones[4] = {0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u};
         mma_chain1(acc1, ones, b[nt]);
-        const float F = (m < M) ? ldexpf(1.0f, 14 - E) : 0.0f;
+        const float F = (m < M) ? __uint_as_float((uint32_t)(14 - E + 127) << 23) : 0.0f;   // 2^(14-E)
         const float F0 = __shfl_sync(0xffffffffu, F, (2 * t) * 4);
         const float F1 = __shfl_sync(0xffffffffu, F, (2 * t + 1) * 4);
         f[nt] = make_float4(F0, F0 * acc1[0], F1, F1 * acc1[1]);
     }
-    // scales and zeroed partials visible to every warp
+#pragma unroll
+    for (int i = kEarly; i < kDepth; ++i) issue(i, i);
+    // this thread's scale copies (the oldest group) have landed; after the
+    // barrier every thread's have, and the zeroed partials are visible
+    cp_async_wait<kDepth>();
     __syncthreads();
 
-    const unsigned short* sc_w = scs + (size_t)warp * rmax * 16;
+    const unsigned short* sc_w = scs + warp;   // row r of the range: sc_w[8 r]
     auto epilogue = [&](int i, const float (&acc)[MT][4]) {
-        const float s0 = __half2float(__ushort_as_half(sc_w[i * 16 + gid]));
-        const float s1 = __half2float(__ushort_as_half(sc_w[i * 16 + gid + 8]));
+        const float s0 = __half2float(__ushort_as_half(sc_w[(i * 16 + gid) * 8]));
+        const float s1 = __half2float(__ushort_as_half(sc_w[(i * 16 + gid + 8) * 8]));
 #pragma unroll
         for (int nt = 0; nt < MT; ++nt) {
             const int m0 = nt * 8 + 2 * t, m1 = m0 + 1;
@@ -306,15 +316,15 @@ gemv_kernel(const GemvArgs a) {
             const float v2 = s1 * fmaf(f[nt].x, acc[nt][2], -f[nt].y);   // row gid + 8, token m0
             const float v3 = s1 * fmaf(f[nt].z, acc[nt][3], -f[nt].w);   // row gid + 8, token m1
             if (M <= kPrivateMaxM) {
-                // [warp][tile][row][M], one writer per element
+                // [warp][tile][row][M]: each element written once, by its warp
                 float* pw = part + (((size_t)warp * rmax + i) * 16) * M;
                 if (m0 < M) {
-                    pw[gid * M + m0] += v0;
-                    pw[(gid + 8) * M + m0] += v2;
+                    pw[gid * M + m0] = v0;
+                    pw[(gid + 8) * M + m0] = v2;
                 }
                 if (m1 < M) {
-                    pw[gid * M + m1] += v1;
-                    pw[(gid + 8) * M + m1] += v3;
+                    pw[gid * M + m1] = v1;
+                    pw[(gid + 8) * M + m1] = v3;
                 }
             } else {
                 float* row = part + (size_t)i * 16 * MP;   // [tile][row][MP], shared by the warps
@@ -331,6 +341,7 @@ gemv_kernel(const GemvArgs a) {
     };
 
     if (active) {
+        int slot = 0;   // ring slot of tile i (kDepth is even: tile i + 1 sits in slot + 1)
         for (int i = 0; i < R; i += 2) {
             const bool two = i + 1 < R;
             // tiles i and i + 1 have landed (at most kDepth - 2 newer groups pending)
@@ -339,9 +350,9 @@ gemv_kernel(const GemvArgs a) {
             uint32_t w[2][4];
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                const unsigned char* slot = ring + ((i + q) % kDepth) * kSlotBytes;
-                const uint2 v0 = *reinterpret_cast<const uint2*>(slot + gid * 32 + 8 * t);
-                const uint2 v1 = *reinterpret_cast<const uint2*>(slot + (gid + 8) * 32 + 8 * t);
+                const unsigned char* sp = ring + (slot + q) * kSlotBytes;
+                const uint2 v0 = *reinterpret_cast<const uint2*>(sp + gid * 32 + 8 * t);
+                const uint2 v1 = *reinterpret_cast<const uint2*>(sp + (gid + 8) * 32 + 8 * t);
                 w[q][0] = v0.x;   // row gid,     word 2t      (MMA rows 0-7,  k-slots 2t, 2t+1)
                 w[q][1] = v1.x;   // row gid + 8, word 2t      (MMA rows 8-15)
                 w[q][2] = v0.y;   // row gid,     word 2t + 1  (k-slots 2t+8, 2t+9)
@@ -351,10 +362,11 @@ gemv_kernel(const GemvArgs a) {
             pair_mmas<MT>(acc, w, b);
             // both slots fully read by every lane: refill them kDepth tiles ahead
             __syncwarp();
-            issue(i + kDepth);
-            issue(i + 1 + kDepth);
+            issue(i + kDepth, slot);
+            issue(i + 1 + kDepth, slot + 1);
             epilogue(i, acc[0]);
             if (two) epilogue(i + 1, acc[1]);
+            slot = slot + 2 == kDepth ? 0 : slot + 2;
         }
     }
     cp_async_wait<0>();
@@ -365,7 +377,7 @@ gemv_kernel(const GemvArgs a) {
     auto row_value = [&](int tl, int r, int m) -> float {
         if (M <= kPrivateMaxM) {
             float s = 0.0f;
-            for (int w2 = 0; w2 < kWarps; ++w2) s += part[(((size_t)w2 * rmax + tl) * 16 + r) * M + m];
+            for (int w2 = 0; w2 < gs; ++w2) s += part[(((size_t)w2 * rmax + tl) * 16 + r) * M + m];
             return s;
         }
         return part[((size_t)tl * 16 + r) * MP + m];
@@ -439,15 +451,19 @@ Plan make_plan(int M, int N, int K, bool rot, int sms) {
     p.T = (N + 15) / 16;
     p.S = (p.G + kSliceGroups - 1) / kSliceGroups;
     p.MT = (M + 7) / 8;
-    const int per_sm = p.MT == 1 ? GemvCfg<1>::kCtasPerSm : GemvCfg<2>::kCtasPerSm;
-    const int cmax = sms * per_sm;
-    p.cps = p.S >= cmax ? 1 : cmax / p.S;
-    if (p.cps > p.T) p.cps = p.T;
+    // one wave: as many CTAs as fit on every SM at once, by registers (the
+    // launch bound) and by shared memory (which grows with the range length)
     const int need = (p.T + kMaxTiles - 1) / kMaxTiles;   // ranges short enough for the shared partials
-    if (p.cps < need) p.cps = need;
+    for (int per_sm = p.MT == 1 ? GemvCfg<1>::kCtasPerSm : GemvCfg<2>::kCtasPerSm; per_sm >= 1; --per_sm) {
+        const int cmax = sms * per_sm;
+        p.cps = p.S >= cmax ? 1 : cmax / p.S;
+        if (p.cps > p.T) p.cps = p.T;
+        if (p.cps < need) p.cps = need;
+        p.rmax = (p.T + p.cps - 1) / p.cps;
+        p.smem = smem_total(p.rmax, M, 8 * p.MT);
+        if ((size_t)per_sm * (p.smem + kCtaSmemReserve) <= kSmemPerSm) break;
+    }
     p.ctas = p.S * p.cps;
-    p.rmax = (p.T + p.cps - 1) / p.cps;
-    p.smem = smem_total(p.rmax, M, 8 * p.MT);
     size_t off = 0;
     p.off_xr = off;
     if (rot) off = align_up(off + (size_t)M * K * 4, 256);
