@@ -267,7 +267,7 @@ def bench_decode(tern, sweep: DecodeSweep, steps: int, warmup: int, ws_count: in
         torch.cuda.synchronize()
         barrier(ws_count)
     ms = max_over_ranks(ms, ws_count)
-    launches = 2 * sum(len(p) for p in sweep.layers)
+    launches = sum(len(p) for p in sweep.layers)        # one kernel per tern_gemv call
 
     # end to end through the same API: H2D of every projection's x, the sweep,
     # D2H of every y; pinned host buffers, copies inside the timed region.
