@@ -33,32 +33,43 @@
 //         y += s_g * (2^(14 - E) * acc - 2^(14 - E) * acc1),
 //     so a row of zero weights (q = 1 everywhere) gives exactly 0.
 //
-// Work split.  K is cut into slices of up to 8 groups; a CTA owns one slice
-// and a contiguous range of 16-row tiles, and warp w of the CTA owns group w of
-// the slice for the whole range: it stages that group's activation once, into
-// registers, and streams its own 32-byte column of every tile (16 rows x 32 B =
-// one 16-byte cp.async per lane) through a private shared-memory ring, kDepth
-// tiles ahead; the first kDepth go out before the programmatic-dependent-launch
-// wait.  Two tiles per step run as two independent MMA chains.  Row partial
-// sums go to shared memory (private per warp for M <= 4, shared atomics
-// beyond).  With one slice the CTA writes y; with several, each CTA stores its
-// partial tile sums to the workspace and the last CTA to finish a tile (an
-// arrival counter) adds the slices in slice order and writes y.  y is written
-// exactly once per element: no pre-zeroing, no global float atomics.
+// Work split.  K is cut into S = ceil(G / 8) slices of whole groups (balanced
+// to within one group), and N into ranges of 16-row tiles; a CTA owns one
+// (slice, range) pair, and the CTAs of slice 0 come first in the grid.  Inside
+// a CTA the slice's groups are dealt to the 8 warps as segments: every warp
+// takes floor(Gs / 8) whole groups over the full range, and each of the Gs mod
+// 8 groups left over is cut into eight tile chunks, one per warp.  A warp
+// stages one segment's activation (from a copy of the slice's x in shared
+// memory) into registers and streams its own 32-byte column of every tile of
+// the segment (16 rows x 32 B = one 16-byte cp.async per lane) through a
+// private shared-memory ring, kDepth units ahead; the first kDepth units go out
+// before the programmatic-dependent-launch wait.  Two tiles per step run as two
+// independent MMA chains.  Row partials go to shared memory (private per warp
+// for M <= 4, shared atomics beyond) and are summed over the CTA's warps.
+// With one slice the CTA stores its rows of y.  With several, the slice-0 CTA
+// of a range clears the range's rows of y right after the PDL wait and then
+// counts itself into the range's flag word; every other CTA of the range, once
+// its loop is done (long after the clearing), waits for that count, counts
+// itself and adds its row sums into y with global reductions.  The flag
+// counts modulo S (atomicInc), so it is back at 0 when the call ends.  The
+// order in which the S slice sums meet is not fixed: the last bits of y may
+// differ from run to run.
+#include <mutex>
+#include <type_traits>
+
 #include "tern_fwht.cuh"
 
 namespace tern {
 namespace {
 
 constexpr int kGroup = 128;            // weights per scale
-constexpr int kSliceGroups = 8;        // groups per K-slice = warps per CTA
-constexpr int kWarps = 8;
+constexpr int kWarps = 8;              // warps per CTA
 constexpr int kThreads = kWarps * 32;
-constexpr int kDepth = 12;             // tiles in flight per warp (even)
-constexpr int kEarly = 4;              // of which issued before the activation is staged
-constexpr int kSlotBytes = 16 * 32;    // one warp's share of a tile: 16 rows x 32 B
-constexpr int kMaxTiles = 32;          // tiles per CTA (bounds the shared partials and scales)
+constexpr int kDepth = 6;              // units (tile x group) in flight per warp (even)
+constexpr int kSlotBytes = 16 * 32;    // one unit: 16 rows x 32 B of codes
+constexpr int kMaxTiles = 32;          // tiles per range (bounds partials and scales in shared memory)
 constexpr int kPrivateMaxM = 4;        // private per-warp partials up to this many tokens
+constexpr size_t kXSmemMax = 16384;    // the slice's activation is copied to shared memory up to this size
 constexpr size_t kSmemPerSm = 228 * 1024;   // shared memory of one SM
 constexpr size_t kCtaSmemReserve = 1024;    // taken by the system from each resident CTA
 
@@ -71,26 +82,14 @@ struct GemvArgs {
     const uint32_t* codes;      // [N][K/16]
     const __half* scales;       // [N][K/128]
     float* y;                   // [M][N]
-    float* partial;             // [S][T][M][16]
-    unsigned* counter;          // [T]
+    unsigned* flag;             // [cps] per-range flag words (S > 1), 0 between calls
     int M, N, K, G, T, S, cps, rmax;
+    int gpad;                   // scale row pitch in shared memory (halves)
+    int xpitch;                 // activation row pitch in shared memory (elements); 0: read x from global
+    uint32_t off_sc, off_x, off_part;   // shared-memory offsets (bytes)
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
-// dynamic shared memory: [code rings | scales [row][8] | row partials | finalize flags]
-__host__ __device__ inline size_t smem_sc() { return (size_t)kWarps * kDepth * kSlotBytes; }
-__host__ __device__ inline size_t smem_part(int rmax) {
-    return smem_sc() + align_up((size_t)kWarps * rmax * 16 * 2, 16);
-}
-// private: [8 warps][rmax][16][M]; shared: [rmax][16][MP]
-__host__ __device__ inline size_t part_floats(int rmax, int M, int MP) {
-    return M <= kPrivateMaxM ? (size_t)kWarps * rmax * 16 * M : (size_t)rmax * 16 * MP;
-}
-__host__ __device__ inline size_t smem_fin(int rmax, int M, int MP) {
-    return smem_part(rmax) + part_floats(rmax, M, MP) * 4;
-}
-__host__ __device__ inline size_t smem_total(int rmax, int M, int MP) { return smem_fin(rmax, M, MP) + (size_t)rmax * 4; }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1, bool accumulate) {
@@ -139,7 +138,7 @@ __device__ __forceinline__ void mma_chain1(float (&acc)[4], const uint32_t (&w)[
     }
 }
 
-// Two tiles of the warp's group at once: 2 x MT independent MMA chains sharing
+// Two units of the same group at once: 2 x MT independent MMA chains sharing
 // the B fragments, each in the slot order of mma_chain1 (so each keeps the
 // ones-pass rounding).
 template <int MT>
@@ -158,156 +157,268 @@ __device__ __forceinline__ void pair_mmas(float (&acc)[2][MT][4], const uint32_t
     }
 }
 
-// ---- per-warp asynchronous copies (cp.async, 16 bytes per lane) ----
+// ---- asynchronous copies (cp.async) ----
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0)
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int MT, bool XF32>
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- the per-range flag word ----
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint64_t now_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+constexpr uint64_t kFlagWaitNs = 1000000000ull;   // 1 s: far beyond any real wait
+
+__device__ int g_gemv_error;   // sticky device error word of this translation unit
+
+// Scales of a slice [gA, gB): the copy starts at group g_lo and is `width`
+// groups wide; 16-byte chunks when every slice starts and ends on a multiple
+// of 8 groups, 4-byte pairs when G is even, single halves otherwise.
+__host__ __device__ inline int scale_mode(int G, int gA, int gB) {
+    if (G % 8 == 0 && gA % 8 == 0 && (gB - gA) % 8 == 0) return 16;
+    return G % 2 == 0 ? 4 : 2;
+}
+__host__ __device__ inline int scale_lo(int G, int gA, int gB) { return scale_mode(G, gA, gB) == 4 ? (gA & ~1) : gA; }
+__host__ __device__ inline int scale_width(int G, int gA, int gB) {
+    return scale_mode(G, gA, gB) == 4 ? ((gB + 1) & ~1) - (gA & ~1) : gB - gA;
+}
+
+// ONE: the single-token case (M = 1), whose epilogue keeps one value per row.
+template <int MT, bool XF32, bool ONE>
 __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kCtasPerSm)
 gemv_kernel(const GemvArgs a) {
+    using XT = typename std::conditional<XF32, float, __nv_bfloat16>::type;
     constexpr int MP = 8 * MT;
     extern __shared__ __align__(16) unsigned char smem[];
-    const int rmax = a.rmax;
-    const int M = a.M;
-    unsigned short* scs = reinterpret_cast<unsigned short*>(smem + smem_sc());   // [rmax * 16][8]
-    float* part = reinterpret_cast<float*>(smem + smem_part(rmax));
-    int* fin = reinterpret_cast<int*>(smem + smem_fin(rmax, M, MP));           // [rmax]
-
+    const int M = ONE ? 1 : a.M;
+    const int N = a.N, G = a.G, S = a.S, rmax = a.rmax, gpad = a.gpad;
+    const int W = a.K / 16;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, t = lane & 3;
-    const int N = a.N, G = a.G, T = a.T, S = a.S;
-    const int W = a.K / 16;
-    const int sigma = blockIdx.x / a.cps, cslot = blockIdx.x - sigma * a.cps;
-    const int g0 = sigma * kSliceGroups;
-    const int gs = min(kSliceGroups, G - g0);
-    const int tile_lo = (int)((long long)T * cslot / a.cps);
-    const int tile_hi = (int)((long long)T * (cslot + 1) / a.cps);
-    const int R = tile_hi - tile_lo;
-    const bool active = warp < gs;
-    const int g = g0 + (active ? warp : 0);
+    const int sigma = blockIdx.x / a.cps, clu = blockIdx.x - sigma * a.cps;   // slice, range
+    const int gA = (int)((long long)G * sigma / S), gB = (int)((long long)G * (sigma + 1) / S);
+    const int Gs = gB - gA;
+    const int tile_lo = (int)((long long)a.T * clu / a.cps);
+    const int R = (int)((long long)a.T * (clu + 1) / a.cps) - tile_lo;
+    const int na = Gs / kWarps, nb = Gs - na * kWarps, nseg = na + nb;
+    const int g_lo = scale_lo(G, gA, gB);
 
-    // this warp's ring; lane l copies row l/2, 16-byte half l%2 of its group's 32 bytes
+    unsigned short* sc = reinterpret_cast<unsigned short*>(smem + a.off_sc);   // [R * 16][gpad]
+    float* part = reinterpret_cast<float*>(smem + a.off_part);
+
+    // segment s of this warp: s < na is group gA + warp + 8 s over all R tiles;
+    // s >= na is left-over group gA + 8 na + (s - na) over tile chunk
+    // (warp + s - na) mod 8 (the chunk rotates so no warp takes every short one)
+    auto seg_group = [&](int s) { return s < na ? gA + warp + kWarps * s : gA + kWarps * na + (s - na); };
+    auto seg_lo = [&](int s) { return s < na ? 0 : R * ((warp + s - na) & 7) / kWarps; };
+    auto seg_hi = [&](int s) { return s < na ? R : R * (((warp + s - na) & 7) + 1) / kWarps; };
+
+    // ---- this warp's ring: unit u in slot u mod kDepth; lane l copies row l/2,
+    // 16-byte half l%2 of the unit's 32 bytes ----
     unsigned char* ring = smem + (size_t)warp * kDepth * kSlotBytes;
-    const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
-    const int crow0 = tile_lo * 16 + (lane >> 1);
-    const uint32_t* csrc = a.codes + (size_t)crow0 * W + g * 8 + (lane & 1) * 4;
-    const size_t cstep = (size_t)16 * W;   // words per tile
-    // tile i into ring slot `slot` (= i mod kDepth)
-    auto issue = [&](int i, int slot) {
-        if (active && i < R) {
-            const bool ok = crow0 + 16 * i < N;
-            cp_async16(ring_s + (uint32_t)(slot * kSlotBytes + lane * 16), ok ? csrc + (size_t)i * cstep : a.codes,
-                       ok);
+    const uint32_t ring_s = smem_addr(ring) + (uint32_t)lane * 16u;
+    const int crow = lane >> 1;
+    const size_t cstep = (size_t)16 * W;   // words from one tile to the next
+    // issue cursor: segment, units left in it, this lane's next row and source
+    int is = 0, ileft = 0, irow = 0;
+    const uint32_t* iptr = a.codes;
+    auto iseg_begin = [&](int s) {
+        while (s < nseg && seg_lo(s) >= seg_hi(s)) ++s;
+        is = s;
+        if (s < nseg) {
+            const int lo = seg_lo(s);
+            ileft = seg_hi(s) - lo;
+            irow = (tile_lo + lo) * 16 + crow;
+            iptr = a.codes + (size_t)irow * W + seg_group(s) * 8 + (lane & 1) * 4;
         }
-        cp_async_commit();   // one group per tile, empty past the end, so the waits count uniformly
+    };
+    iseg_begin(0);
+    auto issue = [&](int slot) {
+        if (is < nseg) {
+            const bool ok = irow < N;
+            cp_async16(ring_s + (uint32_t)(slot * kSlotBytes), ok ? iptr : a.codes, ok);
+            iptr += cstep;
+            irow += 16;
+            if (--ileft == 0) iseg_begin(is + 1);
+        }
+        cp_async_commit();   // one group per unit, empty past the end, so the waits count uniformly
     };
 
     pdl_launch_dependents();
-    // codes and scales are never the previous kernel's output: start streaming
-    // both before the PDL wait.  The scales of the whole range come first, as
-    // one commit group: a row's 8 slice scales are one 16-byte chunk when G is
-    // a multiple of 8 (one copy per row), else they are gathered one by one.
-    if (G % kSliceGroups == 0) {
-        const uint32_t scs_s = static_cast<uint32_t>(__cvta_generic_to_shared(scs));
-        for (int i = threadIdx.x; i < R * 16; i += kThreads) {
-            const int row = tile_lo * 16 + i;
-            const bool ok = row < N;
-            cp_async16(scs_s + (uint32_t)i * 16u, a.scales + (size_t)(ok ? row : 0) * G + g0, ok);
+    // Codes and scales are never the previous kernel's output: the range's
+    // scales (one commit group) and the first kDepth units of every warp go
+    // out before the PDL wait.
+    {
+        const int row0 = tile_lo * 16, rows = R * 16;
+        const int mode = scale_mode(G, gA, gB);
+        const uint32_t sc_s = smem_addr(sc);
+        if (mode == 16) {
+            const int cpr = Gs / 8;
+            for (int i = threadIdx.x; i < rows * cpr; i += kThreads) {
+                const int r = i / cpr, c = i - r * cpr;
+                const bool ok = row0 + r < N;
+                cp_async16(sc_s + (uint32_t)(r * gpad + 8 * c) * 2u,
+                           ok ? a.scales + (size_t)(row0 + r) * G + gA + 8 * c : a.scales, ok);
+            }
+        } else if (mode == 4) {
+            const int cpr = scale_width(G, gA, gB) / 2;
+            for (int i = threadIdx.x; i < rows * cpr; i += kThreads) {
+                const int r = i / cpr, c = i - r * cpr;
+                const bool ok = row0 + r < N;
+                cp_async4(sc_s + (uint32_t)(r * gpad + 2 * c) * 2u,
+                          ok ? a.scales + (size_t)(row0 + r) * G + g_lo + 2 * c : a.scales, ok);
+            }
+        } else {
+            for (int i = threadIdx.x; i < rows * Gs; i += kThreads) {
+                const int r = i / Gs, c = i - r * Gs;
+                sc[r * gpad + c] = row0 + r < N ? __half_as_ushort(a.scales[(size_t)(row0 + r) * G + gA + c])
+                                                : (unsigned short)0;
+            }
         }
-    } else {
-        for (int i = threadIdx.x; i < R * 16 * kSliceGroups; i += kThreads) {
-            const int row = tile_lo * 16 + (i >> 3), gg = i & 7;
-            scs[i] = (row < N && gg < gs) ? __half_as_ushort(a.scales[(size_t)row * G + g0 + gg])
-                                          : (unsigned short)0;
+        cp_async_commit();
+    }
+#pragma unroll
+    for (int i = 0; i < kDepth; ++i) issue(i);
+    pdl_wait();
+    // the slice's activation (possibly the previous kernel's output) into shared memory
+    if (a.xpitch) {
+        const uint32_t xs_s = smem_addr(smem + a.off_x);
+        const int cpm = Gs * kGroup * (int)sizeof(XT) / 16;   // 16-byte chunks per token
+        const char* xg = reinterpret_cast<const char*>(a.x) + (size_t)gA * kGroup * sizeof(XT);
+        for (int i = threadIdx.x; i < M * cpm; i += kThreads) {
+            const int m = i / cpm, c = i - m * cpm;
+            cp_async16(xs_s + (uint32_t)(m * a.xpitch * (int)sizeof(XT) + 16 * c),
+                       xg + (size_t)m * a.K * sizeof(XT) + 16 * c, true);
         }
     }
     cp_async_commit();
-#pragma unroll
-    for (int i = 0; i < kEarly; ++i) issue(i, i);
-    pdl_wait();
-    if (M > kPrivateMaxM)   // shared partials take atomics; private ones are written once each
-        for (int i = threadIdx.x; i < (int)part_floats(rmax, M, MP); i += kThreads) part[i] = 0.0f;
-
-    // stage this warp's group: lane (gid, t) holds token nt*8+gid, k = 32t .. 32t+31
-    uint32_t b[MT][16];
-    float4 f[MT];   // (F, F*acc1) of tokens 2t and 2t+1 of each token tile
-#pragma unroll
-    for (int nt = 0; nt < MT; ++nt) {
-        const int m = nt * 8 + gid;
-        float v[32];
-        if (active && m < M) {
-            const size_t off = (size_t)m * a.K + (size_t)g * kGroup + 32 * t;
-            if (XF32) {
-                const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) + off);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 u = src[q];
-                    v[4 * q] = u.x;
-                    v[4 * q + 1] = u.y;
-                    v[4 * q + 2] = u.z;
-                    v[4 * q + 3] = u.w;
-                }
-            } else {
-                const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) + off);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 u = src[q];
-                    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        v[8 * q + 2 * e] = __uint_as_float(uw[e] << 16);
-                        v[8 * q + 2 * e + 1] = __uint_as_float(uw[e] & 0xFFFF0000u);
-                    }
-                }
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+    // y of the range starts at zero: the slice-0 CTA clears it (after the PDL
+    // wait, since the previous kernel may still read y) and counts itself into
+    // the range's flag once the zeros are visible to the whole GPU
+    if (S > 1 && sigma == 0) {
+        const int row0 = tile_lo * 16, nrow = min(R * 16, N - row0);
+        for (int i = threadIdx.x; i < M * nrow; i += kThreads) {
+            const int m = i / nrow, r = i - m * nrow;
+            a.y[(size_t)m * N + row0 + r] = 0.0f;
         }
-        float mx = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(v[e]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        // E with mx * 2^(E + 10) < 2^15: mx < 2^ex for ex = biased exponent - 126
-        const int be = (int)(__float_as_uint(mx) >> 23);   // mx >= 0
-        int E = 0;
-        if (mx > 0.0f && be < 255) E = max(-100, min(5 - (max(be, 1) - 126), 110));
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            // exact power of two 2^(E + 10 - 2j'), exponent within [-100, 120]
-            const float c = __uint_as_float((uint32_t)(E + 10 - 2 * (j < 6 ? j : j - 6) + 127) << 23);
-            const __half2 lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);       // k = 32t+j, +8
-            const __half2 hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c); // k = 32t+16+j, +24
-            b[nt][2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
-            b[nt][2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
-        }
-        // the -1 correction: the same chain on the all-ones pattern; every row of
-        // the result is the same, lane (gid, t) holds tokens 2t, 2t+1
-        float acc1[4];
-        const uint32_t ones[4] = {0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u};
-        mma_chain1(acc1, ones, b[nt]);
-        const float F = (m < M) ? __uint_as_float((uint32_t)(14 - E + 127) << 23) : 0.0f;   // 2^(14-E)
-        const float F0 = __shfl_sync(0xffffffffu, F, (2 * t) * 4);
-        const float F1 = __shfl_sync(0xffffffffu, F, (2 * t + 1) * 4);
-        f[nt] = make_float4(F0, F0 * acc1[0], F1, F1 * acc1[1]);
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) atomicInc(a.flag + clu, (unsigned)(S - 1));
     }
-#pragma unroll
-    for (int i = kEarly; i < kDepth; ++i) issue(i, i);
-    // this thread's scale copies (the oldest group) have landed; after the
-    // barrier every thread's have, and the zeroed partials are visible
-    cp_async_wait<kDepth>();
+    // private partials: a warp's first segment (when it spans the range) stores
+    // every tile, later ones add; with no such segment, or with shared atomics,
+    // start from zeros
+    const int part_n = M <= kPrivateMaxM ? kWarps * rmax * 16 * M : rmax * 16 * MP;
+    if (M > kPrivateMaxM || na == 0)
+        for (int i = threadIdx.x; i < part_n; i += kThreads) part[i] = 0.0f;
+    cp_async_wait<0>();
     __syncthreads();
 
-    const unsigned short* sc_w = scs + warp;   // row r of the range: sc_w[8 r]
-    auto epilogue = [&](int i, const float (&acc)[MT][4]) {
-        const float s0 = __half2float(__ushort_as_half(sc_w[(i * 16 + gid) * 8]));
-        const float s1 = __half2float(__ushort_as_half(sc_w[(i * 16 + gid + 8) * 8]));
+    // ---- stage one group's activation: lane (gid, t) holds token nt*8+gid,
+    // k = 32t .. 32t+31 of the group ----
+    const XT* xsrc = a.xpitch ? reinterpret_cast<const XT*>(smem + a.off_x) : reinterpret_cast<const XT*>(a.x);
+    const size_t xrow = a.xpitch ? (size_t)a.xpitch : (size_t)a.K;
+    const int xg0 = a.xpitch ? gA : 0;
+    uint32_t b[MT][16];
+    float4 f[MT];   // (F, F*acc1) of tokens 2t and 2t+1 of each token tile
+    auto stage = [&](int g) {
+#pragma unroll
+        for (int nt = 0; nt < MT; ++nt) {
+            const int m = nt * 8 + gid;
+            float v[32];
+            if (m < M) {
+                const XT* src = xsrc + (size_t)m * xrow + (size_t)(g - xg0) * kGroup + 32 * t;
+                if (XF32) {
+                    const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 u = s4[q];
+                        v[4 * q] = u.x;
+                        v[4 * q + 1] = u.y;
+                        v[4 * q + 2] = u.z;
+                        v[4 * q + 3] = u.w;
+                    }
+                } else {
+                    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 u = s4[q];
+                        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            v[8 * q + 2 * e] = __uint_as_float(uw[e] << 16);
+                            v[8 * q + 2 * e + 1] = __uint_as_float(uw[e] & 0xFFFF0000u);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+            }
+            float mx = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(v[e]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            // E with mx * 2^(E + 10) < 2^15: mx < 2^ex for ex = biased exponent - 126
+            const int be = (int)(__float_as_uint(mx) >> 23);   // mx >= 0
+            int E = 0;
+            if (mx > 0.0f && be < 255) E = max(-100, min(5 - (max(be, 1) - 126), 110));
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                // exact power of two 2^(E + 10 - 2j'), exponent within [-100, 120]
+                const float c = __uint_as_float((uint32_t)(E + 10 - 2 * (j < 6 ? j : j - 6) + 127) << 23);
+                const __half2 lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);       // k = 32t+j, +8
+                const __half2 hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c); // k = 32t+16+j, +24
+                b[nt][2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
+                b[nt][2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
+            // the -1 correction: the same chain on the all-ones pattern; every row of
+            // the result is the same, lane (gid, t) holds tokens 2t, 2t+1
+            float acc1[4];
+            const uint32_t ones[4] = {0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u};
+            mma_chain1(acc1, ones, b[nt]);
+            const float F = (m < M) ? __uint_as_float((uint32_t)(14 - E + 127) << 23) : 0.0f;   // 2^(14-E)
+            const float F0 = __shfl_sync(0xffffffffu, F, (2 * t) * 4);
+            const float F1 = __shfl_sync(0xffffffffu, F, (2 * t + 1) * 4);
+            f[nt] = make_float4(F0, F0 * acc1[0], F1, F1 * acc1[1]);
+        }
+    };
+
+    // ---- one unit's rows into the partials: sp = this lane's scale of row gid,
+    // pw = the unit's private partial rows (M <= 4) ----
+    auto epilogue = [&](auto add_c, const unsigned short* sp, float* pw, int i, const float (&acc)[MT][4]) {
+        constexpr bool ADD = decltype(add_c)::value;
+        const float s0 = __half2float(__ushort_as_half(sp[0]));
+        const float s1 = __half2float(__ushort_as_half(sp[8 * gpad]));
+        if (ONE) {
+            // token 0 sits in lanes t == 0, element 0 (row gid) and 2 (row gid + 8)
+            const float v0 = s0 * fmaf(f[0].x, acc[0][0], -f[0].y);
+            const float v2 = s1 * fmaf(f[0].x, acc[0][2], -f[0].y);
+            if (t == 0) {
+                pw[gid] = ADD ? pw[gid] + v0 : v0;
+                pw[gid + 8] = ADD ? pw[gid + 8] + v2 : v2;
+            }
+            return;
+        }
 #pragma unroll
         for (int nt = 0; nt < MT; ++nt) {
             const int m0 = nt * 8 + 2 * t, m1 = m0 + 1;
@@ -316,15 +427,14 @@ gemv_kernel(const GemvArgs a) {
             const float v2 = s1 * fmaf(f[nt].x, acc[nt][2], -f[nt].y);   // row gid + 8, token m0
             const float v3 = s1 * fmaf(f[nt].z, acc[nt][3], -f[nt].w);   // row gid + 8, token m1
             if (M <= kPrivateMaxM) {
-                // [warp][tile][row][M]: each element written once, by its warp
-                float* pw = part + (((size_t)warp * rmax + i) * 16) * M;
+                // [warp][tile][row][M], written only by its warp
                 if (m0 < M) {
-                    pw[gid * M + m0] = v0;
-                    pw[(gid + 8) * M + m0] = v2;
+                    pw[gid * M + m0] = ADD ? pw[gid * M + m0] + v0 : v0;
+                    pw[(gid + 8) * M + m0] = ADD ? pw[(gid + 8) * M + m0] + v2 : v2;
                 }
                 if (m1 < M) {
-                    pw[gid * M + m1] = v1;
-                    pw[(gid + 8) * M + m1] = v3;
+                    pw[gid * M + m1] = ADD ? pw[gid * M + m1] + v1 : v1;
+                    pw[(gid + 8) * M + m1] = ADD ? pw[(gid + 8) * M + m1] + v3 : v3;
                 }
             } else {
                 float* row = part + (size_t)i * 16 * MP;   // [tile][row][MP], shared by the warps
@@ -340,82 +450,105 @@ gemv_kernel(const GemvArgs a) {
         }
     };
 
-    if (active) {
-        int slot = 0;   // ring slot of tile i (kDepth is even: tile i + 1 sits in slot + 1)
-        for (int i = 0; i < R; i += 2) {
-            const bool two = i + 1 < R;
-            // tiles i and i + 1 have landed (at most kDepth - 2 newer groups pending)
+    // ---- the segments ----
+    int slot = 0;   // ring slot of the next unit to consume
+    const unsigned char* rd = ring + gid * 32 + 8 * t;   // this lane's words within a slot
+    const int sstep = 16 * gpad;                          // scale halves per tile
+    const int pstep = 16 * M;                             // private partial floats per tile
+    auto run_segment = [&](auto add_c, int lo, int hi, int g) {
+        const unsigned short* sp = sc + (lo * 16 + gid) * gpad + (g - g_lo);
+        float* pw = part + ((size_t)warp * rmax + lo) * pstep;
+        for (int i = lo; i < hi; i += 2) {
+            const bool two = i + 1 < hi;
+            const int slot1 = slot + 1 == kDepth ? 0 : slot + 1;
+            // units i and i + 1 have landed (at most kDepth - 2 newer groups pending)
             cp_async_wait<kDepth - 2>();
             __syncwarp();
             uint32_t w[2][4];
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                const unsigned char* sp = ring + (slot + q) * kSlotBytes;
-                const uint2 v0 = *reinterpret_cast<const uint2*>(sp + gid * 32 + 8 * t);
-                const uint2 v1 = *reinterpret_cast<const uint2*>(sp + (gid + 8) * 32 + 8 * t);
+                const unsigned char* sp8 = rd + (q ? slot1 : slot) * kSlotBytes;
+                const uint2 v0 = *reinterpret_cast<const uint2*>(sp8);
+                const uint2 v1 = *reinterpret_cast<const uint2*>(sp8 + 8 * 32);
                 w[q][0] = v0.x;   // row gid,     word 2t      (MMA rows 0-7,  k-slots 2t, 2t+1)
                 w[q][1] = v1.x;   // row gid + 8, word 2t      (MMA rows 8-15)
                 w[q][2] = v0.y;   // row gid,     word 2t + 1  (k-slots 2t+8, 2t+9)
                 w[q][3] = v1.y;   // row gid + 8, word 2t + 1
             }
             float acc[2][MT][4];
-            pair_mmas<MT>(acc, w, b);
-            // both slots fully read by every lane: refill them kDepth tiles ahead
+            if (two) {
+                pair_mmas<MT>(acc, w, b);
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < MT; ++nt) mma_chain1(acc[0][nt], w[0], b[nt]);
+            }
+            // the consumed slots are fully read by every lane: refill them kDepth units ahead
             __syncwarp();
-            issue(i + kDepth, slot);
-            issue(i + 1 + kDepth, slot + 1);
-            epilogue(i, acc[0]);
-            if (two) epilogue(i + 1, acc[1]);
-            slot = slot + 2 == kDepth ? 0 : slot + 2;
+            issue(slot);
+            if (two) issue(slot1);
+            epilogue(add_c, sp, pw, i, acc[0]);
+            if (two) epilogue(add_c, sp + sstep, pw + pstep, i + 1, acc[1]);
+            sp += 2 * sstep;
+            pw += 2 * pstep;
+            slot = two ? (slot1 + 1 == kDepth ? 0 : slot1 + 1) : slot1;
         }
+    };
+    for (int s = 0; s < nseg; ++s) {
+        const int lo = seg_lo(s), hi = seg_hi(s);
+        if (lo >= hi) continue;
+        const int g = seg_group(s);
+        stage(g);
+        if (s > 0 && na > 0) run_segment(std::true_type{}, lo, hi, g);
+        else run_segment(std::false_type{}, lo, hi, g);
     }
     cp_async_wait<0>();
     __syncthreads();
 
-    // ---- reduce the warps' partials into rows ----
-    const int nvals = R * 16 * M;
+    // ---- the CTA's row sums ----
+    const int nv = R * 16 * M;
     auto row_value = [&](int tl, int r, int m) -> float {
         if (M <= kPrivateMaxM) {
             float s = 0.0f;
-            for (int w2 = 0; w2 < gs; ++w2) s += part[(((size_t)w2 * rmax + tl) * 16 + r) * M + m];
+            for (int w2 = 0; w2 < kWarps; ++w2) s += part[(((size_t)w2 * rmax + tl) * 16 + r) * M + m];
             return s;
         }
         return part[((size_t)tl * 16 + r) * MP + m];
     };
     if (S == 1) {
-        for (int i = threadIdx.x; i < nvals; i += kThreads) {
+        for (int i = threadIdx.x; i < nv; i += kThreads) {
             const int m = i / (R * 16), rr = i - m * (R * 16);
             const int r = tile_lo * 16 + rr;
             if (r < N) a.y[(size_t)m * N + r] = row_value(rr >> 4, rr & 15, m);
         }
         return;
     }
-    float* P = a.partial + ((size_t)sigma * T + tile_lo) * 16 * M;
-    for (int i = threadIdx.x; i < nvals; i += kThreads) {
-        const int tl = i / (16 * M), rem = i - tl * 16 * M;
-        const int m = rem / 16, r = rem - m * 16;
-        P[i] = row_value(tl, r, m);   // [tile][m][16]
+    // ---- several slices: add the CTA's row sums into y.  A slice other than 0
+    // first waits (bounded) until the slice-0 CTA has cleared the rows -- it
+    // did so right after the PDL wait, so by now the count is normally there --
+    // and counts itself; the S-th count returns the flag to 0. ----
+    __shared__ int go;
+    if (sigma != 0) {
+        if (threadIdx.x == 0) {
+            bool ok = ld_acquire(a.flag + clu) != 0u;
+            if (!ok) {
+                const uint64_t t0 = now_ns();
+                for (uint32_t it = 1; !ok; ++it) {
+                    ok = ld_acquire(a.flag + clu) != 0u;
+                    if (!ok && (it & 63u) == 0 && now_ns() - t0 > kFlagWaitNs) break;
+                }
+            }
+            if (ok) atomicInc(a.flag + clu, (unsigned)(S - 1));
+            else report_device_error(&g_gemv_error, kDevErrGemvConsumerWait);
+            go = ok;
+        }
+        __syncthreads();
+        if (!go) return;   // reported: y is left incomplete rather than wrong-ordered
     }
-    __threadfence();
-    __syncthreads();
-    for (int i = threadIdx.x; i < R; i += kThreads)
-        fin[i] = (atomicAdd(a.counter + tile_lo + i, 1u) == (unsigned)(S - 1));
-    __syncthreads();
-    __threadfence();
-    for (int i = threadIdx.x; i < nvals; i += kThreads) {
-        const int tl = i / (16 * M);
-        if (!fin[tl]) continue;
-        const int rem = i - tl * 16 * M;
-        const int m = rem / 16, r = rem - m * 16;
-        const int tile_g = tile_lo + tl;
-        const size_t off = (size_t)tile_g * 16 * M + rem;
-        float sum = 0.0f;
-        for (int sg = 0; sg < S; ++sg) sum += __ldcg(a.partial + (size_t)sg * T * 16 * M + off);
-        const int row = tile_g * 16 + r;
-        if (row < N) a.y[(size_t)m * N + row] = sum;
+    for (int i = threadIdx.x; i < nv; i += kThreads) {
+        const int m = i / (R * 16), rr = i - m * (R * 16);
+        const int r = tile_lo * 16 + rr;
+        if (r < N) atomicAdd(a.y + (size_t)m * N + r, row_value(rr >> 4, rr & 15, m));
     }
-    for (int i = threadIdx.x; i < R; i += kThreads)
-        if (fin[i]) a.counter[tile_lo + i] = 0u;
 }
 
 // Rotation prologue for the fused path: xr (fp32 [M][K]) = H_4096 (s (.) x) / 64,
@@ -440,39 +573,118 @@ rotate_f32_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restrict_
 // Host side.
 // ---------------------------------------------------------------------------
 struct Plan {
-    int G, T, S, cps, ctas, rmax, MT;
+    int G, T, S, cps, ctas, rmax, MT, gpad, xpitch;
+    uint32_t off_sc, off_x, off_part;
     size_t smem;
-    size_t off_xr, off_partial, off_counter, bytes;
 };
 
-Plan make_plan(int M, int N, int K, bool rot, int sms) {
+// Shared-memory layout for `cps` ranges (ring | scales | x slice | partials).
+void layout(Plan& p, int M, int cps, size_t xsize) {
+    p.cps = cps;
+    p.rmax = (p.T + cps - 1) / cps;
+    const int gsmax = (p.G + p.S - 1) / p.S;
+    p.xpitch = (size_t)M * gsmax * kGroup * xsize <= kXSmemMax ? gsmax * kGroup : 0;
+    const int MP = 8 * p.MT;
+    size_t off = (size_t)kWarps * kDepth * kSlotBytes;
+    p.off_sc = (uint32_t)off;
+    off = align_up(off + (size_t)p.rmax * 16 * p.gpad * 2, 16);
+    p.off_x = (uint32_t)off;
+    off = align_up(off + (p.xpitch ? (size_t)M * p.xpitch * xsize : 0), 16);
+    p.off_part = (uint32_t)off;
+    off += (M <= kPrivateMaxM ? (size_t)kWarps * p.rmax * 16 * M : (size_t)p.rmax * 16 * MP) * 4;
+    p.smem = off;
+}
+
+// The device-independent part of the plan: slices and the scale pitch.
+Plan base_plan(int M, int N, int K) {
     Plan p{};
     p.G = K / kGroup;
     p.T = (N + 15) / 16;
-    p.S = (p.G + kSliceGroups - 1) / kSliceGroups;
+    p.S = (p.G + kWarps - 1) / kWarps;
     p.MT = (M + 7) / 8;
-    // one wave: as many CTAs as fit on every SM at once, by registers (the
-    // launch bound) and by shared memory (which grows with the range length)
+    int w = 0;
+    for (int s = 0; s < p.S; ++s) {
+        const int gA = (int)((long long)p.G * s / p.S), gB = (int)((long long)p.G * (s + 1) / p.S);
+        w = std::max(w, scale_width(p.G, gA, gB));
+    }
+    p.gpad = (int)align_up((size_t)w, 8);   // row pitch a multiple of 16 bytes
+    return p;
+}
+
+// Lets the kernel use the device's whole per-block shared memory; returns the
+// dynamic part it may take.
+template <int MT, bool XF32, bool ONE>
+cudaError_t kernel_smem_limit(int dev, int* limit) {
+    static int optin_of[64] = {};
+    if (!optin_of[dev]) {
+        int optin = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, gemv_kernel<MT, XF32, ONE>);
+        if (e != cudaSuccess) return e;
+        optin -= (int)fa.sharedSizeBytes;   // the kernel's static shared memory comes first
+        e = cudaFuncSetAttribute(gemv_kernel<MT, XF32, ONE>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        if (e != cudaSuccess) return e;
+        optin_of[dev] = optin;
+    }
+    *limit = optin_of[dev];
+    return cudaSuccess;
+}
+
+// One wave: as many CTAs as fit at once, by registers (the launch bound) and
+// by shared memory (which grows with the range length).
+template <int MT, bool XF32, bool ONE>
+tern_status make_plan(int M, int N, int K, int sms, int dev, Plan* out) {
+    int limit = 0;
+    if (kernel_smem_limit<MT, XF32, ONE>(dev, &limit) != cudaSuccess) return TERN_ERR_CUDA;
+    Plan p = base_plan(M, N, K);
+    const size_t xs = XF32 ? 4 : 2;
     const int need = (p.T + kMaxTiles - 1) / kMaxTiles;   // ranges short enough for the shared partials
-    for (int per_sm = p.MT == 1 ? GemvCfg<1>::kCtasPerSm : GemvCfg<2>::kCtasPerSm; per_sm >= 1; --per_sm) {
-        const int cmax = sms * per_sm;
-        p.cps = p.S >= cmax ? 1 : cmax / p.S;
-        if (p.cps > p.T) p.cps = p.T;
-        if (p.cps < need) p.cps = need;
-        p.rmax = (p.T + p.cps - 1) / p.cps;
-        p.smem = smem_total(p.rmax, M, 8 * p.MT);
+    int cps = 1;
+    for (int per_sm = GemvCfg<MT>::kCtasPerSm; per_sm >= 1; --per_sm) {
+        cps = std::max(need, std::min(p.T, std::max(1, sms * per_sm / p.S)));
+        layout(p, M, cps, xs);
         if ((size_t)per_sm * (p.smem + kCtaSmemReserve) <= kSmemPerSm) break;
     }
+    // very long slices: shorter ranges (more than one wave) until a CTA fits
+    while (p.smem > (size_t)limit && p.rmax > 1) layout(p, M, (p.T + p.rmax - 2) / (p.rmax - 1), xs);
+    if (p.smem > (size_t)limit) return TERN_ERR_SHAPE;
     p.ctas = p.S * p.cps;
-    size_t off = 0;
-    p.off_xr = off;
-    if (rot) off = align_up(off + (size_t)M * K * 4, 256);
-    p.off_partial = off;
-    if (p.S > 1) off = align_up(off + (size_t)p.S * p.T * 16 * M * 4, 256);
-    p.off_counter = off;
-    if (p.S > 1) off = align_up(off + (size_t)p.T * 4, 256);
-    p.bytes = off > 0 ? off : 256;
-    return p;
+    *out = p;
+    return TERN_OK;
+}
+
+// Plans depend on the shape and the device only: keep the recent ones.
+struct PlanKey {
+    int M, N, K, dev;
+    bool xf32;
+};
+std::mutex g_plan_mu;
+constexpr int kPlanCache = 64;
+PlanKey g_plan_key[kPlanCache];
+Plan g_plan_val[kPlanCache];
+int g_plan_n = 0, g_plan_next = 0;
+
+template <int MT, bool XF32, bool ONE>
+tern_status cached_plan(int M, int N, int K, int sms, Plan* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TERN_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return TERN_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    for (int i = 0; i < g_plan_n; ++i) {
+        const PlanKey& k = g_plan_key[i];
+        if (k.M == M && k.N == N && k.K == K && k.dev == dev && k.xf32 == XF32) {
+            *out = g_plan_val[i];
+            return TERN_OK;
+        }
+    }
+    const tern_status st = make_plan<MT, XF32, ONE>(M, N, K, sms, dev, out);
+    if (st != TERN_OK) return st;
+    const int slot = g_plan_n < kPlanCache ? g_plan_n++ : (g_plan_next++ % kPlanCache);
+    g_plan_key[slot] = PlanKey{M, N, K, dev, XF32};
+    g_plan_val[slot] = *out;
+    return TERN_OK;
 }
 
 tern_status validate(const void* x, const uint32_t* codes, const void* scales, const float* y, int M, int N, int K) {
@@ -484,25 +696,36 @@ tern_status validate(const void* x, const uint32_t* codes, const void* scales, c
     return TERN_OK;
 }
 
+// Workspace: [range flag words, when K spans several slices | fp32 rotated x,
+// for the rotation-fused call].  The flags count back to 0 at the end of every
+// call, so a zero-filled workspace stays ready for the next one.
+size_t flag_bytes(int N, int K) {
+    const int G = K / kGroup;
+    return G > kWarps ? align_up((size_t)((N + 15) / 16) * 4, 256) : 0;
+}
 size_t workspace_bytes(int M, int N, int K, bool rot) {
     if (M < 1 || M > 16 || N < 1 || K < kGroup || K % kGroup != 0) return 0;
-    // partials and counters depend on (S, T) only, never on the device
-    return make_plan(M, N, K, rot, 1 << 20).bytes;
+    return flag_bytes(N, K) + (rot ? align_up((size_t)M * K * 4, 256) : 0);
 }
 
-template <int MT, bool XF32>
-cudaError_t launch_gemv(const GemvArgs& args, const Plan& p, cudaStream_t stream) {
-    static int attr_bytes[64] = {};   // the attribute is per function and device
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (attr_bytes[dev] < (int)p.smem) {
-        e = cudaFuncSetAttribute(gemv_kernel<MT, XF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-        if (e != cudaSuccess) return e;
-        attr_bytes[dev] = (int)p.smem;
-    }
-    return launch_pdl(gemv_kernel<MT, XF32>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, args);
+template <int MT, bool XF32, bool ONE>
+tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
+    Plan p;
+    const tern_status st = cached_plan<MT, XF32, ONE>(args.M, args.N, args.K, sms, &p);
+    if (st != TERN_OK) return st;
+    args.G = p.G;
+    args.T = p.T;
+    args.S = p.S;
+    args.cps = p.cps;
+    args.rmax = p.rmax;
+    args.gpad = p.gpad;
+    args.xpitch = p.xpitch;
+    args.off_sc = p.off_sc;
+    args.off_x = p.off_x;
+    args.off_part = p.off_part;
+    const cudaError_t e =
+        launch_pdl(gemv_kernel<MT, XF32, ONE>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, args);
+    return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
 
 tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const void* scales, float* y, int M,
@@ -510,51 +733,56 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
     int sms = 0;
     tern_status st = check_device(&sms);
     if (st != TERN_OK) return st;
-    const Plan p = make_plan(M, N, K, signs != nullptr, sms);
-    if (p.bytes > 256 || signs) {
-        if (!workspace || workspace_bytes_ < p.bytes) return TERN_ERR_WORKSPACE;
+    const size_t fb = flag_bytes(N, K);
+    if (fb > 0 || signs) {
+        if (!workspace || workspace_bytes_ < workspace_bytes(M, N, K, signs != nullptr)) return TERN_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TERN_ERR_ALIGN;
     }
-    char* ws = reinterpret_cast<char*>(workspace);
-    GemvArgs args;
+    GemvArgs args{};
+    args.flag = fb > 0 ? reinterpret_cast<unsigned*>(workspace) : nullptr;
     args.x = x;
     args.codes = codes;
     args.scales = reinterpret_cast<const __half*>(scales);
     args.y = y;
-    args.partial = p.S > 1 ? reinterpret_cast<float*>(ws + p.off_partial) : nullptr;
-    args.counter = p.S > 1 ? reinterpret_cast<unsigned*>(ws + p.off_counter) : nullptr;
     args.M = M;
     args.N = N;
     args.K = K;
-    args.G = p.G;
-    args.T = p.T;
-    args.S = p.S;
-    args.cps = p.cps;
-    args.rmax = p.rmax;
+    const int MT = (M + 7) / 8;
     int launches = 1;
-    cudaError_t e;
     if (signs) {
-        float* xr = reinterpret_cast<float*>(ws + p.off_xr);
-        e = launch_pdl(rotate_f32_kernel, dim3(K / kFwhtN, M), dim3(kFwhtThreads), 0, stream, true,
-                       reinterpret_cast<const __nv_bfloat16*>(x), signs, xr, K);
+        float* xr = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + fb);
+        const cudaError_t e = launch_pdl(rotate_f32_kernel, dim3(K / kFwhtN, M), dim3(kFwhtThreads), 0, stream,
+                                         true, reinterpret_cast<const __nv_bfloat16*>(x), signs, xr, K);
         if (e != cudaSuccess) return TERN_ERR_CUDA;
         args.x = xr;
         launches = 2;
-        e = p.MT == 1 ? launch_gemv<1, true>(args, p, stream) : launch_gemv<2, true>(args, p, stream);
+        st = M == 1 ? launch_gemv<1, true, true>(args, sms, stream)
+             : MT == 1 ? launch_gemv<1, true, false>(args, sms, stream)
+                       : launch_gemv<2, true, false>(args, sms, stream);
     } else {
-        e = p.MT == 1 ? launch_gemv<1, false>(args, p, stream) : launch_gemv<2, false>(args, p, stream);
+        st = M == 1 ? launch_gemv<1, false, true>(args, sms, stream)
+             : MT == 1 ? launch_gemv<1, false, false>(args, sms, stream)
+                       : launch_gemv<2, false, false>(args, sms, stream);
     }
-    if (e != cudaSuccess) return TERN_ERR_CUDA;
+    if (st != TERN_OK) return st;
     set_launch_count(launches);
     return TERN_OK;
 }
 
 }  // namespace
 
-// The decode product's kernels wait on nothing outside their own CTA, so they
-// never raise a device error word; the reader reports a clean state.
+// Reads and clears the decode product's device error word (set when a slice's
+// bounded wait for its range's clearing gave up).
 cudaError_t read_gemv_device_error(int* code) {
-    *code = 0;
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemv_error, sizeof(int));
+    if (e != cudaSuccess) return e;
+    if (v != 0) {
+        const int z = 0;
+        e = cudaMemcpyToSymbol(g_gemv_error, &z, sizeof(int));
+        if (e != cudaSuccess) return e;
+    }
+    *code = v;
     return cudaSuccess;
 }
 
@@ -564,7 +792,8 @@ using namespace tern;
 
 extern "C" size_t tern_gemv_workspace_bytes(int M, int N, int K) {
     // covers both the plain and the rotation-fused call of the same shape
-    return workspace_bytes(M, N, K, (K % kFwhtN) == 0);
+    const size_t b = workspace_bytes(M, N, K, (K % kFwhtN) == 0);
+    return b > 0 ? b : (M >= 1 && M <= 16 && N >= 1 && K >= kGroup && K % kGroup == 0 ? 256 : 0);
 }
 
 extern "C" tern_status tern_gemv(const void* x, const uint32_t* codes, const void* scales, float* y, int M,
@@ -573,7 +802,7 @@ extern "C" tern_status tern_gemv(const void* x, const uint32_t* codes, const voi
     const tern_status v = validate(x, codes, scales, y, M, N, K);
     if (v != TERN_OK) return v;
     const size_t need = workspace_bytes(M, N, K, false);
-    if (need > 256 && (!workspace || workspace_bytes_ < need)) return TERN_ERR_WORKSPACE;
+    if (need > 0 && (!workspace || workspace_bytes_ < need)) return TERN_ERR_WORKSPACE;
     return run(x, nullptr, codes, scales, y, M, N, K, workspace, workspace_bytes_, (cudaStream_t)stream);
 }
 
@@ -596,13 +825,10 @@ extern "C" tern_status tern_fwht_gemm(const void* x, const int8_t* signs, const 
 // Some callers cannot allocate device memory for a workspace: code that runs
 // where an allocation may not happen (inside a custom allocator's own callback,
 // a caching allocator that must not recurse, an embedded runtime that owns all
-// device memory up front).  For them the product's scratch -- the per-slice
-// partial row sums and the per-tile arrival counters -- lives in one fixed
-// array in the library's own device memory.  Every GPU that loads the library
-// holds this array (TERN_NOALLOC_SCRATCH_BYTES) until the process exits.
+// device memory up front).  For them the product's only scratch -- the range
+// flag words -- lives in one fixed array in the library's own device memory,
+// which every GPU that loads the library holds until the process exits.
 // ---------------------------------------------------------------------------
-#include <mutex>
-
 namespace tern {
 namespace {
 
@@ -639,18 +865,15 @@ extern "C" tern_status tern_gemv_noalloc(const void* x, const uint32_t* codes, c
     set_launch_count(0);
     const tern_status v = validate(x, codes, scales, y, M, N, K);
     if (v != TERN_OK) return v;
-    if (tern::workspace_bytes(M, N, K, false) > kNoAllocScratchBytes) return TERN_ERR_WORKSPACE;
+    const size_t need = tern::workspace_bytes(M, N, K, false);
+    if (need > kNoAllocScratchBytes) return TERN_ERR_WORKSPACE;
     int sms = 0;
     tern_status st = check_device(&sms);
     if (st != TERN_OK) return st;
     void* scratch = nullptr;
     if (noalloc_scratch(&scratch) != cudaSuccess) return TERN_ERR_CUDA;
-    // the array keeps the previous call's contents: the arrival counters must
-    // start at zero, so clear them on the stream first (no allocation involved)
-    const Plan p = make_plan(M, N, K, false, sms);
-    if (p.S > 1 &&
-        cudaMemsetAsync(static_cast<char*>(scratch) + p.off_counter, 0, (size_t)p.T * 4, (cudaStream_t)stream) !=
-            cudaSuccess)
-        return TERN_ERR_CUDA;
+    // the flags count back to 0 at the end of every call; clearing them first
+    // keeps a call correct even after an earlier one stopped on a device error
+    if (need > 0 && cudaMemsetAsync(scratch, 0, need, (cudaStream_t)stream) != cudaSuccess) return TERN_ERR_CUDA;
     return run(x, nullptr, codes, scales, y, M, N, K, scratch, kNoAllocScratchBytes, (cudaStream_t)stream);
 }

@@ -109,43 +109,50 @@ tern_status tern_validate_host(const uint32_t *codes, int N, int K, long long *b
 /* ---------------------------------------------------------------------- */
 
 /* Workspace bytes tern_gemv and tern_fwht_gemm need for (M, N, K); 0 on bad
- * input.  The size covers both calls.  It holds the per-K-slice partial row
- * sums and one arrival counter per 16-row tile (and, for tern_fwht_gemm, the
- * fp32 rotated activation). */
+ * input.  The size covers both calls (at least 256).  It holds one 32-bit flag
+ * word per 16-row tile when K > 1024 (the K-slice sums of a row range are
+ * added into y, and the flag orders the range's clearing before the additions)
+ * and, for tern_fwht_gemm, the fp32 rotated activation (M * K * 4 bytes).
+ * The workspace must be zero-filled once before its first use; every call
+ * leaves its flags at zero again.  Calls that share a workspace must not run
+ * concurrently (use one stream, or one workspace per stream).  After a device
+ * error (tern_device_error) zero-fill it again. */
 size_t tern_gemv_workspace_bytes(int M, int N, int K);
 
 /* y (fp32 [M][N]) = x W^T with W given by (codes, scales).
  * 1 <= M <= 16, N >= 1, K >= 128 with K % 128 == 0.  One kernel launch.
- * For K <= 1024 the workspace may be NULL.  y is written once per element
- * (no pre-zeroing needed).  Results agree with the exact product to within
- * 1e-3 * sum_k |x w| + 1e-6 per element, and a row of zero weights gives
- * exactly 0.  The fp32 sums within a K-slice are combined with shared-memory
- * atomics, so the last bits may vary from run to run.  |x| must stay below
- * 2^100 (larger values overflow the fp16 staging). */
+ * For K <= 1024 the workspace may be NULL.  No pre-zeroing of y is needed (the
+ * kernel clears what it adds into).
+ * Results agree with the exact product to within 1e-3 * sum_k |x w| + 1e-6 per
+ * element, and a row of zero weights gives exactly 0.  When K spans more than
+ * 8 groups (K > 1024) the K-slice sums are added into y with global float
+ * reductions, and for M > 4 the group sums within a slice meet in shared-memory
+ * atomics; in either case the last bits of y may vary from run to run.
+ * |x| must stay below 2^100 (larger values overflow the fp16 staging). */
 tern_status tern_gemv(const void *x, const uint32_t *codes, const void *scales, float *y,
                       int M, int N, int K, void *workspace, size_t workspace_bytes,
                       tern_stream_t stream);
 
 /* Fixed size of the library-owned scratch array behind tern_gemv_noalloc. */
-#define TERN_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define TERN_NOALLOC_SCRATCH_BYTES (256u << 10)
 
 /* The same product as tern_gemv, for callers that cannot allocate device
  * memory (code running inside an allocator's own callback, a caching
  * allocator that must not recurse into itself, a runtime that hands out all
  * device memory up front): it takes no workspace and allocates nothing.  The
  * pages describe no counterpart; this is a library convenience.
- *   - Its scratch (per-slice partial sums, per-tile arrival counters) is one
- *     file-scope device array of TERN_NOALLOC_SCRATCH_BYTES that every GPU
- *     loading the library holds until the process exits.
- *   - Shapes whose scratch, tern_gemv_workspace_bytes(M, N, K), exceeds that
- *     size are rejected with TERN_ERR_WORKSPACE and nothing is launched.
+ *   - Its scratch (the range flag words) is one file-scope device array of
+ *     TERN_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds
+ *     until the process exits.  Shapes whose scratch,
+ *     tern_gemv_workspace_bytes(M, N, K) without the rotation part, exceeds
+ *     it (N above 1,048,576 rows) are rejected with TERN_ERR_WORKSPACE and
+ *     nothing is launched.
  *   - The first call on a device looks up the array's device address (once,
- *     with that device current); make that first call before any stream
- *     capture.
- *   - Each call clears the arrival counters on `stream` before the product
+ *     with that device current) and plans the shape; make that first call
+ *     before any stream capture.
+ *   - Each call clears the flags it uses on `stream` before the product
  *     kernel.  All calls share the one array, so calls whose kernels overlap
- *     on the GPU (different streams, or devices sharing nothing else) race:
- *     order them.
+ *     on the GPU (different streams) race: order them.
  * Arguments, layout, results and tolerance as for tern_gemv. */
 tern_status tern_gemv_noalloc(const void *x, const uint32_t *codes, const void *scales, float *y,
                               int M, int N, int K, tern_stream_t stream);

@@ -110,19 +110,21 @@ def test_argument_errors_never_launch(tern):
     # alignment
     assert lib.tern_gemv(P + 2, P, P, P, 1, 16, 128, P, 1 << 20, None) == 3
     assert lib.tern_fwht(P, P + 8, P, 1, 4096, None) == 3
-    # workspace (needed once K spans more than one 1024-wide slice)
+    # workspace: flag words once K spans more than one 1024-wide slice, plus the
+    # rotated x for the fused call
     need = tern.gemv_workspace_bytes(1, 16, 2048)
-    assert need > 256
-    assert lib.tern_gemv(P, P, P, P, 1, 16, 2048, P, need - 1, None) == 4
+    assert need >= 256
     assert lib.tern_gemv(P, P, P, P, 1, 16, 2048, None, need, None) == 4
+    assert lib.tern_gemv(P, P, P, P, 1, 16, 2048, P, need - 1, None) == 4
     assert lib.tern_fwht_gemm(P, P, P, P, P, 1, 16, 4096, None, 1 << 30, None) == 4
+    assert lib.tern_fwht_gemm(P, P, P, P, P, 2, 16, 4096, P, 2 * 4096 * 4 - 1, None) == 4
     assert tern.gemv_workspace_bytes(17, 16, 128) == 0
 
-
 def test_workspace_sizes(tern):
-    # partial sums: slices of 8 groups x 16-row tiles x 16 rows x M fp32, then a
-    # uint32 counter per tile; the rotation-fused call adds M x K fp32
-    assert tern.gemv_workspace_bytes(1, 17408, 5120) == 5 * 1088 * 16 * 4 + 1088 * 4
-    assert tern.gemv_workspace_bytes(16, 10, 17408) == 17 * 1 * 16 * 16 * 4 + 256
-    assert tern.gemv_workspace_bytes(2, 12288, 4096) == 2 * 4096 * 4 + 4 * 768 * 16 * 2 * 4 + 768 * 4
+    # one flag word per 16-row tile once K > 1024 (256-byte aligned), then the
+    # fp32 rotated x for the fused call when K % 4096 == 0
+    assert tern.gemv_workspace_bytes(1, 17408, 5120) == (1088 * 4 + 255) // 256 * 256
+    assert tern.gemv_workspace_bytes(16, 10, 17408) == 256
+    assert tern.gemv_workspace_bytes(2, 12288, 4096) == 768 * 4 + 2 * 4096 * 4
+    assert tern.gemv_workspace_bytes(16, 12288, 8192) == 768 * 4 + 16 * 8192 * 4
     assert tern.gemv_workspace_bytes(1, 256, 512) == 256      # one slice: nothing needed

@@ -281,3 +281,16 @@ def test_fwht_gemm_full_size_sampled(tern, orc, M):
     rows = np.unique(rs.integers(0, N, 512))
     y_ref, a_ref = orc.rotate_matmul(p.x, p.signs, host_codes(codes)[rows], p.s[rows])
     assert_fp32_close(y.cpu().numpy()[:, rows], y_ref, a_ref, what=f"rot full M={M}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 300, 512), (1, 1000, 5120), (3, 777, 17408), (6, 129, 2176)])
+def test_gemv_overwrites_prefilled_y(tern, orc, M, N, K):
+    """y holding NaN before the call is fully overwritten, for one K-slice and
+    for several (whose sums are added into a y the kernel clears first)."""
+    p = synth.problem(900 + M, M, N, K, tag=f"nan{N}x{K}")
+    codes = tern.pack(dev_trits(p.t))
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    tern.gemv(dev_bf16(p.x), codes, dev_scales(p.s), y=y)
+    torch.cuda.synchronize()
+    y_ref, a_ref = orc.matmul(p.x, host_codes(codes), p.s)
+    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what=f"prefilled y M={M} N={N} K={K}")

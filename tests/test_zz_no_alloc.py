@@ -1,10 +1,11 @@
 """The decode product for callers that cannot allocate device memory.
 
-tern_gemv_noalloc takes no workspace: its scratch (the partial row sums of each
-K-slice and the arrival counters of each row tile) is a fixed array inside the
-library.  It exists for code that must not call cudaMalloc -- for instance code
-running inside an allocator's own callback, or under a runtime that owns all
-device memory -- and so cannot provide the workspace tern_gemv asks for.
+tern_gemv_noalloc takes no workspace: its scratch (one flag word per row range,
+ordering the range's clearing of y before the K-slice additions) is a fixed
+array inside the library.  It exists for code that must not call cudaMalloc --
+for instance code running inside an allocator's own callback, or under a
+runtime that owns all device memory -- and so cannot provide the workspace
+tern_gemv asks for.
 
 These checks call it through the C ABI and compare it with tern_gemv on the
 same inputs, twice in a row (the second call starts from whatever the first
@@ -21,8 +22,8 @@ import torch
 import synth
 from tests._util import assert_fp32_close, dev_bf16, dev_scales, dev_trits, host_codes
 
-TERN_ERR_WORKSPACE = 4
-NOALLOC_BYTES = 8 << 20
+TERN_ERR_NULL, TERN_ERR_SHAPE, TERN_ERR_ALIGN, TERN_ERR_WORKSPACE = 1, 2, 3, 4
+NOALLOC_BYTES = 256 << 10
 
 
 @pytest.fixture(scope="module")
@@ -41,9 +42,19 @@ def _call_noalloc(tern, x, codes, s, y):
     assert st == 0, f"tern_gemv_noalloc status {st}"
 
 
+def test_noalloc_validates_before_any_device_use(tern):
+    """Bad shapes, NULL and misaligned pointers are refused up front."""
+    P = 4096   # a fake aligned address: the checks come before any device use
+    lib = tern.lib()
+    assert lib.tern_gemv_noalloc(P, P, P, P, 17, 64, 128, None) == TERN_ERR_SHAPE
+    assert lib.tern_gemv_noalloc(P, P, P, P, 1, 64, 100, None) == TERN_ERR_SHAPE
+    assert lib.tern_gemv_noalloc(None, P, P, P, 1, 64, 128, None) == TERN_ERR_NULL
+    assert lib.tern_gemv_noalloc(P, P + 4, P, P, 1, 64, 128, None) == TERN_ERR_ALIGN
+
+
 def test_noalloc_rejects_oversized_shapes_without_launching(tern):
     """A shape whose scratch exceeds the fixed array is refused up front."""
-    M, N, K = 16, 17408, 17408
+    M, N, K = 1, 1100000, 2048
     assert tern.gemv_workspace_bytes(M, N, K) > NOALLOC_BYTES
     P = 4096   # a fake aligned address: the size check comes before any device use
     assert tern.lib().tern_gemv_noalloc(P, P, P, P, M, N, K, None) == TERN_ERR_WORKSPACE
@@ -55,7 +66,6 @@ def test_noalloc_rejects_oversized_shapes_without_launching(tern):
 def test_noalloc_matches_gemv_twice(tern, orc, M, N, K):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    assert tern.gemv_workspace_bytes(M, N, K) <= NOALLOC_BYTES
     p = synth.problem(500 + M, M, N, K, tag=f"na{N}x{K}")
     x, codes, s = dev_bf16(p.x), tern.pack(dev_trits(p.t)), dev_scales(p.s)
     y_ref_dev = tern.gemv(x, codes, s)
