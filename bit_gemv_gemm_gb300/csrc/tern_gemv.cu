@@ -39,9 +39,9 @@
 // a CTA the slice's groups are dealt to the 8 warps as segments: every warp
 // takes floor(Gs / 8) whole groups over the full range, and each of the Gs mod
 // 8 groups left over is cut into eight tile chunks, one per warp.  A warp
-// stages one segment's activation (from a copy of the slice's x in shared
-// memory) into registers and streams its own 32-byte column of every tile of
-// the segment (16 rows x 32 B = one 16-byte cp.async per lane) through a
+// stages one segment's activation into registers and streams its own
+// 32-byte column of every tile of the segment (16 rows x 32 B = one 16-byte
+// cp.async per lane) through a
 // private shared-memory ring, kDepth units ahead; the first kDepth units go out
 // before the programmatic-dependent-launch wait.  Two tiles per step run as two
 // independent MMA chains.  Row partials go to shared memory (private per warp
@@ -69,7 +69,6 @@ constexpr int kDepth = 6;              // units (tile x group) in flight per war
 constexpr int kSlotBytes = 16 * 32;    // one unit: 16 rows x 32 B of codes
 constexpr int kMaxTiles = 32;          // tiles per range (bounds partials and scales in shared memory)
 constexpr int kPrivateMaxM = 4;        // private per-warp partials up to this many tokens
-constexpr size_t kXSmemMax = 16384;    // the slice's activation is copied to shared memory up to this size
 constexpr size_t kSmemPerSm = 228 * 1024;   // shared memory of one SM
 constexpr size_t kCtaSmemReserve = 1024;    // taken by the system from each resident CTA
 
@@ -85,8 +84,7 @@ struct GemvArgs {
     unsigned* flag;             // [cps] per-range flag words (S > 1), 0 between calls
     int M, N, K, G, T, S, cps, rmax;
     int gpad;                   // scale row pitch in shared memory (halves)
-    int xpitch;                 // activation row pitch in shared memory (elements); 0: read x from global
-    uint32_t off_sc, off_x, off_part;   // shared-memory offsets (bytes)
+    uint32_t off_sc, off_part;  // shared-memory offsets (bytes)
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -298,18 +296,6 @@ gemv_kernel(const GemvArgs a) {
 #pragma unroll
     for (int i = 0; i < kDepth; ++i) issue(i);
     pdl_wait();
-    // the slice's activation (possibly the previous kernel's output) into shared memory
-    if (a.xpitch) {
-        const uint32_t xs_s = smem_addr(smem + a.off_x);
-        const int cpm = Gs * kGroup * (int)sizeof(XT) / 16;   // 16-byte chunks per token
-        const char* xg = reinterpret_cast<const char*>(a.x) + (size_t)gA * kGroup * sizeof(XT);
-        for (int i = threadIdx.x; i < M * cpm; i += kThreads) {
-            const int m = i / cpm, c = i - m * cpm;
-            cp_async16(xs_s + (uint32_t)(m * a.xpitch * (int)sizeof(XT) + 16 * c),
-                       xg + (size_t)m * a.K * sizeof(XT) + 16 * c, true);
-        }
-    }
-    cp_async_commit();
     // y of the range starts at zero: the slice-0 CTA clears it (after the PDL
     // wait, since the previous kernel may still read y) and counts itself into
     // the range's flag once the zeros are visible to the whole GPU
@@ -329,14 +315,11 @@ gemv_kernel(const GemvArgs a) {
     const int part_n = M <= kPrivateMaxM ? kWarps * rmax * 16 * M : rmax * 16 * MP;
     if (M > kPrivateMaxM || na == 0)
         for (int i = threadIdx.x; i < part_n; i += kThreads) part[i] = 0.0f;
-    cp_async_wait<0>();
-    __syncthreads();
 
-    // ---- stage one group's activation: lane (gid, t) holds token nt*8+gid,
+    // ---- stage one group's activation (read from global memory, possibly the
+    // previous kernel's output): lane (gid, t) holds token nt*8+gid,
     // k = 32t .. 32t+31 of the group ----
-    const XT* xsrc = a.xpitch ? reinterpret_cast<const XT*>(smem + a.off_x) : reinterpret_cast<const XT*>(a.x);
-    const size_t xrow = a.xpitch ? (size_t)a.xpitch : (size_t)a.K;
-    const int xg0 = a.xpitch ? gA : 0;
+    const XT* xsrc = reinterpret_cast<const XT*>(a.x);
     uint32_t b[MT][16];
     float4 f[MT];   // (F, F*acc1) of tokens 2t and 2t+1 of each token tile
     auto stage = [&](int g) {
@@ -345,7 +328,7 @@ gemv_kernel(const GemvArgs a) {
             const int m = nt * 8 + gid;
             float v[32];
             if (m < M) {
-                const XT* src = xsrc + (size_t)m * xrow + (size_t)(g - xg0) * kGroup + 32 * t;
+                const XT* src = xsrc + (size_t)m * a.K + (size_t)g * kGroup + 32 * t;
                 if (XF32) {
                     const float4* s4 = reinterpret_cast<const float4*>(src);
 #pragma unroll
@@ -493,6 +476,14 @@ gemv_kernel(const GemvArgs a) {
             slot = two ? (slot1 + 1 == kDepth ? 0 : slot1 + 1) : slot1;
         }
     };
+    // this thread's scale copies (the oldest group) have landed; after the
+    // barrier every thread's have, and the zeroed partials are visible
+    cp_async_wait<kDepth>();
+    __syncthreads();
+    // the range's flag, read now so the load overlaps the loop (a slice other
+    // than 0 needs it non-zero before adding into y)
+    unsigned flag_seen = 1u;
+    if (S > 1 && sigma != 0 && threadIdx.x == 0) flag_seen = ld_acquire(a.flag + clu);
     for (int s = 0; s < nseg; ++s) {
         const int lo = seg_lo(s), hi = seg_hi(s);
         if (lo >= hi) continue;
@@ -529,7 +520,7 @@ gemv_kernel(const GemvArgs a) {
     __shared__ int go;
     if (sigma != 0) {
         if (threadIdx.x == 0) {
-            bool ok = ld_acquire(a.flag + clu) != 0u;
+            bool ok = flag_seen != 0u || ld_acquire(a.flag + clu) != 0u;
             if (!ok) {
                 const uint64_t t0 = now_ns();
                 for (uint32_t it = 1; !ok; ++it) {
@@ -573,23 +564,19 @@ rotate_f32_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restrict_
 // Host side.
 // ---------------------------------------------------------------------------
 struct Plan {
-    int G, T, S, cps, ctas, rmax, MT, gpad, xpitch;
-    uint32_t off_sc, off_x, off_part;
+    int G, T, S, cps, ctas, rmax, MT, gpad;
+    uint32_t off_sc, off_part;
     size_t smem;
 };
 
-// Shared-memory layout for `cps` ranges (ring | scales | x slice | partials).
-void layout(Plan& p, int M, int cps, size_t xsize) {
+// Shared-memory layout for `cps` ranges (ring | scales | partials).
+void layout(Plan& p, int M, int cps) {
     p.cps = cps;
     p.rmax = (p.T + cps - 1) / cps;
-    const int gsmax = (p.G + p.S - 1) / p.S;
-    p.xpitch = (size_t)M * gsmax * kGroup * xsize <= kXSmemMax ? gsmax * kGroup : 0;
     const int MP = 8 * p.MT;
     size_t off = (size_t)kWarps * kDepth * kSlotBytes;
     p.off_sc = (uint32_t)off;
     off = align_up(off + (size_t)p.rmax * 16 * p.gpad * 2, 16);
-    p.off_x = (uint32_t)off;
-    off = align_up(off + (p.xpitch ? (size_t)M * p.xpitch * xsize : 0), 16);
     p.off_part = (uint32_t)off;
     off += (M <= kPrivateMaxM ? (size_t)kWarps * p.rmax * 16 * M : (size_t)p.rmax * 16 * MP) * 4;
     p.smem = off;
@@ -639,16 +626,15 @@ tern_status make_plan(int M, int N, int K, int sms, int dev, Plan* out) {
     int limit = 0;
     if (kernel_smem_limit<MT, XF32, ONE>(dev, &limit) != cudaSuccess) return TERN_ERR_CUDA;
     Plan p = base_plan(M, N, K);
-    const size_t xs = XF32 ? 4 : 2;
     const int need = (p.T + kMaxTiles - 1) / kMaxTiles;   // ranges short enough for the shared partials
     int cps = 1;
     for (int per_sm = GemvCfg<MT>::kCtasPerSm; per_sm >= 1; --per_sm) {
         cps = std::max(need, std::min(p.T, std::max(1, sms * per_sm / p.S)));
-        layout(p, M, cps, xs);
+        layout(p, M, cps);
         if ((size_t)per_sm * (p.smem + kCtaSmemReserve) <= kSmemPerSm) break;
     }
     // very long slices: shorter ranges (more than one wave) until a CTA fits
-    while (p.smem > (size_t)limit && p.rmax > 1) layout(p, M, (p.T + p.rmax - 2) / (p.rmax - 1), xs);
+    while (p.smem > (size_t)limit && p.rmax > 1) layout(p, M, (p.T + p.rmax - 2) / (p.rmax - 1));
     if (p.smem > (size_t)limit) return TERN_ERR_SHAPE;
     p.ctas = p.S * p.cps;
     *out = p;
@@ -719,9 +705,7 @@ tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
     args.cps = p.cps;
     args.rmax = p.rmax;
     args.gpad = p.gpad;
-    args.xpitch = p.xpitch;
     args.off_sc = p.off_sc;
-    args.off_x = p.off_x;
     args.off_part = p.off_part;
     const cudaError_t e =
         launch_pdl(gemv_kernel<MT, XF32, ONE>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, args);
