@@ -24,6 +24,16 @@
 //     accumulating fp32 in tensor memory;
 //   * four epilogue warps read the accumulator with tcgen05.ld and store y
 //     (fp32 or bf16) with coalesced stores along n.
+// Scheduling is stream-K: the (tile, 64-wide K stage) iterations, tile-major,
+// are cut into one equal contiguous share per CTA, so no SM idles behind a
+// partial last wave.  A CTA's share is a run of segments, each a stretch of
+// one tile's K stages; a CTA runs its (at most two) partial segments first and
+// its whole tiles after.  A segment that covers its whole tile is written to y
+// directly.  A partial one adds its fp32 accumulator into the tile's fp32 sum
+// in the workspace with vector reductions, fences and counts itself into the
+// tile's counter (one per epilogue warp's 32 rows); the CTA that counts last
+// reads the sum, writes y and clears the sum and the counter.  No CTA or warp
+// waits for another; the partial sums meet in no fixed order.
 // Stage hand-offs use mbarriers (TMA transaction counts, thread arrivals and
 // tcgen05.commit).  Every wait is bounded: after a second it raises a CTA abort
 // flag and the device error word, every role drains what it issued, tensor
@@ -60,12 +70,51 @@ constexpr size_t kSmemBar = kSmemC + (size_t)kStages * kCStageBytes;
 constexpr size_t kSmemMisc = kSmemBar + (size_t)(3 * kStages + 3) * 8;
 constexpr size_t kSmemBytes = kSmemMisc + 16 + 1024;   // + alignment slack
 
+constexpr int kMaxCtas = 160;                 // stream-K shares (the grid) at most
+constexpr int kTileFloats = kBM * kBN;         // one tile's fp32 sum: [256 tokens / 4][128 rows][4]
+
 struct GemmArgs {
     const __half* scales;
     void* y;
+    float* sums;                // [tiles][kTileFloats] fp32 sums of split tiles, 0 between calls
+    unsigned* counters;         // [tiles][4 lane quadrants], 0 between calls
+    int stream_k;               // 0: whole tiles blockIdx.x, + gridDim.x, ...; 1: stream-K shares
     int y_is_bf16;
     int M, N, K;
 };
+
+// The stream-K share of CTA c: iterations [T c / P, T (c + 1) / P).
+__host__ __device__ inline long long share_begin(long long T, int P, int c) { return T * c / P; }
+// The CTA whose share holds iteration g.
+__device__ inline int share_of(long long T, int P, long long g) {
+    int c = (int)((g * P) / T);
+    while (c + 1 < P && share_begin(T, P, c + 1) <= g) ++c;
+    while (c > 0 && share_begin(T, P, c) > g) --c;
+    return c;
+}
+// Segment s of the share [g0, g1): its tile and K stages [ks0, ks1).  The
+// share's first and last tiles (the partial ones) come first, then the whole
+// tiles between them in order.
+struct Segment {
+    int tile, ks0, ks1;
+};
+__device__ inline int segment_count(long long g0, long long g1, int KS) {
+    if (g1 <= g0) return 0;   // (whole-tile schedule: see the kernel)
+    const int t0 = (int)(g0 / KS), t1 = (int)((g1 - 1) / KS);
+    return t1 - t0 + 1;
+}
+__device__ inline Segment segment_at(long long g0, long long g1, int KS, int s) {
+    const int t0 = (int)(g0 / KS), t1 = (int)((g1 - 1) / KS);
+    const int first_lo = (int)(g0 - (long long)t0 * KS);
+    const int last_hi = (int)(g1 - (long long)t1 * KS);
+    if (s == 0) return Segment{t0, first_lo, t0 == t1 ? last_hi : KS};
+    if (s == 1) return Segment{t1, 0, last_hi};
+    return Segment{t0 + s - 1, 0, KS};   // s >= 2: whole tiles t0 + 1 .. t1 - 1
+}
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
 
 __device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
@@ -128,6 +177,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     const int m_tiles = (M + kBN - 1) / kBN;
     const int n_tiles = (N + kBM - 1) / kBM;
     const int total = m_tiles * n_tiles;
+    const long long TI = (long long)total * KS;   // stream-K iterations
+    const int P = gridDim.x;
+    const long long g0 = share_begin(TI, P, blockIdx.x), g1 = share_begin(TI, P, blockIdx.x + 1);
+    // whole-tile schedule: tiles blockIdx.x, blockIdx.x + P, ...; stream-K: the share's segments
+    const int nseg = a.stream_k ? segment_count(g0, g1, KS) : (total - (int)blockIdx.x + P - 1) / P;
+    auto segment = [&](int sg) -> Segment {
+        return a.stream_k ? segment_at(g0, g1, KS, sg) : Segment{(int)blockIdx.x + sg * P, 0, KS};
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -167,9 +224,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            for (int sg = 0; sg < nseg && ok; ++sg) {
+                const Segment seg = segment(sg);
+                const int tile = seg.tile, ks0 = seg.ks0, ks1 = seg.ks1;
                 const int nt = tile / m_tiles, mt = tile - nt * m_tiles;
-                for (int ks = 0; ks < KS; ++ks, ++it) {
+                for (int ks = ks0; ks < ks1; ++ks, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
                     if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -198,14 +257,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         if (lane == 0) {
             uint32_t it = 0, tc = 0;
             bool ok = true, issued = false;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tc) {
+            for (int sg = 0; sg < nseg && ok; ++sg, ++tc) {
+                const Segment seg = segment(sg);
+                const int ks0 = seg.ks0, ks1 = seg.ks1;
                 if (!mbar_wait_bounded(dempty_bar, (tc & 1u) ^ 1u, abort_flag, kWaitLimitNs)) {
                     fail(kDevErrGemmMmaWait);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                for (int ks = 0; ks < KS; ++ks, ++it) {
+                for (int ks = ks0; ks < ks1; ++ks, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
                     if (!mbar_wait_bounded(full_bar(s), ph, abort_flag, kWaitLimitNs) ||
@@ -220,7 +281,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         // A: 8 columns (16 bf16) per K=16 step; B: advance 32 bytes inside the swizzle atom
                         mma_f16_ts(tmem + kTmemD, tmem + kTmemA + 32u * s + 8u * kk, bdesc + (uint64_t)(2 * kk),
-                                   kIdesc, (ks | kk) != 0 ? 1u : 0u);
+                                   kIdesc, (ks != ks0 || kk != 0) ? 1u : 0u);
                     }
                     issued = true;
                     mma_commit(empty_bar(s));
@@ -238,8 +299,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // ------------------------------ epilogue ------------------------------
         const int q = warp & 3;
         const int rl = q * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + kTmemD;
         uint32_t tc = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tc) {
+        for (int sg = 0; sg < nseg; ++sg, ++tc) {
+            const Segment seg = segment(sg);
+            const int tile = seg.tile, ks0 = seg.ks0, ks1 = seg.ks1;
             const int nt = tile / m_tiles, mt = tile - nt * m_tiles;
             const int row = nt * kBM + rl;
             if (!mbar_wait_bounded(dfull_bar, tc & 1u, abort_flag, kWaitLimitNs)) {
@@ -247,30 +311,79 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 break;
             }
             tc_fence_after();
+            auto put = [&](int m, float v) {
+                if (a.y_is_bf16)
+                    reinterpret_cast<__nv_bfloat16*>(a.y)[(size_t)m * N + row] = __float2bfloat16_rn(v);
+                else
+                    reinterpret_cast<float*>(a.y)[(size_t)m * N + row] = v;
+            };
+            if (ks0 == 0 && ks1 == KS) {
+                // the whole tile: straight to y
+                for (int c = 0; c < kBN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_x32(trow + 32u * c, v);
+                    tmem_ld_wait();
+                    if (c == kBN / 32 - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(dempty_bar);
+                    }
+                    if (row < N) {
+                        const int m0 = mt * kBN + 32 * c;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (m0 + i < M) put(m0 + i, __uint_as_float(v[i]));
+                    }
+                }
+                continue;
+            }
+            // part of the tile: add the accumulator into the tile's fp32 sum (laid out
+            // [token / 4][row][4], so a warp's lanes cover 512 contiguous bytes)
+            float* sum = a.sums + (size_t)tile * kTileFloats;
             for (int c = 0; c < kBN / 32; ++c) {
                 uint32_t v[32];
-                tmem_ld_x32(tmem + ((uint32_t)(q * 32) << 16) + kTmemD + 32u * c, v);
+                tmem_ld_x32(trow + 32u * c, v);
                 tmem_ld_wait();
                 if (c == kBN / 32 - 1) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(dempty_bar);
                 }
-                if (row < N) {
-                    const int m0 = mt * kBN + 32 * c;
-                    if (a.y_is_bf16) {
-                        __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(a.y);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (m0 + i < M) y[(size_t)(m0 + i) * N + row] = __float2bfloat16_rn(__uint_as_float(v[i]));
-                    } else {
-                        float* y = reinterpret_cast<float*>(a.y);
+                for (int i = 0; i < 8; ++i)
+                    red_add_v4(sum + ((size_t)(8 * c + i) * kBM + rl) * 4, __uint_as_float(v[4 * i]),
+                               __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                               __uint_as_float(v[4 * i + 3]));
+            }
+            // each warp counts its own 32 rows (one counter per tile and lane
+            // quadrant), so the four warps never wait for one another
+            __threadfence();
+            __syncwarp();
+            const int c_lo = share_of(TI, P, (long long)tile * KS), c_hi = share_of(TI, P, (long long)tile * KS + KS - 1);
+            unsigned last = 0;
+            if (lane == 0) last = atomicAdd(a.counters + 4 * tile + q, 1u) == (unsigned)(c_hi - c_lo);
+            if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+            // the last of the tile's CTAs for these rows: the sum is complete
+            __threadfence();
+            for (int c = 0; c < kBN / 64; ++c) {
+                float4 t[16];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (m0 + i < M) y[(size_t)(m0 + i) * N + row] = __uint_as_float(v[i]);
+                for (int i = 0; i < 16; ++i)
+                    t[i] = __ldcg(reinterpret_cast<const float4*>(sum + ((size_t)(16 * c + i) * kBM + rl) * 4));
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    __stcg(reinterpret_cast<float4*>(sum + ((size_t)(16 * c + i) * kBM + rl) * 4),
+                           make_float4(0.0f, 0.0f, 0.0f, 0.0f));
+                    const int m0 = mt * kBN + 64 * c + 4 * i;
+                    if (row < N) {
+                        if (m0 < M) put(m0, t[i].x);
+                        if (m0 + 1 < M) put(m0 + 1, t[i].y);
+                        if (m0 + 2 < M) put(m0 + 2, t[i].z);
+                        if (m0 + 3 < M) put(m0 + 3, t[i].w);
                     }
                 }
             }
+            if (lane == 0) a.counters[4 * tile + q] = 0u;
         }
     } else {
         // ------------------------------ unpack ------------------------------
@@ -280,14 +393,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + kTmemA + 16u * h;
         uint32_t it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        for (int sg = 0; sg < nseg && ok; ++sg) {
+            const Segment seg = segment(sg);
+            const int tile = seg.tile, ks0 = seg.ks0, ks1 = seg.ks1;
             const int nt = tile / m_tiles;
             const int row = nt * kBM + rl;
             const __half* srow = a.scales + (size_t)(row < N ? row : 0) * G;
             uint32_t s2 = 0;
-            unsigned short s_next = row < N ? __half_as_ushort(__ldg(srow)) : (unsigned short)0;
-            for (int ks = 0; ks < KS; ++ks, ++it) {
-                if ((ks & 1) == 0) {
+            // the segment's first group scale, then each next one a group ahead
+            unsigned short s_next = row < N ? __half_as_ushort(__ldg(srow + (ks0 >> 1))) : (unsigned short)0;
+            for (int ks = ks0; ks < ks1; ++ks, ++it) {
+                if (ks == ks0 || (ks & 1) == 0) {
                     // this group's scale as a bf16 pair; fetch the next group's
                     const float sf = __half2float(__ushort_as_half(s_next));
                     const __nv_bfloat16 sb = __float2bfloat16_rn(sf);
@@ -377,21 +493,47 @@ cudaError_t read_gemm_device_error(int* code) {
 
 using namespace tern;
 
+// Workspace: [counters: tiles x 4 uint32, 256-byte aligned | fp32 sums: one
+// kBN x kBM tile per output tile].  The grid never exceeds kMaxCtas shares nor
+// the number of iterations.
+namespace tern {
+namespace {
+int gemm_tiles(int M, int N) { return ((M + kBN - 1) / kBN) * ((N + kBM - 1) / kBM); }
+int gemm_shares(int M, int N, int K, int sms) {
+    const long long it = (long long)gemm_tiles(M, N) * (K / kBK);
+    long long p = sms < kMaxCtas ? sms : kMaxCtas;
+    if (p > it) p = it;
+    return (int)p;
+}
+// Stream-K pays for its split tiles with a tail: the fp32 sums' reductions,
+// the fence and the last CTA's read-back, measured on GB300 at about the time
+// of 30 K stages.  It is used when the whole-tile waves would idle longer.
+constexpr int kStreamKTailStages = 30;
+bool use_stream_k(int M, int N, int K, int P) {
+    const long long tiles = gemm_tiles(M, N), KS = K / kBK;
+    const long long whole = (tiles + P - 1) / P * KS;
+    const long long shared = (tiles * KS + P - 1) / P + kStreamKTailStages;
+    return shared < whole;
+}
+size_t gemm_counter_bytes(int M, int N) { return ((size_t)gemm_tiles(M, N) * 4 * 4 + 255) / 256 * 256; }
+}  // namespace
+}  // namespace tern
+
 extern "C" size_t tern_gemm_workspace_bytes(int M, int N, int K) {
     if (M < 1 || N < 1 || K < 128 || K % 128 != 0) return 0;
-    return 0;   // the prefill kernel needs no scratch memory
+    return gemm_counter_bytes(M, N) + (size_t)gemm_tiles(M, N) * kTileFloats * 4;
 }
 
 extern "C" tern_status tern_gemm(const void* x, const uint32_t* codes, const void* scales, void* y,
                                  int y_is_bf16, int M, int N, int K, void* workspace,
                                  size_t workspace_bytes, tern_stream_t stream) {
     set_launch_count(0);
-    (void)workspace;
-    (void)workspace_bytes;
     if (M < 1 || N < 1 || K < 128 || K % 128 != 0) return TERN_ERR_SHAPE;
     if ((long long)M * N >= (1LL << 40) || (long long)N * K >= (1LL << 40)) return TERN_ERR_SHAPE;
     if (!x || !codes || !scales || !y) return TERN_ERR_NULL;
     if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(y)) return TERN_ERR_ALIGN;
+    if (!workspace || workspace_bytes < tern_gemm_workspace_bytes(M, N, K)) return TERN_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TERN_ERR_ALIGN;
     int sms = 0;
     tern_status st = check_device(&sms);
     if (st != TERN_OK) return st;
@@ -419,8 +561,12 @@ extern "C" tern_status tern_gemm(const void* x, const uint32_t* codes, const voi
     args.M = M;
     args.N = N;
     args.K = K;
-    const int total = ((M + kBN - 1) / kBN) * ((N + kBM - 1) / kBM);
-    const int grid = total < sms ? total : sms;
+    args.counters = reinterpret_cast<unsigned*>(workspace);
+    args.sums = reinterpret_cast<float*>(static_cast<char*>(workspace) + gemm_counter_bytes(M, N));
+    const int shares = gemm_shares(M, N, K, sms);
+    args.stream_k = use_stream_k(M, N, K, shares) ? 1 : 0;
+    const int tiles = gemm_tiles(M, N);
+    const int grid = args.stream_k ? shares : (tiles < shares ? tiles : shares);
     cudaError_t e = launch_pdl(gemm_kernel, dim3(grid), dim3(kThreads), kSmemBytes, (cudaStream_t)stream, true, mx,
                                mc, args);
     if (e != cudaSuccess) return TERN_ERR_CUDA;

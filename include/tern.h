@@ -181,13 +181,22 @@ tern_status tern_fwht_gemm(const void *x, const int8_t *signs, const uint32_t *c
 /* compute-bound phase)                                                    */
 /* ---------------------------------------------------------------------- */
 
-/* Workspace bytes tern_gemm needs; 0 on bad input. */
+/* Workspace bytes tern_gemm needs; 0 on bad input.  It holds one counter per
+ * (256-token x 128-row tile, 32-row quarter) and one 128 KB fp32 sum per tile
+ * (for tiles whose K range is split between CTAs): 34 MB for a 512 x 17408
+ * output.  It must be zero-filled once before its first use; every call
+ * leaves its counters at zero again.  Calls that share a workspace must not
+ * run concurrently.  After a device error (tern_device_error) zero-fill it
+ * again. */
 size_t tern_gemm_workspace_bytes(int M, int N, int K);
 
 /* y = x W^T on the tcgen05 tensor cores: each weight is unpacked on chip to
  * bf16 t * bf16(s_g) (the group scale rounded to bf16 and folded in), the
  * product accumulates in fp32 in tensor memory, and y is written as fp32
  * (y_is_bf16 == 0) or bf16 rounded to nearest even (y_is_bf16 != 0).
+ * The (tile, K-stage) iterations are shared out evenly over the SMs
+ * (stream-K); the parts of a tile split between CTAs are added in fp32 in no
+ * fixed order, so the last bits of such tiles may vary from run to run.
  * M >= 1, N >= 1 with N % 16 == 0, K >= 128 with K % 128 == 0. */
 tern_status tern_gemm(const void *x, const uint32_t *codes, const void *scales, void *y,
                       int y_is_bf16, int M, int N, int K, void *workspace,

@@ -119,6 +119,9 @@ def test_argument_errors_never_launch(tern):
     assert lib.tern_fwht_gemm(P, P, P, P, P, 1, 16, 4096, None, 1 << 30, None) == 4
     assert lib.tern_fwht_gemm(P, P, P, P, P, 2, 16, 4096, P, 2 * 4096 * 4 - 1, None) == 4
     assert tern.gemv_workspace_bytes(17, 16, 128) == 0
+    assert lib.tern_gemm(P, P, P, P, 0, 64, 256, 512, None, 1 << 30, None) == 4
+    need = tern.gemm_workspace_bytes(64, 256, 512)
+    assert lib.tern_gemm(P, P, P, P, 0, 64, 256, 512, P, need - 1, None) == 4
 
 def test_workspace_sizes(tern):
     # one flag word per 16-row tile once K > 1024 (256-byte aligned), then the
@@ -128,3 +131,13 @@ def test_workspace_sizes(tern):
     assert tern.gemv_workspace_bytes(2, 12288, 4096) == 768 * 4 + 2 * 4096 * 4
     assert tern.gemv_workspace_bytes(16, 12288, 8192) == 768 * 4 + 16 * 8192 * 4
     assert tern.gemv_workspace_bytes(1, 256, 512) == 256      # one slice: nothing needed
+
+
+def test_gemm_workspace_sizes(tern):
+    # counters: tiles x 4 uint32 (256-byte aligned); one 256 x 128 fp32 sum per tile
+    def want(M, N, K):
+        tiles = -(-M // 256) * -(-N // 128)
+        return (tiles * 16 + 255) // 256 * 256 + tiles * 256 * 128 * 4
+    for M, N, K in [(512, 17408, 5120), (512, 5120, 17408), (1, 128, 128), (300, 130, 640), (17, 1000, 128)]:
+        assert tern.gemm_workspace_bytes(M, N, K) == want(M, N, K)
+    assert tern.gemm_workspace_bytes(0, 128, 128) == 0

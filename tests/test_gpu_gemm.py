@@ -102,3 +102,22 @@ def test_gemm_back_to_back(tern, orc):
         y_ref, a_ref = orc.matmul(p.x, host_codes(ins[i][1]), p.s)
         for j in range(2):
             assert_fp32_close(outs[2 * i + j].cpu().numpy(), y_ref, a_ref, rel=GEMM_REL, what=f"bb {i}")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 8192), (300, 130, 4096), (512, 384, 17408), (40, 128, 2048)])
+def test_gemm_stream_k_split_tiles(tern, orc, M, N, K):
+    """Shapes with few tiles and deep K run on the stream-K schedule: each tile's
+    K stages are spread over many CTAs (dozens for the smallest) whose fp32
+    parts meet in the workspace sums; ragged M and N included."""
+    p = synth.problem(600 + M, M, N, K, tag=f"sk{N}x{K}")
+    y, codes = run(tern, p)
+    y_ref, a_ref = orc.matmul(p.x, host_codes(codes), p.s)
+    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, rel=GEMM_REL, what=f"stream-K M={M} N={N} K={K}")
+    # the counters and sums are back at zero: a second call on the same workspace agrees
+    ws = tern.workspace(tern.gemm_workspace_bytes(M, N, K))
+    y1 = tern.gemm(dev_bf16(p.x), codes, dev_scales(p.s), ws=ws)
+    y2 = tern.gemm(dev_bf16(p.x), codes, dev_scales(p.s), ws=ws)
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    assert_fp32_close(y2.cpu().numpy(), y_ref, a_ref, rel=GEMM_REL, what=f"stream-K second call M={M}")
+    assert_fp32_close(y1.cpu().numpy(), y_ref, a_ref, rel=GEMM_REL, what=f"stream-K first call M={M}")
