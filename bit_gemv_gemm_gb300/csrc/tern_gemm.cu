@@ -52,7 +52,7 @@ __device__ int g_gemm_error;
 constexpr int kBM = 128;                    // weight rows per tile (tensor-memory lanes)
 constexpr int kBN = 256;                    // tokens per tile (MMA N)
 constexpr int kBK = 64;                     // K per stage
-constexpr int kStages = 4;
+constexpr int kStages = 6;                  // K stages in flight (34 KB of shared memory each)
 constexpr int kXStageBytes = kBN * kBK * 2; // 32 KB
 constexpr int kCStageBytes = kBM * kBK / 4; // 2 KB of codes
 constexpr int kNumWarps = 14;               // 0 TMA, 1 MMA, 2-5 epilogue, 6-13 unpack
