@@ -484,13 +484,69 @@ gemv_kernel(const GemvArgs a) {
     // than 0 needs it non-zero before adding into y)
     unsigned flag_seen = 1u;
     if (S > 1 && sigma != 0 && threadIdx.x == 0) flag_seen = ld_acquire(a.flag + clu);
-    for (int s = 0; s < nseg; ++s) {
-        const int lo = seg_lo(s), hi = seg_hi(s);
-        if (lo >= hi) continue;
-        const int g = seg_group(s);
+    if (ONE && na == 1 && nb == 0) {
+        // The common decode case: one token and one group per warp over the
+        // whole range.  Whole turns of the ring run with compile-time slots,
+        // and a refill's source is the row base plus a per-tile stride (rows
+        // past N read row N - 1; their sums are never written to y).
+        const int g = gA + warp;
         stage(g);
-        if (s > 0 && na > 0) run_segment(std::true_type{}, lo, hi, g);
-        else run_segment(std::false_type{}, lo, hi, g);
+        const uint32_t* src_base = a.codes + (size_t)g * 8 + (lane & 1) * 4;
+        const int crow0 = tile_lo * 16 + crow;
+        const uint32_t ring_lane = smem_addr(ring) + (uint32_t)lane * 16u;
+        auto refill = [&](int u, int slot_) {
+            if (u < R) {
+                const int r = min(crow0 + 16 * u, N - 1);
+                cp_async16(ring_lane + (uint32_t)(slot_ * kSlotBytes), src_base + (size_t)r * W, true);
+            }
+            cp_async_commit();
+        };
+        const unsigned short* sp = sc + gid * gpad + (g - g_lo);
+        float* pw = part + (size_t)warp * rmax * 16;
+        auto fast_step = [&](int i, int s0, int s1, bool two) {
+            cp_async_wait<kDepth - 2>();
+            __syncwarp();
+            uint32_t w[2][4];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const unsigned char* sp8 = rd + (q ? s1 : s0) * kSlotBytes;
+                const uint2 v0 = *reinterpret_cast<const uint2*>(sp8);
+                const uint2 v1 = *reinterpret_cast<const uint2*>(sp8 + 8 * 32);
+                w[q][0] = v0.x;
+                w[q][1] = v1.x;
+                w[q][2] = v0.y;
+                w[q][3] = v1.y;
+            }
+            float acc[2][MT][4];
+            if (two) {
+                pair_mmas<MT>(acc, w, b);
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < MT; ++nt) mma_chain1(acc[0][nt], w[0], b[nt]);
+            }
+            __syncwarp();
+            refill(i + kDepth, s0);
+            if (two) refill(i + 1 + kDepth, s1);
+            epilogue(std::false_type{}, sp, pw, i, acc[0]);
+            if (two) epilogue(std::false_type{}, sp + sstep, pw + pstep, i + 1, acc[1]);
+            sp += 2 * sstep;
+            pw += 2 * pstep;
+        };
+        int i = 0;
+        for (; i + kDepth <= R; i += kDepth) {
+#pragma unroll
+            for (int q = 0; q < kDepth; q += 2) fast_step(i + q, q, q + 1, true);
+        }
+        for (int q = 0; i < R; i += 2, q += 2) fast_step(i, q, q + 1, i + 1 < R);
+    } else {
+        for (int s = 0; s < nseg; ++s) {
+            const int lo = seg_lo(s), hi = seg_hi(s);
+            if (lo >= hi) continue;
+            const int g = seg_group(s);
+            stage(g);
+            if (s > 0 && na > 0) run_segment(std::true_type{}, lo, hi, g);
+            else run_segment(std::false_type{}, lo, hi, g);
+        }
     }
     cp_async_wait<0>();
     __syncthreads();
