@@ -200,7 +200,9 @@ __host__ __device__ inline int scale_width(int G, int gA, int gB) {
 }
 
 // ONE: the single-token case (M = 1), whose epilogue keeps one value per row.
-template <int MT, bool XF32, bool ONE>
+// LEAN (with ONE, when G is a multiple of 8): every warp has exactly one group
+// over its CTA's whole range, and only the lean loop is compiled.
+template <int MT, bool XF32, bool ONE, bool LEAN = false>
 __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kCtasPerSm)
 gemv_kernel(const GemvArgs a) {
     using XT = typename std::conditional<XF32, float, __nv_bfloat16>::type;
@@ -484,7 +486,7 @@ gemv_kernel(const GemvArgs a) {
     // than 0 needs it non-zero before adding into y)
     unsigned flag_seen = 1u;
     if (S > 1 && sigma != 0 && threadIdx.x == 0) flag_seen = ld_acquire(a.flag + clu);
-    if (ONE && na == 1 && nb == 0) {
+    if (LEAN) {
         // The common decode case: one token and one group per warp over the
         // whole range.  Whole turns of the ring run with compile-time slots,
         // and a refill's source is the row base plus a per-tile stride (rows
@@ -656,7 +658,7 @@ Plan base_plan(int M, int N, int K) {
 
 // Lets the kernel use the device's whole per-block shared memory; returns the
 // dynamic part it may take.
-template <int MT, bool XF32, bool ONE>
+template <int MT, bool XF32, bool ONE, bool LEAN>
 cudaError_t kernel_smem_limit(int dev, int* limit) {
     static int optin_of[64] = {};
     if (!optin_of[dev]) {
@@ -664,10 +666,10 @@ cudaError_t kernel_smem_limit(int dev, int* limit) {
         cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return e;
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, gemv_kernel<MT, XF32, ONE>);
+        e = cudaFuncGetAttributes(&fa, gemv_kernel<MT, XF32, ONE, LEAN>);
         if (e != cudaSuccess) return e;
         optin -= (int)fa.sharedSizeBytes;   // the kernel's static shared memory comes first
-        e = cudaFuncSetAttribute(gemv_kernel<MT, XF32, ONE>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        e = cudaFuncSetAttribute(gemv_kernel<MT, XF32, ONE, LEAN>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (e != cudaSuccess) return e;
         optin_of[dev] = optin;
     }
@@ -677,10 +679,10 @@ cudaError_t kernel_smem_limit(int dev, int* limit) {
 
 // One wave: as many CTAs as fit at once, by registers (the launch bound) and
 // by shared memory (which grows with the range length).
-template <int MT, bool XF32, bool ONE>
+template <int MT, bool XF32, bool ONE, bool LEAN>
 tern_status make_plan(int M, int N, int K, int sms, int dev, Plan* out) {
     int limit = 0;
-    if (kernel_smem_limit<MT, XF32, ONE>(dev, &limit) != cudaSuccess) return TERN_ERR_CUDA;
+    if (kernel_smem_limit<MT, XF32, ONE, LEAN>(dev, &limit) != cudaSuccess) return TERN_ERR_CUDA;
     Plan p = base_plan(M, N, K);
     const int need = (p.T + kMaxTiles - 1) / kMaxTiles;   // ranges short enough for the shared partials
     int cps = 1;
@@ -708,7 +710,7 @@ PlanKey g_plan_key[kPlanCache];
 Plan g_plan_val[kPlanCache];
 int g_plan_n = 0, g_plan_next = 0;
 
-template <int MT, bool XF32, bool ONE>
+template <int MT, bool XF32, bool ONE, bool LEAN>
 tern_status cached_plan(int M, int N, int K, int sms, Plan* out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TERN_ERR_CUDA;
@@ -721,7 +723,7 @@ tern_status cached_plan(int M, int N, int K, int sms, Plan* out) {
             return TERN_OK;
         }
     }
-    const tern_status st = make_plan<MT, XF32, ONE>(M, N, K, sms, dev, out);
+    const tern_status st = make_plan<MT, XF32, ONE, LEAN>(M, N, K, sms, dev, out);
     if (st != TERN_OK) return st;
     const int slot = g_plan_n < kPlanCache ? g_plan_n++ : (g_plan_next++ % kPlanCache);
     g_plan_key[slot] = PlanKey{M, N, K, dev, XF32};
@@ -750,10 +752,10 @@ size_t workspace_bytes(int M, int N, int K, bool rot) {
     return flag_bytes(N, K) + (rot ? align_up((size_t)M * K * 4, 256) : 0);
 }
 
-template <int MT, bool XF32, bool ONE>
+template <int MT, bool XF32, bool ONE, bool LEAN = false>
 tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
     Plan p;
-    const tern_status st = cached_plan<MT, XF32, ONE>(args.M, args.N, args.K, sms, &p);
+    const tern_status st = cached_plan<MT, XF32, ONE, LEAN>(args.M, args.N, args.K, sms, &p);
     if (st != TERN_OK) return st;
     args.G = p.G;
     args.T = p.T;
@@ -764,7 +766,7 @@ tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
     args.off_sc = p.off_sc;
     args.off_part = p.off_part;
     const cudaError_t e =
-        launch_pdl(gemv_kernel<MT, XF32, ONE>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, args);
+        launch_pdl(gemv_kernel<MT, XF32, ONE, LEAN>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, args);
     return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
 
@@ -788,6 +790,8 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
     args.N = N;
     args.K = K;
     const int MT = (M + 7) / 8;
+    // K a multiple of 1024: slices of exactly 8 groups, one group per warp
+    const bool lean = (K / kGroup) % kWarps == 0;
     int launches = 1;
     if (signs) {
         float* xr = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + fb);
@@ -796,11 +800,13 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
         if (e != cudaSuccess) return TERN_ERR_CUDA;
         args.x = xr;
         launches = 2;
-        st = M == 1 ? launch_gemv<1, true, true>(args, sms, stream)
+        st = M == 1 ? (lean ? launch_gemv<1, true, true, true>(args, sms, stream)
+                            : launch_gemv<1, true, true>(args, sms, stream))
              : MT == 1 ? launch_gemv<1, true, false>(args, sms, stream)
                        : launch_gemv<2, true, false>(args, sms, stream);
     } else {
-        st = M == 1 ? launch_gemv<1, false, true>(args, sms, stream)
+        st = M == 1 ? (lean ? launch_gemv<1, false, true, true>(args, sms, stream)
+                            : launch_gemv<1, false, true>(args, sms, stream))
              : MT == 1 ? launch_gemv<1, false, false>(args, sms, stream)
                        : launch_gemv<2, false, false>(args, sms, stream);
     }
