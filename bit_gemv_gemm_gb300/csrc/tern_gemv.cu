@@ -42,8 +42,8 @@
 // stages one segment's activation into registers and streams its own
 // 32-byte column of every tile of the segment (16 rows x 32 B = one 16-byte
 // cp.async per lane) through a
-// private shared-memory ring, kDepth units ahead; the first kDepth units go out
-// before the programmatic-dependent-launch wait.  Two tiles per step run as two
+// private shared-memory ring, kDepth units ahead; the first kEarly units go out
+// before the programmatic-dependent-launch wait, the rest after staging.  Two tiles per step run as two
 // independent MMA chains.  Row partials go to shared memory (private per warp
 // for M <= 4, shared atomics beyond) and are summed over the CTA's warps.
 // With one slice the CTA stores its rows of y.  With several, the slice-0 CTA
@@ -65,7 +65,8 @@ namespace {
 constexpr int kGroup = 128;            // weights per scale
 constexpr int kWarps = 8;              // warps per CTA
 constexpr int kThreads = kWarps * 32;
-constexpr int kDepth = 6;              // units (tile x group) in flight per warp (even)
+constexpr int kDepth = 4;              // units (tile x group) in flight per warp (even)
+constexpr int kEarly = 4;              // of which issued before the PDL wait, the rest after staging
 constexpr int kSlotBytes = 16 * 32;    // one unit: 16 rows x 32 B of codes
 constexpr int kMaxTiles = 32;          // tiles per range (bounds partials and scales in shared memory)
 constexpr int kPrivateMaxM = 4;        // private per-warp partials up to this many tokens
@@ -184,6 +185,10 @@ __device__ __forceinline__ uint64_t now_ns() {
     return t;
 }
 constexpr uint64_t kFlagWaitNs = 1000000000ull;   // 1 s: far beyond any real wait
+// Counts into a range flag modulo `wrap + 1` without waiting for the old value.
+__device__ __forceinline__ void red_inc(unsigned* p, unsigned wrap) {
+    asm volatile("red.relaxed.gpu.global.inc.u32 [%0], %1;" ::"l"(p), "r"(wrap) : "memory");
+}
 
 __device__ int g_gemv_error;   // sticky device error word of this translation unit
 
@@ -264,8 +269,9 @@ gemv_kernel(const GemvArgs a) {
 
     pdl_launch_dependents();
     // Codes and scales are never the previous kernel's output: the range's
-    // scales (one commit group) and the first kDepth units of every warp go
-    // out before the PDL wait.
+    // scales (one commit group) and the first kEarly units of every warp go
+    // out before the PDL wait, the others once the warp has staged its
+    // activation (a warp held up issuing copies is late to stage).
     {
         const int row0 = tile_lo * 16, rows = R * 16;
         const int mode = scale_mode(G, gA, gB);
@@ -296,7 +302,7 @@ gemv_kernel(const GemvArgs a) {
         cp_async_commit();
     }
 #pragma unroll
-    for (int i = 0; i < kDepth; ++i) issue(i);
+    for (int i = 0; i < kEarly; ++i) issue(i);
     pdl_wait();
     // y of the range starts at zero: the slice-0 CTA clears it (after the PDL
     // wait, since the previous kernel may still read y) and counts itself into
@@ -309,7 +315,7 @@ gemv_kernel(const GemvArgs a) {
         }
         __threadfence();
         __syncthreads();
-        if (threadIdx.x == 0) atomicInc(a.flag + clu, (unsigned)(S - 1));
+        if (threadIdx.x == 0) red_inc(a.flag + clu, (unsigned)(S - 1));
     }
     // private partials: a warp's first segment (when it spans the range) stores
     // every tile, later ones add; with no such segment, or with shared atomics,
@@ -480,7 +486,8 @@ gemv_kernel(const GemvArgs a) {
     };
     // this thread's scale copies (the oldest group) have landed; after the
     // barrier every thread's have, and the zeroed partials are visible
-    cp_async_wait<kDepth>();
+    static_assert(kEarly >= 2 && kEarly <= kDepth && kDepth % 2 == 0, "ring accounting");
+    cp_async_wait<kEarly>();
     __syncthreads();
     // the range's flag, read now so the load overlaps the loop (a slice other
     // than 0 needs it non-zero before adding into y)
@@ -493,6 +500,8 @@ gemv_kernel(const GemvArgs a) {
         // past N read row N - 1; their sums are never written to y).
         const int g = gA + warp;
         stage(g);
+#pragma unroll
+        for (int u = kEarly; u < kDepth; ++u) issue(u);
         const uint32_t* src_base = a.codes + (size_t)g * 8 + (lane & 1) * 4;
         const int crow0 = tile_lo * 16 + crow;
         const uint32_t ring_lane = smem_addr(ring) + (uint32_t)lane * 16u;
@@ -541,11 +550,17 @@ gemv_kernel(const GemvArgs a) {
         }
         for (int q = 0; i < R; i += 2, q += 2) fast_step(i, q, q + 1, i + 1 < R);
     } else {
+        bool rest_issued = false;
         for (int s = 0; s < nseg; ++s) {
             const int lo = seg_lo(s), hi = seg_hi(s);
             if (lo >= hi) continue;
             const int g = seg_group(s);
             stage(g);
+            if (!rest_issued) {
+#pragma unroll
+                for (int u = kEarly; u < kDepth; ++u) issue(u);
+                rest_issued = true;
+            }
             if (s > 0 && na > 0) run_segment(std::true_type{}, lo, hi, g);
             else run_segment(std::false_type{}, lo, hi, g);
         }
@@ -586,7 +601,7 @@ gemv_kernel(const GemvArgs a) {
                     if (!ok && (it & 63u) == 0 && now_ns() - t0 > kFlagWaitNs) break;
                 }
             }
-            if (ok) atomicInc(a.flag + clu, (unsigned)(S - 1));
+            if (ok) red_inc(a.flag + clu, (unsigned)(S - 1));
             else report_device_error(&g_gemv_error, kDevErrGemvConsumerWait);
             go = ok;
         }
