@@ -489,10 +489,12 @@ gemv_kernel(const GemvArgs a) {
     static_assert(kEarly >= 2 && kEarly <= kDepth && kDepth % 2 == 0, "ring accounting");
     cp_async_wait<kEarly>();
     __syncthreads();
-    // the range's flag, read now so the load overlaps the loop (a slice other
-    // than 0 needs it non-zero before adding into y)
-    unsigned flag_seen = 1u;
-    if (S > 1 && sigma != 0 && threadIdx.x == 0) flag_seen = ld_acquire(a.flag + clu);
+    // the range's flag, read ahead so the load overlaps the loop (a slice other
+    // than 0 needs it non-zero before adding into y); the lean loop reads it a
+    // ring turn in, after the slice-0 CTA has had time to clear y
+    const bool flag_reader = S > 1 && sigma != 0 && threadIdx.x == 0;
+    unsigned flag_seen = 0u;
+    if (!LEAN && flag_reader) flag_seen = ld_acquire(a.flag + clu);
     if (LEAN) {
         // The common decode case: one token and one group per warp over the
         // whole range.  Whole turns of the ring run with compile-time slots,
@@ -545,6 +547,7 @@ gemv_kernel(const GemvArgs a) {
         };
         int i = 0;
         for (; i + kDepth <= R; i += kDepth) {
+            if (i == kDepth && flag_reader) flag_seen = ld_acquire(a.flag + clu);
 #pragma unroll
             for (int q = 0; q < kDepth; q += 2) fast_step(i + q, q, q + 1, true);
         }
