@@ -307,16 +307,32 @@ gemv_kernel(const GemvArgs a) {
     // y of the range starts at zero: the slice-0 CTA clears it (after the PDL
     // wait, since the previous kernel may still read y) and counts itself into
     // the range's flag once the zeros are visible to the whole GPU
+    // (the lean loop issues the clearing stores here but fences and counts a
+    // ring turn later, when the stores have long landed, instead of holding
+    // the CTA at a barrier now)
+    __shared__ unsigned cleared_warps;
     if (S > 1 && sigma == 0) {
         const int row0 = tile_lo * 16, nrow = min(R * 16, N - row0);
         for (int i = threadIdx.x; i < M * nrow; i += kThreads) {
             const int m = i / nrow, r = i - m * nrow;
             a.y[(size_t)m * N + row0 + r] = 0.0f;
         }
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) red_inc(a.flag + clu, (unsigned)(S - 1));
+        if (!LEAN) {
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) red_inc(a.flag + clu, (unsigned)(S - 1));
+        } else if (threadIdx.x == 0) {
+            cleared_warps = 0u;   // published to the other warps by the barrier below
+        }
     }
+    // a lean slice-0 warp: its clearing stores are visible; the eighth to say
+    // so counts the range's clearing into the flag
+    auto count_cleared = [&]() {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0 && atomicAdd(&cleared_warps, 1u) == (unsigned)(kWarps - 1))
+            red_inc(a.flag + clu, (unsigned)(S - 1));
+    };
     // private partials: a warp's first segment (when it spans the range) stores
     // every tile, later ones add; with no such segment, or with shared atomics,
     // start from zeros
@@ -545,13 +561,22 @@ gemv_kernel(const GemvArgs a) {
             sp += 2 * sstep;
             pw += 2 * pstep;
         };
+        const bool clearer = S > 1 && sigma == 0;
+        bool counted = false;
         int i = 0;
         for (; i + kDepth <= R; i += kDepth) {
-            if (i == kDepth && flag_reader) flag_seen = ld_acquire(a.flag + clu);
+            if (i == kDepth) {
+                if (flag_reader) flag_seen = ld_acquire(a.flag + clu);
+                if (clearer) {
+                    count_cleared();
+                    counted = true;
+                }
+            }
 #pragma unroll
             for (int q = 0; q < kDepth; q += 2) fast_step(i + q, q, q + 1, true);
         }
         for (int q = 0; i < R; i += 2, q += 2) fast_step(i, q, q + 1, i + 1 < R);
+        if (clearer && !counted) count_cleared();   // a range of less than two ring turns
     } else {
         bool rest_issued = false;
         for (int s = 0; s < nseg; ++s) {
