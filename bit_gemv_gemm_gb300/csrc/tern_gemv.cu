@@ -205,8 +205,8 @@ __host__ __device__ inline int scale_width(int G, int gA, int gB) {
 }
 
 // ONE: the single-token case (M = 1), whose epilogue keeps one value per row.
-// LEAN (with ONE, when G is a multiple of 8): every warp has exactly one group
-// over its CTA's whole range, and only the lean loop is compiled.
+// LEAN (when G is a multiple of 8): every warp has exactly one group over its
+// CTA's whole range, and only the lean loop is compiled.
 template <int MT, bool XF32, bool ONE, bool LEAN = false>
 __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kCtasPerSm)
 gemv_kernel(const GemvArgs a) {
@@ -512,8 +512,8 @@ gemv_kernel(const GemvArgs a) {
     unsigned flag_seen = 0u;
     if (!LEAN && flag_reader) flag_seen = ld_acquire(a.flag + clu);
     if (LEAN) {
-        // The common decode case: one token and one group per warp over the
-        // whole range.  Whole turns of the ring run with compile-time slots,
+        // The common case: one group per warp over the whole range (K a
+        // multiple of 1024).  Whole turns of the ring run with compile-time slots,
         // and a refill's source is the row base plus a per-tile stride (rows
         // past N read row N - 1; their sums are never written to y).
         const int g = gA + warp;
@@ -531,7 +531,7 @@ gemv_kernel(const GemvArgs a) {
             cp_async_commit();
         };
         const unsigned short* sp = sc + gid * gpad + (g - g_lo);
-        float* pw = part + (size_t)warp * rmax * 16;
+        float* pw = part + (size_t)warp * rmax * pstep;   // private partials (M <= 4)
         auto fast_step = [&](int i, int s0, int s1, bool two) {
             cp_async_wait<kDepth - 2>();
             __syncwarp();
@@ -845,13 +845,17 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
         launches = 2;
         st = M == 1 ? (lean ? launch_gemv<1, true, true, true>(args, sms, stream)
                             : launch_gemv<1, true, true>(args, sms, stream))
-             : MT == 1 ? launch_gemv<1, true, false>(args, sms, stream)
-                       : launch_gemv<2, true, false>(args, sms, stream);
+             : MT == 1 ? (lean ? launch_gemv<1, true, false, true>(args, sms, stream)
+                               : launch_gemv<1, true, false>(args, sms, stream))
+                       : (lean ? launch_gemv<2, true, false, true>(args, sms, stream)
+                               : launch_gemv<2, true, false>(args, sms, stream));
     } else {
         st = M == 1 ? (lean ? launch_gemv<1, false, true, true>(args, sms, stream)
                             : launch_gemv<1, false, true>(args, sms, stream))
-             : MT == 1 ? launch_gemv<1, false, false>(args, sms, stream)
-                       : launch_gemv<2, false, false>(args, sms, stream);
+             : MT == 1 ? (lean ? launch_gemv<1, false, false, true>(args, sms, stream)
+                               : launch_gemv<1, false, false>(args, sms, stream))
+                       : (lean ? launch_gemv<2, false, false, true>(args, sms, stream)
+                               : launch_gemv<2, false, false>(args, sms, stream));
     }
     if (st != TERN_OK) return st;
     set_launch_count(launches);
