@@ -566,7 +566,7 @@ def main() -> None:
                    "l2": "inputs larger than L2 (4.55 GB of weights per step vs 129 MB L2)",
                    "parallelism": f"replicas x{ws_count}", "cuda_graph": True},
         "hbm_frac": value / ws_count / hbm,
-        "roofline": {"bound": "hbm", "kernel": "gemv_kernel + prologue (per tern_gemv call)",
+        "roofline": {"bound": "hbm", "kernel": "gemv_kernel (one launch per tern_gemv call)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": f"{peaks['_source']} hbm_gbs",
                      "traffic": load_traffic("gemv_kernel", GEMV_SRC)},

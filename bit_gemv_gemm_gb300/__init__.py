@@ -47,6 +47,7 @@ EXPORTS = {
     "tern_device_error": (_I, [_P]),
     "tern_last_launch_count": (_I, []),
     "tern_gemv_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
+    "tern_wait_selftest": (_I, [_I, _I, _P]),
 }
 
 
@@ -241,6 +242,16 @@ def device_error() -> int:
     code = ctypes.c_int(0)
     _check("tern_device_error", lib().tern_device_error(ctypes.byref(code)))
     return int(code.value)
+
+
+SELFTEST_RANGE_FLAG, SELFTEST_MBARRIER = 0, 1
+DEVERR_GEMM_MMA_WAIT, DEVERR_GEMV_RANGE_FLAG_WAIT = 0x103, 0x202
+
+
+def wait_selftest(which: int, limit_us: int, stream=None) -> None:
+    """Runs one bounded wait on something nothing completes (tern_wait_selftest);
+    the code it reports is read with device_error()."""
+    _check("tern_wait_selftest", lib().tern_wait_selftest(which, limit_us, _stream(stream)))
 
 
 def last_launch_count() -> int:

@@ -66,6 +66,21 @@ size_t tern_packed_bytes(int N, int K) {
 
 int tern_last_launch_count(void) { return g_last_launches.load(std::memory_order_relaxed); }
 
+tern_status tern_wait_selftest(int which, int limit_us, tern_stream_t stream) {
+    set_launch_count(0);
+    if ((which != TERN_SELFTEST_RANGE_FLAG && which != TERN_SELFTEST_MBARRIER) || limit_us < 1 ||
+        limit_us > 1000000)
+        return TERN_ERR_SHAPE;
+    const tern_status d = check_device(nullptr);
+    if (d != TERN_OK) return d;
+    const uint64_t ns = 1000ull * (uint64_t)limit_us;
+    const cudaError_t e = which == TERN_SELFTEST_RANGE_FLAG ? launch_flag_wait_selftest(ns, stream)
+                                                            : launch_mbar_wait_selftest(ns, stream);
+    if (e != cudaSuccess) return TERN_ERR_CUDA;
+    set_launch_count(1);
+    return TERN_OK;
+}
+
 tern_status tern_device_error(int* code) {
     if (!code) return TERN_ERR_NULL;
     *code = 0;

@@ -17,13 +17,12 @@ namespace tern {
 // ----------------------------------------------------------------------------
 enum DeviceError : int {
     kDevErrNone = 0,
-    kDevErrGemmProducerWait = 0x101,   // TMA producer gave up waiting for a free stage
-    kDevErrGemmUnpackWait = 0x102,     // unpack warps gave up waiting for raw tiles / free slots
-    kDevErrGemmMmaWait = 0x103,        // MMA issuer gave up waiting for operands / TMEM
-    kDevErrGemmEpilogueWait = 0x104,   // epilogue gave up waiting for an accumulator
-    kDevErrGemmTeardownWait = 0x105,   // teardown gave up waiting for in-flight work
-    kDevErrGemvProducerWait = 0x201,   // decode producer gave up waiting for a free ring slot
-    kDevErrGemvConsumerWait = 0x202,   // decode warps gave up waiting for a code tile
+    kDevErrGemmProducerWait = TERN_DEVERR_GEMM_PRODUCER_WAIT,
+    kDevErrGemmUnpackWait = TERN_DEVERR_GEMM_UNPACK_WAIT,
+    kDevErrGemmMmaWait = TERN_DEVERR_GEMM_MMA_WAIT,
+    kDevErrGemmEpilogueWait = TERN_DEVERR_GEMM_EPILOGUE_WAIT,
+    kDevErrGemmTeardownWait = TERN_DEVERR_GEMM_TEARDOWN_WAIT,
+    kDevErrGemvConsumerWait = TERN_DEVERR_GEMV_RANGE_FLAG_WAIT,
 };
 
 // Each translation unit whose kernels wait on barriers (the prefill and the
@@ -34,6 +33,34 @@ __device__ __forceinline__ void report_device_error(int* word, int code) {
 }
 cudaError_t read_gemm_device_error(int* code);
 cudaError_t read_gemv_device_error(int* code);
+// One-CTA kernels that run a bounded wait nothing completes (tern_wait_selftest).
+cudaError_t launch_flag_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
+cudaError_t launch_mbar_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
+
+// ----------------------------------------------------------------------------
+// Bounded waits.  No kernel of the library spins without a time limit: a wait
+// that runs out returns false, and its caller reports a code into its sticky
+// word and returns, so the context stays usable.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Waits until the word at p is non-zero, for at most limit_ns.
+__device__ __forceinline__ bool wait_flag_nonzero(const unsigned* p, uint64_t limit_ns) {
+    if (ld_acquire_gpu(p) != 0u) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (ld_acquire_gpu(p) != 0u) return true;
+        if ((it & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
 
 // ----------------------------------------------------------------------------
 // Programmatic dependent launch (PDL).

@@ -489,6 +489,33 @@ cudaError_t read_gemm_device_error(int* code) {
     return cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(int));
 }
 
+// Two roles of a CTA waiting on mbarriers that nobody arrives at, as the
+// prefill roles wait on each other: warp 0's wait runs out after limit_ns, it
+// raises the CTA's abort flag and reports; warp 1, in a wait with the products'
+// own 1 s limit, sees the flag and returns at once instead of running out.
+__global__ void __launch_bounds__(64) mbar_wait_selftest_kernel(uint64_t limit_ns) {
+    using namespace sm100;
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ volatile int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bars[0]), 1);
+        mbar_init(smem_u32(&bars[1]), 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (lane == 0 && !mbar_wait_bounded(smem_u32(&bars[warp]), 0u, &abort_flag, warp == 0 ? limit_ns : kWaitLimitNs) &&
+        !abort_flag) {
+        abort_flag = 1;
+        report_device_error(&g_gemm_error, kDevErrGemmMmaWait);
+    }
+}
+cudaError_t launch_mbar_wait_selftest(uint64_t limit_ns, cudaStream_t stream) {
+    mbar_wait_selftest_kernel<<<1, 64, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 }  // namespace tern
 
 using namespace tern;

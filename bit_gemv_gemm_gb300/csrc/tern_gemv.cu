@@ -174,16 +174,6 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 }
 
 // ---- the per-range flag word ----
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ uint64_t now_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
 constexpr uint64_t kFlagWaitNs = 1000000000ull;   // 1 s: far beyond any real wait
 // Counts into a range flag modulo `wrap + 1` without waiting for the old value.
 __device__ __forceinline__ void red_inc(unsigned* p, unsigned wrap) {
@@ -510,7 +500,7 @@ gemv_kernel(const GemvArgs a) {
     // ring turn in, after the slice-0 CTA has had time to clear y
     const bool flag_reader = S > 1 && sigma != 0 && threadIdx.x == 0;
     unsigned flag_seen = 0u;
-    if (!LEAN && flag_reader) flag_seen = ld_acquire(a.flag + clu);
+    if (!LEAN && flag_reader) flag_seen = ld_acquire_gpu(a.flag + clu);
     if (LEAN) {
         // The common case: one group per warp over the whole range (K a
         // multiple of 1024).  Whole turns of the ring run with compile-time slots,
@@ -566,7 +556,7 @@ gemv_kernel(const GemvArgs a) {
         int i = 0;
         for (; i + kDepth <= R; i += kDepth) {
             if (i == kDepth) {
-                if (flag_reader) flag_seen = ld_acquire(a.flag + clu);
+                if (flag_reader) flag_seen = ld_acquire_gpu(a.flag + clu);
                 if (clearer) {
                     count_cleared();
                     counted = true;
@@ -621,14 +611,7 @@ gemv_kernel(const GemvArgs a) {
     __shared__ int go;
     if (sigma != 0) {
         if (threadIdx.x == 0) {
-            bool ok = flag_seen != 0u || ld_acquire(a.flag + clu) != 0u;
-            if (!ok) {
-                const uint64_t t0 = now_ns();
-                for (uint32_t it = 1; !ok; ++it) {
-                    ok = ld_acquire(a.flag + clu) != 0u;
-                    if (!ok && (it & 63u) == 0 && now_ns() - t0 > kFlagWaitNs) break;
-                }
-            }
+            const bool ok = flag_seen != 0u || wait_flag_nonzero(a.flag + clu, kFlagWaitNs);
             if (ok) red_inc(a.flag + clu, (unsigned)(S - 1));
             else report_device_error(&g_gemv_error, kDevErrGemvConsumerWait);
             go = ok;
@@ -877,6 +860,19 @@ cudaError_t read_gemv_device_error(int* code) {
     }
     *code = v;
     return cudaSuccess;
+}
+
+// The range-flag wait run on a word that nothing ever sets: it gives up after
+// limit_ns and reports the code a K-slice reports when the slice-0 CTA never
+// counts its clearing of y.
+__device__ unsigned g_never_set;   // zero-initialised; no kernel writes it
+__global__ void flag_wait_selftest_kernel(uint64_t limit_ns) {
+    if (threadIdx.x == 0 && !wait_flag_nonzero(&g_never_set, limit_ns))
+        report_device_error(&g_gemv_error, kDevErrGemvConsumerWait);
+}
+cudaError_t launch_flag_wait_selftest(uint64_t limit_ns, cudaStream_t stream) {
+    flag_wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
 }
 
 }  // namespace tern

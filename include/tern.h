@@ -185,7 +185,7 @@ tern_status tern_fwht_gemm(const void *x, const int8_t *signs, const uint32_t *c
  * (256-token x 128-row tile, 32-row quarter) and one 128 KB fp32 sum per tile
  * (for tiles whose K range is split between CTAs): 34 MB for a 512 x 17408
  * output.  It must be zero-filled once before its first use; every call
- * leaves its counters at zero again.  Calls that share a workspace must not
+ * leaves its counters and sums at zero again.  Calls that share a workspace must not
  * run concurrently.  After a device error (tern_device_error) zero-fill it
  * again. */
 size_t tern_gemm_workspace_bytes(int M, int N, int K);
@@ -197,7 +197,7 @@ size_t tern_gemm_workspace_bytes(int M, int N, int K);
  * The (tile, K-stage) iterations are shared out evenly over the SMs
  * (stream-K); the parts of a tile split between CTAs are added in fp32 in no
  * fixed order, so the last bits of such tiles may vary from run to run.
- * M >= 1, N >= 1 with N % 16 == 0, K >= 128 with K % 128 == 0. */
+ * M >= 1, N >= 1, K >= 128 with K % 128 == 0 (TERN_ERR_SHAPE otherwise). */
 tern_status tern_gemm(const void *x, const uint32_t *codes, const void *scales, void *y,
                       int y_is_bf16, int M, int N, int K, void *workspace,
                       size_t workspace_bytes, tern_stream_t stream);
@@ -206,11 +206,41 @@ tern_status tern_gemm(const void *x, const uint32_t *codes, const void *scales, 
 /* Diagnostics                                                             */
 /* ---------------------------------------------------------------------- */
 
-/* Reads and clears the sticky device-side error word of the current device
+/* Device-side error codes: which bounded wait gave up.  Every wait in the
+ * kernels has a time limit (1 s for the waits below); the first wait to run
+ * out stores its code, and the kernel returns with the call's output
+ * incomplete. */
+enum {
+    TERN_DEVERR_GEMM_PRODUCER_WAIT = 0x101,  /* prefill: loader waited for a free stage */
+    TERN_DEVERR_GEMM_UNPACK_WAIT = 0x102,    /* prefill: unpack warps waited for a tile or slot */
+    TERN_DEVERR_GEMM_MMA_WAIT = 0x103,       /* prefill: MMA issuer waited for operands or TMEM */
+    TERN_DEVERR_GEMM_EPILOGUE_WAIT = 0x104,  /* prefill: epilogue waited for an accumulator */
+    TERN_DEVERR_GEMM_TEARDOWN_WAIT = 0x105,  /* prefill: teardown waited for work in flight */
+    TERN_DEVERR_GEMV_RANGE_FLAG_WAIT = 0x202 /* decode: a K-slice waited for y's clearing */
+};
+
+/* Reads and clears the sticky device-side error words of the current device
  * (synchronizes the device).  *code = 0 when no kernel reported an error;
- * otherwise a nonzero code naming the wait that gave up.  Returns TERN_OK or
- * TERN_ERR_CUDA. */
+ * otherwise the TERN_DEVERR_* code of the wait that gave up.  Returns TERN_OK
+ * or TERN_ERR_CUDA. */
 tern_status tern_device_error(int *code);
+
+/* Self-test of the bounded waits (a diagnostic; the method has no counterpart).
+ * Launches one small kernel that runs one of the products' own wait helpers on
+ * something nothing ever completes, with a limit of limit_us microseconds
+ * (1 .. 1,000,000):
+ *   TERN_SELFTEST_RANGE_FLAG -- the decode K-slices' wait on a range flag word;
+ *     reports TERN_DEVERR_GEMV_RANGE_FLAG_WAIT.
+ *   TERN_SELFTEST_MBARRIER -- the prefill roles' mbarrier wait: one role's wait
+ *     runs out, raises the CTA's abort flag and reports
+ *     TERN_DEVERR_GEMM_MMA_WAIT; a second role in a 1 s wait sees the flag and
+ *     returns early, so the kernel ends about limit_us after it starts.
+ * The code is then read with tern_device_error, and the context stays usable.
+ * Returns TERN_ERR_SHAPE for an unknown `which` or a limit out of range
+ * (nothing launched), TERN_ERR_ARCH / TERN_ERR_CUDA as the products do. */
+#define TERN_SELFTEST_RANGE_FLAG 0
+#define TERN_SELFTEST_MBARRIER 1
+tern_status tern_wait_selftest(int which, int limit_us, tern_stream_t stream);
 
 /* The number of kernels the last entry point call launched (for launch
  * accounting in benchmarks); host-side, per process. */

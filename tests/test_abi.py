@@ -122,6 +122,11 @@ def test_argument_errors_never_launch(tern):
     assert lib.tern_gemm(P, P, P, P, 0, 64, 256, 512, None, 1 << 30, None) == 4
     need = tern.gemm_workspace_bytes(64, 256, 512)
     assert lib.tern_gemm(P, P, P, P, 0, 64, 256, 512, P, need - 1, None) == 4
+    # the bounded-wait self-test: an unknown wait or a limit out of range
+    assert lib.tern_wait_selftest(2, 1000, None) == 2
+    assert lib.tern_wait_selftest(-1, 1000, None) == 2
+    assert lib.tern_wait_selftest(tern.SELFTEST_RANGE_FLAG, 0, None) == 2
+    assert lib.tern_wait_selftest(tern.SELFTEST_MBARRIER, 1000001, None) == 2
 
 def test_workspace_sizes(tern):
     # one flag word per 16-row tile once K > 1024 (256-byte aligned), then the
