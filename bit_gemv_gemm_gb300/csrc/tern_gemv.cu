@@ -78,7 +78,8 @@ template <> struct GemvCfg<1> { static constexpr int kCtasPerSm = 3; };
 template <> struct GemvCfg<2> { static constexpr int kCtasPerSm = 2; };
 
 struct GemvArgs {
-    const void* x;              // bf16 [M][K], or fp32 [M][K] when the rotation prologue ran
+    const void* x;              // bf16 [M][K], or the rotation's staged fragments (PRE)
+    const int* xe;              // PRE: the staging exponent E of each (token, group)
     const uint32_t* codes;      // [N][K/16]
     const __half* scales;       // [N][K/128]
     float* y;                   // [M][N]
@@ -106,6 +107,20 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
             : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
     }
+}
+
+// Activation staging: a token's 128 values of one group become fp16
+// x 2^(E + 10 - 2j'), j' the code's position within its 16-bit half (j for
+// slots 0-5, j - 6 for 6 and 7, which are read after a shift by 12), with E
+// such that the largest |x| times 2^(E + 10) stays below 2^15.
+__device__ __forceinline__ int stage_exponent(float mx) {
+    // mx < 2^ex for ex = biased exponent - 126
+    const int be = (int)(__float_as_uint(mx) >> 23);   // mx >= 0
+    return (mx > 0.0f && be < 255) ? max(-100, min(5 - (max(be, 1) - 126), 110)) : 0;
+}
+// the exact power of two 2^(E + 10 - 2j') for slot j, exponent within [-100, 120]
+__device__ __forceinline__ float stage_multiplier(int E, int j) {
+    return __uint_as_float((uint32_t)(E + 10 - 2 * (j < 6 ? j : j - 6) + 127) << 23);
 }
 
 // Slot j's A registers from the four code words by one AND (codes 6, 7, 14, 15
@@ -197,10 +212,9 @@ __host__ __device__ inline int scale_width(int G, int gA, int gB) {
 // ONE: the single-token case (M = 1), whose epilogue keeps one value per row.
 // LEAN (when G is a multiple of 8): every warp has exactly one group over its
 // CTA's whole range, and only the lean loop is compiled.
-template <int MT, bool XF32, bool ONE, bool LEAN = false>
+template <int MT, bool PRE, bool ONE, bool LEAN = false>
 __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kCtasPerSm)
 gemv_kernel(const GemvArgs a) {
-    using XT = typename std::conditional<XF32, float, __nv_bfloat16>::type;
     constexpr int MP = 8 * MT;
     extern __shared__ __align__(16) unsigned char smem[];
     const int M = ONE ? 1 : a.M;
@@ -332,29 +346,41 @@ gemv_kernel(const GemvArgs a) {
 
     // ---- stage one group's activation (read from global memory, possibly the
     // previous kernel's output): lane (gid, t) holds token nt*8+gid,
-    // k = 32t .. 32t+31 of the group ----
-    const XT* xsrc = reinterpret_cast<const XT*>(a.x);
+    // k = 32t .. 32t+31 of the group, as fp16 x 2^(E + 10 - 2j') with E from
+    // the token's largest |x| in the group (the rotation prologue of the fused
+    // call has done this already: PRE) ----
     uint32_t b[MT][16];
     float4 f[MT];   // (F, F*acc1) of tokens 2t and 2t+1 of each token tile
     auto stage = [&](int g) {
 #pragma unroll
         for (int nt = 0; nt < MT; ++nt) {
-            const int m = nt * 8 + gid;
-            float v[32];
-            if (m < M) {
-                const XT* src = xsrc + (size_t)m * a.K + (size_t)g * kGroup + 32 * t;
-                if (XF32) {
-                    const float4* s4 = reinterpret_cast<const float4*>(src);
+            // one staged token: every lane reads token 0 (the other lanes' B
+            // columns belong to tokens that do not exist; their results are
+            // never read)
+            const int m = (ONE && PRE) ? 0 : nt * 8 + gid;
+            int E = 0;
+            if (PRE) {
+                if (m < M) {
+                    const uint4* s4 = reinterpret_cast<const uint4*>(
+                        reinterpret_cast<const uint32_t*>(a.x) + ((size_t)(m * G + g) * 4 + t) * 16);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 u = s4[q];
-                        v[4 * q] = u.x;
-                        v[4 * q + 1] = u.y;
-                        v[4 * q + 2] = u.z;
-                        v[4 * q + 3] = u.w;
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 u = s4[q];
+                        b[nt][4 * q] = u.x;
+                        b[nt][4 * q + 1] = u.y;
+                        b[nt][4 * q + 2] = u.z;
+                        b[nt][4 * q + 3] = u.w;
                     }
+                    E = a.xe[m * G + g];
                 } else {
-                    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) b[nt][q] = 0u;
+                }
+            } else {
+                float v[32];
+                if (m < M) {
+                    const uint4* s4 = reinterpret_cast<const uint4*>(
+                        reinterpret_cast<const __nv_bfloat16*>(a.x) + (size_t)m * a.K + (size_t)g * kGroup + 32 * t);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const uint4 u = s4[q];
@@ -365,28 +391,24 @@ gemv_kernel(const GemvArgs a) {
                             v[8 * q + 2 * e + 1] = __uint_as_float(uw[e] & 0xFFFF0000u);
                         }
                     }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0.0f;
                 }
-            } else {
+                float mx = 0.0f;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = 0.0f;
-            }
-            float mx = 0.0f;
+                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(v[e]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                E = stage_exponent(mx);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(v[e]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            // E with mx * 2^(E + 10) < 2^15: mx < 2^ex for ex = biased exponent - 126
-            const int be = (int)(__float_as_uint(mx) >> 23);   // mx >= 0
-            int E = 0;
-            if (mx > 0.0f && be < 255) E = max(-100, min(5 - (max(be, 1) - 126), 110));
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                // exact power of two 2^(E + 10 - 2j'), exponent within [-100, 120]
-                const float c = __uint_as_float((uint32_t)(E + 10 - 2 * (j < 6 ? j : j - 6) + 127) << 23);
-                const __half2 lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);       // k = 32t+j, +8
-                const __half2 hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c); // k = 32t+16+j, +24
-                b[nt][2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
-                b[nt][2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+                for (int j = 0; j < 8; ++j) {
+                    const float c = stage_multiplier(E, j);
+                    const __half2 lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);       // k = 32t+j, +8
+                    const __half2 hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c); // k = 32t+16+j, +24
+                    b[nt][2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
+                    b[nt][2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+                }
             }
             // the -1 correction: the same chain on the all-ones pattern; every row of
             // the result is the same, lane (gid, t) holds tokens 2t, 2t+1
@@ -626,22 +648,56 @@ gemv_kernel(const GemvArgs a) {
     }
 }
 
-// Rotation prologue for the fused path: xr (fp32 [M][K]) = H_4096 (s (.) x) / 64,
-// kept in fp32 (never rounded to bf16) for the product's staging.
+// Rotation prologue for the fused path: x' = H_4096 (s (.) x) / 64 in fp32,
+// staged for the product exactly as the product stages a bf16 x (per token and
+// group, E from the largest |x'| and fp16 x' 2^(E + 10 - 2j')), so x' is never
+// rounded to bf16.  The fragments are stored in the order the product's lanes
+// hold them: xs[m][g][t][r] (uint32, two halves), lane t's B register r; xe[m][g]
+// = E.  Thread i owns the block's values 16 i .. 16 i + 15: one half of lane
+// t's registers of one group.
 __global__ void __launch_bounds__(kFwhtThreads)
-rotate_f32_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restrict__ signs, float* __restrict__ xr,
-                  int K) {
+rotate_stage_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restrict__ signs,
+                    uint32_t* __restrict__ xs, int* __restrict__ xe, int K) {
     __shared__ float sm[kFwhtSmemFloats];
     pdl_launch_dependents();
     pdl_wait();
-    const int b = blockIdx.x, m = blockIdx.y;
-    const size_t off = (size_t)m * K + (size_t)b * kFwhtN;
-    fwht4096_block(x + off, signs + (size_t)b * kFwhtN, sm);
-    float4* out = reinterpret_cast<float4*>(xr + off);
-    for (int i = threadIdx.x; i < kFwhtN / 4; i += blockDim.x) {
-        const int e = 4 * i;
-        out[i] = make_float4(sm[fwht_pos(e)], sm[fwht_pos(e + 1)], sm[fwht_pos(e + 2)], sm[fwht_pos(e + 3)]);
+    const int blk = blockIdx.x, m = blockIdx.y, G = K / kGroup;
+    fwht4096_block(x + (size_t)m * K + (size_t)blk * kFwhtN, signs + (size_t)blk * kFwhtN, sm);
+    const int i = threadIdx.x;
+    float v[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = sm[fwht_pos(16 * i + e)];
+    float mx = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) mx = fmaxf(mx, fabsf(v[e]));
+    // the eight threads of a group are lanes 8c .. 8c + 7 of one warp
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    const int E = stage_exponent(mx);
+    const int g = blk * (kFwhtN / kGroup) + (i >> 3);
+    const int e0 = 16 * (i & 7);                    // first value within the group
+    const int t = e0 >> 5, half = (e0 >> 4) & 1;    // lane t; this thread forms its registers 2j + half
+    uint32_t r[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float c = stage_multiplier(E, j);
+        const __half2 h = __floats2half2_rn(v[j] * c, v[j + 8] * c);
+        r[j] = *reinterpret_cast<const uint32_t*>(&h);
     }
+    // the thread pair of lane t swaps halves so that each stores eight
+    // consecutive registers: half 0 registers 0-7, half 1 registers 8-15
+    uint32_t o[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, half ? r[q] : r[q + 4], 1);
+        o[2 * q] = half ? got : r[q];
+        o[2 * q + 1] = half ? r[q + 4] : got;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(xs + ((size_t)(m * G + g) * 4 + t) * 16 + 8 * half);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    if ((i & 7) == 0) xe[m * G + g] = E;
 }
 
 // ---------------------------------------------------------------------------
@@ -684,7 +740,7 @@ Plan base_plan(int M, int N, int K) {
 
 // Lets the kernel use the device's whole per-block shared memory; returns the
 // dynamic part it may take.
-template <int MT, bool XF32, bool ONE, bool LEAN>
+template <int MT, bool PRE, bool ONE, bool LEAN>
 cudaError_t kernel_smem_limit(int dev, int* limit) {
     static int optin_of[64] = {};
     if (!optin_of[dev]) {
@@ -692,10 +748,10 @@ cudaError_t kernel_smem_limit(int dev, int* limit) {
         cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return e;
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, gemv_kernel<MT, XF32, ONE, LEAN>);
+        e = cudaFuncGetAttributes(&fa, gemv_kernel<MT, PRE, ONE, LEAN>);
         if (e != cudaSuccess) return e;
         optin -= (int)fa.sharedSizeBytes;   // the kernel's static shared memory comes first
-        e = cudaFuncSetAttribute(gemv_kernel<MT, XF32, ONE, LEAN>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        e = cudaFuncSetAttribute(gemv_kernel<MT, PRE, ONE, LEAN>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (e != cudaSuccess) return e;
         optin_of[dev] = optin;
     }
@@ -705,10 +761,10 @@ cudaError_t kernel_smem_limit(int dev, int* limit) {
 
 // One wave: as many CTAs as fit at once, by registers (the launch bound) and
 // by shared memory (which grows with the range length).
-template <int MT, bool XF32, bool ONE, bool LEAN>
+template <int MT, bool PRE, bool ONE, bool LEAN>
 tern_status make_plan(int M, int N, int K, int sms, int dev, Plan* out) {
     int limit = 0;
-    if (kernel_smem_limit<MT, XF32, ONE, LEAN>(dev, &limit) != cudaSuccess) return TERN_ERR_CUDA;
+    if (kernel_smem_limit<MT, PRE, ONE, LEAN>(dev, &limit) != cudaSuccess) return TERN_ERR_CUDA;
     Plan p = base_plan(M, N, K);
     const int need = (p.T + kMaxTiles - 1) / kMaxTiles;   // ranges short enough for the shared partials
     int cps = 1;
@@ -728,7 +784,7 @@ tern_status make_plan(int M, int N, int K, int sms, int dev, Plan* out) {
 // Plans depend on the shape and the device only: keep the recent ones.
 struct PlanKey {
     int M, N, K, dev;
-    bool xf32;
+    bool pre;
 };
 std::mutex g_plan_mu;
 constexpr int kPlanCache = 64;
@@ -736,7 +792,7 @@ PlanKey g_plan_key[kPlanCache];
 Plan g_plan_val[kPlanCache];
 int g_plan_n = 0, g_plan_next = 0;
 
-template <int MT, bool XF32, bool ONE, bool LEAN>
+template <int MT, bool PRE, bool ONE, bool LEAN>
 tern_status cached_plan(int M, int N, int K, int sms, Plan* out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TERN_ERR_CUDA;
@@ -744,15 +800,15 @@ tern_status cached_plan(int M, int N, int K, int sms, Plan* out) {
     std::lock_guard<std::mutex> lk(g_plan_mu);
     for (int i = 0; i < g_plan_n; ++i) {
         const PlanKey& k = g_plan_key[i];
-        if (k.M == M && k.N == N && k.K == K && k.dev == dev && k.xf32 == XF32) {
+        if (k.M == M && k.N == N && k.K == K && k.dev == dev && k.pre == PRE) {
             *out = g_plan_val[i];
             return TERN_OK;
         }
     }
-    const tern_status st = make_plan<MT, XF32, ONE, LEAN>(M, N, K, sms, dev, out);
+    const tern_status st = make_plan<MT, PRE, ONE, LEAN>(M, N, K, sms, dev, out);
     if (st != TERN_OK) return st;
     const int slot = g_plan_n < kPlanCache ? g_plan_n++ : (g_plan_next++ % kPlanCache);
-    g_plan_key[slot] = PlanKey{M, N, K, dev, XF32};
+    g_plan_key[slot] = PlanKey{M, N, K, dev, PRE};
     g_plan_val[slot] = *out;
     return TERN_OK;
 }
@@ -775,13 +831,13 @@ size_t flag_bytes(int N, int K) {
 }
 size_t workspace_bytes(int M, int N, int K, bool rot) {
     if (M < 1 || M > 16 || N < 1 || K < kGroup || K % kGroup != 0) return 0;
-    return flag_bytes(N, K) + (rot ? align_up((size_t)M * K * 4, 256) : 0);
+    return flag_bytes(N, K) + (rot ? align_up((size_t)M * K * 2 + (size_t)M * (K / kGroup) * 4, 256) : 0);
 }
 
-template <int MT, bool XF32, bool ONE, bool LEAN = false>
+template <int MT, bool PRE, bool ONE, bool LEAN = false>
 tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
     Plan p;
-    const tern_status st = cached_plan<MT, XF32, ONE, LEAN>(args.M, args.N, args.K, sms, &p);
+    const tern_status st = cached_plan<MT, PRE, ONE, LEAN>(args.M, args.N, args.K, sms, &p);
     if (st != TERN_OK) return st;
     args.G = p.G;
     args.T = p.T;
@@ -792,7 +848,7 @@ tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
     args.off_sc = p.off_sc;
     args.off_part = p.off_part;
     const cudaError_t e =
-        launch_pdl(gemv_kernel<MT, XF32, ONE, LEAN>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, args);
+        launch_pdl(gemv_kernel<MT, PRE, ONE, LEAN>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, args);
     return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
 
@@ -820,11 +876,14 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
     const bool lean = (K / kGroup) % kWarps == 0;
     int launches = 1;
     if (signs) {
-        float* xr = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + fb);
-        const cudaError_t e = launch_pdl(rotate_f32_kernel, dim3(K / kFwhtN, M), dim3(kFwhtThreads), 0, stream,
-                                         true, reinterpret_cast<const __nv_bfloat16*>(x), signs, xr, K);
+        // staged x': M x K halves, then M x G exponents
+        uint32_t* xs = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(workspace) + fb);
+        int* xe = reinterpret_cast<int*>(xs + (size_t)M * K / 2);
+        const cudaError_t e = launch_pdl(rotate_stage_kernel, dim3(K / kFwhtN, M), dim3(kFwhtThreads), 0, stream,
+                                         true, reinterpret_cast<const __nv_bfloat16*>(x), signs, xs, xe, K);
         if (e != cudaSuccess) return TERN_ERR_CUDA;
-        args.x = xr;
+        args.x = xs;
+        args.xe = xe;
         launches = 2;
         st = M == 1 ? (lean ? launch_gemv<1, true, true, true>(args, sms, stream)
                             : launch_gemv<1, true, true>(args, sms, stream))

@@ -112,7 +112,8 @@ tern_status tern_validate_host(const uint32_t *codes, int N, int K, long long *b
  * input.  The size covers both calls (at least 256).  It holds one 32-bit flag
  * word per 16-row tile when K > 1024 (the K-slice sums of a row range are
  * added into y, and the flag orders the range's clearing before the additions)
- * and, for tern_fwht_gemm, the fp32 rotated activation (M * K * 4 bytes).
+ * and, for tern_fwht_gemm, the rotated activation as the product stages it
+ * (M * K fp16 values and one int32 exponent per token and 128-group).
  * The workspace must be zero-filled once before its first use; every call
  * leaves its flags at zero again.  Calls that share a workspace must not run
  * concurrently (use one stream, or one workspace per stream).  After a device
@@ -169,8 +170,10 @@ tern_status tern_fwht(const void *x, const int8_t *signs, void *y, int M, int K,
                       tern_stream_t stream);
 
 /* Rotation fused into the product: y (fp32 [M][N]) = rot(x) W^T.  A rotation
- * prologue kernel leaves the rotated activation in fp32 in the workspace
- * (L2-resident, never rounded to bf16) and the product stages it from there.
+ * prologue kernel computes the rotated activation in fp32 and stages it in the
+ * workspace (L2-resident) as the product stages any activation: per token and
+ * 128-group, fp16 values scaled by a power of two chosen from the group's
+ * largest magnitude.  It is never rounded to bf16.
  * 1 <= M <= 16, K % 4096 == 0; workspace as for tern_gemv (required). */
 tern_status tern_fwht_gemm(const void *x, const int8_t *signs, const uint32_t *codes,
                            const void *scales, float *y, int M, int N, int K,

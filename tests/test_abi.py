@@ -111,13 +111,14 @@ def test_argument_errors_never_launch(tern):
     assert lib.tern_gemv(P + 2, P, P, P, 1, 16, 128, P, 1 << 20, None) == 3
     assert lib.tern_fwht(P, P + 8, P, 1, 4096, None) == 3
     # workspace: flag words once K spans more than one 1024-wide slice, plus the
-    # rotated x for the fused call
+    # staged rotated x for the fused call
     need = tern.gemv_workspace_bytes(1, 16, 2048)
     assert need >= 256
     assert lib.tern_gemv(P, P, P, P, 1, 16, 2048, None, need, None) == 4
     assert lib.tern_gemv(P, P, P, P, 1, 16, 2048, P, need - 1, None) == 4
     assert lib.tern_fwht_gemm(P, P, P, P, P, 1, 16, 4096, None, 1 << 30, None) == 4
-    assert lib.tern_fwht_gemm(P, P, P, P, P, 2, 16, 4096, P, 2 * 4096 * 4 - 1, None) == 4
+    need = tern.gemv_workspace_bytes(2, 16, 4096)
+    assert lib.tern_fwht_gemm(P, P, P, P, P, 2, 16, 4096, P, need - 1, None) == 4
     assert tern.gemv_workspace_bytes(17, 16, 128) == 0
     assert lib.tern_gemm(P, P, P, P, 0, 64, 256, 512, None, 1 << 30, None) == 4
     need = tern.gemm_workspace_bytes(64, 256, 512)
@@ -129,12 +130,15 @@ def test_argument_errors_never_launch(tern):
     assert lib.tern_wait_selftest(tern.SELFTEST_MBARRIER, 1000001, None) == 2
 
 def test_workspace_sizes(tern):
-    # one flag word per 16-row tile once K > 1024 (256-byte aligned), then the
-    # fp32 rotated x for the fused call when K % 4096 == 0
-    assert tern.gemv_workspace_bytes(1, 17408, 5120) == (1088 * 4 + 255) // 256 * 256
+    # one flag word per 16-row tile once K > 1024 (256-byte aligned), then, for
+    # the fused call when K % 4096 == 0, the staged rotated x: M x K fp16 values
+    # and one int32 exponent per token and 128-group (256-byte aligned)
+    a256 = lambda v: (v + 255) // 256 * 256
+    assert tern.gemv_workspace_bytes(1, 17408, 5120) == a256(1088 * 4)
     assert tern.gemv_workspace_bytes(16, 10, 17408) == 256
-    assert tern.gemv_workspace_bytes(2, 12288, 4096) == 768 * 4 + 2 * 4096 * 4
-    assert tern.gemv_workspace_bytes(16, 12288, 8192) == 768 * 4 + 16 * 8192 * 4
+    assert tern.gemv_workspace_bytes(2, 12288, 4096) == a256(768 * 4) + a256(2 * 4096 * 2 + 2 * 32 * 4)
+    assert tern.gemv_workspace_bytes(16, 12288, 8192) == a256(768 * 4) + a256(16 * 8192 * 2 + 16 * 64 * 4)
+    assert tern.gemv_workspace_bytes(1, 16, 4096) == 256 + 256 * 33
     assert tern.gemv_workspace_bytes(1, 256, 512) == 256      # one slice: nothing needed
 
 
