@@ -341,6 +341,35 @@ def bench_verify(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int):
     return out
 
 
+def bench_verify_step(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int):
+    """One speculative-verify step as a CUDA graph: k + 1 = 5 tokens through
+    every layer's qkv (5120 -> 6144), gate, up (5120 -> 17408) and down
+    (17408 -> 5120) products, 64 layers, 256 launches.  The drafter and the
+    work between the products (attention, activations) are not part of it:
+    each product reads a fixed activation."""
+    import torch
+    import synth
+    M = synth.VERIFY_STEP_M
+    layers = len(sweep.layers)
+    x5 = synth.device_activations(6, "VS.x5120", (M, 5120))
+    x17 = synth.device_activations(6, "VS.x17408", (M, 17408))
+    ys = {N: torch.empty((M, N), dtype=torch.float32, device="cuda") for N in (6144, 17408, 5120)}
+    ws = tern.workspace(max(tern.gemv_workspace_bytes(M, N, K) for (K, N) in ((5120, 6144), (5120, 17408),
+                                                                              (17408, 5120))))
+
+    def run():
+        for l in range(layers):
+            tern.gemv(x5, qkv[l][0], qkv[l][1], y=ys[6144], ws=ws)
+            for (_, K, N, codes, s) in sweep.layers[l]:
+                tern.gemv(x5 if K == 5120 else x17, codes, s, y=ys[N], ws=ws)
+
+    g = graph_of(run)
+    ms = time_graph(g, max(3, steps // 10), warmup)
+    wb = layers * (weight_bytes(6144, 5120) + 2 * weight_bytes(17408, 5120) + weight_bytes(5120, 17408))
+    return {"M": M, "layers": layers, "launches": 4 * layers, "us_per_step": ms * 1e3,
+            "weight_GBps": wb / (ms * 1e-3) / 1e9, "tokens_per_s": M / (ms * 1e-3)}
+
+
 def bench_rotated(tern, steps: int, warmup: int, copies: int = 40):
     import torch
     import synth
@@ -542,6 +571,7 @@ def main() -> None:
     rows = {}
     if "verify" not in skip:
         rows["verify"] = bench_verify(tern, sweep, qkv, args.steps, args.warmup)
+        rows["verify_step"] = bench_verify_step(tern, sweep, qkv, args.steps, args.warmup)
     if "rotated" not in skip:
         rows["rotated"] = bench_rotated(tern, args.steps, args.warmup)
     if "prefill" not in skip:

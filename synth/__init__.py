@@ -113,6 +113,7 @@ def problem(seed: int, M: int, N: int, K: int, trit_dist: str = SPARSE40,
 TINY = dict(M=1, K=512, N=256, trit_dist=UNIFORM, scale_dist=SCALE_UNIFORM, seed=0)
 DECODE_SHAPES = [(5120, 17408), (17408, 5120)]          # (K, N): gate/up, down
 VERIFY_M = [1, 2, 4, 5, 8, 16]
+VERIFY_STEP_M = 5                                         # draft depth k = 4, plus one
 VERIFY_SHAPES = [(5120, 17408), (5120, 6144)]
 ROTATED = dict(K=4096, N=12288, M=(1, 16))
 PREFILL_M = 512

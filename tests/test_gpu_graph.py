@@ -1,0 +1,159 @@
+"""The products replayed from CUDA graphs, the way the benchmark runs them.
+
+A sequence of calls (programmatic dependent launch between consecutive
+kernels, one workspace shared by all of them) is captured once and replayed;
+the outputs are filled with NaN before the checked replay, so every element
+must be written by that replay.  Each product is compared with the oracle on
+sampled outputs at full size, within the tolerance of its kind:
+|y - y_ref| <= 1e-3 * sum_k |x w| + 1e-6 for the decode products, and the
+bf16-output bound 8e-3 * sum_k |x w| + 1e-6 for the prefill products.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests._util import assert_fp32_close, dev_bf16, dev_scales, dev_trits, host_codes
+
+pytestmark = pytest.mark.gpu
+
+BF16_REL = 8e-3
+
+
+@pytest.fixture(scope="module")
+def tern():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_gemv_gemm_gb300 import build
+    build.build()
+    import bit_gemv_gemm_gb300 as t
+    return t
+
+
+def capture(fn):
+    """Warm up on a side stream, then capture fn into a CUDA graph."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def sample(M, N, seed, n=1500):
+    rs = np.random.default_rng(seed)
+    ms, ns = rs.integers(0, M, n), rs.integers(0, N, n)
+    ms[:4], ns[:4] = M - 1, [0, N - 1, N - 2, N // 2]
+    return ms, ns
+
+
+def replay_and_check(tern, orc, g, probs, ys, rel=1e-3, what=""):
+    for _ in range(2):
+        g.replay()
+    for y in ys:
+        y.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    for i, ((p, codes), y) in enumerate(zip(probs, ys)):
+        ms, ns = sample(p.M, p.N, 77 + i)
+        y_ref, a_ref = orc.matmul_sampled(p.x, host_codes(codes), p.s, ms, ns)
+        got = y.to(torch.float64).cpu().numpy()[ms, ns]
+        assert_fp32_close(got, y_ref, a_ref, rel=rel, what=f"{what} product {i} ({p.M}x{p.N}x{p.K})")
+
+
+def test_verify_step_graph(tern, orc):
+    """Speculative verify: k + 1 = 5 tokens through two layers' qkv, gate,
+    up and down products, one graph."""
+    M = synth.VERIFY_STEP_M
+    shapes = [(5120, 6144), (5120, 17408), (5120, 17408), (17408, 5120)] * 2
+    probs = []
+    for i, (K, N) in enumerate(shapes):
+        p = synth.problem(1100 + i, M, N, K, tag=f"vs{i}")
+        probs.append((p, tern.pack(dev_trits(p.t))))
+    xs = [dev_bf16(p.x) for p, _ in probs]
+    ss = [dev_scales(p.s) for p, _ in probs]
+    ys = [torch.empty((M, p.N), dtype=torch.float32, device="cuda") for p, _ in probs]
+    ws = tern.workspace(max(tern.gemv_workspace_bytes(M, N, K) for K, N in shapes))
+
+    def run():
+        for i, (p, codes) in enumerate(probs):
+            tern.gemv(xs[i], codes, ss[i], y=ys[i], ws=ws)
+
+    replay_and_check(tern, orc, capture(run), probs, ys, what="verify step")
+
+
+def test_decode_sweep_graph(tern, orc):
+    """Single-token decode: two layers' gate, up and down products, one graph."""
+    shapes = [(5120, 17408), (5120, 17408), (17408, 5120)] * 2
+    probs = []
+    for i, (K, N) in enumerate(shapes):
+        p = synth.problem(1200 + i, 1, N, K, tag=f"ds{i}")
+        probs.append((p, tern.pack(dev_trits(p.t))))
+    xs = [dev_bf16(p.x) for p, _ in probs]
+    ss = [dev_scales(p.s) for p, _ in probs]
+    ys = [torch.empty((1, p.N), dtype=torch.float32, device="cuda") for p, _ in probs]
+    ws = tern.workspace(max(tern.gemv_workspace_bytes(1, N, K) for K, N in shapes))
+
+    def run():
+        for i, (p, codes) in enumerate(probs):
+            tern.gemv(xs[i], codes, ss[i], y=ys[i], ws=ws)
+
+    replay_and_check(tern, orc, capture(run), probs, ys, what="decode")
+
+
+def test_prefill_layer_graph(tern, orc):
+    """pp512: one layer's gate, up, qkv and down products (bf16 out), one graph;
+    the down product runs the stream-K schedule."""
+    M = synth.PREFILL_M
+    probs = []
+    for i, (name, K, N) in enumerate(synth.PREFILL_LAYER):
+        p = synth.problem(1300 + i, M, N, K, tag=f"pl{name}")
+        probs.append((p, tern.pack(dev_trits(p.t))))
+    xs = [dev_bf16(p.x) for p, _ in probs]
+    ss = [dev_scales(p.s) for p, _ in probs]
+    ys = [torch.empty((M, p.N), dtype=torch.bfloat16, device="cuda") for p, _ in probs]
+    ws = tern.workspace(max(tern.gemm_workspace_bytes(M, N, K) for _, K, N in synth.PREFILL_LAYER))
+
+    def run():
+        for i, (p, codes) in enumerate(probs):
+            tern.gemm(xs[i], codes, ss[i], y=ys[i], ws=ws)
+
+    replay_and_check(tern, orc, capture(run), probs, ys, rel=BF16_REL, what="prefill")
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_fused_rotation_graph(tern, orc, M):
+    """The rotated workload, two fused calls with different activations and
+    weights, one graph."""
+    K, N = synth.ROTATED["K"], synth.ROTATED["N"]
+    ps = [synth.problem(1400 + M + c, M, N, K, with_signs=True, tag=f"fr{c}") for c in range(2)]
+    codes = [tern.pack(dev_trits(p.t)) for p in ps]
+    xs = [dev_bf16(p.x) for p in ps]
+    ss = [dev_scales(p.s) for p in ps]
+    sg = [torch.from_numpy(p.signs).cuda() for p in ps]
+    ys = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in ps]
+    ws = tern.workspace(tern.gemv_workspace_bytes(M, N, K))
+
+    def run():
+        for c in range(2):
+            tern.fwht_gemm(xs[c], sg[c], codes[c], ss[c], y=ys[c], ws=ws)
+
+    g = capture(run)
+    for _ in range(2):
+        g.replay()
+    for y in ys:
+        y.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    rs = np.random.default_rng(M)
+    rows = np.unique(rs.integers(0, N, 384))
+    for c, p in enumerate(ps):
+        y_ref, a_ref = orc.rotate_matmul(p.x, p.signs, host_codes(codes[c])[rows], p.s[rows])
+        assert_fp32_close(ys[c].cpu().numpy()[:, rows], y_ref, a_ref, what=f"rotated graph M={M} call {c}")
