@@ -57,6 +57,10 @@ def _load():
                 "orc_unpack": (ctypes.c_longlong, [_P, _I, _I, _P]),
                 "orc_matmul": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _I]),
                 "orc_matmul_sampled": (_I, [_P, _P, _P, _I, _P, _P, _I, _P, _P, _I]),
+                "orc_bin_pack": (ctypes.c_longlong, [_P, _I, _I, _P]),
+                "orc_bin_unpack": (_I, [_P, _I, _I, _P]),
+                "orc_bin_matmul": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _I]),
+                "orc_bin_matmul_sampled": (_I, [_P, _P, _P, _I, _P, _P, _I, _P, _P, _I]),
                 "orc_mlx_affine": (ctypes.c_float, [_I, ctypes.c_float, ctypes.c_float]),
                 "orc_hadamard_explicit": (_I, [_I, _P]),
                 "orc_fwht": (_I, [_P, _I]),
@@ -113,6 +117,61 @@ def unpack(codes: np.ndarray, K: int) -> tuple[np.ndarray, int]:
     if bad < 0:
         raise ValueError("K must be a multiple of 16")
     return t, int(bad)
+
+
+def bin_pack(t: np.ndarray) -> tuple[np.ndarray, int]:
+    """The 1-bit sibling: t int8 [N, K] in {-1, +1} -> (words uint32 [N, K/32],
+    count of entries that are not +-1)."""
+    t = _c(t, np.int8)
+    N, K = t.shape
+    words = np.empty((N, K // 32), dtype=np.uint32)
+    bad = _load().orc_bin_pack(_ptr(t), N, K, _ptr(words))
+    if bad < 0:
+        raise ValueError("K must be a multiple of 32")
+    return words, int(bad)
+
+
+def bin_unpack(words: np.ndarray, K: int) -> np.ndarray:
+    """words uint32 [N, K/32] -> t int8 [N, K] = 2b - 1."""
+    words = _c(words, np.uint32)
+    N = words.shape[0]
+    t = np.empty((N, K), dtype=np.int8)
+    if _load().orc_bin_unpack(_ptr(words), N, K, _ptr(t)) != 0:
+        raise ValueError("K must be a multiple of 32")
+    return t
+
+
+def bin_matmul(x_bf16: np.ndarray, words: np.ndarray, scales_f16: np.ndarray,
+               nthreads: int = 0) -> tuple[np.ndarray, np.ndarray]:
+    """y[m, n] = sum_k x[m, k] (2 b[n, k] - 1) s[n, k // 128] in double, and the
+    error scale a = sum_k |x w|; returns (y, a)."""
+    x = _bits16(x_bf16)
+    s = _bits16(scales_f16)
+    words = _c(words, np.uint32)
+    M, K = x.shape
+    N = words.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    a = np.empty((M, N), dtype=np.float64)
+    if _load().orc_bin_matmul(_ptr(x), _ptr(words), _ptr(s), M, N, K, _ptr(y), _ptr(a), nthreads) != 0:
+        raise ValueError("bad shape")
+    return y, a
+
+
+def bin_matmul_sampled(x_bf16: np.ndarray, words: np.ndarray, scales_f16: np.ndarray,
+                       ms: np.ndarray, ns: np.ndarray, nthreads: int = 0):
+    """The binary product at outputs (ms[i], ns[i]) only; returns (y, a)."""
+    x = _bits16(x_bf16)
+    s = _bits16(scales_f16)
+    words = _c(words, np.uint32)
+    K = x.shape[1]
+    ms = _c(ms, np.int32)
+    ns = _c(ns, np.int32)
+    y = np.empty(len(ms), dtype=np.float64)
+    a = np.empty(len(ms), dtype=np.float64)
+    if _load().orc_bin_matmul_sampled(_ptr(x), _ptr(words), _ptr(s), K, _ptr(ms), _ptr(ns), len(ms),
+                                      _ptr(y), _ptr(a), nthreads) != 0:
+        raise ValueError("bad shape")
+    return y, a
 
 
 def _bits16(a: np.ndarray) -> np.ndarray:

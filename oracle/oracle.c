@@ -29,6 +29,14 @@
  *     H[i][j] = (-1)^popcount(i & j), and s an explicit +-1 sign vector
  *     ([post] section 3).  The inverse is x = s (.) (H_B x' / sqrt(B)).
  *
+ *   - The 1-bit sibling ("binary g128"): the card names it at 1.125 bits per
+ *     weight ([card] "Highlights" and "Benchmarks"), one bit per weight
+ *     plus the same FP16 scale per 128.  The card's MLX packing (s_mlx = 2 s_g,
+ *     bias = -s_g, [card] "MLX packaging") reproduces exactly +-s_g from a
+ *     bit b in {0, 1}, so a weight is (2b - 1) * s_g.  Reading for the unstated
+ *     order, as for the ternary codes: bit k%32 of little-endian uint32 word
+ *     k/32 of the row.
+ *
  * Parity pins live in the "not gpu" tests: brute-force dense matmul from an
  * explicitly expanded W, exhaustive pack/unpack patterns, the explicit
  * Hadamard matrix for n <= 64, H*H = n*I, Parseval, closed forms on e_0 and
@@ -225,6 +233,111 @@ int orc_matmul_sampled(const uint16_t *x, const uint32_t *codes,
             a[i] = aa;
     }
     return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The 1-bit sibling: b in {0, 1}, w = (2b - 1) * s_g, 32 bits per uint32.   */
+/* ------------------------------------------------------------------------ */
+
+/* Packs t[N][K] in {-1, +1} into words[N][K/32]: bit k%32 of word k/32 is 1
+ * for t = +1.  Any other entry is counted and stored as 0 (t = -1).  Returns
+ * the count, or -1 if K is not a multiple of 32. */
+long long orc_bin_pack(const int8_t *t, int N, int K, uint32_t *words)
+{
+    if (N < 0 || K < 0 || K % 32 != 0)
+        return -1;
+    long long bad = 0;
+    int W = K / 32;
+    for (int n = 0; n < N; ++n)
+        for (int w = 0; w < W; ++w) {
+            uint32_t word = 0;
+            for (int i = 0; i < 32; ++i) {
+                int v = t[(size_t)n * K + (size_t)w * 32 + i];
+                if (v == 1)
+                    word |= 1u << i;
+                else if (v != -1)
+                    ++bad;
+            }
+            words[(size_t)n * W + w] = word;
+        }
+    return bad;
+}
+
+/* One bit, read straight from the layout. */
+static int orc_bit(const uint32_t *words, int K, int n, int k)
+{
+    return (int)((words[(size_t)n * (K / 32) + k / 32] >> (k % 32)) & 1u);
+}
+
+/* Unpacks words[N][K/32] into t[N][K] = 2b - 1.  Returns 0, or -1 on a bad K. */
+int orc_bin_unpack(const uint32_t *words, int N, int K, int8_t *t)
+{
+    if (N < 0 || K < 0 || K % 32 != 0)
+        return -1;
+    for (int n = 0; n < N; ++n)
+        for (int k = 0; k < K; ++k)
+            t[(size_t)n * K + k] = (int8_t)(2 * orc_bit(words, K, n, k) - 1);
+    return 0;
+}
+
+/* One output of the binary product: y = sum_k x[m][k] (2b[n][k] - 1) s[n][k/128]
+ * and a = sum_k |x[m][k] w[n][k]|. */
+static void orc_bin_dot(const uint16_t *x, const uint32_t *words,
+                        const uint16_t *scales, int K, int m, int n,
+                        double *y, double *a)
+{
+    int G = K / 128;
+    double acc = 0.0, mag = 0.0;
+    for (int k = 0; k < K; ++k) {
+        double w = (double)(2 * orc_bit(words, K, n, k) - 1) *
+                   orc_f16_to_f64(scales[(size_t)n * G + k / 128]);
+        double p = orc_bf16_to_f64(x[(size_t)m * K + k]) * w;
+        acc += p;
+        mag += fabs(p);
+    }
+    *y = acc;
+    if (a)
+        *a = mag;
+}
+
+/* y[M][N] (and a[M][N] if a != NULL) for x bf16 [M][K], words [N][K/32],
+ * scales fp16 [N][K/128].  Returns 0, or -2 for a bad shape. */
+int orc_bin_matmul(const uint16_t *x, const uint32_t *words, const uint16_t *scales,
+                   int M, int N, int K, double *y, double *a, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || K % 128 != 0)
+        return -2;
+    orc_set_threads(nthreads);
+    long long total = (long long)M * N;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (long long i = 0; i < total; ++i) {
+        double yy, aa;
+        orc_bin_dot(x, words, scales, K, (int)(i / N), (int)(i % N), &yy, &aa);
+        y[i] = yy;
+        if (a)
+            a[i] = aa;
+    }
+    return 0;
+}
+
+/* The binary product at chosen outputs only: (ms[i], ns[i]) for i < count. */
+int orc_bin_matmul_sampled(const uint16_t *x, const uint32_t *words,
+                           const uint16_t *scales, int K, const int *ms,
+                           const int *ns, int count, double *y, double *a,
+                           int nthreads)
+{
+    if (K < 0 || K % 128 != 0)
+        return -2;
+    orc_set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int i = 0; i < count; ++i) {
+        double yy, aa;
+        orc_bin_dot(x, words, scales, K, ms[i], ns[i], &yy, &aa);
+        y[i] = yy;
+        if (a)
+            a[i] = aa;
+    }
+    return 0;
 }
 
 /* ------------------------------------------------------------------------ */

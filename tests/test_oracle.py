@@ -370,3 +370,128 @@ def test_rotate_matmul_bruteforce(orc):
     W = dense_w(p.t, p.s)
     assert np.allclose(y, xr @ W.T, rtol=1e-10, atol=1e-10)
     assert np.allclose(a, np.abs(xr) @ np.abs(W).T, rtol=1e-10)
+
+
+# --------------------------------------------------------------------------
+# the 1-bit sibling (binary g128): w = (2b - 1) s_g, bit k%32 of word k/32
+# --------------------------------------------------------------------------
+
+def binary_trits(seed: int, name: str, shape) -> np.ndarray:
+    return np.where(synth.trits(seed, name, shape, synth.UNIFORM) >= 0, 1, -1).astype(np.int8)
+
+
+def test_bin_pack_golden_words(orc):
+    rows = []
+    with open(os.path.join(GOLDEN, "bin_pack_examples.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            parts = line.split()
+            rows.append(([int(v) for v in parts[:32]], int(parts[32], 16)))
+    assert len(rows) >= 8
+    t = np.array([r[0] for r in rows], dtype=np.int8)
+    words, bad = orc.bin_pack(t)
+    assert bad == 0
+    assert [int(w) for w in words[:, 0]] == [r[1] for r in rows]
+    assert np.array_equal(orc.bin_unpack(words, 32), t)
+
+
+def test_bin_pack_every_position_and_roundtrip(orc):
+    """A single +1 at any position k of a row sets bit k % 32 of word k / 32
+    only; random rows survive the round trip."""
+    K = 128
+    for k in range(K):
+        t = -np.ones((1, K), dtype=np.int8)
+        t[0, k] = 1
+        words, bad = orc.bin_pack(t)
+        want = np.zeros(K // 32, dtype=np.uint32)
+        want[k // 32] = np.uint32(1) << np.uint32(k % 32)
+        assert bad == 0 and np.array_equal(words[0], want), k
+    t = binary_trits(21, "rt", (37, 2048))
+    words, bad = orc.bin_pack(t)
+    assert bad == 0
+    assert np.array_equal(orc.bin_unpack(words, 2048), t)
+
+
+def test_bin_pack_invalid_values_counted(orc):
+    t = np.array([[1, -1, 0, 2] + [1] * 28], dtype=np.int8)
+    words, bad = orc.bin_pack(t)
+    assert bad == 2
+    # invalid entries are stored as -1 (bit 0)
+    assert int(words[0, 0]) == (0xFFFFFFFF & ~0b1110)
+
+
+def test_bin_packed_size_and_bitrate(orc):
+    g = json.load(open(os.path.join(GOLDEN, "bitrates.json")))
+    N, K = 48, 1024
+    words, _ = orc.bin_pack(binary_trits(22, "sz", (N, K)))
+    s = synth.scales(22, "s", (N, K // 128))
+    nbytes = words.nbytes + s.nbytes
+    assert nbytes == N * K // 8 + N * K // 64
+    assert 8.0 * nbytes / (N * K) == g["binary_bpw"]["value"]   # 1 + 16/128, exact
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 128), (1, 8, 128), (4, 8, 256), (3, 5, 384), (2, 40, 1024)])
+def test_bin_matmul_matches_dense_bruteforce(orc, M, N, K):
+    t = binary_trits(30 + N, "bf", (N, K))
+    s = synth.scales(30 + N, "s", (N, K // 128))
+    x = synth.activations(30 + N, "x", (M, K))
+    words, _ = orc.bin_pack(t)
+    y, a = orc.bin_matmul(x, words, s)
+    xf = bf16_bits_to_f64(x)
+    W = dense_w(t, s)
+    assert np.allclose(y, xf @ W.T, rtol=1e-12, atol=1e-12)
+    assert np.allclose(a, np.abs(xf) @ np.abs(W).T, rtol=1e-12, atol=1e-12)
+
+
+def test_bin_matmul_equals_ternary_oracle_on_pm1(orc):
+    """On weights in {-1, +1} the binary product is the ternary product of the
+    same trits, through the ternary packing and the ternary dot product."""
+    M, N, K = 3, 17, 640
+    t = binary_trits(31, "tt", (N, K))
+    s = synth.scales(31, "s", (N, K // 128))
+    x = synth.activations(31, "x", (M, K))
+    yb, ab = orc.bin_matmul(x, orc.bin_pack(t)[0], s)
+    yt, at = orc.matmul(x, orc.pack(t)[0], s)
+    assert np.array_equal(yb, yt) and np.array_equal(ab, at)
+
+
+def test_bin_matmul_closed_forms(orc):
+    """All weights +1: y = sum_g s_g sum_{k in g} x_k; flipping every sign
+    negates y; a one-hot x picks +-s of one column; powers of two scale y
+    exactly."""
+    M, N, K = 2, 6, 384
+    s = synth.scales(32, "s", (N, K // 128))
+    x = synth.activations(32, "x", (M, K))
+    ones = np.ones((N, K), dtype=np.int8)
+    y, _ = orc.bin_matmul(x, orc.bin_pack(ones)[0], s)
+    xf = bf16_bits_to_f64(x).reshape(M, K // 128, 128).sum(-1)      # exact sums of bf16 values
+    assert np.array_equal(y, xf @ s.astype(np.float64).T)
+    ym, _ = orc.bin_matmul(x, orc.bin_pack(-ones)[0], s)
+    assert np.array_equal(ym, -y)
+    t = binary_trits(33, "oh", (N, K))
+    words = orc.bin_pack(t)[0]
+    ks = [0, 31, 32, 127, 128, 383]
+    xo = np.zeros((len(ks), K), dtype=np.uint16)
+    for i, k in enumerate(ks):
+        xo[i, k] = 0x3F80
+    yo, _ = orc.bin_matmul(xo, words, s)
+    W = dense_w(t, s)
+    for i, k in enumerate(ks):
+        assert np.array_equal(yo[i], W[:, k])
+    y1, _ = orc.bin_matmul(x, words, s)
+    y2, _ = orc.bin_matmul(x, words, (s.astype(np.float32) * 4).astype(np.float16))
+    assert np.array_equal(y2, 4 * y1)
+
+
+def test_bin_matmul_sampled_equals_full(orc):
+    M, N, K = 3, 29, 512
+    t = binary_trits(34, "sm", (N, K))
+    s = synth.scales(34, "s", (N, K // 128))
+    x = synth.activations(34, "x", (M, K))
+    words = orc.bin_pack(t)[0]
+    y, a = orc.bin_matmul(x, words, s)
+    ms = np.repeat(np.arange(M), N)
+    ns = np.tile(np.arange(N), M)
+    ys, as_ = orc.bin_matmul_sampled(x, words, s, ms, ns)
+    assert np.array_equal(ys, y.reshape(-1)) and np.array_equal(as_, a.reshape(-1))
