@@ -370,6 +370,36 @@ def bench_verify_step(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int):
             "weight_GBps": wb / (ms * 1e-3) / 1e9, "tokens_per_s": M / (ms * 1e-3)}
 
 
+def bench_binary(tern, steps: int, warmup: int, hbm: float, copies: int = 16):
+    """The 1-bit sibling format at M = 1: per decode shape, `copies` distinct
+    matrices (more bytes than L2) called back to back in one graph."""
+    import torch
+    import synth
+    out = []
+    for (K, N) in synth.DECODE_SHAPES:
+        mats = []
+        for c in range(copies):
+            t = synth.device_binary(7, f"B{c}.{K}.t", (N, K))
+            mats.append((tern.bin_pack(t), synth.device_scales(7, f"B{c}.{K}.s", (N, K // 128))))
+            del t
+        xs = [synth.device_activations(7, f"B{c}.{K}.x", (1, K)) for c in range(copies)]
+        y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+        ws = tern.workspace(tern.gemv_workspace_bytes(1, N, K))
+
+        def run():
+            for c in range(copies):
+                tern.bin_gemv(xs[c], mats[c][0], mats[c][1], y=y, ws=ws)
+
+        g = graph_of(run)
+        ms = time_graph(g, max(3, steps // 4), warmup)
+        per = ms / copies * 1e-3
+        wb = N * K // 8 + N * K // 64
+        out.append({"M": 1, "K": K, "N": N, "us": per * 1e6, "weight_bytes": wb,
+                    "weight_GBps": wb / per / 1e9, "hbm_frac": wb / per / 1e9 / hbm})
+        del mats
+    return out
+
+
 def bench_rotated(tern, steps: int, warmup: int, copies: int = 40):
     import torch
     import synth
@@ -538,7 +568,7 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=DECODE_LAYERS)
-    ap.add_argument("--skip", default="", help="comma list of parts to skip: verify,rotated,prefill,cpu")
+    ap.add_argument("--skip", default="", help="comma list of parts to skip: verify,rotated,binary,prefill,cpu")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -574,6 +604,8 @@ def main() -> None:
         rows["verify_step"] = bench_verify_step(tern, sweep, qkv, args.steps, args.warmup)
     if "rotated" not in skip:
         rows["rotated"] = bench_rotated(tern, args.steps, args.warmup)
+    if "binary" not in skip:
+        rows["binary"] = bench_binary(tern, args.steps, args.warmup, hbm)
     if "prefill" not in skip:
         rows["pp512"] = bench_prefill(tern, sweep, qkv, args.steps, args.warmup, peaks, dev_index)
 

@@ -48,6 +48,11 @@ EXPORTS = {
     "tern_last_launch_count": (_I, []),
     "tern_gemv_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "tern_wait_selftest": (_I, [_I, _I, _P]),
+    "tern_bin_packed_bytes": (_SZ, [_I, _I]),
+    "tern_bin_pack": (_I, [_P, _I, _I, _P, _P, _P]),
+    "tern_bin_pack_host": (_I, [_P, _I, _I, _P, _P]),
+    "tern_bin_unpack_host": (_I, [_P, _I, _I, _P]),
+    "tern_bin_gemv": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
 }
 
 
@@ -136,6 +141,37 @@ def pack(t: torch.Tensor, codes: torch.Tensor | None = None, bad_count: torch.Te
     return codes
 
 
+def bin_pack(t: torch.Tensor, words: torch.Tensor | None = None, bad_count: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    """Device packer of the 1-bit format: int8 [N, K] in {-1, +1} -> uint32
+    words [N, K/32] (as int32 storage), bit k%32 of word k/32 set for +1."""
+    N, K = t.shape
+    if words is None:
+        words = torch.empty((N, K // 32), dtype=torch.int32, device=t.device)
+    bp = _dev(bad_count, torch.int32, "bad_count") if bad_count is not None else None
+    _check("tern_bin_pack", lib().tern_bin_pack(_dev(t, torch.int8, "t"), N, K, _dev(words, torch.int32, "words"),
+                                                bp, _stream(stream)))
+    return words
+
+
+def bin_pack_host(t: np.ndarray) -> tuple[np.ndarray, int]:
+    t = np.ascontiguousarray(t, dtype=np.int8)
+    N, K = t.shape
+    words = np.empty((N, K // 32), dtype=np.uint32)
+    bad = ctypes.c_longlong(0)
+    _check("tern_bin_pack_host", lib().tern_bin_pack_host(t.ctypes.data, N, K, words.ctypes.data,
+                                                          ctypes.byref(bad)))
+    return words, int(bad.value)
+
+
+def bin_unpack_host(words: np.ndarray, K: int) -> np.ndarray:
+    words = np.ascontiguousarray(words, dtype=np.uint32)
+    N = words.shape[0]
+    t = np.empty((N, K), dtype=np.int8)
+    _check("tern_bin_unpack_host", lib().tern_bin_unpack_host(words.ctypes.data, N, K, t.ctypes.data))
+    return t
+
+
 def pack_host(t: np.ndarray) -> tuple[np.ndarray, int]:
     t = np.ascontiguousarray(t, dtype=np.int8)
     N, K = t.shape
@@ -176,6 +212,22 @@ def gemv(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y: torch.Te
         ws = workspace(gemv_workspace_bytes(M, N, K), x.device)
     _check("tern_gemv", lib().tern_gemv(
         _dev(x, torch.bfloat16, "x"), _dev(codes, torch.int32, "codes"), _dev(scales, torch.float16, "scales"),
+        _dev(y, torch.float32, "y"), M, N, K, _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return y
+
+
+def bin_gemv(x: torch.Tensor, words: torch.Tensor, scales: torch.Tensor, y: torch.Tensor | None = None,
+             ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The 1-bit sibling: y (fp32 [M, N]) = x W^T for M = 1..16, W = (2b - 1) s;
+    x bf16 [M, K], words int32 [N, K/32], scales fp16 [N, K/128]."""
+    M, K = x.shape
+    N = words.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(gemv_workspace_bytes(M, N, K), x.device)
+    _check("tern_bin_gemv", lib().tern_bin_gemv(
+        _dev(x, torch.bfloat16, "x"), _dev(words, torch.int32, "words"), _dev(scales, torch.float16, "scales"),
         _dev(y, torch.float32, "y"), M, N, K, _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
     return y
 

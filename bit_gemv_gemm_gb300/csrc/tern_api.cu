@@ -136,6 +136,41 @@ tern_status tern_unpack_host(const uint32_t* codes, int N, int K, int8_t* t, lon
     return TERN_OK;
 }
 
+// The 1-bit sibling: bit k%32 of word k/32 is 1 for +1; anything but +-1 is
+// counted and stored as -1.
+tern_status tern_bin_pack_host(const int8_t* t, int N, int K, uint32_t* words, long long* bad_count) {
+    if (N < 0 || K < 0 || K % 32 != 0) return TERN_ERR_SHAPE;
+    if ((N > 0 && K > 0) && (!t || !words)) return TERN_ERR_NULL;
+    long long bad = 0;
+    const size_t nwords = (size_t)N * (size_t)(K / 32);
+    for (size_t w = 0; w < nwords; ++w) {
+        const int8_t* src = t + w * 32;
+        uint32_t word = 0;
+        for (int i = 0; i < 32; ++i) {
+            const int v = src[i];
+            bad += (v != 1 && v != -1);
+            word |= (v == 1 ? 1u : 0u) << i;
+        }
+        words[w] = word;
+    }
+    if (bad_count) *bad_count = bad;
+    return TERN_OK;
+}
+
+tern_status tern_bin_unpack_host(const uint32_t* words, int N, int K, int8_t* t) {
+    if (N < 0 || K < 0 || K % 32 != 0) return TERN_ERR_SHAPE;
+    if ((N > 0 && K > 0) && (!t || !words)) return TERN_ERR_NULL;
+    const size_t nwords = (size_t)N * (size_t)(K / 32);
+    for (size_t w = 0; w < nwords; ++w)
+        for (int i = 0; i < 32; ++i) t[w * 32 + i] = ((words[w] >> i) & 1u) ? (int8_t)1 : (int8_t)-1;
+    return TERN_OK;
+}
+
+size_t tern_bin_packed_bytes(int N, int K) {
+    if (N < 0 || K < 0 || K % 128 != 0) return 0;
+    return (size_t)N * (size_t)K / 8 + (size_t)N * (size_t)K / 64;
+}
+
 tern_status tern_validate_host(const uint32_t* codes, int N, int K, long long* bad_count) {
     if (N < 0 || K < 0 || K % 16 != 0) return TERN_ERR_SHAPE;
     if ((N > 0 && K > 0) && !codes) return TERN_ERR_NULL;

@@ -68,6 +68,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kDepth = 4;              // units (tile x group) in flight per warp (even)
 constexpr int kEarly = 4;              // of which issued before the PDL wait, the rest after staging
 constexpr int kSlotBytes = 16 * 32;    // one unit: 16 rows x 32 B of codes
+constexpr int kBinSlotBytes = 16 * 16; // one unit of the 1-bit layout: 16 rows x 16 B
 constexpr int kMaxTiles = 32;          // tiles per range (bounds partials and scales in shared memory)
 constexpr int kPrivateMaxM = 4;        // private per-warp partials up to this many tokens
 constexpr size_t kSmemPerSm = 228 * 1024;   // shared memory of one SM
@@ -171,10 +172,53 @@ __device__ __forceinline__ void pair_mmas(float (&acc)[2][MT][4], const uint32_t
     }
 }
 
+// ---- the 1-bit sibling: bit k%32 of a word is weight k, w = (2b - 1) s ----
+// Slot s (0..15) of a word as an fp16 pair: bits s and s + 16 read as
+// b * 2^(s' - 24), s' = s for s <= 11 (mantissa, or the low exponent bits for
+// 10 and 11), s - 12 for the rest (read after a shift by 12).
+__device__ __forceinline__ uint32_t bin_slot(uint32_t w, uint32_t w12, int s) {
+    return s < 12 ? (w & (0x00010001u << s)) : (w12 & (0x00010001u << (s - 12)));
+}
+// One unit's chain for one token tile from this lane's two words (rows gid
+// and gid + 8, word t of the group): MMA j takes slots j and j + 8.
+__device__ __forceinline__ void bin_chain1(float (&acc)[4], uint32_t w0, uint32_t w1, const uint32_t (&b)[16]) {
+    const uint32_t u0 = w0 >> 12, u1 = w1 >> 12;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        mma16816(acc, bin_slot(w0, u0, j), bin_slot(w1, u1, j), bin_slot(w0, u0, j + 8), bin_slot(w1, u1, j + 8),
+                 b[2 * j], b[2 * j + 1], j > 0);
+}
+template <int MT>
+__device__ __forceinline__ void bin_pair_mmas(float (&acc)[2][MT][4], const uint32_t (&w)[2][2],
+                                              const uint32_t (&b)[MT][16]) {
+    uint32_t u[2][2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        u[q][0] = w[q][0] >> 12;
+        u[q][1] = w[q][1] >> 12;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int nt = 0; nt < MT; ++nt)
+                mma16816(acc[q][nt], bin_slot(w[q][0], u[q][0], j), bin_slot(w[q][1], u[q][1], j),
+                         bin_slot(w[q][0], u[q][0], j + 8), bin_slot(w[q][1], u[q][1], j + 8), b[nt][2 * j],
+                         b[nt][2 * j + 1], j > 0);
+}
+// the exact power of two 2^(E + 10 - s') for slot s of the 1-bit layout
+__device__ __forceinline__ float bin_stage_multiplier(int E, int s) {
+    return __uint_as_float((uint32_t)(E + 10 - (s < 12 ? s : s - 12) + 127) << 23);
+}
+
 // ---- asynchronous copies (cp.async) ----
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
                  : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0)
@@ -212,18 +256,23 @@ __host__ __device__ inline int scale_width(int G, int gA, int gB) {
 // ONE: the single-token case (M = 1), whose epilogue keeps one value per row.
 // LEAN (when G is a multiple of 8): every warp has exactly one group over its
 // CTA's whole range, and only the lean loop is compiled.
-template <int MT, bool PRE, bool ONE, bool LEAN = false>
+// BIN: the 1-bit sibling format (lean loop only): slice sigma is groups
+// 8 sigma .. 8 sigma + 7, and a warp whose group is past G has no units.
+template <int MT, bool PRE, bool ONE, bool LEAN = false, bool BIN = false>
 __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kCtasPerSm)
 gemv_kernel(const GemvArgs a) {
+    static_assert(!BIN || (LEAN && !PRE), "the 1-bit layout runs the lean loop on bf16 activations");
     constexpr int MP = 8 * MT;
+    constexpr int SLOT = BIN ? kBinSlotBytes : kSlotBytes;
     extern __shared__ __align__(16) unsigned char smem[];
     const int M = ONE ? 1 : a.M;
     const int N = a.N, G = a.G, S = a.S, rmax = a.rmax, gpad = a.gpad;
-    const int W = a.K / 16;
+    const int W = a.K / (BIN ? 32 : 16);   // code words per row
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, t = lane & 3;
     const int sigma = blockIdx.x / a.cps, clu = blockIdx.x - sigma * a.cps;   // slice, range
-    const int gA = (int)((long long)G * sigma / S), gB = (int)((long long)G * (sigma + 1) / S);
+    const int gA = BIN ? kWarps * sigma : (int)((long long)G * sigma / S);
+    const int gB = BIN ? min(gA + kWarps, G) : (int)((long long)G * (sigma + 1) / S);
     const int Gs = gB - gA;
     const int tile_lo = (int)((long long)a.T * clu / a.cps);
     const int R = (int)((long long)a.T * (clu + 1) / a.cps) - tile_lo;
@@ -242,7 +291,7 @@ gemv_kernel(const GemvArgs a) {
 
     // ---- this warp's ring: unit u in slot u mod kDepth; lane l copies row l/2,
     // 16-byte half l%2 of the unit's 32 bytes ----
-    unsigned char* ring = smem + (size_t)warp * kDepth * kSlotBytes;
+    unsigned char* ring = smem + (size_t)warp * kDepth * SLOT;
     const uint32_t ring_s = smem_addr(ring) + (uint32_t)lane * 16u;
     const int crow = lane >> 1;
     const size_t cstep = (size_t)16 * W;   // words from one tile to the next
@@ -305,8 +354,27 @@ gemv_kernel(const GemvArgs a) {
         }
         cp_async_commit();
     }
+    // the lean loop's refill: unit u of the warp's group is tile u of the range
+    // (rows past N read row N - 1; their sums are never written to y).  Lane l
+    // copies row l / 2, half l % 2 of the unit's 32 (2-bit) or 16 (1-bit) bytes.
+    const int lean_g = gA + warp;
+    const bool lean_has = !BIN || lean_g < gB;
+    const uint32_t* src_base = a.codes + (size_t)lean_g * (BIN ? 4 : 8) + (lane & 1) * (BIN ? 2 : 4);
+    const int crow0 = tile_lo * 16 + crow;
+    const uint32_t ring_lane = smem_addr(ring) + (uint32_t)lane * (BIN ? 8u : 16u);
+    auto refill = [&](int u, int slot_) {
+        if (lean_has && u < R) {
+            const int r = min(crow0 + 16 * u, N - 1);
+            if (BIN) cp_async8(ring_lane + (uint32_t)(slot_ * SLOT), src_base + (size_t)r * W);
+            else cp_async16(ring_lane + (uint32_t)(slot_ * SLOT), src_base + (size_t)r * W, true);
+        }
+        cp_async_commit();
+    };
 #pragma unroll
-    for (int i = 0; i < kEarly; ++i) issue(i);
+    for (int i = 0; i < kEarly; ++i) {
+        if (BIN) refill(i, i);
+        else issue(i);
+    }
     pdl_wait();
     // y of the range starts at zero: the slice-0 CTA clears it (after the PDL
     // wait, since the previous kernel may still read y) and counts itself into
@@ -403,22 +471,36 @@ gemv_kernel(const GemvArgs a) {
                 E = stage_exponent(mx);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float c = stage_multiplier(E, j);
-                    const __half2 lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);       // k = 32t+j, +8
-                    const __half2 hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c); // k = 32t+16+j, +24
+                    __half2 lo, hi;
+                    if (BIN) {
+                        // MMA j takes slots j (k = 32t+j, +16) and j + 8 (k = 32t+j+8, +24)
+                        const float c0 = bin_stage_multiplier(E, j), c1 = bin_stage_multiplier(E, j + 8);
+                        lo = __floats2half2_rn(v[j] * c0, v[j + 16] * c0);
+                        hi = __floats2half2_rn(v[j + 8] * c1, v[j + 24] * c1);
+                    } else {
+                        const float c = stage_multiplier(E, j);
+                        lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);       // k = 32t+j, +8
+                        hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c); // k = 32t+16+j, +24
+                    }
                     b[nt][2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
                     b[nt][2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
                 }
             }
             // the -1 correction: the same chain on the all-ones pattern; every row of
             // the result is the same, lane (gid, t) holds tokens 2t, 2t+1
+            // (the 1-bit layout: w = (2b - 1) s, so y = s F (2 acc - acc1))
             float acc1[4];
-            const uint32_t ones[4] = {0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u};
-            mma_chain1(acc1, ones, b[nt]);
+            if (BIN) {
+                bin_chain1(acc1, 0xFFFFFFFFu, 0xFFFFFFFFu, b[nt]);
+            } else {
+                const uint32_t ones[4] = {0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u};
+                mma_chain1(acc1, ones, b[nt]);
+            }
             const float F = (m < M) ? __uint_as_float((uint32_t)(14 - E + 127) << 23) : 0.0f;   // 2^(14-E)
             const float F0 = __shfl_sync(0xffffffffu, F, (2 * t) * 4);
             const float F1 = __shfl_sync(0xffffffffu, F, (2 * t + 1) * 4);
-            f[nt] = make_float4(F0, F0 * acc1[0], F1, F1 * acc1[1]);
+            constexpr float kq = BIN ? 2.0f : 1.0f;
+            f[nt] = make_float4(kq * F0, F0 * acc1[0], kq * F1, F1 * acc1[1]);
         }
     };
 
@@ -471,7 +553,7 @@ gemv_kernel(const GemvArgs a) {
 
     // ---- the segments ----
     int slot = 0;   // ring slot of the next unit to consume
-    const unsigned char* rd = ring + gid * 32 + 8 * t;   // this lane's words within a slot
+    const unsigned char* rd = ring + gid * (BIN ? 16 : 32) + (BIN ? 4 : 8) * t;   // this lane's words in a slot
     const int sstep = 16 * gpad;                          // scale halves per tile
     const int pstep = 16 * M;                             // private partial floats per tile
     auto run_segment = [&](auto add_c, int lo, int hi, int g) {
@@ -525,45 +607,60 @@ gemv_kernel(const GemvArgs a) {
     if (!LEAN && flag_reader) flag_seen = ld_acquire_gpu(a.flag + clu);
     if (LEAN) {
         // The common case: one group per warp over the whole range (K a
-        // multiple of 1024).  Whole turns of the ring run with compile-time slots,
-        // and a refill's source is the row base plus a per-tile stride (rows
-        // past N read row N - 1; their sums are never written to y).
-        const int g = gA + warp;
+        // multiple of 1024, or any K for the 1-bit layout).  Whole turns of the
+        // ring run with compile-time slots, and a refill's source is the row
+        // base plus a per-tile stride.
+        const int g = lean_g;
+        const bool clearer = S > 1 && sigma == 0;
+        if (!lean_has) {
+            // a warp with no group (the last slice of a 1-bit K that is not a
+            // multiple of 1024): its partials stay zero
+            if (clearer) count_cleared();
+        } else {
         stage(g);
 #pragma unroll
-        for (int u = kEarly; u < kDepth; ++u) issue(u);
-        const uint32_t* src_base = a.codes + (size_t)g * 8 + (lane & 1) * 4;
-        const int crow0 = tile_lo * 16 + crow;
-        const uint32_t ring_lane = smem_addr(ring) + (uint32_t)lane * 16u;
-        auto refill = [&](int u, int slot_) {
-            if (u < R) {
-                const int r = min(crow0 + 16 * u, N - 1);
-                cp_async16(ring_lane + (uint32_t)(slot_ * kSlotBytes), src_base + (size_t)r * W, true);
-            }
-            cp_async_commit();
-        };
+        for (int u = kEarly; u < kDepth; ++u) {
+            if (BIN) refill(u, u);
+            else issue(u);
+        }
         const unsigned short* sp = sc + gid * gpad + (g - g_lo);
         float* pw = part + (size_t)warp * rmax * pstep;   // private partials (M <= 4)
         auto fast_step = [&](int i, int s0, int s1, bool two) {
             cp_async_wait<kDepth - 2>();
             __syncwarp();
-            uint32_t w[2][4];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const unsigned char* sp8 = rd + (q ? s1 : s0) * kSlotBytes;
-                const uint2 v0 = *reinterpret_cast<const uint2*>(sp8);
-                const uint2 v1 = *reinterpret_cast<const uint2*>(sp8 + 8 * 32);
-                w[q][0] = v0.x;
-                w[q][1] = v1.x;
-                w[q][2] = v0.y;
-                w[q][3] = v1.y;
-            }
             float acc[2][MT][4];
-            if (two) {
-                pair_mmas<MT>(acc, w, b);
-            } else {
+            if constexpr (BIN) {
+                uint32_t w[2][2];
 #pragma unroll
-                for (int nt = 0; nt < MT; ++nt) mma_chain1(acc[0][nt], w[0], b[nt]);
+                for (int q = 0; q < 2; ++q) {
+                    const unsigned char* sp8 = rd + (q ? s1 : s0) * SLOT;
+                    w[q][0] = *reinterpret_cast<const uint32_t*>(sp8);            // row gid,     word t
+                    w[q][1] = *reinterpret_cast<const uint32_t*>(sp8 + 8 * 16);   // row gid + 8, word t
+                }
+                if (two) {
+                    bin_pair_mmas<MT>(acc, w, b);
+                } else {
+#pragma unroll
+                    for (int nt = 0; nt < MT; ++nt) bin_chain1(acc[0][nt], w[0][0], w[0][1], b[nt]);
+                }
+            } else {
+                uint32_t w[2][4];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const unsigned char* sp8 = rd + (q ? s1 : s0) * SLOT;
+                    const uint2 v0 = *reinterpret_cast<const uint2*>(sp8);
+                    const uint2 v1 = *reinterpret_cast<const uint2*>(sp8 + 8 * 32);
+                    w[q][0] = v0.x;
+                    w[q][1] = v1.x;
+                    w[q][2] = v0.y;
+                    w[q][3] = v1.y;
+                }
+                if (two) {
+                    pair_mmas<MT>(acc, w, b);
+                } else {
+#pragma unroll
+                    for (int nt = 0; nt < MT; ++nt) mma_chain1(acc[0][nt], w[0], b[nt]);
+                }
             }
             __syncwarp();
             refill(i + kDepth, s0);
@@ -573,7 +670,6 @@ gemv_kernel(const GemvArgs a) {
             sp += 2 * sstep;
             pw += 2 * pstep;
         };
-        const bool clearer = S > 1 && sigma == 0;
         bool counted = false;
         int i = 0;
         for (; i + kDepth <= R; i += kDepth) {
@@ -589,6 +685,7 @@ gemv_kernel(const GemvArgs a) {
         }
         for (int q = 0; i < R; i += 2, q += 2) fast_step(i, q, q + 1, i + 1 < R);
         if (clearer && !counted) count_cleared();   // a range of less than two ring turns
+        }
     } else {
         bool rest_issued = false;
         for (int s = 0; s < nseg; ++s) {
@@ -704,7 +801,7 @@ rotate_stage_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restric
 // Host side.
 // ---------------------------------------------------------------------------
 struct Plan {
-    int G, T, S, cps, ctas, rmax, MT, gpad;
+    int G, T, S, cps, ctas, rmax, MT, gpad, slot;
     uint32_t off_sc, off_part;
     size_t smem;
 };
@@ -714,7 +811,7 @@ void layout(Plan& p, int M, int cps) {
     p.cps = cps;
     p.rmax = (p.T + cps - 1) / cps;
     const int MP = 8 * p.MT;
-    size_t off = (size_t)kWarps * kDepth * kSlotBytes;
+    size_t off = (size_t)kWarps * kDepth * p.slot;
     p.off_sc = (uint32_t)off;
     off = align_up(off + (size_t)p.rmax * 16 * p.gpad * 2, 16);
     p.off_part = (uint32_t)off;
@@ -722,16 +819,19 @@ void layout(Plan& p, int M, int cps) {
     p.smem = off;
 }
 
-// The device-independent part of the plan: slices and the scale pitch.
-Plan base_plan(int M, int N, int K) {
+// The device-independent part of the plan: slices and the scale pitch.  The
+// 1-bit layout's slices are groups 8 s .. 8 s + 7 (the last one may be short).
+Plan base_plan(int M, int N, int K, bool bin) {
     Plan p{};
     p.G = K / kGroup;
     p.T = (N + 15) / 16;
     p.S = (p.G + kWarps - 1) / kWarps;
     p.MT = (M + 7) / 8;
+    p.slot = bin ? kBinSlotBytes : kSlotBytes;
     int w = 0;
     for (int s = 0; s < p.S; ++s) {
-        const int gA = (int)((long long)p.G * s / p.S), gB = (int)((long long)p.G * (s + 1) / p.S);
+        const int gA = bin ? kWarps * s : (int)((long long)p.G * s / p.S);
+        const int gB = bin ? std::min(gA + kWarps, p.G) : (int)((long long)p.G * (s + 1) / p.S);
         w = std::max(w, scale_width(p.G, gA, gB));
     }
     p.gpad = (int)align_up((size_t)w, 8);   // row pitch a multiple of 16 bytes
@@ -740,7 +840,7 @@ Plan base_plan(int M, int N, int K) {
 
 // Lets the kernel use the device's whole per-block shared memory; returns the
 // dynamic part it may take.
-template <int MT, bool PRE, bool ONE, bool LEAN>
+template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN>
 cudaError_t kernel_smem_limit(int dev, int* limit) {
     static int optin_of[64] = {};
     if (!optin_of[dev]) {
@@ -748,10 +848,11 @@ cudaError_t kernel_smem_limit(int dev, int* limit) {
         cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return e;
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, gemv_kernel<MT, PRE, ONE, LEAN>);
+        e = cudaFuncGetAttributes(&fa, gemv_kernel<MT, PRE, ONE, LEAN, BIN>);
         if (e != cudaSuccess) return e;
         optin -= (int)fa.sharedSizeBytes;   // the kernel's static shared memory comes first
-        e = cudaFuncSetAttribute(gemv_kernel<MT, PRE, ONE, LEAN>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        e = cudaFuncSetAttribute(gemv_kernel<MT, PRE, ONE, LEAN, BIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin);
         if (e != cudaSuccess) return e;
         optin_of[dev] = optin;
     }
@@ -761,11 +862,11 @@ cudaError_t kernel_smem_limit(int dev, int* limit) {
 
 // One wave: as many CTAs as fit at once, by registers (the launch bound) and
 // by shared memory (which grows with the range length).
-template <int MT, bool PRE, bool ONE, bool LEAN>
+template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN>
 tern_status make_plan(int M, int N, int K, int sms, int dev, Plan* out) {
     int limit = 0;
-    if (kernel_smem_limit<MT, PRE, ONE, LEAN>(dev, &limit) != cudaSuccess) return TERN_ERR_CUDA;
-    Plan p = base_plan(M, N, K);
+    if (kernel_smem_limit<MT, PRE, ONE, LEAN, BIN>(dev, &limit) != cudaSuccess) return TERN_ERR_CUDA;
+    Plan p = base_plan(M, N, K, BIN);
     const int need = (p.T + kMaxTiles - 1) / kMaxTiles;   // ranges short enough for the shared partials
     int cps = 1;
     for (int per_sm = GemvCfg<MT>::kCtasPerSm; per_sm >= 1; --per_sm) {
@@ -784,7 +885,7 @@ tern_status make_plan(int M, int N, int K, int sms, int dev, Plan* out) {
 // Plans depend on the shape and the device only: keep the recent ones.
 struct PlanKey {
     int M, N, K, dev;
-    bool pre;
+    bool pre, bin;
 };
 std::mutex g_plan_mu;
 constexpr int kPlanCache = 64;
@@ -792,7 +893,7 @@ PlanKey g_plan_key[kPlanCache];
 Plan g_plan_val[kPlanCache];
 int g_plan_n = 0, g_plan_next = 0;
 
-template <int MT, bool PRE, bool ONE, bool LEAN>
+template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN>
 tern_status cached_plan(int M, int N, int K, int sms, Plan* out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TERN_ERR_CUDA;
@@ -800,15 +901,15 @@ tern_status cached_plan(int M, int N, int K, int sms, Plan* out) {
     std::lock_guard<std::mutex> lk(g_plan_mu);
     for (int i = 0; i < g_plan_n; ++i) {
         const PlanKey& k = g_plan_key[i];
-        if (k.M == M && k.N == N && k.K == K && k.dev == dev && k.pre == PRE) {
+        if (k.M == M && k.N == N && k.K == K && k.dev == dev && k.pre == PRE && k.bin == BIN) {
             *out = g_plan_val[i];
             return TERN_OK;
         }
     }
-    const tern_status st = make_plan<MT, PRE, ONE, LEAN>(M, N, K, sms, dev, out);
+    const tern_status st = make_plan<MT, PRE, ONE, LEAN, BIN>(M, N, K, sms, dev, out);
     if (st != TERN_OK) return st;
     const int slot = g_plan_n < kPlanCache ? g_plan_n++ : (g_plan_next++ % kPlanCache);
-    g_plan_key[slot] = PlanKey{M, N, K, dev, PRE};
+    g_plan_key[slot] = PlanKey{M, N, K, dev, PRE, BIN};
     g_plan_val[slot] = *out;
     return TERN_OK;
 }
@@ -822,8 +923,8 @@ tern_status validate(const void* x, const uint32_t* codes, const void* scales, c
     return TERN_OK;
 }
 
-// Workspace: [range flag words, when K spans several slices | fp32 rotated x,
-// for the rotation-fused call].  The flags count back to 0 at the end of every
+// Workspace: [range flag words, when K spans several slices | the staged
+// rotated x, for the rotation-fused call].  The flags count back to 0 at the end of every
 // call, so a zero-filled workspace stays ready for the next one.
 size_t flag_bytes(int N, int K) {
     const int G = K / kGroup;
@@ -834,10 +935,10 @@ size_t workspace_bytes(int M, int N, int K, bool rot) {
     return flag_bytes(N, K) + (rot ? align_up((size_t)M * K * 2 + (size_t)M * (K / kGroup) * 4, 256) : 0);
 }
 
-template <int MT, bool PRE, bool ONE, bool LEAN = false>
+template <int MT, bool PRE, bool ONE, bool LEAN = false, bool BIN = false>
 tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
     Plan p;
-    const tern_status st = cached_plan<MT, PRE, ONE, LEAN>(args.M, args.N, args.K, sms, &p);
+    const tern_status st = cached_plan<MT, PRE, ONE, LEAN, BIN>(args.M, args.N, args.K, sms, &p);
     if (st != TERN_OK) return st;
     args.G = p.G;
     args.T = p.T;
@@ -848,12 +949,12 @@ tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
     args.off_sc = p.off_sc;
     args.off_part = p.off_part;
     const cudaError_t e =
-        launch_pdl(gemv_kernel<MT, PRE, ONE, LEAN>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, args);
+        launch_pdl(gemv_kernel<MT, PRE, ONE, LEAN, BIN>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, args);
     return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
 
 tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const void* scales, float* y, int M,
-                int N, int K, void* workspace, size_t workspace_bytes_, cudaStream_t stream) {
+                int N, int K, void* workspace, size_t workspace_bytes_, cudaStream_t stream, bool bin = false) {
     int sms = 0;
     tern_status st = check_device(&sms);
     if (st != TERN_OK) return st;
@@ -891,6 +992,11 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
                                : launch_gemv<1, true, false>(args, sms, stream))
                        : (lean ? launch_gemv<2, true, false, true>(args, sms, stream)
                                : launch_gemv<2, true, false>(args, sms, stream));
+    } else if (bin) {
+        // the 1-bit layout always runs the lean loop
+        st = M == 1 ? launch_gemv<1, false, true, true, true>(args, sms, stream)
+             : MT == 1 ? launch_gemv<1, false, false, true, true>(args, sms, stream)
+                       : launch_gemv<2, false, false, true, true>(args, sms, stream);
     } else {
         st = M == 1 ? (lean ? launch_gemv<1, false, true, true>(args, sms, stream)
                             : launch_gemv<1, false, true>(args, sms, stream))
@@ -952,6 +1058,17 @@ extern "C" tern_status tern_gemv(const void* x, const uint32_t* codes, const voi
     const size_t need = workspace_bytes(M, N, K, false);
     if (need > 0 && (!workspace || workspace_bytes_ < need)) return TERN_ERR_WORKSPACE;
     return run(x, nullptr, codes, scales, y, M, N, K, workspace, workspace_bytes_, (cudaStream_t)stream);
+}
+
+extern "C" tern_status tern_bin_gemv(const void* x, const uint32_t* words, const void* scales, float* y, int M,
+                                     int N, int K, void* workspace, size_t workspace_bytes_,
+                                     tern_stream_t stream) {
+    set_launch_count(0);
+    const tern_status v = validate(x, words, scales, y, M, N, K);
+    if (v != TERN_OK) return v;
+    const size_t need = workspace_bytes(M, N, K, false);
+    if (need > 0 && (!workspace || workspace_bytes_ < need)) return TERN_ERR_WORKSPACE;
+    return run(x, nullptr, words, scales, y, M, N, K, workspace, workspace_bytes_, (cudaStream_t)stream, true);
 }
 
 extern "C" tern_status tern_fwht_gemm(const void* x, const int8_t* signs, const uint32_t* codes,

@@ -1,4 +1,5 @@
-// tern_pack.cu -- device packer: int8 trits -> 2-bit codes, 16 per uint32.
+// tern_pack.cu -- device packers: int8 trits -> 2-bit codes, 16 per uint32,
+// and int8 +-1 -> bits, 32 per uint32 (the 1-bit sibling format).
 //
 // Code q = t + 1 in a 2-bit slot ("prism-ml/Ternary-Bonsai-27B-mlx-2bit" model
 // card, "Memory requirement"); slot k%16 of word k/16, lowest k in the lowest
@@ -41,10 +42,62 @@ pack_kernel(const int4* __restrict__ t, uint32_t* __restrict__ codes, long long 
     }
 }
 
+// The 1-bit sibling: one thread per output word, two 16-byte loads of 32
+// values, bit i of the word set for value i = +1.  Anything but +-1 is
+// counted and stored as -1.
+__global__ void __launch_bounds__(kPackThreads)
+bin_pack_kernel(const int4* __restrict__ t, uint32_t* __restrict__ words_out, long long words,
+                int* __restrict__ bad_count) {
+    int bad = 0;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x; w < words; w += stride) {
+        const int4 v0 = __ldg(t + 2 * w), v1 = __ldg(t + 2 * w + 1);
+        const uint32_t in[8] = {(uint32_t)v0.x, (uint32_t)v0.y, (uint32_t)v0.z, (uint32_t)v0.w,
+                                (uint32_t)v1.x, (uint32_t)v1.y, (uint32_t)v1.z, (uint32_t)v1.w};
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const uint32_t byte = (in[j] >> (8 * b)) & 0xFFu;
+                bad += (byte == 1u || byte == 0xFFu) ? 0 : 1;
+                word |= (byte == 1u ? 1u : 0u) << (4 * j + b);
+            }
+        }
+        words_out[w] = word;
+    }
+    if (bad_count) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+        if ((threadIdx.x & 31) == 0 && bad) atomicAdd(bad_count, bad);
+    }
+}
+
 }  // namespace
 }  // namespace tern
 
 using namespace tern;
+
+extern "C" tern_status tern_bin_pack(const int8_t* t, int N, int K, uint32_t* words, int* bad_count,
+                                     tern_stream_t stream) {
+    set_launch_count(0);
+    if (N < 0 || K < 0 || K % 32 != 0) return TERN_ERR_SHAPE;
+    const long long nwords = (long long)N * (K / 32);
+    if (nwords == 0) return TERN_OK;
+    if (!t || !words) return TERN_ERR_NULL;
+    if (!aligned16(t) || !aligned16(words)) return TERN_ERR_ALIGN;
+    int sms = 0;
+    tern_status st = check_device(&sms);
+    if (st != TERN_OK) return st;
+    long long blocks = (nwords + kPackThreads - 1) / kPackThreads;
+    const long long cap = (long long)sms * 8;
+    if (blocks > cap) blocks = cap;
+    bin_pack_kernel<<<(unsigned)blocks, kPackThreads, 0, (cudaStream_t)stream>>>(
+        reinterpret_cast<const int4*>(t), words, nwords, bad_count);
+    if (cudaGetLastError() != cudaSuccess) return TERN_ERR_CUDA;
+    set_launch_count(1);
+    return TERN_OK;
+}
 
 extern "C" tern_status tern_pack(const int8_t* t, int N, int K, uint32_t* codes, int* bad_count,
                                  tern_stream_t stream) {

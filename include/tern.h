@@ -103,6 +103,30 @@ tern_status tern_unpack_host(const uint32_t *codes, int N, int K, int8_t *t,
 tern_status tern_validate_host(const uint32_t *codes, int N, int K, long long *bad_count);
 
 /* ---------------------------------------------------------------------- */
+/* The 1-bit sibling, binary g128 (card, "Highlights" and "Benchmarks":    */
+/* 1-bit Bonsai at 1.125 bits per weight; "MLX packaging": s_mlx = 2 s_g,   */
+/* bias = -s_g gives exactly +-s_g).  A weight is (2b - 1) * s_g, b the bit */
+/* k%32 of little-endian uint32 word k/32 of its row (the pages fix no      */
+/* order; the same reading as the 2-bit codes).  Scales as above.           */
+/* ---------------------------------------------------------------------- */
+
+/* Packed bytes of an N x K binary-g128 matrix: N*K/8 + N*K/64; 0 on bad input
+ * (K % 128 != 0). */
+size_t tern_bin_packed_bytes(int N, int K);
+
+/* Device packer.  t: int8 [N][K] in {-1,+1}; words: uint32 [N][K/32].  An
+ * entry other than +-1 is written as -1 and counted: if bad_count (device
+ * int, nullable) is given, the count is atomically ADDED to it.  K % 32 == 0,
+ * N >= 0, K >= 0 (TERN_ERR_SHAPE otherwise); t and words 16-byte aligned. */
+tern_status tern_bin_pack(const int8_t *t, int N, int K, uint32_t *words, int *bad_count,
+                          tern_stream_t stream);
+
+/* Host packer and unpacker, same layout and rules (unpack writes 2b - 1). */
+tern_status tern_bin_pack_host(const int8_t *t, int N, int K, uint32_t *words,
+                               long long *bad_count);
+tern_status tern_bin_unpack_host(const uint32_t *words, int N, int K, int8_t *t);
+
+/* ---------------------------------------------------------------------- */
 /* Decode / small-batch product, M = 1..16 (card, "Cross-platform          */
 /* throughput": tg128 is the memory-bandwidth-bound phase; "Speculative    */
 /* decoding: DSpark": verify runs k + 1 tokens)                            */
@@ -133,6 +157,16 @@ size_t tern_gemv_workspace_bytes(int M, int N, int K);
 tern_status tern_gemv(const void *x, const uint32_t *codes, const void *scales, float *y,
                       int M, int N, int K, void *workspace, size_t workspace_bytes,
                       tern_stream_t stream);
+
+/* The same product for the 1-bit sibling format: y (fp32 [M][N]) = x W^T with
+ * W[n][k] = (2 b[n][k] - 1) * s[n][k/128], words uint32 [N][K/32] as
+ * tern_bin_pack writes them.  Shapes, alignment, workspace (the size
+ * tern_gemv_workspace_bytes gives), ordering and error behaviour as for
+ * tern_gemv.  Each weight costs the same tensor-core work as a 2-bit one, at
+ * half the bytes. */
+tern_status tern_bin_gemv(const void *x, const uint32_t *words, const void *scales, float *y,
+                          int M, int N, int K, void *workspace, size_t workspace_bytes,
+                          tern_stream_t stream);
 
 /* Fixed size of the library-owned scratch array behind tern_gemv_noalloc. */
 #define TERN_NOALLOC_SCRATCH_BYTES (256u << 10)

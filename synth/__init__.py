@@ -12,7 +12,8 @@ since the pages give none:
 * trits t in {-1, 0, +1}: iid, either uniform or with P(0) = 0.4, P(+-1) = 0.3;
 * scales: fp16, U[0.005, 0.05] or |N(0, 0.02)| + 1e-3, one per 128 along K;
 * activations x: bf16 rounded from N(0, 1) (round to nearest even);
-* rotation signs: iid uniform over {-1, +1}, int8.
+* rotation signs: iid uniform over {-1, +1}, int8;
+* the 1-bit sibling format's weights: iid uniform over {-1, +1}.
 
 Each tensor draws from its own stream, keyed by (seed, name), so one tensor's
 shape never shifts another tensor's values.
@@ -34,6 +35,18 @@ def rng(seed: int, name: str) -> np.random.Generator:
     """An independent PCG64 stream for tensor `name` under `seed`."""
     key = zlib.crc32(name.encode("utf-8"))
     return np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(seed), key])))
+
+
+def binary(seed: int, name: str, shape) -> np.ndarray:
+    """int8 array of iid values in {-1, +1}, each with probability 1/2 (the
+    1-bit sibling format's weights)."""
+    return np.where(rng(seed, name).random(shape) < 0.5, -1, 1).astype(np.int8)
+
+
+def binary_problem(seed: int, M: int, N: int, K: int, tag: str = "") -> "Problem":
+    """A seeded problem of the 1-bit format: t in {-1, +1}."""
+    return Problem(M, N, K, binary(seed, f"{tag}b", (N, K)), scales(seed, f"{tag}s", (N, K // 128)),
+                   activations(seed, f"{tag}x", (M, K)))
 
 
 def trits(seed: int, name: str, shape, dist: str = SPARSE40) -> np.ndarray:
@@ -144,6 +157,13 @@ def device_trits(seed: int, name: str, shape, dist: str = SPARSE40, device="cuda
     t += (u >= hi).to(torch.int8)
     t -= 1
     return t
+
+
+def device_binary(seed: int, name: str, shape, device="cuda"):
+    """int8 CUDA tensor of iid weights in {-1, +1} (the 1-bit format), P = 1/2."""
+    import torch
+    g = device_generator(seed, name, device)
+    return torch.where(torch.rand(shape, generator=g, device=device) < 0.5, -1, 1).to(torch.int8)
 
 
 def device_scales(seed: int, name: str, shape, dist: str = SCALE_HALFNORMAL, device="cuda"):

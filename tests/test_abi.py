@@ -150,3 +150,45 @@ def test_gemm_workspace_sizes(tern):
     for M, N, K in [(512, 17408, 5120), (512, 5120, 17408), (1, 128, 128), (300, 130, 640), (17, 1000, 128)]:
         assert tern.gemm_workspace_bytes(M, N, K) == want(M, N, K)
     assert tern.gemm_workspace_bytes(0, 128, 128) == 0
+
+
+# --------------------------------------------------------------------------
+# the 1-bit sibling format
+# --------------------------------------------------------------------------
+
+def test_bin_host_pack_matches_oracle(tern, orc):
+    t = synth.binary(40, "hp", (33, 1024))
+    words, bad = tern.bin_pack_host(t)
+    want, wbad = orc.bin_pack(t)
+    assert bad == wbad == 0
+    assert np.array_equal(words, want)
+    assert np.array_equal(tern.bin_unpack_host(words, 1024), t)
+    assert tern.lib().tern_bin_packed_bytes(33, 1024) == words.nbytes + 33 * 8 * 2
+
+
+def test_bin_host_pack_invalid_entries(tern, orc):
+    t = synth.binary(41, "inv", (4, 64))
+    t[0, 3] = 0
+    t[2, 40] = 2
+    t[3, 63] = -7
+    words, bad = tern.bin_pack_host(t)
+    want, wbad = orc.bin_pack(t)
+    assert bad == wbad == 3
+    assert np.array_equal(words, want)
+
+
+def test_bin_argument_errors_never_launch(tern):
+    lib = tern.lib()
+    P = 4096
+    assert lib.tern_bin_pack(P, 4, 48, P, None, None) == 2          # K % 32
+    assert lib.tern_bin_pack(P, 4, 64, None, None, None) == 1
+    assert lib.tern_bin_pack(P + 8, 4, 64, P, None, None) == 3
+    assert lib.tern_bin_packed_bytes(4, 96) == 0
+    assert lib.tern_bin_gemv(P, P, P, P, 0, 16, 128, P, 1 << 20, None) == 2
+    assert lib.tern_bin_gemv(P, P, P, P, 17, 16, 128, P, 1 << 20, None) == 2
+    assert lib.tern_bin_gemv(P, P, P, P, 1, 16, 96, P, 1 << 20, None) == 2
+    assert lib.tern_bin_gemv(None, P, P, P, 1, 16, 128, P, 1 << 20, None) == 1
+    assert lib.tern_bin_gemv(P, P + 4, P, P, 1, 16, 128, P, 1 << 20, None) == 3
+    need = tern.gemv_workspace_bytes(1, 16, 2048)
+    assert lib.tern_bin_gemv(P, P, P, P, 1, 16, 2048, None, need, None) == 4
+    assert lib.tern_bin_gemv(P, P, P, P, 1, 16, 2048, P, need - 1, None) == 4

@@ -1,0 +1,100 @@
+"""GPU parity of the 1-bit sibling format (binary g128, w = (2b - 1) s_g).
+
+The device packer must agree with the oracle's packing bit for bit.  The
+product is held to the decode tolerance |y - y_ref| <= 1e-3 * sum_k |x w| + 1e-6
+against the oracle's double-precision product; a one-hot activation picks
++-s_g of a column, which the kernel computes exactly.  Shapes span full and
+short K-slices (a slice is 8 groups of 128; K = 640, 1152 and 2176 leave
+warps with no group), ragged N, and the token counts 1..16.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests._util import assert_fp32_close, dev_bf16, dev_scales, dev_trits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tern():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_gemv_gemm_gb300 import build
+    build.build()
+    import bit_gemv_gemm_gb300 as t
+    return t
+
+
+def words_host(words: torch.Tensor) -> np.ndarray:
+    return words.cpu().numpy().view(np.uint32)
+
+
+@pytest.mark.parametrize("N,K", [(37, 128), (1000, 2048), (3, 17408)])
+def test_bin_pack_matches_oracle(tern, orc, N, K):
+    t = synth.binary(50, f"p{N}", (N, K))
+    t[0, 5] = 0                      # invalid: counted, stored as -1
+    bad = torch.zeros(1, dtype=torch.int32, device="cuda")
+    words = tern.bin_pack(dev_trits(t), bad_count=bad)
+    want, wbad = orc.bin_pack(t)
+    assert int(bad.item()) == wbad == 1
+    assert np.array_equal(words_host(words), want)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (1, 1000, 5120), (3, 777, 17408), (6, 129, 2176),
+                                   (5, 200, 640), (16, 300, 1152), (2, 48, 128), (8, 129, 1024),
+                                   (1, 16, 128)])
+def test_bin_gemv_matches_oracle(tern, orc, M, N, K):
+    p = synth.binary_problem(60 + M, M, N, K, tag=f"g{N}x{K}")
+    words = tern.bin_pack(dev_trits(p.t))
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    tern.bin_gemv(dev_bf16(p.x), words, dev_scales(p.s), y=y)
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    y_ref, a_ref = orc.bin_matmul(p.x, words_host(words), p.s)
+    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what=f"binary M={M} N={N} K={K}")
+
+
+def test_bin_gemv_one_hot_exact(tern):
+    """x = e_k picks (2b[n][k] - 1) s[n][k / 128] exactly, at every slot position."""
+    N, K = 64, 256
+    t = synth.binary(70, "oh", (N, K))
+    s = synth.scales(70, "s", (N, K // 128))
+    words = tern.bin_pack(dev_trits(t))
+    W = t.astype(np.float64) * np.repeat(s.astype(np.float64), 128, axis=1)
+    ks = [0, 9, 10, 11, 12, 15, 16, 27, 28, 31, 32, 100, 127, 128, 200, 255]
+    for i in range(0, len(ks), 8):
+        chunk = ks[i:i + 8]
+        x = np.zeros((len(chunk), K), dtype=np.uint16)
+        for j, k in enumerate(chunk):
+            x[j, k] = 0x3F80
+        y = tern.bin_gemv(dev_bf16(x), words, dev_scales(s)).cpu().numpy()
+        for j, k in enumerate(chunk):
+            assert np.array_equal(y[j].astype(np.float64), W[:, k]), k
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 5120, 17408), (1, 17408, 5120), (5, 5120, 6144), (16, 5120, 17408)])
+def test_bin_gemv_full_size_sampled(tern, orc, M, K, N):
+    p = synth.binary_problem(80 + M, M, N, K, tag=f"f{K}")
+    words = tern.bin_pack(dev_trits(p.t))
+    y = tern.bin_gemv(dev_bf16(p.x), words, dev_scales(p.s))
+    torch.cuda.synchronize()
+    rs = np.random.default_rng(K + N + M)
+    ms, ns = rs.integers(0, M, 3000), rs.integers(0, N, 3000)
+    ms[:4], ns[:4] = M - 1, [0, N - 1, N - 2, N // 2]
+    y_ref, a_ref = orc.bin_matmul_sampled(p.x, words_host(words), p.s, ms, ns)
+    assert_fp32_close(y.cpu().numpy()[ms, ns], y_ref, a_ref, what=f"binary full M={M} {K}->{N}")
+
+
+def test_bin_and_ternary_agree_on_pm1(tern, orc):
+    """The same +-1 weights through both layouts and both kernel variants."""
+    M, N, K = 3, 500, 5120
+    p = synth.binary_problem(90, M, N, K, tag="both")
+    x, s = dev_bf16(p.x), dev_scales(p.s)
+    yb = tern.bin_gemv(x, tern.bin_pack(dev_trits(p.t)), s)
+    yt = tern.gemv(x, tern.pack(dev_trits(p.t)), s)
+    torch.cuda.synchronize()
+    y_ref, a_ref = orc.bin_matmul(p.x, orc.bin_pack(p.t)[0], p.s)
+    assert_fp32_close(yb.cpu().numpy(), y_ref, a_ref, what="binary kernel")
+    assert_fp32_close(yt.cpu().numpy(), y_ref, a_ref, what="ternary kernel on +-1")
