@@ -371,11 +371,12 @@ def bench_verify_step(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int):
 
 
 def bench_binary(tern, steps: int, warmup: int, hbm: float, copies: int = 16):
-    """The 1-bit sibling format at M = 1: per decode shape, `copies` distinct
-    matrices (more bytes than L2) called back to back in one graph."""
+    """The 1-bit sibling format.  Decode (M = 1): per decode shape, `copies`
+    distinct matrices (more bytes than L2) called back to back in one graph.
+    Prefill (M = 512): per layer shape, 4 distinct matrices in one graph."""
     import torch
     import synth
-    out = []
+    out = {"decode": [], "pp512": []}
     for (K, N) in synth.DECODE_SHAPES:
         mats = []
         for c in range(copies):
@@ -394,8 +395,28 @@ def bench_binary(tern, steps: int, warmup: int, hbm: float, copies: int = 16):
         ms = time_graph(g, max(3, steps // 4), warmup)
         per = ms / copies * 1e-3
         wb = N * K // 8 + N * K // 64
-        out.append({"M": 1, "K": K, "N": N, "us": per * 1e6, "weight_bytes": wb,
-                    "weight_GBps": wb / per / 1e9, "hbm_frac": wb / per / 1e9 / hbm})
+        out["decode"].append({"M": 1, "K": K, "N": N, "us": per * 1e6, "weight_bytes": wb,
+                              "weight_GBps": wb / per / 1e9, "hbm_frac": wb / per / 1e9 / hbm})
+        del mats
+    M = synth.PREFILL_M
+    for (name, K, N) in synth.PREFILL_LAYER:
+        mats = []
+        for c in range(4):
+            t = synth.device_binary(8, f"BP{c}.{name}.t", (N, K))
+            mats.append((tern.bin_pack(t), synth.device_scales(8, f"BP{c}.{name}.s", (N, K // 128))))
+            del t
+        x = synth.device_activations(8, f"BP.{name}.x", (M, K))
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        ws = tern.workspace(tern.gemm_workspace_bytes(M, N, K))
+
+        def run(mats=mats, x=x, y=y, ws=ws):
+            for c in range(4):
+                tern.bin_gemm(x, mats[c][0], mats[c][1], y=y, ws=ws)
+
+        g = graph_of(run)
+        ms = time_graph(g, max(2, steps // 20), max(1, warmup // 2))
+        per = ms / 4 * 1e-3
+        out["pp512"].append({"name": name, "K": K, "N": N, "us": per * 1e6, "TFLOPs": 2.0 * M * N * K / per / 1e12})
         del mats
     return out
 

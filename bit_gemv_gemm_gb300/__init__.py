@@ -53,6 +53,7 @@ EXPORTS = {
     "tern_bin_pack_host": (_I, [_P, _I, _I, _P, _P]),
     "tern_bin_unpack_host": (_I, [_P, _I, _I, _P]),
     "tern_bin_gemv": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
+    "tern_bin_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
 }
 
 
@@ -308,3 +309,22 @@ def wait_selftest(which: int, limit_us: int, stream=None) -> None:
 
 def last_launch_count() -> int:
     return int(lib().tern_last_launch_count())
+
+
+def bin_gemm(x: torch.Tensor, words: torch.Tensor, scales: torch.Tensor, y: torch.Tensor | None = None,
+             out_dtype=torch.float32, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The 1-bit sibling format on the tcgen05 tensor cores: y ([M, N], fp32 or
+    bf16) = x W^T, W = (2b - 1) s, any M >= 1."""
+    M, K = x.shape
+    N = words.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    if y.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("y must be float32 or bfloat16")
+    if ws is None:
+        ws = workspace(gemm_workspace_bytes(M, N, K), x.device)
+    _check("tern_bin_gemm", lib().tern_bin_gemm(
+        _dev(x, torch.bfloat16, "x"), _dev(words, torch.int32, "words"), _dev(scales, torch.float16, "scales"),
+        _dev(y, y.dtype, "y"), 1 if y.dtype == torch.bfloat16 else 0, M, N, K,
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return y

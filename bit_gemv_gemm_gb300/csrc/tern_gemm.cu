@@ -80,6 +80,7 @@ struct GemmArgs {
     unsigned* counters;         // [tiles][4 lane quadrants], 0 between calls
     int stream_k;               // 0: whole tiles blockIdx.x, + gridDim.x, ...; 1: stream-K shares
     int y_is_bf16;
+    int bin;                    // 1: the 1-bit layout (words [N][K/32]), else 2-bit codes [N][K/16]
     int M, N, K;
 };
 
@@ -149,6 +150,26 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t s2, uint32_t (&
     for (int p = 0; p < 4; ++p) {
         o[p] = prmt(v[2 * p], v[2 * p + 1], 0x5410u);       // (w_{2p},   w_{2p+1})
         o[p + 4] = prmt(v[2 * p], v[2 * p + 1], 0x7632u);   // (w_{2p+8}, w_{2p+9})
+    }
+}
+
+// 32 weights of one word of the 1-bit layout -> 16 bf16 pairs (k, k+1) of
+// (2b - 1) * s.  Bits j and j + 16 sit 16 bits apart, so one shift puts both
+// at bit 7 of their halves (the bf16 exponent's low bit): the halves read as
+// b * 2^-126, and fma(., 2^127, -1) = 2b - 1 exactly.
+__device__ __forceinline__ void unpack_word_bin(uint32_t w, uint32_t s2, uint32_t (&o)[16]) {
+    constexpr uint32_t kTwo127 = 0x7F007F00u;   // bf16 2^127, both halves
+    constexpr uint32_t kMinus1 = 0xBF80BF80u;   // bf16 -1, both halves
+    uint32_t v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t m = (j <= 7 ? (w << (7 - j)) : (w >> (j - 7))) & 0x00800080u;
+        v[j] = bf16x2_mul(bf16x2_fma(m, kTwo127, kMinus1), s2);   // (w_j, w_{j+16})
+    }
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        o[p] = prmt(v[2 * p], v[2 * p + 1], 0x5410u);       // (w_{2p},    w_{2p+1})
+        o[p + 8] = prmt(v[2 * p], v[2 * p + 1], 0x7632u);   // (w_{2p+16}, w_{2p+17})
     }
 }
 
@@ -239,8 +260,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     mbar_arrive_expect_tx(full_bar(s), kXStageBytes + kCStageBytes);
                     tma_load_2d(sbase + (uint32_t)(kSmemX + (size_t)s * kXStageBytes), &tmap_x, ks * kBK, mt * kBN,
                                 full_bar(s));
-                    tma_load_2d(sbase + (uint32_t)(kSmemC + (size_t)s * kCStageBytes), &tmap_c, ks * (kBK / 16),
-                                nt * kBM, full_bar(s));
+                    // the 1-bit layout: a 16-byte box of 128 weights per row (two
+                    // stages), starting at the even stage so that x stays 16-byte aligned
+                    tma_load_2d(sbase + (uint32_t)(kSmemC + (size_t)s * kCStageBytes), &tmap_c,
+                                a.bin ? (ks & ~1) * (kBK / 32) : ks * (kBK / 16), nt * kBM, full_bar(s));
                 }
             }
             if (!ok) {
@@ -423,16 +446,21 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                     break;
                 }
                 tc_fence_after();
-                const uint2 w = *reinterpret_cast<const uint2*>(smem + kSmemC + (size_t)s * kCStageBytes +
-                                                                 (size_t)rl * 16 + 8 * h);
+                const unsigned char* crow = smem + kSmemC + (size_t)s * kCStageBytes + (size_t)rl * 16;
                 uint32_t o[16];
-                uint32_t o0[8], o1[8];
-                unpack_word(w.x, s2, o0);
-                unpack_word(w.y, s2, o1);
+                if (a.bin) {
+                    // word (ks odd ? 2 : 0) + h of the row's two-stage box
+                    unpack_word_bin(*reinterpret_cast<const uint32_t*>(crow + 8 * (ks & 1) + 4 * h), s2, o);
+                } else {
+                    const uint2 w = *reinterpret_cast<const uint2*>(crow + 8 * h);
+                    uint32_t o0[8], o1[8];
+                    unpack_word(w.x, s2, o0);
+                    unpack_word(w.y, s2, o1);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    o[i] = o0[i];
-                    o[8 + i] = o1[i];
+                    for (int i = 0; i < 8; ++i) {
+                        o[i] = o0[i];
+                        o[8 + i] = o1[i];
+                    }
                 }
                 tmem_st_x16(tbase + 32u * s, o);
                 tmem_st_wait();
@@ -551,9 +579,9 @@ extern "C" size_t tern_gemm_workspace_bytes(int M, int N, int K) {
     return gemm_counter_bytes(M, N) + (size_t)gemm_tiles(M, N) * kTileFloats * 4;
 }
 
-extern "C" tern_status tern_gemm(const void* x, const uint32_t* codes, const void* scales, void* y,
-                                 int y_is_bf16, int M, int N, int K, void* workspace,
-                                 size_t workspace_bytes, tern_stream_t stream) {
+namespace {
+tern_status run_gemm(const void* x, const uint32_t* codes, const void* scales, void* y, int y_is_bf16, int M, int N,
+                     int K, void* workspace, size_t workspace_bytes, tern_stream_t stream, bool bin) {
     set_launch_count(0);
     if (M < 1 || N < 1 || K < 128 || K % 128 != 0) return TERN_ERR_SHAPE;
     if ((long long)M * N >= (1LL << 40) || (long long)N * K >= (1LL << 40)) return TERN_ERR_SHAPE;
@@ -568,8 +596,8 @@ extern "C" tern_status tern_gemm(const void* x, const uint32_t* codes, const voi
     CUtensorMap mx, mc;
     if (!make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, kBK, kBN,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT32, codes, (uint64_t)(K / 16), (uint64_t)N,
-                     (uint64_t)(K / 16) * 4, kBK / 16, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !make_map_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT32, codes, (uint64_t)(K / (bin ? 32 : 16)), (uint64_t)N,
+                     (uint64_t)(K / (bin ? 32 : 16)) * 4, kBK / 16, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
         return TERN_ERR_CUDA;
 
     static bool attr_set[64] = {};
@@ -585,6 +613,7 @@ extern "C" tern_status tern_gemm(const void* x, const uint32_t* codes, const voi
     args.scales = reinterpret_cast<const __half*>(scales);
     args.y = y;
     args.y_is_bf16 = y_is_bf16 ? 1 : 0;
+    args.bin = bin ? 1 : 0;
     args.M = M;
     args.N = N;
     args.K = K;
@@ -599,4 +628,17 @@ extern "C" tern_status tern_gemm(const void* x, const uint32_t* codes, const voi
     if (e != cudaSuccess) return TERN_ERR_CUDA;
     set_launch_count(1);
     return TERN_OK;
+}
+}  // namespace
+
+extern "C" tern_status tern_gemm(const void* x, const uint32_t* codes, const void* scales, void* y,
+                                 int y_is_bf16, int M, int N, int K, void* workspace,
+                                 size_t workspace_bytes, tern_stream_t stream) {
+    return run_gemm(x, codes, scales, y, y_is_bf16, M, N, K, workspace, workspace_bytes, stream, false);
+}
+
+extern "C" tern_status tern_bin_gemm(const void* x, const uint32_t* words, const void* scales, void* y,
+                                     int y_is_bf16, int M, int N, int K, void* workspace,
+                                     size_t workspace_bytes, tern_stream_t stream) {
+    return run_gemm(x, words, scales, y, y_is_bf16, M, N, K, workspace, workspace_bytes, stream, true);
 }

@@ -239,6 +239,14 @@ tern_status tern_gemm(const void *x, const uint32_t *codes, const void *scales, 
                       int y_is_bf16, int M, int N, int K, void *workspace,
                       size_t workspace_bytes, tern_stream_t stream);
 
+/* The same product for the 1-bit sibling format (words uint32 [N][K/32] as
+ * tern_bin_pack writes them): each weight is unpacked to bf16
+ * (2b - 1) * bf16(s_g).  Shapes, workspace (tern_gemm_workspace_bytes),
+ * output types and error behaviour as for tern_gemm. */
+tern_status tern_bin_gemm(const void *x, const uint32_t *words, const void *scales, void *y,
+                          int y_is_bf16, int M, int N, int K, void *workspace,
+                          size_t workspace_bytes, tern_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* Diagnostics                                                             */
 /* ---------------------------------------------------------------------- */

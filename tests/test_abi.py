@@ -192,3 +192,8 @@ def test_bin_argument_errors_never_launch(tern):
     need = tern.gemv_workspace_bytes(1, 16, 2048)
     assert lib.tern_bin_gemv(P, P, P, P, 1, 16, 2048, None, need, None) == 4
     assert lib.tern_bin_gemv(P, P, P, P, 1, 16, 2048, P, need - 1, None) == 4
+    assert lib.tern_bin_gemm(P, P, P, P, 0, 0, 16, 128, P, 1 << 20, None) == 2
+    assert lib.tern_bin_gemm(P, P, P, P, 0, 4, 16, 96, P, 1 << 20, None) == 2
+    assert lib.tern_bin_gemm(P, None, P, P, 0, 4, 16, 128, P, 1 << 20, None) == 1
+    need = tern.gemm_workspace_bytes(64, 256, 512)
+    assert lib.tern_bin_gemm(P, P, P, P, 0, 64, 256, 512, P, need - 1, None) == 4

@@ -98,3 +98,59 @@ def test_bin_and_ternary_agree_on_pm1(tern, orc):
     y_ref, a_ref = orc.bin_matmul(p.x, orc.bin_pack(p.t)[0], p.s)
     assert_fp32_close(yb.cpu().numpy(), y_ref, a_ref, what="binary kernel")
     assert_fp32_close(yt.cpu().numpy(), y_ref, a_ref, what="ternary kernel on +-1")
+
+
+# --------------------------------------------------------------------------
+# the prefill product on the 1-bit layout (tcgen05).  Each weight is unpacked
+# to (2b - 1) * bf16(s): the fp32 output is held to 2^-8 * sum_k |x w| + 1e-6,
+# the bf16 output to 8e-3 * sum_k |x w| + 1e-6, as for the 2-bit layout.
+# --------------------------------------------------------------------------
+
+GEMM_REL = 2.0 ** -8
+BF16_REL = 8e-3
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (5, 200, 256), (200, 256, 1024), (300, 130, 640),
+                                   (512, 512, 2048), (17, 1000, 128), (256, 256, 8192), (40, 128, 2048)])
+def test_bin_gemm_matches_oracle(tern, orc, M, N, K):
+    p = synth.binary_problem(100 + M, M, N, K, tag=f"m{N}x{K}")
+    words = tern.bin_pack(dev_trits(p.t))
+    y = tern.bin_gemm(dev_bf16(p.x), words, dev_scales(p.s))
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    y_ref, a_ref = orc.bin_matmul(p.x, words_host(words), p.s)
+    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, rel=GEMM_REL, what=f"binary gemm M={M} N={N} K={K}")
+
+
+def test_bin_gemm_bf16_and_one_hot(tern, orc):
+    M, N, K = 256, 384, 512
+    p = synth.binary_problem(110, M, N, K, tag="b16")
+    words = tern.bin_pack(dev_trits(p.t))
+    y = tern.bin_gemm(dev_bf16(p.x), words, dev_scales(p.s), out_dtype=torch.bfloat16)
+    y_ref, a_ref = orc.bin_matmul(p.x, words_host(words), p.s)
+    assert_fp32_close(y.to(torch.float64).cpu().numpy(), y_ref, a_ref, rel=BF16_REL, what="binary gemm bf16")
+    # one-hot rows of x pick (2b - 1) * bf16(s) exactly
+    x = np.zeros((M, K), dtype=np.uint16)
+    for m in range(M):
+        x[m, (37 * m) % K] = 0x3F80
+    y = tern.bin_gemm(dev_bf16(x), words, dev_scales(p.s)).cpu().numpy()
+    sb = torch.from_numpy(p.s.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    W = p.t.astype(np.float64) * np.repeat(sb, 128, axis=1)
+    for m in range(M):
+        assert np.array_equal(y[m].astype(np.float64), W[:, (37 * m) % K]), m
+
+
+@pytest.mark.parametrize("name,K,N", [(n, k, nn) for (n, k, nn) in synth.PREFILL_LAYER])
+def test_bin_gemm_prefill_layer_sampled(tern, orc, name, K, N):
+    M = synth.PREFILL_M
+    p = synth.binary_problem(120, M, N, K, tag=f"bp{name}")
+    words = tern.bin_pack(dev_trits(p.t))
+    y = tern.bin_gemm(dev_bf16(p.x), words, dev_scales(p.s), out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    rs = np.random.default_rng(K + N + 1)
+    ms, ns = rs.integers(0, M, 3000), rs.integers(0, N, 3000)
+    ms[:4], ns[:4] = M - 1, [0, N - 1, N - 2, N // 2]
+    y_ref, a_ref = orc.bin_matmul_sampled(p.x, words_host(words), p.s, ms, ns)
+    assert_fp32_close(y.to(torch.float64).cpu().numpy()[ms, ns], y_ref, a_ref, rel=BF16_REL,
+                      what=f"binary pp512 {name}")

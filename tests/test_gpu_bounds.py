@@ -102,6 +102,23 @@ def test_gemv_writes_only_its_output(tern, orc, M, N, K):
     assert_fp32_close(y.t.cpu().numpy(), y_ref, a_ref, what=f"canary gemv M={M} N={N} K={K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 5120), (3, 777, 17408), (6, 129, 2176), (16, 200, 640)])
+def test_bin_gemv_writes_only_its_output(tern, orc, M, N, K):
+    p = synth.binary_problem(750 + M, M, N, K, tag=f"cb{N}x{K}")
+    words = Guarded((N, K // 32), torch.int32)
+    tern.bin_pack(dev_trits(p.t), words=words.t)
+    assert words.margins_intact()
+    ws = workspace(tern.gemv_workspace_bytes(M, N, K))
+    y = Guarded((M, N), torch.float32)
+    for _ in range(2):
+        tern.bin_gemv(dev_bf16(p.x), words.t, dev_scales(p.s), y=y.t, ws=ws.t)
+        assert y.margins_intact() and ws.margins_intact()
+        assert ws.inner_zero(), "the range flags are not back at zero"
+    assert tern.device_error() == 0
+    y_ref, a_ref = orc.bin_matmul(p.x, words.t.cpu().numpy().view(np.uint32), p.s)
+    assert_fp32_close(y.t.cpu().numpy(), y_ref, a_ref, what=f"canary binary M={M} N={N} K={K}")
+
+
 @pytest.mark.parametrize("M", [1, 16])
 def test_fwht_gemm_writes_only_its_output(tern, orc, M):
     N, K = 600, 4096

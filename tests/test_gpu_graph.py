@@ -157,3 +157,31 @@ def test_fused_rotation_graph(tern, orc, M):
     for c, p in enumerate(ps):
         y_ref, a_ref = orc.rotate_matmul(p.x, p.signs, host_codes(codes[c])[rows], p.s[rows])
         assert_fp32_close(ys[c].cpu().numpy()[:, rows], y_ref, a_ref, what=f"rotated graph M={M} call {c}")
+
+
+def test_binary_decode_graph(tern, orc):
+    """The 1-bit product: two layers' gate, up and down at M = 1, one graph."""
+    shapes = [(5120, 17408), (5120, 17408), (17408, 5120)] * 2
+    probs = [synth.binary_problem(1500 + i, 1, N, K, tag=f"bg{i}") for i, (K, N) in enumerate(shapes)]
+    words = [tern.bin_pack(dev_trits(p.t)) for p in probs]
+    xs = [dev_bf16(p.x) for p in probs]
+    ss = [dev_scales(p.s) for p in probs]
+    ys = [torch.empty((1, p.N), dtype=torch.float32, device="cuda") for p in probs]
+    ws = tern.workspace(max(tern.gemv_workspace_bytes(1, N, K) for K, N in shapes))
+
+    def run():
+        for i in range(len(probs)):
+            tern.bin_gemv(xs[i], words[i], ss[i], y=ys[i], ws=ws)
+
+    g = capture(run)
+    for _ in range(2):
+        g.replay()
+    for y in ys:
+        y.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    for i, p in enumerate(probs):
+        ms, ns = sample(1, p.N, 88 + i)
+        y_ref, a_ref = orc.bin_matmul_sampled(p.x, words[i].cpu().numpy().view(np.uint32), p.s, ms, ns)
+        assert_fp32_close(ys[i].cpu().numpy()[ms, ns], y_ref, a_ref, what=f"binary graph product {i}")
