@@ -121,3 +121,16 @@ def test_gemm_stream_k_split_tiles(tern, orc, M, N, K):
     assert tern.device_error() == 0
     assert_fp32_close(y2.cpu().numpy(), y_ref, a_ref, rel=GEMM_REL, what=f"stream-K second call M={M}")
     assert_fp32_close(y1.cpu().numpy(), y_ref, a_ref, rel=GEMM_REL, what=f"stream-K first call M={M}")
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 64, 65536), (1100, 48, 1024), (8, 4096, 128)])
+def test_gemm_extreme_shapes(tern, orc, M, N, K):
+    """Very deep K on few tiles (stream-K over hundreds of stages), many
+    token tiles on one row tile, and the shortest K."""
+    p = synth.problem(1700 + M, M, N, K, tag=f"xe{N}x{K}")
+    y, codes = run(tern, p)
+    rs = np.random.default_rng(M + N + K)
+    ms, ns = rs.integers(0, M, 2000), rs.integers(0, N, 2000)
+    ms[0], ns[0] = M - 1, N - 1
+    y_ref, a_ref = orc.matmul_sampled(p.x, host_codes(codes), p.s, ms, ns)
+    assert_fp32_close(y.cpu().numpy()[ms, ns], y_ref, a_ref, rel=GEMM_REL, what=f"extreme gemm M={M} N={N} K={K}")

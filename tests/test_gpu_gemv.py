@@ -294,3 +294,24 @@ def test_gemv_overwrites_prefilled_y(tern, orc, M, N, K):
     torch.cuda.synchronize()
     y_ref, a_ref = orc.matmul(p.x, host_codes(codes), p.s)
     assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what=f"prefilled y M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 64, 131072), (16, 40, 65536), (1, 262144, 1024), (3, 131091, 2048),
+                                   (1, 1, 128), (16, 1, 17408)])
+def test_gemv_extreme_shapes(tern, orc, M, N, K):
+    """Very deep K (128 to 1024 groups: up to 128 K-slices per row range),
+    very tall N (16,384 tiles: several CTAs per SM of ranges), and single
+    rows; sampled outputs against the oracle."""
+    p = synth.problem(1600 + M, M, N, K, tag=f"x{N}x{K}")
+    codes = tern.pack(dev_trits(p.t))
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    tern.gemv(dev_bf16(p.x), codes, dev_scales(p.s), y=y)
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    rs = np.random.default_rng(N + K)
+    n = min(2000, M * N)
+    ms, ns = rs.integers(0, M, n), rs.integers(0, N, n)
+    ms[0], ns[0] = M - 1, N - 1
+    y_ref, a_ref = orc.matmul_sampled(p.x, host_codes(codes), p.s, ms, ns)
+    assert_fp32_close(y.cpu().numpy()[ms, ns], y_ref, a_ref, what=f"extreme M={M} N={N} K={K}")
+    assert torch.isfinite(y).all()
