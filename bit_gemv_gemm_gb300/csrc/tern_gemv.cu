@@ -41,10 +41,10 @@
 // 8 groups left over is cut into eight tile chunks, one per warp.  A warp
 // stages one segment's activation into registers and streams its own
 // 32-byte column of every tile of the segment (16 rows x 32 B = one 16-byte
-// cp.async per lane) through a
-// private shared-memory ring, kDepth units ahead; the first kEarly units go out
-// before the programmatic-dependent-launch wait, the rest after staging.  Two tiles per step run as two
-// independent MMA chains.  Row partials go to shared memory (private per warp
+// cp.async per lane) through a private shared-memory ring, kDepth units ahead;
+// the first kEarly units go out before the programmatic-dependent-launch wait,
+// the rest after staging.  Two tiles per step run as two independent MMA
+// chains.  Row partials go to shared memory (private per warp
 // for M <= 4, shared atomics beyond) and are summed over the CTA's warps.
 // With one slice the CTA stores its rows of y.  With several, the slice-0 CTA
 // of a range clears the range's rows of y right after the PDL wait and then
@@ -54,6 +54,16 @@
 // counts modulo S (atomicInc), so it is back at 0 when the call ends.  The
 // order in which the S slice sums meet is not fixed: the last bits of y may
 // differ from run to run.
+//
+// The 1-bit sibling format (w = (2b - 1) s, bit k%32 of word k/32) runs the
+// same kernel with BIN set: a unit is 16 rows x 16 bytes, slot s of a word is
+// bits s and s + 16 (read as b * 2^(s' - 24)), MMA j takes slots j and j + 8,
+// and y = s F (2 acc - acc1).
+//
+// The rotation-fused call runs rotate_stage_kernel first: it rotates x, then
+// stages it exactly as the product would (exponent and scaled fp16 values, in
+// B-fragment order) into the workspace, and the product (PRE) loads the
+// fragments as they are.
 #include <mutex>
 #include <type_traits>
 
