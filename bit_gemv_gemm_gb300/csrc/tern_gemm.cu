@@ -24,9 +24,14 @@
 //     accumulating fp32 in tensor memory;
 //   * four epilogue warps read the accumulator with tcgen05.ld and store y
 //     (fp32 or bf16) with coalesced stores along n.
-// Scheduling is stream-K: the (tile, 64-wide K stage) iterations, tile-major,
-// are cut into one equal contiguous share per CTA, so no SM idles behind a
-// partial last wave.  A CTA's share is a run of segments, each a stretch of
+// The 1-bit sibling format (w = (2b - 1) s) runs the same kernel: its code box
+// is 16 bytes per row too, but spans two K stages (starting at the even one, so
+// the TMA x coordinate stays 16-byte aligned), and the unpack turns bits j and
+// j + 16 of a word into bf16 2b - 1 with one shift and one FMA.
+// Scheduling takes whole tiles on a persistent grid, or stream-K where whole
+// tiles would leave SMs idle longer than stream-K's tail costs: the (tile,
+// 64-wide K stage) iterations, tile-major, are cut into one equal contiguous
+// share per CTA, so no SM idles behind a partial last wave.  A CTA's share is a run of segments, each a stretch of
 // one tile's K stages; a CTA runs its (at most two) partial segments first and
 // its whole tiles after.  A segment that covers its whole tile is written to y
 // directly.  A partial one adds its fp32 accumulator into the tile's fp32 sum
