@@ -134,3 +134,22 @@ def test_gemm_extreme_shapes(tern, orc, M, N, K):
     ms[0], ns[0] = M - 1, N - 1
     y_ref, a_ref = orc.matmul_sampled(p.x, host_codes(codes), p.s, ms, ns)
     assert_fp32_close(y.cpu().numpy()[ms, ns], y_ref, a_ref, rel=GEMM_REL, what=f"extreme gemm M={M} N={N} K={K}")
+
+
+def test_gemm_large_and_mixed_scales(tern, orc):
+    """Scales up to a few hundred, mixed with small ones per group and row
+    (the unpack's q * 2^-126 trick and the bf16 scale must hold over the whole
+    fp16 scale range, not only the small scales of the synthetic workloads)."""
+    M, N, K = 300, 256, 1024
+    p = synth.problem(1800, M, N, K, tag="bigs")
+    rs = np.random.default_rng(1800)
+    big = rs.random((N, K // 128)) < 0.3
+    s = np.where(big, rs.uniform(4.0, 300.0, (N, K // 128)), rs.uniform(0.01, 3.9, (N, K // 128))).astype(np.float16)
+    s[:32, :] = np.float16(3.99)
+    s[32:64, 0] = np.float16(60000.0)    # near the fp16 maximum
+    codes = tern.pack(dev_trits(p.t))
+    y = tern.gemm(dev_bf16(p.x), codes, dev_scales(s))
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    y_ref, a_ref = orc.matmul(p.x, host_codes(codes), s)
+    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, rel=GEMM_REL, what="mixed scales")
