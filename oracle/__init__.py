@@ -61,6 +61,7 @@ def _load():
                 "orc_bin_unpack": (_I, [_P, _I, _I, _P]),
                 "orc_bin_matmul": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _I]),
                 "orc_bin_matmul_sampled": (_I, [_P, _P, _P, _I, _P, _P, _I, _P, _P, _I]),
+                "orc_scales_from_g64": (ctypes.c_longlong, [_P, _I, _I, _P]),
                 "orc_mlx_affine": (ctypes.c_float, [_I, ctypes.c_float, ctypes.c_float]),
                 "orc_hadamard_explicit": (_I, [_I, _P]),
                 "orc_fwht": (_I, [_P, _I]),
@@ -172,6 +173,18 @@ def bin_matmul_sampled(x_bf16: np.ndarray, words: np.ndarray, scales_f16: np.nda
                                       _ptr(y), _ptr(a), nthreads) != 0:
         raise ValueError("bad shape")
     return y, a
+
+
+def scales_from_g64(s64: np.ndarray) -> tuple[np.ndarray, int]:
+    """fp16 scales [N, K/64] of the group-size-64 pack -> ([N, K/128], count of
+    groups whose two halves differ)."""
+    s64 = _bits16(np.ascontiguousarray(s64))
+    N, G2 = s64.shape
+    out = np.empty((N, G2 // 2), dtype=np.uint16)
+    bad = _load().orc_scales_from_g64(_ptr(s64), N, G2 * 64, _ptr(out))
+    if bad < 0:
+        raise ValueError("K must be a multiple of 128")
+    return out.view(np.float16), int(bad)
 
 
 def _bits16(a: np.ndarray) -> np.ndarray:

@@ -341,6 +341,30 @@ int orc_bin_matmul_sampled(const uint16_t *x, const uint32_t *words,
 }
 
 /* ------------------------------------------------------------------------ */
+/* The group-size-64 pack ([card] "Shipped components"): the same g128       */
+/* weights, each scale repeated in both 64-value halves of its group.        */
+/* ------------------------------------------------------------------------ */
+
+/* s128[n][g] = s64[n][2g] for fp16 bit patterns s64 [N][K/64].  A group
+ * whose two halves differ (bit for bit) is counted; its first half's scale is
+ * kept.  Returns the count, or -1 if K is not a multiple of 128. */
+long long orc_scales_from_g64(const uint16_t *s64, int N, int K, uint16_t *s128)
+{
+    if (N < 0 || K < 0 || K % 128 != 0)
+        return -1;
+    long long bad = 0;
+    int G = K / 128;
+    for (int n = 0; n < N; ++n)
+        for (int g = 0; g < G; ++g) {
+            uint16_t a = s64[(size_t)n * 2 * G + 2 * g], b = s64[(size_t)n * 2 * G + 2 * g + 1];
+            if (a != b)
+                ++bad;
+            s128[(size_t)n * G + g] = a;
+        }
+    return bad;
+}
+
+/* ------------------------------------------------------------------------ */
 /* MLX affine 2-bit dequantisation, w = s_mlx * q + bias, in float.          */
 /* ([card] "MLX packaging": a group stores a scale and a bias.)              */
 /* ------------------------------------------------------------------------ */

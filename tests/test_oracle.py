@@ -495,3 +495,22 @@ def test_bin_matmul_sampled_equals_full(orc):
     ns = np.tile(np.arange(N), M)
     ys, as_ = orc.bin_matmul_sampled(x, words, s, ms, ns)
     assert np.array_equal(ys, y.reshape(-1)) and np.array_equal(as_, a.reshape(-1))
+
+
+# --------------------------------------------------------------------------
+# the group-size-64 pack's scales: each g128 scale repeated in both halves
+# --------------------------------------------------------------------------
+
+def test_scales_from_g64(orc):
+    s128 = synth.scales(60, "g64", (7, 5))
+    s64 = np.repeat(s128, 2, axis=1)                  # the repeated layout, built independently
+    out, bad = orc.scales_from_g64(s64)
+    assert bad == 0 and np.array_equal(out.view(np.uint16), s128.view(np.uint16))
+    s64[2, 3] = np.float16(0.5)                       # second half of group 1 differs
+    s64[6, 8] = np.float16(-0.0)                      # first half of group 4 differs (bitwise)
+    out, bad = orc.scales_from_g64(s64)
+    assert bad == 2
+    assert out[2, 1] == s128[2, 1] and out[6, 4].view(np.uint16) == np.float16(-0.0).view(np.uint16)
+    # the card's pack sizes agree with one fp16 per 64 weights instead of per 128
+    g = json.load(open(os.path.join(GOLDEN, "bitrates.json")))
+    assert abs(g["lm_pack_g64_gb"]["value"] / g["lm_pack_g128_gb"]["value"] - (2 + 16 / 64) / (2 + 16 / 128)) < 1e-3
