@@ -49,6 +49,8 @@ EXPORTS = {
     "tern_gemv_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "tern_wait_selftest": (_I, [_I, _I, _P]),
     "tern_bin_packed_bytes": (_SZ, [_I, _I]),
+    "tern_scales_from_g64": (_I, [_P, _I, _I, _P, _P, _P]),
+    "tern_scales_from_g64_host": (_I, [_P, _I, _I, _P, _P]),
     "tern_bin_pack": (_I, [_P, _I, _I, _P, _P, _P]),
     "tern_bin_pack_host": (_I, [_P, _I, _I, _P, _P]),
     "tern_bin_unpack_host": (_I, [_P, _I, _I, _P]),
@@ -140,6 +142,27 @@ def pack(t: torch.Tensor, codes: torch.Tensor | None = None, bad_count: torch.Te
     _check("tern_pack", lib().tern_pack(_dev(t, torch.int8, "t"), N, K, _dev(codes, torch.int32, "codes"),
                                         bp, _stream(stream)))
     return codes
+
+
+def scales_from_g64(s64: torch.Tensor, K: int, mismatch: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Scales of the group-size-64 pack (fp16 [N, K/64], each g128 scale
+    repeated) -> g128 scales fp16 [N, K/128]; differing halves are counted."""
+    N = s64.shape[0]
+    out = torch.empty((N, K // 128), dtype=torch.float16, device=s64.device)
+    mp = _dev(mismatch, torch.int32, "mismatch") if mismatch is not None else None
+    _check("tern_scales_from_g64", lib().tern_scales_from_g64(_dev(s64, torch.float16, "s64"), N, K,
+                                                              _dev(out, torch.float16, "s128"), mp, _stream(stream)))
+    return out
+
+
+def scales_from_g64_host(s64: np.ndarray, K: int) -> tuple[np.ndarray, int]:
+    s64 = np.ascontiguousarray(s64, dtype=np.float16)
+    N = s64.shape[0]
+    out = np.empty((N, K // 128), dtype=np.float16)
+    bad = ctypes.c_longlong(0)
+    _check("tern_scales_from_g64_host", lib().tern_scales_from_g64_host(s64.ctypes.data, N, K, out.ctypes.data,
+                                                                        ctypes.byref(bad)))
+    return out, int(bad.value)
 
 
 def bin_pack(t: torch.Tensor, words: torch.Tensor | None = None, bad_count: torch.Tensor | None = None,

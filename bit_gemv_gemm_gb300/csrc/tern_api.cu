@@ -166,6 +166,21 @@ tern_status tern_bin_unpack_host(const uint32_t* words, int N, int K, int8_t* t)
     return TERN_OK;
 }
 
+tern_status tern_scales_from_g64_host(const void* s64, int N, int K, void* s128, long long* mismatch) {
+    if (N < 0 || K < 0 || K % 128 != 0) return TERN_ERR_SHAPE;
+    if ((N > 0 && K > 0) && (!s64 || !s128)) return TERN_ERR_NULL;
+    const uint16_t* in = static_cast<const uint16_t*>(s64);
+    uint16_t* out = static_cast<uint16_t*>(s128);
+    long long bad = 0;
+    const size_t groups = (size_t)N * (size_t)(K / 128);
+    for (size_t i = 0; i < groups; ++i) {
+        bad += in[2 * i] != in[2 * i + 1];
+        out[i] = in[2 * i];
+    }
+    if (mismatch) *mismatch = bad;
+    return TERN_OK;
+}
+
 size_t tern_bin_packed_bytes(int N, int K) {
     if (N < 0 || K < 0 || K % 128 != 0) return 0;
     return (size_t)N * (size_t)K / 8 + (size_t)N * (size_t)K / 64;

@@ -73,10 +73,52 @@ bin_pack_kernel(const int4* __restrict__ t, uint32_t* __restrict__ words_out, lo
     }
 }
 
+// The group-size-64 pack's scales: group g of a row is the pair (2g, 2g + 1),
+// which the pack repeats; one thread per output scale keeps the first and
+// counts pairs that differ bit for bit.
+__global__ void __launch_bounds__(kPackThreads)
+scales_g64_kernel(const unsigned short* __restrict__ s64, unsigned short* __restrict__ s128, long long groups,
+                  int* __restrict__ mismatch) {
+    int bad = 0;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < groups; i += stride) {
+        const unsigned int pair = reinterpret_cast<const unsigned int*>(s64)[i];   // (s[2g], s[2g+1])
+        const unsigned short lo = (unsigned short)(pair & 0xFFFFu), hi = (unsigned short)(pair >> 16);
+        bad += lo != hi;
+        s128[i] = lo;
+    }
+    if (mismatch) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+        if ((threadIdx.x & 31) == 0 && bad) atomicAdd(mismatch, bad);
+    }
+}
+
 }  // namespace
 }  // namespace tern
 
 using namespace tern;
+
+extern "C" tern_status tern_scales_from_g64(const void* s64, int N, int K, void* s128, int* mismatch,
+                                            tern_stream_t stream) {
+    set_launch_count(0);
+    if (N < 0 || K < 0 || K % 128 != 0) return TERN_ERR_SHAPE;
+    const long long groups = (long long)N * (K / 128);
+    if (groups == 0) return TERN_OK;
+    if (!s64 || !s128) return TERN_ERR_NULL;
+    if (!aligned16(s64) || !aligned16(s128)) return TERN_ERR_ALIGN;
+    int sms = 0;
+    tern_status st = check_device(&sms);
+    if (st != TERN_OK) return st;
+    long long blocks = (groups + kPackThreads - 1) / kPackThreads;
+    const long long cap = (long long)sms * 8;
+    if (blocks > cap) blocks = cap;
+    scales_g64_kernel<<<(unsigned)blocks, kPackThreads, 0, (cudaStream_t)stream>>>(
+        reinterpret_cast<const unsigned short*>(s64), reinterpret_cast<unsigned short*>(s128), groups, mismatch);
+    if (cudaGetLastError() != cudaSuccess) return TERN_ERR_CUDA;
+    set_launch_count(1);
+    return TERN_OK;
+}
 
 extern "C" tern_status tern_bin_pack(const int8_t* t, int N, int K, uint32_t* words, int* bad_count,
                                      tern_stream_t stream) {

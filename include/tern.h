@@ -102,6 +102,19 @@ tern_status tern_unpack_host(const uint32_t *codes, int N, int K, int8_t *t,
 /* Host validator: counts code-3 slots in codes [N][K/16] into *bad_count. */
 tern_status tern_validate_host(const uint32_t *codes, int N, int K, long long *bad_count);
 
+/* The group-size-64 pack ([card] "Shipped components": the same g128
+ * representation with each scale repeated in both 64-value halves of its
+ * group, 7.59 GB against 7.17): its scales s64, fp16 [N][K/64], become the
+ * g128 scales s128, fp16 [N][K/128], with s128[n][g] = s64[n][2g].  A group
+ * whose halves differ bit for bit is counted (into *mismatch, a device int
+ * the call ADDS to, for the device version; stored, for the host one) and
+ * keeps its first half's scale.  The codes are taken to be in the layout
+ * above; the pages give no other bit order for that pack.  K % 128 == 0,
+ * N >= 0 (TERN_ERR_SHAPE otherwise); pointers 16-byte aligned. */
+tern_status tern_scales_from_g64(const void *s64, int N, int K, void *s128, int *mismatch,
+                                 tern_stream_t stream);
+tern_status tern_scales_from_g64_host(const void *s64, int N, int K, void *s128, long long *mismatch);
+
 /* ---------------------------------------------------------------------- */
 /* The 1-bit sibling, binary g128 (card, "Highlights" and "Benchmarks":    */
 /* 1-bit Bonsai at 1.125 bits per weight; "MLX packaging": s_mlx = 2 s_g,   */

@@ -197,3 +197,16 @@ def test_bin_argument_errors_never_launch(tern):
     assert lib.tern_bin_gemm(P, None, P, P, 0, 4, 16, 128, P, 1 << 20, None) == 1
     need = tern.gemm_workspace_bytes(64, 256, 512)
     assert lib.tern_bin_gemm(P, P, P, P, 0, 64, 256, 512, P, need - 1, None) == 4
+
+
+def test_scales_from_g64_host_matches_oracle(tern, orc):
+    s128 = synth.scales(61, "g64h", (9, 12))
+    s64 = np.repeat(s128, 2, axis=1)
+    s64[4, 7] = np.float16(1.5)
+    out, bad = tern.scales_from_g64_host(s64, 12 * 128)
+    want, wbad = orc.scales_from_g64(s64)
+    assert bad == wbad == 1
+    assert np.array_equal(out.view(np.uint16), want.view(np.uint16))
+    lib = tern.lib()
+    assert lib.tern_scales_from_g64(4096, 4, 192, 4096, None, None) == 2      # K % 128
+    assert lib.tern_scales_from_g64(None, 4, 256, 4096, None, None) == 1

@@ -315,3 +315,29 @@ def test_gemv_extreme_shapes(tern, orc, M, N, K):
     y_ref, a_ref = orc.matmul_sampled(p.x, host_codes(codes), p.s, ms, ns)
     assert_fp32_close(y.cpu().numpy()[ms, ns], y_ref, a_ref, what=f"extreme M={M} N={N} K={K}")
     assert torch.isfinite(y).all()
+
+
+def test_scales_from_g64_device(tern, orc):
+    """The group-size-64 pack's scales on the device: bit-exact against the
+    oracle, differing halves counted, and the product on the converted scales
+    equal to the product on the g128 scales."""
+    N, K = 1000, 5120
+    s128 = synth.scales(62, "g64d", (N, K // 128))
+    s64 = np.repeat(s128, 2, axis=1)
+    s64[10, 3] = np.float16(0.25)
+    s64[999, 79] = np.float16(-1.0)
+    mism = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = tern.scales_from_g64(torch.from_numpy(s64).cuda(), K, mismatch=mism)
+    want, wbad = orc.scales_from_g64(s64)
+    assert int(mism.item()) == wbad == 2
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), want.view(np.uint16))
+    s64 = np.repeat(s128, 2, axis=1)
+    p = synth.problem(63, 1, N, K, tag="g64p")
+    codes = tern.pack(dev_trits(p.t))
+    x = dev_bf16(p.x)
+    y64 = tern.gemv(x, codes, tern.scales_from_g64(torch.from_numpy(s64).cuda(), K))
+    y128 = tern.gemv(x, codes, dev_scales(s128))
+    torch.cuda.synchronize()
+    y_ref, a_ref = orc.matmul(p.x, host_codes(codes), s128)
+    assert_fp32_close(y64.cpu().numpy(), y_ref, a_ref, what="g64 scales")
+    assert_fp32_close(y128.cpu().numpy(), y_ref, a_ref, what="g128 scales")
