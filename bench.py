@@ -341,6 +341,38 @@ def bench_verify(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int):
     return out
 
 
+def bench_fused_gate_up(tern, sweep: DecodeSweep, steps: int, warmup: int, hbm: float):
+    """The decode sweep with each layer's gate and up weights stored as one
+    5120 -> 34816 matrix (one call for both, as an engine that keeps a fused
+    gate_up projection would run it) and the same down calls: how much of the
+    per-call fixed cost two matrices in one launch recover."""
+    import torch
+    import synth
+    layers = len(sweep.layers)
+    gu = []
+    for l in range(layers):
+        t = synth.device_trits(9, f"GU{l}.t", (2 * 17408, 5120))
+        gu.append((tern.pack(t), synth.device_scales(9, f"GU{l}.s", (2 * 17408, 40))))
+        del t
+    x5 = [synth.device_activations(9, f"GU{l}.x", (1, 5120)) for l in range(layers)]
+    x17 = [synth.device_activations(9, f"GD{l}.x", (1, 17408)) for l in range(layers)]
+    ygu = torch.empty((1, 2 * 17408), dtype=torch.float32, device="cuda")
+    yd = torch.empty((1, 5120), dtype=torch.float32, device="cuda")
+    ws = tern.workspace(max(tern.gemv_workspace_bytes(1, 2 * 17408, 5120), tern.gemv_workspace_bytes(1, 5120, 17408)))
+
+    def run():
+        for l in range(layers):
+            tern.gemv(x5[l], gu[l][0], gu[l][1], y=ygu, ws=ws)
+            d = sweep.layers[l][2]
+            tern.gemv(x17[l], d[3], d[4], y=yd, ws=ws)
+
+    g = graph_of(run)
+    ms = time_graph(g, max(3, steps // 4), warmup)
+    wb = layers * (weight_bytes(2 * 17408, 5120) + weight_bytes(5120, 17408))
+    gbps = wb / (ms * 1e-3) / 1e9
+    return {"layers": layers, "launches": 2 * layers, "ms_per_step": ms, "weight_GBps": gbps, "hbm_frac": gbps / hbm}
+
+
 def bench_verify_step(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int):
     """One speculative-verify step as a CUDA graph: k + 1 = 5 tokens through
     every layer's qkv (5120 -> 6144), gate, up (5120 -> 17408) and down
@@ -589,7 +621,7 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=DECODE_LAYERS)
-    ap.add_argument("--skip", default="", help="comma list of parts to skip: verify,rotated,binary,prefill,cpu")
+    ap.add_argument("--skip", default="", help="comma list of parts to skip: fused,verify,rotated,binary,prefill,cpu")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -620,6 +652,8 @@ def main() -> None:
     achieved = dec["alg_bytes"] / (dec["ms"] * 1e-3) / 1e9
     hbm = peaks["hbm_gbs"]
     rows = {}
+    if "fused" not in skip:
+        rows["fused_gate_up"] = bench_fused_gate_up(tern, sweep, args.steps, args.warmup, hbm)
     if "verify" not in skip:
         rows["verify"] = bench_verify(tern, sweep, qkv, args.steps, args.warmup)
         rows["verify_step"] = bench_verify_step(tern, sweep, qkv, args.steps, args.warmup)
