@@ -230,35 +230,54 @@ class DecodeSweep:
     def weight_bytes(self) -> int:
         return sum(weight_bytes(N, K) for projs in self.layers for (_, K, N, _, _) in projs)
 
-    def buffers(self, M: int, seed: int = 2):
-        """Per-projection x, y and one shared workspace for M tokens."""
+    def buffers(self, M: int, seed: int = 2, pair: bool = True):
+        """x, y and one shared workspace for M tokens.  With `pair`, gate and up
+        read one activation (as in the model); otherwise every projection has
+        its own."""
         import torch
         import synth
         xs, ys = [], []
         for l, projs in enumerate(self.layers):
             for (name, K, N, _, _) in projs:
-                xs.append(synth.device_activations(seed, f"L{l}.{name}.x{M}", (M, K)))
+                if not (pair and name == "up"):
+                    xs.append(synth.device_activations(seed, f"L{l}.{name}.x{M}", (M, K)))
                 ys.append(torch.empty((M, N), dtype=torch.float32, device="cuda"))
-        ws = self.tern.workspace(max(self.tern.gemv_workspace_bytes(M, N, K) for (_, K, N) in self.shapes))
-        return xs, ys, ws
+        need = [self.tern.gemv_workspace_bytes(M, N, K) for (_, K, N) in self.shapes]
+        need.append(int(self.tern.lib().tern_gemv_pair_workspace_bytes(M, 17408, 17408, 5120)))
+        return xs, ys, self.tern.workspace(max(need))
 
-    def run(self, xs, ys, ws):
+    def run(self, xs, ys, ws, pair: bool = True):
+        """One decode step: with `pair`, gate and up in one tern_gemv_pair call
+        on their shared activation, then down; otherwise three tern_gemv calls."""
+        if pair:
+            for l, (g, u, d) in enumerate(self.layers):
+                self.tern.gemv_pair(xs[2 * l], g[3], g[4], u[3], u[4], y_a=ys[3 * l], y_b=ys[3 * l + 1], ws=ws)
+                self.tern.gemv(xs[2 * l + 1], d[3], d[4], y=ys[3 * l + 2], ws=ws)
+            return
         i = 0
         for projs in self.layers:
             for (_, K, N, codes, s) in projs:
                 self.tern.gemv(xs[i], codes, s, y=ys[i], ws=ws)
                 i += 1
 
-    def alg_bytes(self, M: int) -> int:
-        return sum(weight_bytes(N, K) + 2 * M * K + 4 * M * N
-                   for projs in self.layers for (_, K, N, _, _) in projs)
+    def launches(self, pair: bool = True) -> int:
+        return (2 if pair else 3) * len(self.layers)
+
+    def alg_bytes(self, M: int, pair: bool = True) -> int:
+        """Codes, scales, x (read once per call) and y of one step."""
+        b = 0
+        for projs in self.layers:
+            for (name, K, N, _, _) in projs:
+                b += weight_bytes(N, K) + 4 * M * N + (0 if (pair and name == "up") else 2 * M * K)
+        return b
 
 
-def bench_decode(tern, sweep: DecodeSweep, steps: int, warmup: int, ws_count: int, dev_index: int):
+def bench_decode(tern, sweep: DecodeSweep, steps: int, warmup: int, ws_count: int, dev_index: int,
+                 pair: bool = True):
     import torch
     M = 1
-    xs, ys, ws = sweep.buffers(M)
-    g = graph_of(lambda: sweep.run(xs, ys, ws))
+    xs, ys, ws = sweep.buffers(M, pair=pair)
+    g = graph_of(lambda: sweep.run(xs, ys, ws, pair))
     time_graph(g, 2, warmup)                       # warm
     with ClockSampler(dev_index) as clk:
         barrier(ws_count)
@@ -267,7 +286,7 @@ def bench_decode(tern, sweep: DecodeSweep, steps: int, warmup: int, ws_count: in
         torch.cuda.synchronize()
         barrier(ws_count)
     ms = max_over_ranks(ms, ws_count)
-    launches = sum(len(p) for p in sweep.layers)        # one kernel per tern_gemv call
+    launches = sweep.launches(pair)                    # one kernel per tern_gemv / tern_gemv_pair call
 
     # end to end through the same API: H2D of every projection's x, the sweep,
     # D2H of every y; pinned host buffers, copies inside the timed region.
@@ -285,7 +304,7 @@ def bench_decode(tern, sweep: DecodeSweep, steps: int, warmup: int, ws_count: in
     for y in ys:
         yviews.append(yout[off:off + y.numel()].view(y.shape))
         off += y.numel()
-    g2 = graph_of(lambda: sweep.run(views, yviews, ws))
+    g2 = graph_of(lambda: sweep.run(views, yviews, ws, pair))
     st = torch.cuda.current_stream()
 
     def e2e_step():
@@ -308,7 +327,7 @@ def bench_decode(tern, sweep: DecodeSweep, steps: int, warmup: int, ws_count: in
     del xh, yh
     return {
         "ms": ms, "clocks": clk.summary(), "launches_per_step": launches,
-        "weight_bytes": sweep.weight_bytes(), "alg_bytes": sweep.alg_bytes(M),
+        "weight_bytes": sweep.weight_bytes(), "alg_bytes": sweep.alg_bytes(M, pair),
         "e2e_ms": e2e_ms, "h2d": xhost.numel() * 2, "d2h": yhost.numel() * 4,
     }
 
@@ -653,6 +672,10 @@ def main() -> None:
     hbm = peaks["hbm_gbs"]
     rows = {}
     if "fused" not in skip:
+        sep = bench_decode(tern, sweep, args.steps, args.warmup, 1, dev_index, pair=False)
+        sgb = sep["weight_bytes"] / (sep["ms"] * 1e-3) / 1e9
+        rows["separate_calls"] = {"launches": sep["launches_per_step"], "ms_per_step": sep["ms"],
+                                  "weight_GBps": sgb, "hbm_frac": sgb / hbm}
         rows["fused_gate_up"] = bench_fused_gate_up(tern, sweep, args.steps, args.warmup, hbm)
     if "verify" not in skip:
         rows["verify"] = bench_verify(tern, sweep, qkv, args.steps, args.warmup)
@@ -677,13 +700,14 @@ def main() -> None:
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"decode GEMV M=1 sweep, {args.layers} layers x (gate 5120->17408, "
-                               f"up 5120->17408, down 17408->5120), distinct weights",
+        "config": {"workload": f"decode GEMV M=1 sweep, {args.layers} layers x (gate 5120->17408 and "
+                               f"up 5120->17408 reading one activation in one tern_gemv_pair call, "
+                               f"down 17408->5120), distinct weights",
                    "M": 1, "layers": args.layers, "weight_bytes_per_step": dec["weight_bytes"],
                    "l2": "inputs larger than L2 (4.55 GB of weights per step vs 129 MB L2)",
                    "parallelism": f"replicas x{ws_count}", "cuda_graph": True},
         "hbm_frac": value / ws_count / hbm,
-        "roofline": {"bound": "hbm", "kernel": "gemv_kernel (one launch per tern_gemv call)",
+        "roofline": {"bound": "hbm", "kernel": "gemv_kernel (one launch per tern_gemv_pair or tern_gemv call)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": f"{peaks['_source']} hbm_gbs",
                      "traffic": load_traffic("gemv_kernel", GEMV_SRC)},

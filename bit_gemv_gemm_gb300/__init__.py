@@ -47,6 +47,8 @@ EXPORTS = {
     "tern_device_error": (_I, [_P]),
     "tern_last_launch_count": (_I, []),
     "tern_gemv_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
+    "tern_gemv_pair_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "tern_gemv_pair": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
     "tern_wait_selftest": (_I, [_I, _I, _P]),
     "tern_bin_packed_bytes": (_SZ, [_I, _I]),
     "tern_scales_from_g64": (_I, [_P, _I, _I, _P, _P, _P]),
@@ -254,6 +256,26 @@ def bin_gemv(x: torch.Tensor, words: torch.Tensor, scales: torch.Tensor, y: torc
         _dev(x, torch.bfloat16, "x"), _dev(words, torch.int32, "words"), _dev(scales, torch.float16, "scales"),
         _dev(y, torch.float32, "y"), M, N, K, _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
     return y
+
+
+def gemv_pair(x: torch.Tensor, codes_a: torch.Tensor, scales_a: torch.Tensor, codes_b: torch.Tensor,
+              scales_b: torch.Tensor, y_a: torch.Tensor | None = None, y_b: torch.Tensor | None = None,
+              ws: torch.Tensor | None = None, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Two products of the same activation in one launch: (x W_a^T, x W_b^T)."""
+    M, K = x.shape
+    Na, Nb = codes_a.shape[0], codes_b.shape[0]
+    if y_a is None:
+        y_a = torch.empty((M, Na), dtype=torch.float32, device=x.device)
+    if y_b is None:
+        y_b = torch.empty((M, Nb), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(int(lib().tern_gemv_pair_workspace_bytes(M, Na, Nb, K)), x.device)
+    _check("tern_gemv_pair", lib().tern_gemv_pair(
+        _dev(x, torch.bfloat16, "x"), _dev(codes_a, torch.int32, "codes_a"), _dev(scales_a, torch.float16, "scales_a"),
+        _dev(y_a, torch.float32, "y_a"), Na, _dev(codes_b, torch.int32, "codes_b"),
+        _dev(scales_b, torch.float16, "scales_b"), _dev(y_b, torch.float32, "y_b"), Nb, M, K,
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return y_a, y_b
 
 
 def gemv_noalloc(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor | None = None,

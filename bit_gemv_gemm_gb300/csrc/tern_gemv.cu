@@ -94,6 +94,12 @@ struct GemvArgs {
     const uint32_t* codes;      // [N][K/16]
     const __half* scales;       // [N][K/128]
     float* y;                   // [M][N]
+    // a pair call: a second matrix (N2 rows, T2 tiles) read with the same x;
+    // ranges [cps1, cps) are its, [0, cps1) the first one's (cps1 = cps otherwise)
+    const uint32_t* codes2;
+    const __half* scales2;
+    float* y2;
+    int N2, T2, cps1;
     unsigned* flag;             // [cps] per-range flag words (S > 1), 0 between calls
     int M, N, K, G, T, S, cps, rmax;
     int gpad;                   // scale row pitch in shared memory (halves)
@@ -276,16 +282,25 @@ gemv_kernel(const GemvArgs a) {
     constexpr int SLOT = BIN ? kBinSlotBytes : kSlotBytes;
     extern __shared__ __align__(16) unsigned char smem[];
     const int M = ONE ? 1 : a.M;
-    const int N = a.N, G = a.G, S = a.S, rmax = a.rmax, gpad = a.gpad;
+    const int G = a.G, S = a.S, rmax = a.rmax, gpad = a.gpad;
     const int W = a.K / (BIN ? 32 : 16);   // code words per row
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, t = lane & 3;
     const int sigma = blockIdx.x / a.cps, clu = blockIdx.x - sigma * a.cps;   // slice, range
+    // the matrix this range belongs to (a pair call's ranges never straddle the two)
+    const bool second = clu >= a.cps1;
+    const uint32_t* const codes = second ? a.codes2 : a.codes;
+    const __half* const scales = second ? a.scales2 : a.scales;
+    float* const yv = second ? a.y2 : a.y;
+    const int N = second ? a.N2 : a.N;
+    const int Tm = second ? a.T2 : a.T;
+    const int cpsm = second ? a.cps - a.cps1 : a.cps1;
+    const int clm = second ? clu - a.cps1 : clu;
     const int gA = BIN ? kWarps * sigma : (int)((long long)G * sigma / S);
     const int gB = BIN ? min(gA + kWarps, G) : (int)((long long)G * (sigma + 1) / S);
     const int Gs = gB - gA;
-    const int tile_lo = (int)((long long)a.T * clu / a.cps);
-    const int R = (int)((long long)a.T * (clu + 1) / a.cps) - tile_lo;
+    const int tile_lo = (int)((long long)Tm * clm / cpsm);
+    const int R = (int)((long long)Tm * (clm + 1) / cpsm) - tile_lo;
     const int na = Gs / kWarps, nb = Gs - na * kWarps, nseg = na + nb;
     const int g_lo = scale_lo(G, gA, gB);
 
@@ -307,7 +322,7 @@ gemv_kernel(const GemvArgs a) {
     const size_t cstep = (size_t)16 * W;   // words from one tile to the next
     // issue cursor: segment, units left in it, this lane's next row and source
     int is = 0, ileft = 0, irow = 0;
-    const uint32_t* iptr = a.codes;
+    const uint32_t* iptr = codes;
     auto iseg_begin = [&](int s) {
         while (s < nseg && seg_lo(s) >= seg_hi(s)) ++s;
         is = s;
@@ -315,14 +330,14 @@ gemv_kernel(const GemvArgs a) {
             const int lo = seg_lo(s);
             ileft = seg_hi(s) - lo;
             irow = (tile_lo + lo) * 16 + crow;
-            iptr = a.codes + (size_t)irow * W + seg_group(s) * 8 + (lane & 1) * 4;
+            iptr = codes + (size_t)irow * W + seg_group(s) * 8 + (lane & 1) * 4;
         }
     };
     iseg_begin(0);
     auto issue = [&](int slot) {
         if (is < nseg) {
             const bool ok = irow < N;
-            cp_async16(ring_s + (uint32_t)(slot * kSlotBytes), ok ? iptr : a.codes, ok);
+            cp_async16(ring_s + (uint32_t)(slot * kSlotBytes), ok ? iptr : codes, ok);
             iptr += cstep;
             irow += 16;
             if (--ileft == 0) iseg_begin(is + 1);
@@ -345,7 +360,7 @@ gemv_kernel(const GemvArgs a) {
                 const int r = i / cpr, c = i - r * cpr;
                 const bool ok = row0 + r < N;
                 cp_async16(sc_s + (uint32_t)(r * gpad + 8 * c) * 2u,
-                           ok ? a.scales + (size_t)(row0 + r) * G + gA + 8 * c : a.scales, ok);
+                           ok ? scales + (size_t)(row0 + r) * G + gA + 8 * c : scales, ok);
             }
         } else if (mode == 4) {
             const int cpr = scale_width(G, gA, gB) / 2;
@@ -353,12 +368,12 @@ gemv_kernel(const GemvArgs a) {
                 const int r = i / cpr, c = i - r * cpr;
                 const bool ok = row0 + r < N;
                 cp_async4(sc_s + (uint32_t)(r * gpad + 2 * c) * 2u,
-                          ok ? a.scales + (size_t)(row0 + r) * G + g_lo + 2 * c : a.scales, ok);
+                          ok ? scales + (size_t)(row0 + r) * G + g_lo + 2 * c : scales, ok);
             }
         } else {
             for (int i = threadIdx.x; i < rows * Gs; i += kThreads) {
                 const int r = i / Gs, c = i - r * Gs;
-                sc[r * gpad + c] = row0 + r < N ? __half_as_ushort(a.scales[(size_t)(row0 + r) * G + gA + c])
+                sc[r * gpad + c] = row0 + r < N ? __half_as_ushort(scales[(size_t)(row0 + r) * G + gA + c])
                                                 : (unsigned short)0;
             }
         }
@@ -369,7 +384,7 @@ gemv_kernel(const GemvArgs a) {
     // copies row l / 2, half l % 2 of the unit's 32 (2-bit) or 16 (1-bit) bytes.
     const int lean_g = gA + warp;
     const bool lean_has = !BIN || lean_g < gB;
-    const uint32_t* src_base = a.codes + (size_t)lean_g * (BIN ? 4 : 8) + (lane & 1) * (BIN ? 2 : 4);
+    const uint32_t* src_base = codes + (size_t)lean_g * (BIN ? 4 : 8) + (lane & 1) * (BIN ? 2 : 4);
     const int crow0 = tile_lo * 16 + crow;
     const uint32_t ring_lane = smem_addr(ring) + (uint32_t)lane * (BIN ? 8u : 16u);
     auto refill = [&](int u, int slot_) {
@@ -397,7 +412,7 @@ gemv_kernel(const GemvArgs a) {
         const int row0 = tile_lo * 16, nrow = min(R * 16, N - row0);
         for (int i = threadIdx.x; i < M * nrow; i += kThreads) {
             const int m = i / nrow, r = i - m * nrow;
-            a.y[(size_t)m * N + row0 + r] = 0.0f;
+            yv[(size_t)m * N + row0 + r] = 0.0f;
         }
         if (!LEAN) {
             __threadfence();
@@ -729,7 +744,7 @@ gemv_kernel(const GemvArgs a) {
         for (int i = threadIdx.x; i < nv; i += kThreads) {
             const int m = i / (R * 16), rr = i - m * (R * 16);
             const int r = tile_lo * 16 + rr;
-            if (r < N) a.y[(size_t)m * N + r] = row_value(rr >> 4, rr & 15, m);
+            if (r < N) yv[(size_t)m * N + r] = row_value(rr >> 4, rr & 15, m);
         }
         return;
     }
@@ -751,7 +766,7 @@ gemv_kernel(const GemvArgs a) {
     for (int i = threadIdx.x; i < nv; i += kThreads) {
         const int m = i / (R * 16), rr = i - m * (R * 16);
         const int r = tile_lo * 16 + rr;
-        if (r < N) atomicAdd(a.y + (size_t)m * N + r, row_value(rr >> 4, rr & 15, m));
+        if (r < N) atomicAdd(yv + (size_t)m * N + r, row_value(rr >> 4, rr & 15, m));
     }
 }
 
@@ -812,6 +827,7 @@ rotate_stage_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restric
 // ---------------------------------------------------------------------------
 struct Plan {
     int G, T, S, cps, ctas, rmax, MT, gpad, slot;
+    int T2, cps1;   // a pair call: the second matrix's tiles (T counts both) and the first's ranges
     uint32_t off_sc, off_part;
     size_t smem;
 };
@@ -819,7 +835,17 @@ struct Plan {
 // Shared-memory layout for `cps` ranges (ring | scales | partials).
 void layout(Plan& p, int M, int cps) {
     p.cps = cps;
-    p.rmax = (p.T + cps - 1) / cps;
+    if (p.T2 > 0) {
+        // a pair call: the ranges are shared out in proportion to the tiles,
+        // at least one each, so no range straddles the two matrices
+        const int T1 = p.T - p.T2;
+        p.cps = cps = std::max(cps, 2);
+        p.cps1 = std::min(cps - 1, std::max(1, (int)(((long long)cps * T1 + p.T / 2) / p.T)));
+        p.rmax = std::max((T1 + p.cps1 - 1) / p.cps1, (p.T2 + cps - p.cps1 - 1) / (cps - p.cps1));
+    } else {
+        p.cps1 = cps;
+        p.rmax = (p.T + cps - 1) / cps;
+    }
     const int MP = 8 * p.MT;
     size_t off = (size_t)kWarps * kDepth * p.slot;
     p.off_sc = (uint32_t)off;
@@ -831,10 +857,11 @@ void layout(Plan& p, int M, int cps) {
 
 // The device-independent part of the plan: slices and the scale pitch.  The
 // 1-bit layout's slices are groups 8 s .. 8 s + 7 (the last one may be short).
-Plan base_plan(int M, int N, int K, bool bin) {
+Plan base_plan(int M, int N, int K, bool bin, int N2 = 0) {
     Plan p{};
     p.G = K / kGroup;
-    p.T = (N + 15) / 16;
+    p.T2 = (N2 + 15) / 16;
+    p.T = (N + 15) / 16 + p.T2;
     p.S = (p.G + kWarps - 1) / kWarps;
     p.MT = (M + 7) / 8;
     p.slot = bin ? kBinSlotBytes : kSlotBytes;
@@ -873,10 +900,10 @@ cudaError_t kernel_smem_limit(int dev, int* limit) {
 // One wave: as many CTAs as fit at once, by registers (the launch bound) and
 // by shared memory (which grows with the range length).
 template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN>
-tern_status make_plan(int M, int N, int K, int sms, int dev, Plan* out) {
+tern_status make_plan(int M, int N, int K, int N2, int sms, int dev, Plan* out) {
     int limit = 0;
     if (kernel_smem_limit<MT, PRE, ONE, LEAN, BIN>(dev, &limit) != cudaSuccess) return TERN_ERR_CUDA;
-    Plan p = base_plan(M, N, K, BIN);
+    Plan p = base_plan(M, N, K, BIN, N2);
     const int need = (p.T + kMaxTiles - 1) / kMaxTiles;   // ranges short enough for the shared partials
     int cps = 1;
     for (int per_sm = GemvCfg<MT>::kCtasPerSm; per_sm >= 1; --per_sm) {
@@ -885,7 +912,8 @@ tern_status make_plan(int M, int N, int K, int sms, int dev, Plan* out) {
         if ((size_t)per_sm * (p.smem + kCtaSmemReserve) <= kSmemPerSm) break;
     }
     // very long slices: shorter ranges (more than one wave) until a CTA fits
-    while (p.smem > (size_t)limit && p.rmax > 1) layout(p, M, (p.T + p.rmax - 2) / (p.rmax - 1));
+    while (p.smem > (size_t)limit && p.rmax > 1)
+        layout(p, M, std::max(p.cps + 1, (p.T + p.rmax - 2) / (p.rmax - 1) + (p.T2 > 0 ? 1 : 0)));
     if (p.smem > (size_t)limit) return TERN_ERR_SHAPE;
     p.ctas = p.S * p.cps;
     *out = p;
@@ -894,7 +922,7 @@ tern_status make_plan(int M, int N, int K, int sms, int dev, Plan* out) {
 
 // Plans depend on the shape and the device only: keep the recent ones.
 struct PlanKey {
-    int M, N, K, dev;
+    int M, N, K, N2, dev;
     bool pre, bin;
 };
 std::mutex g_plan_mu;
@@ -904,22 +932,22 @@ Plan g_plan_val[kPlanCache];
 int g_plan_n = 0, g_plan_next = 0;
 
 template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN>
-tern_status cached_plan(int M, int N, int K, int sms, Plan* out) {
+tern_status cached_plan(int M, int N, int K, int N2, int sms, Plan* out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TERN_ERR_CUDA;
     if (dev < 0 || dev >= 64) return TERN_ERR_DEVICE;
     std::lock_guard<std::mutex> lk(g_plan_mu);
     for (int i = 0; i < g_plan_n; ++i) {
         const PlanKey& k = g_plan_key[i];
-        if (k.M == M && k.N == N && k.K == K && k.dev == dev && k.pre == PRE && k.bin == BIN) {
+        if (k.M == M && k.N == N && k.K == K && k.N2 == N2 && k.dev == dev && k.pre == PRE && k.bin == BIN) {
             *out = g_plan_val[i];
             return TERN_OK;
         }
     }
-    const tern_status st = make_plan<MT, PRE, ONE, LEAN, BIN>(M, N, K, sms, dev, out);
+    const tern_status st = make_plan<MT, PRE, ONE, LEAN, BIN>(M, N, K, N2, sms, dev, out);
     if (st != TERN_OK) return st;
     const int slot = g_plan_n < kPlanCache ? g_plan_n++ : (g_plan_next++ % kPlanCache);
-    g_plan_key[slot] = PlanKey{M, N, K, dev, PRE, BIN};
+    g_plan_key[slot] = PlanKey{M, N, K, N2, dev, PRE, BIN};
     g_plan_val[slot] = *out;
     return TERN_OK;
 }
@@ -948,10 +976,12 @@ size_t workspace_bytes(int M, int N, int K, bool rot) {
 template <int MT, bool PRE, bool ONE, bool LEAN = false, bool BIN = false>
 tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
     Plan p;
-    const tern_status st = cached_plan<MT, PRE, ONE, LEAN, BIN>(args.M, args.N, args.K, sms, &p);
+    const tern_status st = cached_plan<MT, PRE, ONE, LEAN, BIN>(args.M, args.N, args.K, args.N2, sms, &p);
     if (st != TERN_OK) return st;
     args.G = p.G;
-    args.T = p.T;
+    args.T = p.T - p.T2;   // the first matrix's tiles
+    args.T2 = p.T2;
+    args.cps1 = p.cps1;
     args.S = p.S;
     args.cps = p.cps;
     args.rmax = p.rmax;
@@ -963,14 +993,23 @@ tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
     return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
 
+// A pair call (N2 > 0) reads one x for two matrices; its flag words cover the
+// tiles of both.
+size_t pair_flag_bytes(int N, int N2, int K) {
+    const int G = K / kGroup;
+    return G > kWarps ? align_up((size_t)((N + 15) / 16 + (N2 + 15) / 16) * 4, 256) : 0;
+}
+
 tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const void* scales, float* y, int M,
-                int N, int K, void* workspace, size_t workspace_bytes_, cudaStream_t stream, bool bin = false) {
+                int N, int K, void* workspace, size_t workspace_bytes_, cudaStream_t stream, bool bin = false,
+                const uint32_t* codes2 = nullptr, const void* scales2 = nullptr, float* y2 = nullptr, int N2 = 0) {
     int sms = 0;
     tern_status st = check_device(&sms);
     if (st != TERN_OK) return st;
-    const size_t fb = flag_bytes(N, K);
+    const size_t fb = N2 > 0 ? pair_flag_bytes(N, N2, K) : flag_bytes(N, K);
     if (fb > 0 || signs) {
-        if (!workspace || workspace_bytes_ < workspace_bytes(M, N, K, signs != nullptr)) return TERN_ERR_WORKSPACE;
+        const size_t need = N2 > 0 ? fb : workspace_bytes(M, N, K, signs != nullptr);
+        if (!workspace || workspace_bytes_ < need) return TERN_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TERN_ERR_ALIGN;
     }
     GemvArgs args{};
@@ -982,6 +1021,10 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
     args.M = M;
     args.N = N;
     args.K = K;
+    args.codes2 = N2 > 0 ? codes2 : codes;
+    args.scales2 = reinterpret_cast<const __half*>(N2 > 0 ? scales2 : scales);
+    args.y2 = N2 > 0 ? y2 : y;
+    args.N2 = N2;
     const int MT = (M + 7) / 8;
     // K a multiple of 1024: slices of exactly 8 groups, one group per warp
     const bool lean = (K / kGroup) % kWarps == 0;
@@ -1068,6 +1111,26 @@ extern "C" tern_status tern_gemv(const void* x, const uint32_t* codes, const voi
     const size_t need = workspace_bytes(M, N, K, false);
     if (need > 0 && (!workspace || workspace_bytes_ < need)) return TERN_ERR_WORKSPACE;
     return run(x, nullptr, codes, scales, y, M, N, K, workspace, workspace_bytes_, (cudaStream_t)stream);
+}
+
+extern "C" size_t tern_gemv_pair_workspace_bytes(int M, int N_a, int N_b, int K) {
+    if (M < 1 || M > 16 || N_a < 1 || N_b < 1 || K < kGroup || K % kGroup != 0) return 0;
+    return std::max<size_t>(256, pair_flag_bytes(N_a, N_b, K));
+}
+
+extern "C" tern_status tern_gemv_pair(const void* x, const uint32_t* codes_a, const void* scales_a, float* y_a,
+                                      int N_a, const uint32_t* codes_b, const void* scales_b, float* y_b, int N_b,
+                                      int M, int K, void* workspace, size_t workspace_bytes_, tern_stream_t stream) {
+    set_launch_count(0);
+    tern_status v = validate(x, codes_a, scales_a, y_a, M, N_a, K);
+    if (v != TERN_OK) return v;
+    v = validate(x, codes_b, scales_b, y_b, M, N_b, K);
+    if (v != TERN_OK) return v;
+    if ((long long)N_a + N_b >= (1 << 28)) return TERN_ERR_SHAPE;
+    const size_t need = pair_flag_bytes(N_a, N_b, K);
+    if (need > 0 && (!workspace || workspace_bytes_ < need)) return TERN_ERR_WORKSPACE;
+    return run(x, nullptr, codes_a, scales_a, y_a, M, N_a, K, workspace, workspace_bytes_, (cudaStream_t)stream,
+               false, codes_b, scales_b, y_b, N_b);
 }
 
 extern "C" tern_status tern_bin_gemv(const void* x, const uint32_t* words, const void* scales, float* y, int M,

@@ -171,6 +171,19 @@ tern_status tern_gemv(const void *x, const uint32_t *codes, const void *scales, 
                       int M, int N, int K, void *workspace, size_t workspace_bytes,
                       tern_stream_t stream);
 
+/* Two products that read the same activation, in one launch (for example the
+ * gate and up projections of a layer): y_a = x W_a^T (fp32 [M][N_a]) and
+ * y_b = x W_b^T (fp32 [M][N_b]), each matrix as for tern_gemv.  The row
+ * ranges are shared out between the two matrices in proportion to their rows,
+ * so the fixed cost of a launch (the dependency wait and the tail) is paid once
+ * for both.  y_a and y_b must not overlap.  The workspace is
+ * tern_gemv_pair_workspace_bytes(M, N_a, N_b, K) bytes, zero-filled once, with
+ * the rules of tern_gemv's.  Shapes, alignment and errors as for tern_gemv. */
+size_t tern_gemv_pair_workspace_bytes(int M, int N_a, int N_b, int K);
+tern_status tern_gemv_pair(const void *x, const uint32_t *codes_a, const void *scales_a, float *y_a, int N_a,
+                           const uint32_t *codes_b, const void *scales_b, float *y_b, int N_b, int M, int K,
+                           void *workspace, size_t workspace_bytes, tern_stream_t stream);
+
 /* The same product for the 1-bit sibling format: y (fp32 [M][N]) = x W^T with
  * W[n][k] = (2 b[n][k] - 1) * s[n][k/128], words uint32 [N][K/32] as
  * tern_bin_pack writes them.  Shapes, alignment, workspace (the size

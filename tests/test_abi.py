@@ -210,3 +210,15 @@ def test_scales_from_g64_host_matches_oracle(tern, orc):
     lib = tern.lib()
     assert lib.tern_scales_from_g64(4096, 4, 192, 4096, None, None) == 2      # K % 128
     assert lib.tern_scales_from_g64(None, 4, 256, 4096, None, None) == 1
+
+
+def test_gemv_pair_argument_errors(tern):
+    lib = tern.lib()
+    P = 4096
+    assert lib.tern_gemv_pair(P, P, P, P, 16, P, P, P, 0, 1, 2048, P, 1 << 20, None) == 2     # N_b = 0
+    assert lib.tern_gemv_pair(P, P, P, P, 16, None, P, P, 16, 1, 2048, P, 1 << 20, None) == 1
+    assert lib.tern_gemv_pair(P, P, P, P, 16, P + 4, P, P, 16, 1, 2048, P, 1 << 20, None) == 3
+    need = tern.lib().tern_gemv_pair_workspace_bytes(1, 17408, 17408, 5120)
+    assert need == (2 * 1088 * 4 + 255) // 256 * 256
+    assert lib.tern_gemv_pair(P, P, P, P, 17408, P, P, P, 17408, 1, 5120, P, need - 1, None) == 4
+    assert tern.lib().tern_gemv_pair_workspace_bytes(1, 16, 16, 1024) == 256

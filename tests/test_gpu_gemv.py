@@ -341,3 +341,27 @@ def test_scales_from_g64_device(tern, orc):
     y_ref, a_ref = orc.matmul(p.x, host_codes(codes), s128)
     assert_fp32_close(y64.cpu().numpy(), y_ref, a_ref, what="g64 scales")
     assert_fp32_close(y128.cpu().numpy(), y_ref, a_ref, what="g128 scales")
+
+
+@pytest.mark.parametrize("M,Na,Nb,K", [(1, 17408, 17408, 5120), (1, 300, 5000, 2048), (3, 777, 129, 17408),
+                                       (16, 64, 48, 1024), (5, 1000, 1000, 640), (1, 16, 16, 128)])
+def test_gemv_pair_matches_two_products(tern, orc, M, Na, Nb, K):
+    """Two matrices read with one activation in one launch: each output against
+    the oracle, ragged row counts, one and several K-slices, twice on the same
+    workspace."""
+    pa = synth.problem(1900 + M, M, Na, K, tag=f"pa{Na}x{K}")
+    pb = synth.problem(1950 + M, M, Nb, K, tag=f"pb{Nb}x{K}")
+    x = dev_bf16(pa.x)
+    ca, cb = tern.pack(dev_trits(pa.t)), tern.pack(dev_trits(pb.t))
+    sa, sb = dev_scales(pa.s), dev_scales(pb.s)
+    ws = tern.workspace(int(tern.lib().tern_gemv_pair_workspace_bytes(M, Na, Nb, K)))
+    ya_ref, aa_ref = orc.matmul(pa.x, host_codes(ca), pa.s)
+    yb_ref, ab_ref = orc.matmul(pa.x, host_codes(cb), pb.s)
+    for call in range(2):
+        ya = torch.full((M, Na), float("nan"), dtype=torch.float32, device="cuda")
+        yb = torch.full((M, Nb), float("nan"), dtype=torch.float32, device="cuda")
+        tern.gemv_pair(x, ca, sa, cb, sb, y_a=ya, y_b=yb, ws=ws)
+        torch.cuda.synchronize()
+        assert tern.device_error() == 0
+        assert_fp32_close(ya.cpu().numpy(), ya_ref, aa_ref, what=f"pair a call {call} M={M} {Na}/{Nb} K={K}")
+        assert_fp32_close(yb.cpu().numpy(), yb_ref, ab_ref, what=f"pair b call {call} M={M} {Na}/{Nb} K={K}")
