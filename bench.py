@@ -394,10 +394,10 @@ def bench_fused_gate_up(tern, sweep: DecodeSweep, steps: int, warmup: int, hbm: 
 
 def bench_verify_step(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int):
     """One speculative-verify step as a CUDA graph: k + 1 = 5 tokens through
-    every layer's qkv (5120 -> 6144), gate, up (5120 -> 17408) and down
-    (17408 -> 5120) products, 64 layers, 256 launches.  The drafter and the
-    work between the products (attention, activations) are not part of it:
-    each product reads a fixed activation."""
+    every layer's qkv (5120 -> 6144), gate and up (5120 -> 17408, one pair call
+    on their shared activation) and down (17408 -> 5120) products, 64 layers,
+    192 launches.  The drafter and the work between the products (attention,
+    activations) are not part of it: each call reads a fixed activation."""
     import torch
     import synth
     M = synth.VERIFY_STEP_M
@@ -408,16 +408,20 @@ def bench_verify_step(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int):
     ws = tern.workspace(max(tern.gemv_workspace_bytes(M, N, K) for (K, N) in ((5120, 6144), (5120, 17408),
                                                                               (17408, 5120))))
 
+    yu = torch.empty((M, 17408), dtype=torch.float32, device="cuda")
+    ws = tern.workspace(max(ws.numel(), int(tern.lib().tern_gemv_pair_workspace_bytes(M, 17408, 17408, 5120))))
+
     def run():
         for l in range(layers):
             tern.gemv(x5, qkv[l][0], qkv[l][1], y=ys[6144], ws=ws)
-            for (_, K, N, codes, s) in sweep.layers[l]:
-                tern.gemv(x5 if K == 5120 else x17, codes, s, y=ys[N], ws=ws)
+            g_, u_, d_ = sweep.layers[l]
+            tern.gemv_pair(x5, g_[3], g_[4], u_[3], u_[4], y_a=ys[17408], y_b=yu, ws=ws)
+            tern.gemv(x17, d_[3], d_[4], y=ys[5120], ws=ws)
 
     g = graph_of(run)
     ms = time_graph(g, max(3, steps // 10), warmup)
     wb = layers * (weight_bytes(6144, 5120) + 2 * weight_bytes(17408, 5120) + weight_bytes(5120, 17408))
-    return {"M": M, "layers": layers, "launches": 4 * layers, "us_per_step": ms * 1e3,
+    return {"M": M, "layers": layers, "launches": 3 * layers, "us_per_step": ms * 1e3,
             "weight_GBps": wb / (ms * 1e-3) / 1e9, "tokens_per_s": M / (ms * 1e-3)}
 
 

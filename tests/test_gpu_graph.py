@@ -185,3 +185,40 @@ def test_binary_decode_graph(tern, orc):
         ms, ns = sample(1, p.N, 88 + i)
         y_ref, a_ref = orc.bin_matmul_sampled(p.x, words[i].cpu().numpy().view(np.uint32), p.s, ms, ns)
         assert_fp32_close(ys[i].cpu().numpy()[ms, ns], y_ref, a_ref, what=f"binary graph product {i}")
+
+
+def test_pair_decode_graph(tern, orc):
+    """The decode step as the benchmark runs it: per layer, gate and up in one
+    pair call on their shared activation, then down; two layers, one graph."""
+    probs, xs = [], []
+    for l in range(2):
+        pg = synth.problem(1600 + 3 * l, 1, 17408, 5120, tag=f"pg{l}")
+        pu = synth.problem(1601 + 3 * l, 1, 17408, 5120, tag=f"pu{l}")
+        pd = synth.problem(1602 + 3 * l, 1, 5120, 17408, tag=f"pd{l}")
+        for p in (pg, pu, pd):
+            probs.append((p, tern.pack(dev_trits(p.t))))
+        xs += [dev_bf16(pg.x), dev_bf16(pd.x)]
+    ss = [dev_scales(p.s) for p, _ in probs]
+    ys = [torch.empty((1, p.N), dtype=torch.float32, device="cuda") for p, _ in probs]
+    ws = tern.workspace(max(int(tern.lib().tern_gemv_pair_workspace_bytes(1, 17408, 17408, 5120)),
+                            tern.gemv_workspace_bytes(1, 5120, 17408)))
+
+    def run():
+        for l in range(2):
+            g, u, d = 3 * l, 3 * l + 1, 3 * l + 2
+            tern.gemv_pair(xs[2 * l], probs[g][1], ss[g], probs[u][1], ss[u], y_a=ys[g], y_b=ys[u], ws=ws)
+            tern.gemv(xs[2 * l + 1], probs[d][1], ss[d], y=ys[d], ws=ws)
+
+    g = capture(run)
+    for _ in range(2):
+        g.replay()
+    for y in ys:
+        y.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    for i, (p, codes) in enumerate(probs):
+        x_bits = probs[i - 1][0].x if i % 3 == 1 else p.x          # up reads gate's activation
+        ms, ns = sample(1, p.N, 99 + i)
+        y_ref, a_ref = orc.matmul_sampled(x_bits, host_codes(codes), p.s, ms, ns)
+        assert_fp32_close(ys[i].cpu().numpy()[ms, ns], y_ref, a_ref, what=f"pair graph product {i}")
