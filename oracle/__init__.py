@@ -63,6 +63,8 @@ def _load():
                 "orc_bin_matmul_sampled": (_I, [_P, _P, _P, _I, _P, _P, _I, _P, _P, _I]),
                 "orc_scales_from_g64": (ctypes.c_longlong, [_P, _I, _I, _P]),
                 "orc_mlx_affine": (ctypes.c_float, [_I, ctypes.c_float, ctypes.c_float]),
+                "orc_affine_matmul": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _I]),
+                "orc_affine_matmul_sampled": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _P, _P, _I]),
                 "orc_hadamard_explicit": (_I, [_I, _P]),
                 "orc_fwht": (_I, [_P, _I]),
                 "orc_rotate": (_I, [_P, _P, _I, _I, _I, _P]),
@@ -230,6 +232,42 @@ def matmul_sampled(x_bf16: np.ndarray, codes: np.ndarray, scales_f16: np.ndarray
     if st == -1:
         raise ValueError("invalid code 3 in codes")
     if st != 0:
+        raise ValueError("bad shape")
+    return y, a
+
+
+def affine_matmul(x_bf16: np.ndarray, codes: np.ndarray, scales_f16: np.ndarray, biases_f16: np.ndarray,
+                  nthreads: int = 0) -> tuple[np.ndarray, np.ndarray]:
+    """The affine pack's product: y[m, n] = sum_k x[m, k] (s q[n, k] + b)[n, k // 128]
+    in double, every code 0..3 valid; returns (y, a) with a = sum_k |x w|."""
+    x = _bits16(x_bf16)
+    s = _bits16(scales_f16)
+    b = _bits16(biases_f16)
+    codes = _c(codes, np.uint32)
+    M, K = x.shape
+    N = codes.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    a = np.empty((M, N), dtype=np.float64)
+    if _load().orc_affine_matmul(_ptr(x), _ptr(codes), _ptr(s), _ptr(b), M, N, K, _ptr(y), _ptr(a),
+                                 nthreads) != 0:
+        raise ValueError("bad shape")
+    return y, a
+
+
+def affine_matmul_sampled(x_bf16: np.ndarray, codes: np.ndarray, scales_f16: np.ndarray,
+                          biases_f16: np.ndarray, ms: np.ndarray, ns: np.ndarray, nthreads: int = 0):
+    """The affine product at outputs (ms[i], ns[i]) only; returns (y, a)."""
+    x = _bits16(x_bf16)
+    s = _bits16(scales_f16)
+    b = _bits16(biases_f16)
+    codes = _c(codes, np.uint32)
+    K = x.shape[1]
+    ms = _c(ms, np.int32)
+    ns = _c(ns, np.int32)
+    y = np.empty(len(ms), dtype=np.float64)
+    a = np.empty(len(ms), dtype=np.float64)
+    if _load().orc_affine_matmul_sampled(_ptr(x), _ptr(codes), _ptr(s), _ptr(b), K, _ptr(ms), _ptr(ns),
+                                         len(ms), _ptr(y), _ptr(a), nthreads) != 0:
         raise ValueError("bad shape")
     return y, a
 

@@ -36,6 +36,10 @@
  *     bit b in {0, 1}, so a weight is (2b - 1) * s_g.  Reading for the unstated
  *     order, as for the ternary codes: bit k%32 of little-endian uint32 word
  *     k/32 of the row.
+ *   - The affine pack ([card] "MLX packaging": a scale and a bias per group):
+ *     the same 2-bit slots with all four codes valid and w = s q + b, s and b
+ *     FP16 per 128 weights.  Reading for the unstated order and precision: the
+ *     slot order of the ternary codes, and FP16 biases like the scales.
  *
  * Parity pins live in the "not gpu" tests: brute-force dense matmul from an
  * explicitly expanded W, exhaustive pack/unpack patterns, the explicit
@@ -372,6 +376,72 @@ long long orc_scales_from_g64(const uint16_t *s64, int N, int K, uint16_t *s128)
 float orc_mlx_affine(int q, float s_mlx, float bias)
 {
     return s_mlx * (float)q + bias;
+}
+
+/* The product on an affine pack: the same 2-bit slots, every code 0..3
+ * valid, and per group a FP16 scale s and a FP16 bias b, so that
+ * w[n][k] = s[n][k/128] * q[n][k] + b[n][k/128] ([card] "MLX packaging";
+ * the ternary codes are the case b = -s, the card's literal pair
+ * (2 s_g, -s_g) on codes {0, 1} the 1-bit case).  One output and its error
+ * scale a = sum_k |x w|; every term is exact in double. */
+static void orc_affine_dot(const uint16_t *x, const uint32_t *codes,
+                           const uint16_t *scales, const uint16_t *biases,
+                           int K, int m, int n, double *y, double *a)
+{
+    int G = K / 128;
+    double acc = 0.0, mag = 0.0;
+    for (int k = 0; k < K; ++k) {
+        int q = orc_code(codes, K, n, k);
+        size_t g = (size_t)n * G + k / 128;
+        double w = orc_f16_to_f64(scales[g]) * (double)q + orc_f16_to_f64(biases[g]);
+        double p = orc_bf16_to_f64(x[(size_t)m * K + k]) * w;
+        acc += p;
+        mag += fabs(p);
+    }
+    *y = acc;
+    if (a)
+        *a = mag;
+}
+
+/* y[M][N] (and a[M][N] if a != NULL) for x bf16 [M][K], codes [N][K/16],
+ * scales and biases fp16 [N][K/128].  Returns 0, or -2 for a bad shape. */
+int orc_affine_matmul(const uint16_t *x, const uint32_t *codes, const uint16_t *scales,
+                      const uint16_t *biases, int M, int N, int K, double *y,
+                      double *a, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || K % 128 != 0)
+        return -2;
+    orc_set_threads(nthreads);
+    long long total = (long long)M * N;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (long long i = 0; i < total; ++i) {
+        double yy, aa;
+        orc_affine_dot(x, codes, scales, biases, K, (int)(i / N), (int)(i % N), &yy, &aa);
+        y[i] = yy;
+        if (a)
+            a[i] = aa;
+    }
+    return 0;
+}
+
+/* The affine product at chosen outputs only: (ms[i], ns[i]) for i < count. */
+int orc_affine_matmul_sampled(const uint16_t *x, const uint32_t *codes,
+                              const uint16_t *scales, const uint16_t *biases,
+                              int K, const int *ms, const int *ns, int count,
+                              double *y, double *a, int nthreads)
+{
+    if (K < 0 || K % 128 != 0)
+        return -2;
+    orc_set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int i = 0; i < count; ++i) {
+        double yy, aa;
+        orc_affine_dot(x, codes, scales, biases, K, ms[i], ns[i], &yy, &aa);
+        y[i] = yy;
+        if (a)
+            a[i] = aa;
+    }
+    return 0;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -13,7 +13,10 @@ since the pages give none:
 * scales: fp16, U[0.005, 0.05] or |N(0, 0.02)| + 1e-3, one per 128 along K;
 * activations x: bf16 rounded from N(0, 1) (round to nearest even);
 * rotation signs: iid uniform over {-1, +1}, int8;
-* the 1-bit sibling format's weights: iid uniform over {-1, +1}.
+* the 1-bit sibling format's weights: iid uniform over {-1, +1};
+* an affine pack's 2-bit codes: every slot iid uniform over {0, 1, 2, 3}
+  (drawn as whole random 32-bit words), and fp16 biases b = -u s with
+  u ~ U[1, 2] (a min-max fit of symmetric weights puts b near -1.5 s).
 
 Each tensor draws from its own stream, keyed by (seed, name), so one tensor's
 shape never shifts another tensor's values.
@@ -47,6 +50,36 @@ def binary_problem(seed: int, M: int, N: int, K: int, tag: str = "") -> "Problem
     """A seeded problem of the 1-bit format: t in {-1, +1}."""
     return Problem(M, N, K, binary(seed, f"{tag}b", (N, K)), scales(seed, f"{tag}s", (N, K // 128)),
                    activations(seed, f"{tag}x", (M, K)))
+
+
+def code_words(seed: int, name: str, shape) -> np.ndarray:
+    """uint32 array of iid random words: every 2-bit slot uniform over 0..3."""
+    return rng(seed, name).integers(0, 1 << 32, size=shape, dtype=np.uint64).astype(np.uint32)
+
+
+def biases(seed: int, name: str, s: np.ndarray) -> np.ndarray:
+    """float16 group biases b = -u s, u ~ U[1, 2] iid, for fp16 scales s."""
+    u = rng(seed, name).uniform(1.0, 2.0, size=s.shape)
+    return (-u * s.astype(np.float64)).astype(np.float16)
+
+
+@dataclass
+class AffineProblem:
+    """One seeded problem on an affine pack: w = s q + b per group of 128."""
+    M: int
+    N: int
+    K: int
+    codes: np.ndarray      # uint32 [N, K/16]
+    s: np.ndarray          # float16 [N, K/128]
+    b: np.ndarray          # float16 [N, K/128]
+    x: np.ndarray          # uint16 bf16 bits [M, K]
+
+
+def affine_problem(seed: int, M: int, N: int, K: int, tag: str = "") -> AffineProblem:
+    """A seeded problem on an affine pack (all four codes, biases near -1.5 s)."""
+    s = scales(seed, f"{tag}s", (N, K // 128))
+    return AffineProblem(M, N, K, code_words(seed, f"{tag}c", (N, K // 16)), s, biases(seed, f"{tag}b", s),
+                         activations(seed, f"{tag}x", (M, K)))
 
 
 def trits(seed: int, name: str, shape, dist: str = SPARSE40) -> np.ndarray:
@@ -164,6 +197,22 @@ def device_binary(seed: int, name: str, shape, device="cuda"):
     import torch
     g = device_generator(seed, name, device)
     return torch.where(torch.rand(shape, generator=g, device=device) < 0.5, -1, 1).to(torch.int8)
+
+
+def device_code_words(seed: int, name: str, shape, device="cuda"):
+    """int32 CUDA tensor of iid random words (an affine pack's codes, every
+    2-bit slot uniform over 0..3)."""
+    import torch
+    g = device_generator(seed, name, device)
+    return torch.randint(-(1 << 31), 1 << 31, shape, generator=g, device=device, dtype=torch.int32)
+
+
+def device_biases(seed: int, name: str, s, device="cuda"):
+    """fp16 CUDA tensor b = -u s, u ~ U[1, 2] iid, for fp16 scales s."""
+    import torch
+    g = device_generator(seed, name, device)
+    u = torch.rand(s.shape, generator=g, device=device) + 1.0
+    return (-u * s.float()).to(torch.float16)
 
 
 def device_scales(seed: int, name: str, shape, dist: str = SCALE_HALFNORMAL, device="cuda"):

@@ -514,3 +514,106 @@ def test_scales_from_g64(orc):
     # the card's pack sizes agree with one fp16 per 64 weights instead of per 128
     g = json.load(open(os.path.join(GOLDEN, "bitrates.json")))
     assert abs(g["lm_pack_g64_gb"]["value"] / g["lm_pack_g128_gb"]["value"] - (2 + 16 / 64) / (2 + 16 / 128)) < 1e-3
+
+
+# --------------------------------------------------------------------------
+# the affine pack ("MLX packaging": a scale and a bias per group of 128),
+# w = s q + b with every 2-bit code 0..3 valid
+# --------------------------------------------------------------------------
+
+def pack_codes_np(q: np.ndarray) -> np.ndarray:
+    """uint32 words from codes q [N, K] in 0..3: code k at bits 2 (k % 16) of
+    word k / 16 (the slot order the packing golden words fix), built with
+    numpy independently of the oracle."""
+    N, K = q.shape
+    w = q.astype(np.uint64).reshape(N, K // 16, 16) << (2 * np.arange(16, dtype=np.uint64))
+    return w.sum(-1).astype(np.uint32)
+
+
+def dense_affine_w(q: np.ndarray, s: np.ndarray, b: np.ndarray) -> np.ndarray:
+    return q.astype(np.float64) * np.repeat(s.astype(np.float64), 128, axis=1) + \
+        np.repeat(b.astype(np.float64), 128, axis=1)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 128), (1, 8, 128), (4, 8, 256), (3, 5, 384), (2, 40, 1024)])
+def test_affine_matmul_matches_dense_bruteforce(orc, M, N, K):
+    q = synth.rng(40 + N, "q").integers(0, 4, size=(N, K))
+    s = synth.scales(40 + N, "s", (N, K // 128))
+    b = synth.biases(40 + N, "b", s)
+    x = synth.activations(40 + N, "x", (M, K))
+    y, a = orc.affine_matmul(x, pack_codes_np(q), s, b)
+    xf = bf16_bits_to_f64(x)
+    W = dense_affine_w(q, s, b)
+    assert np.allclose(y, xf @ W.T, rtol=1e-12, atol=1e-12)
+    assert np.allclose(a, np.abs(xf) @ np.abs(W).T, rtol=1e-12, atol=1e-12)
+
+
+def test_affine_packer_agrees_with_ternary_golden_layout(orc):
+    """The test's own packer and the oracle's ternary packer lay codes 0..2 out
+    identically (so the affine pins use the layout the golden words fix)."""
+    t = synth.trits(41, "t", (6, 256), synth.UNIFORM)
+    assert np.array_equal(pack_codes_np(t.astype(np.int64) + 1), orc.pack(t)[0])
+
+
+def test_affine_matmul_ternary_case_is_the_ternary_product(orc):
+    """b = -s on codes q = t + 1 is the ternary product, bit for bit."""
+    p = synth.problem(42, 3, 21, 640)
+    codes, _ = orc.pack(p.t)
+    ya, aa = orc.affine_matmul(p.x, codes, p.s, -p.s)
+    yt, at = orc.matmul(p.x, codes, p.s)
+    assert np.array_equal(ya, yt) and np.array_equal(aa, at)
+
+
+def test_affine_matmul_cards_literal_pair_is_the_binary_product(orc):
+    """The card's MLX pair (2 s_g, -s_g) on codes {0, 1} is the 1-bit product
+    of b = q, bit for bit ("exactly reproduces +-s_g" holds there)."""
+    M, N, K = 2, 13, 512
+    q = (synth.binary(43, "q", (N, K)) > 0).astype(np.int8)          # 0 or 1
+    s = synth.scales(43, "s", (N, K // 128))
+    x = synth.activations(43, "x", (M, K))
+    g = json.load(open(os.path.join(GOLDEN, "bitrates.json")))
+    fa, fb = g["mlx_scale_factor"]["value"], g["mlx_bias_factor"]["value"]
+    s_mlx = (s.astype(np.float64) * fa).astype(np.float16)
+    b_mlx = (s.astype(np.float64) * fb).astype(np.float16)
+    assert np.array_equal(s_mlx.astype(np.float64), 2 * s.astype(np.float64))
+    ya, aa = orc.affine_matmul(x, orc.pack(q - 1)[0], s_mlx, b_mlx)
+    yb, ab = orc.bin_matmul(x, orc.bin_pack(2 * q - 1)[0], s)
+    assert np.array_equal(ya, yb) and np.array_equal(aa, ab)
+
+
+def test_affine_matmul_closed_forms(orc):
+    """All codes 3: y = sum_g (3 s_g + b_g) X_g with X_g the group sums of x;
+    zero scales: y = sum_g b_g X_g; zero scales and biases: y = 0; a one-hot x
+    picks s q + b of one column exactly."""
+    M, N, K = 2, 6, 384
+    s = synth.scales(44, "s", (N, K // 128))
+    b = synth.biases(44, "b", s)
+    x = synth.activations(44, "x", (M, K))
+    X = bf16_bits_to_f64(x).reshape(M, K // 128, 128).sum(-1)     # exact sums of bf16 values
+    threes = np.full((N, K // 16), 0xFFFFFFFF, dtype=np.uint32)
+    y, _ = orc.affine_matmul(x, threes, s, b)
+    assert np.allclose(y, X @ (3 * s.astype(np.float64) + b.astype(np.float64)).T, rtol=1e-13, atol=1e-13)
+    z = np.zeros_like(s)
+    words = synth.code_words(44, "c", (N, K // 16))
+    y, _ = orc.affine_matmul(x, words, z, b)
+    assert np.allclose(y, X @ b.astype(np.float64).T, rtol=1e-13, atol=1e-13)
+    y, a = orc.affine_matmul(x, words, z, z)
+    assert (y == 0).all() and (a == 0).all()
+    q = synth.rng(44, "q").integers(0, 4, size=(N, K))
+    ks = [0, 15, 16, 127, 128, 383]
+    xo = np.zeros((len(ks), K), dtype=np.uint16)
+    for i, k in enumerate(ks):
+        xo[i, k] = 0x3F80
+    yo, _ = orc.affine_matmul(xo, pack_codes_np(q), s, b)
+    W = dense_affine_w(q, s, b)
+    for i, k in enumerate(ks):
+        assert np.array_equal(yo[i], W[:, k])
+
+
+def test_affine_matmul_sampled_equals_full(orc):
+    p = synth.affine_problem(45, 3, 29, 512)
+    y, a = orc.affine_matmul(p.x, p.codes, p.s, p.b)
+    ms = np.repeat(np.arange(3), 29)
+    ns = np.tile(np.arange(29), 3)
+    ys, as_ = orc.affine_matmul_sampled(p.x, p.codes, p.s, p.b, ms, ns)
+    assert np.array_equal(ys, y.reshape(-1)) and np.array_equal(as_, a.reshape(-1))
