@@ -476,6 +476,55 @@ def bench_binary(tern, steps: int, warmup: int, hbm: float, copies: int = 16):
     return out
 
 
+def bench_affine(tern, steps: int, warmup: int, hbm: float, copies: int = 16):
+    """An affine pack (w = s q + b per group of 128, 2.25 bits per weight with
+    the biases).  Decode (M = 1): per decode shape, `copies` distinct matrices
+    (more bytes than L2) called back to back in one graph.  Prefill (M = 512):
+    per layer shape, 4 distinct matrices in one graph."""
+    import torch
+    import synth
+    out = {"decode": [], "pp512": []}
+
+    def mat(seed, key, N, K):
+        s = synth.device_scales(seed, f"{key}.s", (N, K // 128))
+        return (synth.device_code_words(seed, f"{key}.c", (N, K // 16)), s, synth.device_biases(seed, f"{key}.b", s))
+
+    for (K, N) in synth.DECODE_SHAPES:
+        mats = [mat(9, f"A{c}.{K}", N, K) for c in range(copies)]
+        xs = [synth.device_activations(9, f"A{c}.{K}.x", (1, K)) for c in range(copies)]
+        y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+        ws = tern.workspace(tern.gemv_workspace_bytes(1, N, K))
+
+        def run():
+            for c in range(copies):
+                tern.affine_gemv(xs[c], *mats[c], y=y, ws=ws)
+
+        g = graph_of(run)
+        ms = time_graph(g, max(3, steps // 4), warmup)
+        per = ms / copies * 1e-3
+        wb = N * K // 4 + 2 * (N * K // 64)
+        out["decode"].append({"M": 1, "K": K, "N": N, "us": per * 1e6, "weight_bytes": wb,
+                              "weight_GBps": wb / per / 1e9, "hbm_frac": wb / per / 1e9 / hbm})
+        del mats
+    M = synth.PREFILL_M
+    for (name, K, N) in synth.PREFILL_LAYER:
+        mats = [mat(10, f"AP{c}.{name}", N, K) for c in range(4)]
+        x = synth.device_activations(10, f"AP.{name}.x", (M, K))
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        ws = tern.workspace(tern.gemm_workspace_bytes(M, N, K))
+
+        def run(mats=mats, x=x, y=y, ws=ws):
+            for c in range(4):
+                tern.affine_gemm(x, *mats[c], y=y, ws=ws)
+
+        g = graph_of(run)
+        ms = time_graph(g, max(2, steps // 20), max(1, warmup // 2))
+        per = ms / 4 * 1e-3
+        out["pp512"].append({"name": name, "K": K, "N": N, "us": per * 1e6, "TFLOPs": 2.0 * M * N * K / per / 1e12})
+        del mats
+    return out
+
+
 def bench_rotated(tern, steps: int, warmup: int, copies: int = 40):
     import torch
     import synth
@@ -644,7 +693,7 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=DECODE_LAYERS)
-    ap.add_argument("--skip", default="", help="comma list of parts to skip: fused,verify,rotated,binary,prefill,cpu")
+    ap.add_argument("--skip", default="", help="comma list of parts to skip: fused,verify,rotated,binary,affine,prefill,cpu")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -688,6 +737,8 @@ def main() -> None:
         rows["rotated"] = bench_rotated(tern, args.steps, args.warmup)
     if "binary" not in skip:
         rows["binary"] = bench_binary(tern, args.steps, args.warmup, hbm)
+    if "affine" not in skip:
+        rows["affine"] = bench_affine(tern, args.steps, args.warmup, hbm)
     if "prefill" not in skip:
         rows["pp512"] = bench_prefill(tern, sweep, qkv, args.steps, args.warmup, peaks, dev_index)
 

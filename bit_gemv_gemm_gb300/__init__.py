@@ -58,6 +58,8 @@ EXPORTS = {
     "tern_bin_unpack_host": (_I, [_P, _I, _I, _P]),
     "tern_bin_gemv": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
     "tern_bin_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
+    "tern_affine_gemv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
+    "tern_affine_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
 }
 
 
@@ -372,4 +374,42 @@ def bin_gemm(x: torch.Tensor, words: torch.Tensor, scales: torch.Tensor, y: torc
         _dev(x, torch.bfloat16, "x"), _dev(words, torch.int32, "words"), _dev(scales, torch.float16, "scales"),
         _dev(y, y.dtype, "y"), 1 if y.dtype == torch.bfloat16 else 0, M, N, K,
         _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return y
+
+
+def affine_gemv(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
+                y: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """An affine pack: y (fp32 [M, N]) = x W^T for M = 1..16, W = s q + b per
+    group of 128; x bf16 [M, K], codes int32 [N, K/16] (every code 0..3),
+    scales and biases fp16 [N, K/128]."""
+    M, K = x.shape
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(gemv_workspace_bytes(M, N, K), x.device)
+    _check("tern_affine_gemv", lib().tern_affine_gemv(
+        _dev(x, torch.bfloat16, "x"), _dev(codes, torch.int32, "codes"), _dev(scales, torch.float16, "scales"),
+        _dev(biases, torch.float16, "biases"), _dev(y, torch.float32, "y"), M, N, K,
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return y
+
+
+def affine_gemm(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
+                y: torch.Tensor | None = None, out_dtype=torch.float32, ws: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """An affine pack on the tcgen05 tensor cores: y ([M, N], fp32 or bf16) =
+    x W^T, W = s q + b per group of 128, any M >= 1."""
+    M, K = x.shape
+    N = codes.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    if y.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("y must be float32 or bfloat16")
+    if ws is None:
+        ws = workspace(gemm_workspace_bytes(M, N, K), x.device)
+    _check("tern_affine_gemm", lib().tern_affine_gemm(
+        _dev(x, torch.bfloat16, "x"), _dev(codes, torch.int32, "codes"), _dev(scales, torch.float16, "scales"),
+        _dev(biases, torch.float16, "biases"), _dev(y, y.dtype, "y"), 1 if y.dtype == torch.bfloat16 else 0,
+        M, N, K, _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
     return y

@@ -28,6 +28,10 @@
 // is 16 bytes per row too, but spans two K stages (starting at the even one, so
 // the TMA x coordinate stays 16-byte aligned), and the unpack turns bits j and
 // j + 16 of a word into bf16 2b - 1 with one shift and one FMA.
+// An affine pack (w = s q + b per group, every 2-bit code valid) runs it too:
+// per row and group the four weights s q + b are formed in fp32 and rounded
+// once to bf16, and each code picks its weight from that table with one byte
+// permute.
 // Scheduling takes whole tiles on a persistent grid, or stream-K where whole
 // tiles would leave SMs idle longer than stream-K's tail costs: the (tile,
 // 64-wide K stage) iterations, tile-major, are cut into one equal contiguous
@@ -80,6 +84,7 @@ constexpr int kTileFloats = kBM * kBN;         // one tile's fp32 sum: [256 toke
 
 struct GemmArgs {
     const __half* scales;
+    const __half* biases;       // an affine pack's [N][K/128] biases, else null
     void* y;
     float* sums;                // [tiles][kTileFloats] fp32 sums of split tiles, 0 between calls
     unsigned* counters;         // [tiles][4 lane quadrants], 0 between calls
@@ -176,6 +181,37 @@ __device__ __forceinline__ void unpack_word_bin(uint32_t w, uint32_t s2, uint32_
         o[p] = prmt(v[2 * p], v[2 * p + 1], 0x5410u);       // (w_{2p},    w_{2p+1})
         o[p + 8] = prmt(v[2 * p], v[2 * p + 1], 0x7632u);   // (w_{2p+16}, w_{2p+17})
     }
+}
+
+// 16 codes of one word of an affine pack -> 8 bf16 pairs (k, k+1) of s q + b,
+// looked up in the group's table: bf16 weights of codes 0, 1 in lo and 2, 3
+// in hi (code q in bytes 2q, 2q + 1 of the pair).  For codes j and j + 8 the
+// byte selector is [2q_j, 2q_j + 1, 2q_{j+8}, 2q_{j+8} + 1]: one multiply by
+// 0x22 copies each code into two neighbouring nibbles as 2q, the constant adds
+// the +1s, and the high code's nibbles move down by 8 bits.
+__device__ __forceinline__ void unpack_word_affine(uint32_t w, uint32_t lo, uint32_t hi, uint32_t (&o)[8]) {
+    uint32_t v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t m = (w >> (2 * j)) & 0x00030003u;   // q_j at bit 0, q_{j+8} at bit 16
+        const uint32_t t = m * 0x22u + 0x00101010u;        // nibbles 0,1 = 2q_j, 2q_j+1; 4,5 = 2q_{j+8}, 2q_{j+8}+1
+        v[j] = prmt(lo, hi, (t & 0xFFu) | ((t >> 8) & 0xFF00u));   // (w_j, w_{j+8})
+    }
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        o[p] = prmt(v[2 * p], v[2 * p + 1], 0x5410u);       // (w_{2p},   w_{2p+1})
+        o[p + 4] = prmt(v[2 * p], v[2 * p + 1], 0x7632u);   // (w_{2p+8}, w_{2p+9})
+    }
+}
+
+// The bf16 table of one group of an affine pack: (w_0, w_1) and (w_2, w_3),
+// w_q = s q + b in fp32 rounded once.
+__device__ __forceinline__ void affine_table(unsigned short s16, unsigned short b16, uint32_t& lo, uint32_t& hi) {
+    const float sf = __half2float(__ushort_as_half(s16)), bf = __half2float(__ushort_as_half(b16));
+    const __nv_bfloat162 l = __floats2bfloat162_rn(bf, sf + bf);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(fmaf(sf, 2.0f, bf), fmaf(sf, 3.0f, bf));
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -419,6 +455,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         const int h = (warp - 6) >> 2;      // K half of the stage: 0 -> k 0..31, 1 -> k 32..63
         const int rl = q * 32 + lane;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + kTmemA + 16u * h;
+        const bool aff = a.biases != nullptr;
         uint32_t it = 0;
         bool ok = true;
         for (int sg = 0; sg < nseg && ok; ++sg) {
@@ -427,18 +464,27 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             const int nt = tile / m_tiles;
             const int row = nt * kBM + rl;
             const __half* srow = a.scales + (size_t)(row < N ? row : 0) * G;
-            uint32_t s2 = 0;
-            // the segment's first group scale, then each next one a group ahead
+            const __half* brow = aff ? a.biases + (size_t)(row < N ? row : 0) * G : srow;
+            uint32_t s2 = 0, lut_lo = 0, lut_hi = 0;
+            // the segment's first group scale (and bias), then each next one a group ahead
             unsigned short s_next = row < N ? __half_as_ushort(__ldg(srow + (ks0 >> 1))) : (unsigned short)0;
+            unsigned short b_next = aff && row < N ? __half_as_ushort(__ldg(brow + (ks0 >> 1))) : (unsigned short)0;
             for (int ks = ks0; ks < ks1; ++ks, ++it) {
                 if (ks == ks0 || (ks & 1) == 0) {
                     // this group's scale as a bf16 pair; fetch the next group's
-                    const float sf = __half2float(__ushort_as_half(s_next));
-                    const __nv_bfloat16 sb = __float2bfloat16_rn(sf);
-                    const uint32_t sbits = __bfloat16_as_ushort(sb);
-                    s2 = sbits | (sbits << 16);
+                    if (aff) {
+                        affine_table(s_next, b_next, lut_lo, lut_hi);
+                    } else {
+                        const float sf = __half2float(__ushort_as_half(s_next));
+                        const __nv_bfloat16 sb = __float2bfloat16_rn(sf);
+                        const uint32_t sbits = __bfloat16_as_ushort(sb);
+                        s2 = sbits | (sbits << 16);
+                    }
                     const int gn = (ks >> 1) + 1;
-                    if (gn < G && row < N) s_next = __half_as_ushort(__ldg(srow + gn));
+                    if (gn < G && row < N) {
+                        s_next = __half_as_ushort(__ldg(srow + gn));
+                        if (aff) b_next = __half_as_ushort(__ldg(brow + gn));
+                    }
                 }
                 const int s = it % kStages;
                 const uint32_t ph = (it / kStages) & 1u;
@@ -459,8 +505,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
                 } else {
                     const uint2 w = *reinterpret_cast<const uint2*>(crow + 8 * h);
                     uint32_t o0[8], o1[8];
-                    unpack_word(w.x, s2, o0);
-                    unpack_word(w.y, s2, o1);
+                    if (aff) {
+                        unpack_word_affine(w.x, lut_lo, lut_hi, o0);
+                        unpack_word_affine(w.y, lut_lo, lut_hi, o1);
+                    } else {
+                        unpack_word(w.x, s2, o0);
+                        unpack_word(w.y, s2, o1);
+                    }
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         o[i] = o0[i];
@@ -586,7 +637,8 @@ extern "C" size_t tern_gemm_workspace_bytes(int M, int N, int K) {
 
 namespace {
 tern_status run_gemm(const void* x, const uint32_t* codes, const void* scales, void* y, int y_is_bf16, int M, int N,
-                     int K, void* workspace, size_t workspace_bytes, tern_stream_t stream, bool bin) {
+                     int K, void* workspace, size_t workspace_bytes, tern_stream_t stream, bool bin,
+                     const void* biases = nullptr) {
     set_launch_count(0);
     if (M < 1 || N < 1 || K < 128 || K % 128 != 0) return TERN_ERR_SHAPE;
     if ((long long)M * N >= (1LL << 40) || (long long)N * K >= (1LL << 40)) return TERN_ERR_SHAPE;
@@ -616,6 +668,7 @@ tern_status run_gemm(const void* x, const uint32_t* codes, const void* scales, v
     }
     GemmArgs args;
     args.scales = reinterpret_cast<const __half*>(scales);
+    args.biases = reinterpret_cast<const __half*>(biases);
     args.y = y;
     args.y_is_bf16 = y_is_bf16 ? 1 : 0;
     args.bin = bin ? 1 : 0;
@@ -640,6 +693,16 @@ extern "C" tern_status tern_gemm(const void* x, const uint32_t* codes, const voi
                                  int y_is_bf16, int M, int N, int K, void* workspace,
                                  size_t workspace_bytes, tern_stream_t stream) {
     return run_gemm(x, codes, scales, y, y_is_bf16, M, N, K, workspace, workspace_bytes, stream, false);
+}
+
+extern "C" tern_status tern_affine_gemm(const void* x, const uint32_t* codes, const void* scales,
+                                        const void* biases, void* y, int y_is_bf16, int M, int N, int K,
+                                        void* workspace, size_t workspace_bytes, tern_stream_t stream) {
+    set_launch_count(0);
+    if (M < 1 || N < 1 || K < 128 || K % 128 != 0) return TERN_ERR_SHAPE;
+    if (!biases) return TERN_ERR_NULL;
+    if (!aligned16(biases)) return TERN_ERR_ALIGN;
+    return run_gemm(x, codes, scales, y, y_is_bf16, M, N, K, workspace, workspace_bytes, stream, false, biases);
 }
 
 extern "C" tern_status tern_bin_gemm(const void* x, const uint32_t* words, const void* scales, void* y,

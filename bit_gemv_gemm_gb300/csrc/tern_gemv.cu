@@ -17,12 +17,16 @@
 //     2j + 16.  `word & (0x00030003 << 2j)` leaves, in each 16-bit half, the
 //     bit pattern q << 2j.  Read as fp16 that is exactly q * 2^(2j - 24) for
 //     j <= 4 (a subnormal) and q * 2^-14 for j = 5 (the two low exponent
-//     bits), i.e. q * 2^(2j - 24) for every j <= 5.  Codes 6, 7, 14, 15 take
-//     one shift by 12 and reuse the j = 0 and j = 1 masks.  The result is the
-//     MMA A-fragment register directly; q = 0, 1, 2 is exact.
+//     bits), i.e. q * 2^(2j - 24) for every j <= 5 and q = 0, 1, 2.  Codes 6,
+//     7, 14, 15 take one shift by 12 and reuse the j = 0 and j = 1 masks.  The
+//     result is the MMA A-fragment register directly.  An affine pack, whose
+//     code 3 is valid (and would read as 4 in the exponent bits), reads codes
+//     5, 6, 7 and 13, 14, 15 after a shift by 10 instead, as slots 0, 1, 2:
+//     every slot stays a subnormal and every code 0..3 is exact.
 //   * the activation is staged as fp16 B fragments, each value pre-multiplied
 //     by the power of two 2^(E + 10 - 2j') that undoes its slot's
-//     2^(2j' - 24) (j' = j or j - 6), with a per-(token, group) exponent E
+//     2^(2j' - 24) (j' = j or j - 6; j or j - 5 for an affine pack), with a
+//     per-(token, group) exponent E
 //     chosen from the group's max |x| so the largest staged value is below
 //     2^15.  bf16 values stage exactly (8 significant bits into 11).  One MMA
 //     per slot position j accumulates acc = 2^(E - 14) sum_k q_k x_k over 16
@@ -32,6 +36,9 @@
 //     very same rounding, and per row and group
 //         y += s_g * (2^(14 - E) * acc - 2^(14 - E) * acc1),
 //     so a row of zero weights (q = 1 everywhere) gives exactly 0.
+//   * an affine pack (w = s q + b per group, all four codes valid) takes the
+//     same two chains: y += s_g * 2^(14 - E) * acc + b_g * 2^(14 - E) * acc1,
+//     its biases staged in shared memory beside the scales (AFF).
 //
 // Work split.  K is cut into S = ceil(G / 8) slices of whole groups (balanced
 // to within one group), and N into ranges of 16-row tiles; a CTA owns one
@@ -93,6 +100,7 @@ struct GemvArgs {
     const int* xe;              // PRE: the staging exponent E of each (token, group)
     const uint32_t* codes;      // [N][K/16]
     const __half* scales;       // [N][K/128]
+    const __half* biases;       // [N][K/128], an affine pack (AFF) only
     float* y;                   // [M][N]
     // a pair call: a second matrix (N2 rows, T2 tiles) read with the same x;
     // ranges [cps1, cps) are its, [0, cps1) the first one's (cps1 = cps otherwise)
@@ -103,6 +111,7 @@ struct GemvArgs {
     unsigned* flag;             // [cps] per-range flag words (S > 1), 0 between calls
     int M, N, K, G, T, S, cps, rmax;
     int gpad;                   // scale row pitch in shared memory (halves)
+    int boff;                   // AFF: the staged biases' offset from the scales (halves)
     uint32_t off_sc, off_part;  // shared-memory offsets (bytes)
 };
 
@@ -128,7 +137,8 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 
 // Activation staging: a token's 128 values of one group become fp16
 // x 2^(E + 10 - 2j'), j' the code's position within its 16-bit half (j for
-// slots 0-5, j - 6 for 6 and 7, which are read after a shift by 12), with E
+// slots 0-5, j - 6 for 6 and 7, which are read after a shift by 12; with Q3,
+// all four codes valid: j for 0-4, j - 5 for 5-7 after a shift by 10), with E
 // such that the largest |x| times 2^(E + 10) stays below 2^15.
 __device__ __forceinline__ int stage_exponent(float mx) {
     // mx < 2^ex for ex = biased exponent - 126
@@ -136,35 +146,40 @@ __device__ __forceinline__ int stage_exponent(float mx) {
     return (mx > 0.0f && be < 255) ? max(-100, min(5 - (max(be, 1) - 126), 110)) : 0;
 }
 // the exact power of two 2^(E + 10 - 2j') for slot j, exponent within [-100, 120]
+template <bool Q3 = false>
 __device__ __forceinline__ float stage_multiplier(int E, int j) {
-    return __uint_as_float((uint32_t)(E + 10 - 2 * (j < 6 ? j : j - 6) + 127) << 23);
+    constexpr int kSplit = Q3 ? 5 : 6;
+    return __uint_as_float((uint32_t)(E + 10 - 2 * (j < kSplit ? j : j - kSplit) + 127) << 23);
 }
 
 // Slot j's A registers from the four code words by one AND (codes 6, 7, 14, 15
-// after a shift by 12).
+// after a shift by 12; with Q3, codes 5-7 and 13-15 after a shift by 10).
+template <bool Q3>
 __device__ __forceinline__ void slot_regs(int j, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
                                           uint32_t (&r)[4]) {
-    if (j < 6) {
+    constexpr int kSplit = Q3 ? 5 : 6, kShift = 2 * kSplit;
+    if (j < kSplit) {
         const uint32_t mk = 0x00030003u << (2 * j);
         r[0] = w0 & mk;
         r[1] = w1 & mk;
         r[2] = w2 & mk;
         r[3] = w3 & mk;
     } else {
-        const uint32_t mk = 0x00030003u << (2 * (j - 6));
-        r[0] = (w0 >> 12) & mk;
-        r[1] = (w1 >> 12) & mk;
-        r[2] = (w2 >> 12) & mk;
-        r[3] = (w3 >> 12) & mk;
+        const uint32_t mk = 0x00030003u << (2 * (j - kSplit));
+        r[0] = (w0 >> kShift) & mk;
+        r[1] = (w1 >> kShift) & mk;
+        r[2] = (w2 >> kShift) & mk;
+        r[3] = (w3 >> kShift) & mk;
     }
 }
 
 // The chain of one (16-row, 128-weight) unit for one token tile.
+template <bool Q3 = false>
 __device__ __forceinline__ void mma_chain1(float (&acc)[4], const uint32_t (&w)[4], const uint32_t (&b)[16]) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         uint32_t r[4];
-        slot_regs(j, w[0], w[1], w[2], w[3], r);
+        slot_regs<Q3>(j, w[0], w[1], w[2], w[3], r);
         mma16816(acc, r[0], r[1], r[2], r[3], b[2 * j], b[2 * j + 1], j > 0);
     }
 }
@@ -172,14 +187,14 @@ __device__ __forceinline__ void mma_chain1(float (&acc)[4], const uint32_t (&w)[
 // Two units of the same group at once: 2 x MT independent MMA chains sharing
 // the B fragments, each in the slot order of mma_chain1 (so each keeps the
 // ones-pass rounding).
-template <int MT>
+template <int MT, bool Q3 = false>
 __device__ __forceinline__ void pair_mmas(float (&acc)[2][MT][4], const uint32_t (&w)[2][4],
                                           const uint32_t (&b)[MT][16]) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         uint32_t r[2][4];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) slot_regs(j, w[q][0], w[q][1], w[q][2], w[q][3], r[q]);
+        for (int q = 0; q < 2; ++q) slot_regs<Q3>(j, w[q][0], w[q][1], w[q][2], w[q][3], r[q]);
 #pragma unroll
         for (int q = 0; q < 2; ++q)
 #pragma unroll
@@ -274,10 +289,12 @@ __host__ __device__ inline int scale_width(int G, int gA, int gB) {
 // CTA's whole range, and only the lean loop is compiled.
 // BIN: the 1-bit sibling format (lean loop only): slice sigma is groups
 // 8 sigma .. 8 sigma + 7, and a warp whose group is past G has no units.
-template <int MT, bool PRE, bool ONE, bool LEAN = false, bool BIN = false>
+// AFF: an affine pack, w = s q + b (one matrix, bf16 activations).
+template <int MT, bool PRE, bool ONE, bool LEAN = false, bool BIN = false, bool AFF = false>
 __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kCtasPerSm)
 gemv_kernel(const GemvArgs a) {
     static_assert(!BIN || (LEAN && !PRE), "the 1-bit layout runs the lean loop on bf16 activations");
+    static_assert(!AFF || (!BIN && !PRE), "the affine pack has 2-bit codes and bf16 activations");
     constexpr int MP = 8 * MT;
     constexpr int SLOT = BIN ? kBinSlotBytes : kSlotBytes;
     extern __shared__ __align__(16) unsigned char smem[];
@@ -353,30 +370,36 @@ gemv_kernel(const GemvArgs a) {
     {
         const int row0 = tile_lo * 16, rows = R * 16;
         const int mode = scale_mode(G, gA, gB);
-        const uint32_t sc_s = smem_addr(sc);
-        if (mode == 16) {
-            const int cpr = Gs / 8;
-            for (int i = threadIdx.x; i < rows * cpr; i += kThreads) {
-                const int r = i / cpr, c = i - r * cpr;
-                const bool ok = row0 + r < N;
-                cp_async16(sc_s + (uint32_t)(r * gpad + 8 * c) * 2u,
-                           ok ? scales + (size_t)(row0 + r) * G + gA + 8 * c : scales, ok);
+        // the range's [rows][gpad] block of one per-group array (scales, or an
+        // affine pack's biases at `dst`)
+        auto stage_groups = [&](const __half* src, unsigned short* dst) {
+            const uint32_t dst_s = smem_addr(dst);
+            if (mode == 16) {
+                const int cpr = Gs / 8;
+                for (int i = threadIdx.x; i < rows * cpr; i += kThreads) {
+                    const int r = i / cpr, c = i - r * cpr;
+                    const bool ok = row0 + r < N;
+                    cp_async16(dst_s + (uint32_t)(r * gpad + 8 * c) * 2u,
+                               ok ? src + (size_t)(row0 + r) * G + gA + 8 * c : src, ok);
+                }
+            } else if (mode == 4) {
+                const int cpr = scale_width(G, gA, gB) / 2;
+                for (int i = threadIdx.x; i < rows * cpr; i += kThreads) {
+                    const int r = i / cpr, c = i - r * cpr;
+                    const bool ok = row0 + r < N;
+                    cp_async4(dst_s + (uint32_t)(r * gpad + 2 * c) * 2u,
+                              ok ? src + (size_t)(row0 + r) * G + g_lo + 2 * c : src, ok);
+                }
+            } else {
+                for (int i = threadIdx.x; i < rows * Gs; i += kThreads) {
+                    const int r = i / Gs, c = i - r * Gs;
+                    dst[r * gpad + c] = row0 + r < N ? __half_as_ushort(src[(size_t)(row0 + r) * G + gA + c])
+                                                     : (unsigned short)0;
+                }
             }
-        } else if (mode == 4) {
-            const int cpr = scale_width(G, gA, gB) / 2;
-            for (int i = threadIdx.x; i < rows * cpr; i += kThreads) {
-                const int r = i / cpr, c = i - r * cpr;
-                const bool ok = row0 + r < N;
-                cp_async4(sc_s + (uint32_t)(r * gpad + 2 * c) * 2u,
-                          ok ? scales + (size_t)(row0 + r) * G + g_lo + 2 * c : scales, ok);
-            }
-        } else {
-            for (int i = threadIdx.x; i < rows * Gs; i += kThreads) {
-                const int r = i / Gs, c = i - r * Gs;
-                sc[r * gpad + c] = row0 + r < N ? __half_as_ushort(scales[(size_t)(row0 + r) * G + gA + c])
-                                                : (unsigned short)0;
-            }
-        }
+        };
+        stage_groups(scales, sc);
+        if (AFF) stage_groups(a.biases, sc + a.boff);
         cp_async_commit();
     }
     // the lean loop's refill: unit u of the warp's group is tile u of the range
@@ -503,7 +526,7 @@ gemv_kernel(const GemvArgs a) {
                         lo = __floats2half2_rn(v[j] * c0, v[j + 16] * c0);
                         hi = __floats2half2_rn(v[j + 8] * c1, v[j + 24] * c1);
                     } else {
-                        const float c = stage_multiplier(E, j);
+                        const float c = stage_multiplier<AFF>(E, j);
                         lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);       // k = 32t+j, +8
                         hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c); // k = 32t+16+j, +24
                     }
@@ -519,7 +542,7 @@ gemv_kernel(const GemvArgs a) {
                 bin_chain1(acc1, 0xFFFFFFFFu, 0xFFFFFFFFu, b[nt]);
             } else {
                 const uint32_t ones[4] = {0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u};
-                mma_chain1(acc1, ones, b[nt]);
+                mma_chain1<AFF>(acc1, ones, b[nt]);
             }
             const float F = (m < M) ? __uint_as_float((uint32_t)(14 - E + 127) << 23) : 0.0f;   // 2^(14-E)
             const float F0 = __shfl_sync(0xffffffffu, F, (2 * t) * 4);
@@ -535,10 +558,19 @@ gemv_kernel(const GemvArgs a) {
         constexpr bool ADD = decltype(add_c)::value;
         const float s0 = __half2float(__ushort_as_half(sp[0]));
         const float s1 = __half2float(__ushort_as_half(sp[8 * gpad]));
+        // one output: s F acc - s F acc1, or s F acc + b F acc1 for an affine pack
+        float b0 = 0.0f, b1 = 0.0f;
+        if (AFF) {
+            b0 = __half2float(__ushort_as_half(sp[a.boff]));
+            b1 = __half2float(__ushort_as_half(sp[a.boff + 8 * gpad]));
+        }
+        auto out = [&](float s_, float b_, float F_, float a_, float Fa1) {
+            return AFF ? fmaf(s_ * F_, a_, b_ * Fa1) : s_ * fmaf(F_, a_, -Fa1);
+        };
         if (ONE) {
             // token 0 sits in lanes t == 0, element 0 (row gid) and 2 (row gid + 8)
-            const float v0 = s0 * fmaf(f[0].x, acc[0][0], -f[0].y);
-            const float v2 = s1 * fmaf(f[0].x, acc[0][2], -f[0].y);
+            const float v0 = out(s0, b0, f[0].x, acc[0][0], f[0].y);
+            const float v2 = out(s1, b1, f[0].x, acc[0][2], f[0].y);
             if (t == 0) {
                 pw[gid] = ADD ? pw[gid] + v0 : v0;
                 pw[gid + 8] = ADD ? pw[gid + 8] + v2 : v2;
@@ -548,10 +580,10 @@ gemv_kernel(const GemvArgs a) {
 #pragma unroll
         for (int nt = 0; nt < MT; ++nt) {
             const int m0 = nt * 8 + 2 * t, m1 = m0 + 1;
-            const float v0 = s0 * fmaf(f[nt].x, acc[nt][0], -f[nt].y);   // row gid,     token m0
-            const float v1 = s0 * fmaf(f[nt].z, acc[nt][1], -f[nt].w);   // row gid,     token m1
-            const float v2 = s1 * fmaf(f[nt].x, acc[nt][2], -f[nt].y);   // row gid + 8, token m0
-            const float v3 = s1 * fmaf(f[nt].z, acc[nt][3], -f[nt].w);   // row gid + 8, token m1
+            const float v0 = out(s0, b0, f[nt].x, acc[nt][0], f[nt].y);   // row gid,     token m0
+            const float v1 = out(s0, b0, f[nt].z, acc[nt][1], f[nt].w);   // row gid,     token m1
+            const float v2 = out(s1, b1, f[nt].x, acc[nt][2], f[nt].y);   // row gid + 8, token m0
+            const float v3 = out(s1, b1, f[nt].z, acc[nt][3], f[nt].w);   // row gid + 8, token m1
             if (M <= kPrivateMaxM) {
                 // [warp][tile][row][M], written only by its warp
                 if (m0 < M) {
@@ -603,10 +635,10 @@ gemv_kernel(const GemvArgs a) {
             }
             float acc[2][MT][4];
             if (two) {
-                pair_mmas<MT>(acc, w, b);
+                pair_mmas<MT, AFF>(acc, w, b);
             } else {
 #pragma unroll
-                for (int nt = 0; nt < MT; ++nt) mma_chain1(acc[0][nt], w[0], b[nt]);
+                for (int nt = 0; nt < MT; ++nt) mma_chain1<AFF>(acc[0][nt], w[0], b[nt]);
             }
             // the consumed slots are fully read by every lane: refill them kDepth units ahead
             __syncwarp();
@@ -681,10 +713,10 @@ gemv_kernel(const GemvArgs a) {
                     w[q][3] = v1.y;
                 }
                 if (two) {
-                    pair_mmas<MT>(acc, w, b);
+                    pair_mmas<MT, AFF>(acc, w, b);
                 } else {
 #pragma unroll
-                    for (int nt = 0; nt < MT; ++nt) mma_chain1(acc[0][nt], w[0], b[nt]);
+                    for (int nt = 0; nt < MT; ++nt) mma_chain1<AFF>(acc[0][nt], w[0], b[nt]);
                 }
             }
             __syncwarp();
@@ -828,11 +860,13 @@ rotate_stage_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restric
 struct Plan {
     int G, T, S, cps, ctas, rmax, MT, gpad, slot;
     int T2, cps1;   // a pair call: the second matrix's tiles (T counts both) and the first's ranges
+    bool aff;       // an affine pack: biases staged after the scales, boff halves on
+    int boff;
     uint32_t off_sc, off_part;
     size_t smem;
 };
 
-// Shared-memory layout for `cps` ranges (ring | scales | partials).
+// Shared-memory layout for `cps` ranges (ring | scales | biases (AFF) | partials).
 void layout(Plan& p, int M, int cps) {
     p.cps = cps;
     if (p.T2 > 0) {
@@ -849,7 +883,8 @@ void layout(Plan& p, int M, int cps) {
     const int MP = 8 * p.MT;
     size_t off = (size_t)kWarps * kDepth * p.slot;
     p.off_sc = (uint32_t)off;
-    off = align_up(off + (size_t)p.rmax * 16 * p.gpad * 2, 16);
+    p.boff = p.rmax * 16 * p.gpad;   // a multiple of 8 halves: 16-byte aligned
+    off = align_up(off + (size_t)p.rmax * 16 * p.gpad * 2 * (p.aff ? 2 : 1), 16);
     p.off_part = (uint32_t)off;
     off += (M <= kPrivateMaxM ? (size_t)kWarps * p.rmax * 16 * M : (size_t)p.rmax * 16 * MP) * 4;
     p.smem = off;
@@ -857,8 +892,9 @@ void layout(Plan& p, int M, int cps) {
 
 // The device-independent part of the plan: slices and the scale pitch.  The
 // 1-bit layout's slices are groups 8 s .. 8 s + 7 (the last one may be short).
-Plan base_plan(int M, int N, int K, bool bin, int N2 = 0) {
+Plan base_plan(int M, int N, int K, bool bin, int N2 = 0, bool aff = false) {
     Plan p{};
+    p.aff = aff;
     p.G = K / kGroup;
     p.T2 = (N2 + 15) / 16;
     p.T = (N + 15) / 16 + p.T2;
@@ -877,7 +913,7 @@ Plan base_plan(int M, int N, int K, bool bin, int N2 = 0) {
 
 // Lets the kernel use the device's whole per-block shared memory; returns the
 // dynamic part it may take.
-template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN>
+template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN, bool AFF>
 cudaError_t kernel_smem_limit(int dev, int* limit) {
     static int optin_of[64] = {};
     if (!optin_of[dev]) {
@@ -885,11 +921,11 @@ cudaError_t kernel_smem_limit(int dev, int* limit) {
         cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return e;
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, gemv_kernel<MT, PRE, ONE, LEAN, BIN>);
+        e = cudaFuncGetAttributes(&fa, gemv_kernel<MT, PRE, ONE, LEAN, BIN, AFF>);
         if (e != cudaSuccess) return e;
         optin -= (int)fa.sharedSizeBytes;   // the kernel's static shared memory comes first
-        e = cudaFuncSetAttribute(gemv_kernel<MT, PRE, ONE, LEAN, BIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 optin);
+        e = cudaFuncSetAttribute(gemv_kernel<MT, PRE, ONE, LEAN, BIN, AFF>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (e != cudaSuccess) return e;
         optin_of[dev] = optin;
     }
@@ -899,11 +935,11 @@ cudaError_t kernel_smem_limit(int dev, int* limit) {
 
 // One wave: as many CTAs as fit at once, by registers (the launch bound) and
 // by shared memory (which grows with the range length).
-template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN>
+template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN, bool AFF>
 tern_status make_plan(int M, int N, int K, int N2, int sms, int dev, Plan* out) {
     int limit = 0;
-    if (kernel_smem_limit<MT, PRE, ONE, LEAN, BIN>(dev, &limit) != cudaSuccess) return TERN_ERR_CUDA;
-    Plan p = base_plan(M, N, K, BIN, N2);
+    if (kernel_smem_limit<MT, PRE, ONE, LEAN, BIN, AFF>(dev, &limit) != cudaSuccess) return TERN_ERR_CUDA;
+    Plan p = base_plan(M, N, K, BIN, N2, AFF);
     const int need = (p.T + kMaxTiles - 1) / kMaxTiles;   // ranges short enough for the shared partials
     int cps = 1;
     for (int per_sm = GemvCfg<MT>::kCtasPerSm; per_sm >= 1; --per_sm) {
@@ -923,7 +959,7 @@ tern_status make_plan(int M, int N, int K, int N2, int sms, int dev, Plan* out) 
 // Plans depend on the shape and the device only: keep the recent ones.
 struct PlanKey {
     int M, N, K, N2, dev;
-    bool pre, bin;
+    bool pre, bin, aff;
 };
 std::mutex g_plan_mu;
 constexpr int kPlanCache = 64;
@@ -931,7 +967,7 @@ PlanKey g_plan_key[kPlanCache];
 Plan g_plan_val[kPlanCache];
 int g_plan_n = 0, g_plan_next = 0;
 
-template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN>
+template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN, bool AFF>
 tern_status cached_plan(int M, int N, int K, int N2, int sms, Plan* out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TERN_ERR_CUDA;
@@ -939,15 +975,16 @@ tern_status cached_plan(int M, int N, int K, int N2, int sms, Plan* out) {
     std::lock_guard<std::mutex> lk(g_plan_mu);
     for (int i = 0; i < g_plan_n; ++i) {
         const PlanKey& k = g_plan_key[i];
-        if (k.M == M && k.N == N && k.K == K && k.N2 == N2 && k.dev == dev && k.pre == PRE && k.bin == BIN) {
+        if (k.M == M && k.N == N && k.K == K && k.N2 == N2 && k.dev == dev && k.pre == PRE && k.bin == BIN &&
+            k.aff == AFF) {
             *out = g_plan_val[i];
             return TERN_OK;
         }
     }
-    const tern_status st = make_plan<MT, PRE, ONE, LEAN, BIN>(M, N, K, N2, sms, dev, out);
+    const tern_status st = make_plan<MT, PRE, ONE, LEAN, BIN, AFF>(M, N, K, N2, sms, dev, out);
     if (st != TERN_OK) return st;
     const int slot = g_plan_n < kPlanCache ? g_plan_n++ : (g_plan_next++ % kPlanCache);
-    g_plan_key[slot] = PlanKey{M, N, K, N2, dev, PRE, BIN};
+    g_plan_key[slot] = PlanKey{M, N, K, N2, dev, PRE, BIN, AFF};
     g_plan_val[slot] = *out;
     return TERN_OK;
 }
@@ -973,10 +1010,10 @@ size_t workspace_bytes(int M, int N, int K, bool rot) {
     return flag_bytes(N, K) + (rot ? align_up((size_t)M * K * 2 + (size_t)M * (K / kGroup) * 4, 256) : 0);
 }
 
-template <int MT, bool PRE, bool ONE, bool LEAN = false, bool BIN = false>
+template <int MT, bool PRE, bool ONE, bool LEAN = false, bool BIN = false, bool AFF = false>
 tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
     Plan p;
-    const tern_status st = cached_plan<MT, PRE, ONE, LEAN, BIN>(args.M, args.N, args.K, args.N2, sms, &p);
+    const tern_status st = cached_plan<MT, PRE, ONE, LEAN, BIN, AFF>(args.M, args.N, args.K, args.N2, sms, &p);
     if (st != TERN_OK) return st;
     args.G = p.G;
     args.T = p.T - p.T2;   // the first matrix's tiles
@@ -986,10 +1023,12 @@ tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
     args.cps = p.cps;
     args.rmax = p.rmax;
     args.gpad = p.gpad;
+    args.boff = p.boff;
     args.off_sc = p.off_sc;
     args.off_part = p.off_part;
     const cudaError_t e =
-        launch_pdl(gemv_kernel<MT, PRE, ONE, LEAN, BIN>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, args);
+        launch_pdl(gemv_kernel<MT, PRE, ONE, LEAN, BIN, AFF>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true,
+                   args);
     return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
 
@@ -1002,7 +1041,8 @@ size_t pair_flag_bytes(int N, int N2, int K) {
 
 tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const void* scales, float* y, int M,
                 int N, int K, void* workspace, size_t workspace_bytes_, cudaStream_t stream, bool bin = false,
-                const uint32_t* codes2 = nullptr, const void* scales2 = nullptr, float* y2 = nullptr, int N2 = 0) {
+                const uint32_t* codes2 = nullptr, const void* scales2 = nullptr, float* y2 = nullptr, int N2 = 0,
+                const void* biases = nullptr) {
     int sms = 0;
     tern_status st = check_device(&sms);
     if (st != TERN_OK) return st;
@@ -1017,6 +1057,7 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
     args.x = x;
     args.codes = codes;
     args.scales = reinterpret_cast<const __half*>(scales);
+    args.biases = reinterpret_cast<const __half*>(biases);
     args.y = y;
     args.M = M;
     args.N = N;
@@ -1045,6 +1086,13 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
                                : launch_gemv<1, true, false>(args, sms, stream))
                        : (lean ? launch_gemv<2, true, false, true>(args, sms, stream)
                                : launch_gemv<2, true, false>(args, sms, stream));
+    } else if (biases) {
+        st = M == 1 ? (lean ? launch_gemv<1, false, true, true, false, true>(args, sms, stream)
+                            : launch_gemv<1, false, true, false, false, true>(args, sms, stream))
+             : MT == 1 ? (lean ? launch_gemv<1, false, false, true, false, true>(args, sms, stream)
+                               : launch_gemv<1, false, false, false, false, true>(args, sms, stream))
+                       : (lean ? launch_gemv<2, false, false, true, false, true>(args, sms, stream)
+                               : launch_gemv<2, false, false, false, false, true>(args, sms, stream));
     } else if (bin) {
         // the 1-bit layout always runs the lean loop
         st = M == 1 ? launch_gemv<1, false, true, true, true>(args, sms, stream)
@@ -1131,6 +1179,20 @@ extern "C" tern_status tern_gemv_pair(const void* x, const uint32_t* codes_a, co
     if (need > 0 && (!workspace || workspace_bytes_ < need)) return TERN_ERR_WORKSPACE;
     return run(x, nullptr, codes_a, scales_a, y_a, M, N_a, K, workspace, workspace_bytes_, (cudaStream_t)stream,
                false, codes_b, scales_b, y_b, N_b);
+}
+
+extern "C" tern_status tern_affine_gemv(const void* x, const uint32_t* codes, const void* scales, const void* biases,
+                                        float* y, int M, int N, int K, void* workspace, size_t workspace_bytes_,
+                                        tern_stream_t stream) {
+    set_launch_count(0);
+    const tern_status v = validate(x, codes, scales, y, M, N, K);
+    if (v != TERN_OK) return v;
+    if (!biases) return TERN_ERR_NULL;
+    if (!aligned16(biases)) return TERN_ERR_ALIGN;
+    const size_t need = workspace_bytes(M, N, K, false);
+    if (need > 0 && (!workspace || workspace_bytes_ < need)) return TERN_ERR_WORKSPACE;
+    return run(x, nullptr, codes, scales, y, M, N, K, workspace, workspace_bytes_, (cudaStream_t)stream, false,
+               nullptr, nullptr, nullptr, 0, biases);
 }
 
 extern "C" tern_status tern_bin_gemv(const void* x, const uint32_t* words, const void* scales, float* y, int M,

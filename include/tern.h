@@ -194,6 +194,23 @@ tern_status tern_bin_gemv(const void *x, const uint32_t *words, const void *scal
                           int M, int N, int K, void *workspace, size_t workspace_bytes,
                           tern_stream_t stream);
 
+/* The product on an affine pack: y (fp32 [M][N]) = x W^T with
+ *     W[n][k] = s[n][k/128] * q[n][k] + b[n][k/128],
+ * the scale-and-bias form of a group ("prism-ml/Ternary-Bonsai-27B-mlx-2bit"
+ * model card, "MLX packaging").  codes uint32 [N][K/16] in the 2-bit slots of
+ * tern_pack (code k in bits 2 (k % 16) of word k / 16), every code 0..3 valid;
+ * scales and biases fp16 [N][K/128], 16-byte aligned, owned by the caller.
+ * The ternary codes are the case b = -s; the card's own pair (2 s_g, -s_g) on
+ * codes {0, 1} is the 1-bit format.  Shapes, alignment, workspace (the size
+ * tern_gemv_workspace_bytes gives), ordering and error behaviour as for
+ * tern_gemv; a NULL biases pointer is TERN_ERR_NULL.  Results agree with the
+ * exact product to within 1e-3 * sum_k |x w| + 2^-23 * sum_k |x_k b_g(k)|
+ * + 1e-6 per element (the second term covers the rounding of the bias part,
+ * which the scale part may cancel). */
+tern_status tern_affine_gemv(const void *x, const uint32_t *codes, const void *scales, const void *biases,
+                             float *y, int M, int N, int K, void *workspace, size_t workspace_bytes,
+                             tern_stream_t stream);
+
 /* Fixed size of the library-owned scratch array behind tern_gemv_noalloc. */
 #define TERN_NOALLOC_SCRATCH_BYTES (256u << 10)
 
@@ -272,6 +289,17 @@ tern_status tern_gemm(const void *x, const uint32_t *codes, const void *scales, 
 tern_status tern_bin_gemm(const void *x, const uint32_t *words, const void *scales, void *y,
                           int y_is_bf16, int M, int N, int K, void *workspace,
                           size_t workspace_bytes, tern_stream_t stream);
+
+/* The prefill product on an affine pack (W as for tern_affine_gemv): each
+ * weight s q + b is formed in fp32 and rounded once to bf16 before the
+ * tensor-core product, so the fp32 output is within 2^-8 * sum_k |x w| + 1e-6
+ * of the exact product, as for tern_gemm.  Shapes, workspace
+ * (tern_gemm_workspace_bytes), output types and error behaviour as for
+ * tern_gemm; a NULL biases pointer is TERN_ERR_NULL and a misaligned one
+ * TERN_ERR_ALIGN. */
+tern_status tern_affine_gemm(const void *x, const uint32_t *codes, const void *scales, const void *biases,
+                             void *y, int y_is_bf16, int M, int N, int K, void *workspace,
+                             size_t workspace_bytes, tern_stream_t stream);
 
 /* ---------------------------------------------------------------------- */
 /* Diagnostics                                                             */

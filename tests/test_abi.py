@@ -222,3 +222,25 @@ def test_gemv_pair_argument_errors(tern):
     assert need == (2 * 1088 * 4 + 255) // 256 * 256
     assert lib.tern_gemv_pair(P, P, P, P, 17408, P, P, P, 17408, 1, 5120, P, need - 1, None) == 4
     assert tern.lib().tern_gemv_pair_workspace_bytes(1, 16, 16, 1024) == 256
+
+
+def test_affine_argument_errors_never_launch(tern):
+    lib = tern.lib()
+    P = 4096
+    assert lib.tern_affine_gemv(P, P, P, P, P, 0, 16, 128, P, 1 << 20, None) == 2         # M = 0
+    assert lib.tern_affine_gemv(P, P, P, P, P, 17, 16, 128, P, 1 << 20, None) == 2
+    assert lib.tern_affine_gemv(P, P, P, P, P, 1, 16, 96, P, 1 << 20, None) == 2          # K % 128
+    assert lib.tern_affine_gemv(P, P, P, None, P, 1, 16, 128, P, 1 << 20, None) == 1      # no biases
+    assert lib.tern_affine_gemv(P, P, P, P + 2, P, 1, 16, 128, P, 1 << 20, None) == 3     # misaligned biases
+    assert lib.tern_affine_gemv(P, P + 4, P, P, P, 1, 16, 128, P, 1 << 20, None) == 3
+    need = tern.gemv_workspace_bytes(1, 16, 2048)
+    assert lib.tern_affine_gemv(P, P, P, P, P, 1, 16, 2048, None, need, None) == 4
+    assert lib.tern_affine_gemv(P, P, P, P, P, 1, 16, 2048, P, need - 1, None) == 4
+    assert lib.tern_affine_gemm(P, P, P, P, P, 0, 0, 16, 128, P, 1 << 20, None) == 2
+    assert lib.tern_affine_gemm(P, P, P, P, P, 0, 4, 16, 96, P, 1 << 20, None) == 2
+    assert lib.tern_affine_gemm(P, P, P, None, P, 0, 4, 16, 128, P, 1 << 20, None) == 1
+    assert lib.tern_affine_gemm(P, P, P, P + 8, P, 0, 4, 16, 128, P, 1 << 20, None) == 3
+    assert lib.tern_affine_gemm(P, None, P, P, P, 0, 4, 16, 128, P, 1 << 20, None) == 1
+    need = tern.gemm_workspace_bytes(64, 256, 512)
+    assert lib.tern_affine_gemm(P, P, P, P, P, 0, 64, 256, 512, P, need - 1, None) == 4
+    assert tern.last_launch_count() == 0
