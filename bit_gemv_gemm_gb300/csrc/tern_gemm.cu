@@ -214,6 +214,9 @@ __device__ __forceinline__ void affine_table(unsigned short s16, unsigned short 
     hi = *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// AFF: an affine pack (a compile-time switch, so that the other layouts'
+// unpack loop carries no trace of it).
+template <bool AFF>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_c,
             const GemmArgs a) {
@@ -455,7 +458,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         const int h = (warp - 6) >> 2;      // K half of the stage: 0 -> k 0..31, 1 -> k 32..63
         const int rl = q * 32 + lane;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + kTmemA + 16u * h;
-        const bool aff = a.biases != nullptr;
+        constexpr bool aff = AFF;
         uint32_t it = 0;
         bool ok = true;
         for (int sg = 0; sg < nseg && ok; ++sg) {
@@ -472,7 +475,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             for (int ks = ks0; ks < ks1; ++ks, ++it) {
                 if (ks == ks0 || (ks & 1) == 0) {
                     // this group's scale as a bf16 pair; fetch the next group's
-                    if (aff) {
+                    if constexpr (AFF) {
                         affine_table(s_next, b_next, lut_lo, lut_hi);
                     } else {
                         const float sf = __half2float(__ushort_as_half(s_next));
@@ -661,8 +664,10 @@ tern_status run_gemm(const void* x, const uint32_t* codes, const void* scales, v
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TERN_ERR_CUDA;
     if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes) != cudaSuccess)
             return TERN_ERR_CUDA;
         attr_set[dev] = true;
     }
@@ -681,8 +686,8 @@ tern_status run_gemm(const void* x, const uint32_t* codes, const void* scales, v
     args.stream_k = use_stream_k(M, N, K, shares) ? 1 : 0;
     const int tiles = gemm_tiles(M, N);
     const int grid = args.stream_k ? shares : (tiles < shares ? tiles : shares);
-    cudaError_t e = launch_pdl(gemm_kernel, dim3(grid), dim3(kThreads), kSmemBytes, (cudaStream_t)stream, true, mx,
-                               mc, args);
+    cudaError_t e = launch_pdl(biases ? gemm_kernel<true> : gemm_kernel<false>, dim3(grid), dim3(kThreads),
+                               kSmemBytes, (cudaStream_t)stream, true, mx, mc, args);
     if (e != cudaSuccess) return TERN_ERR_CUDA;
     set_launch_count(1);
     return TERN_OK;
