@@ -28,10 +28,10 @@
 // is 16 bytes per row too, but spans two K stages (starting at the even one, so
 // the TMA x coordinate stays 16-byte aligned), and the unpack turns bits j and
 // j + 16 of a word into bf16 2b - 1 with one shift and one FMA.
-// An affine pack (w = s q + b per group, every 2-bit code valid) runs it too:
-// per row and group the four weights s q + b are formed in fp32 and rounded
-// once to bf16, and each code picks its weight from that table with one byte
-// permute.
+// An affine pack (w = s q + b per group, every 2-bit code valid) runs it too
+// (gemm_kernel<true>): per row and group the four weights s q + b are formed
+// in fp32 and rounded once to bf16, and each pair of codes picks its two
+// weights from that table with one byte permute.
 // Scheduling takes whole tiles on a persistent grid, or stream-K where whole
 // tiles would leave SMs idle longer than stream-K's tail costs: the (tile,
 // 64-wide K stage) iterations, tile-major, are cut into one equal contiguous
@@ -184,34 +184,41 @@ __device__ __forceinline__ void unpack_word_bin(uint32_t w, uint32_t s2, uint32_
 }
 
 // 16 codes of one word of an affine pack -> 8 bf16 pairs (k, k+1) of s q + b,
-// looked up in the group's table: bf16 weights of codes 0, 1 in lo and 2, 3
-// in hi (code q in bytes 2q, 2q + 1 of the pair).  For codes j and j + 8 the
-// byte selector is [2q_j, 2q_j + 1, 2q_{j+8}, 2q_{j+8} + 1]: one multiply by
-// 0x22 copies each code into two neighbouring nibbles as 2q, the constant adds
-// the +1s, and the high code's nibbles move down by 8 bits.
+// looked up in the group's table: lo holds the low bytes of the bf16 weights
+// of codes 0..3 (byte q for code q) and hi their high bytes.  Codes j and
+// j + 4 sit 8 bits apart, so one shift and mask leave q_j in bits 0-1 and
+// q_{j+4} in bits 8-9, and one multiply-add by 0x11, 0x4040 turns that into
+// the byte selector [q_j, 4 + q_j, q_{j+4}, 4 + q_{j+4}]: one byte permute
+// then gives the pair (w_j, w_{j+4}), at four operations per two weights like
+// the ternary unpack.
 __device__ __forceinline__ void unpack_word_affine(uint32_t w, uint32_t lo, uint32_t hi, uint32_t (&o)[8]) {
     uint32_t v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t m = (w >> (2 * j)) & 0x00030003u;   // q_j at bit 0, q_{j+8} at bit 16
-        const uint32_t t = m * 0x22u + 0x00101010u;        // nibbles 0,1 = 2q_j, 2q_j+1; 4,5 = 2q_{j+8}, 2q_{j+8}+1
-        v[j] = prmt(lo, hi, (t & 0xFFu) | ((t >> 8) & 0xFF00u));   // (w_j, w_{j+8})
+    for (int i = 0; i < 8; ++i) {
+        const int j = i < 4 ? i : i + 4;                       // codes j and j + 4: 0-3 and 8-11
+        const uint32_t m = (w >> (2 * j)) & 0x0303u;
+        v[i] = prmt(lo, hi, m * 0x11u + 0x4040u);             // (w_j, w_{j+4})
     }
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        o[p] = prmt(v[2 * p], v[2 * p + 1], 0x5410u);       // (w_{2p},   w_{2p+1})
-        o[p + 4] = prmt(v[2 * p], v[2 * p + 1], 0x7632u);   // (w_{2p+8}, w_{2p+9})
+    for (int h = 0; h < 2; ++h) {
+        // v[4h + r] = (w_{8h+r}, w_{8h+r+4})
+        o[4 * h] = prmt(v[4 * h], v[4 * h + 1], 0x5410u);       // (w_{8h},   w_{8h+1})
+        o[4 * h + 1] = prmt(v[4 * h + 2], v[4 * h + 3], 0x5410u); // (w_{8h+2}, w_{8h+3})
+        o[4 * h + 2] = prmt(v[4 * h], v[4 * h + 1], 0x7632u);   // (w_{8h+4}, w_{8h+5})
+        o[4 * h + 3] = prmt(v[4 * h + 2], v[4 * h + 3], 0x7632u); // (w_{8h+6}, w_{8h+7})
     }
 }
 
-// The bf16 table of one group of an affine pack: (w_0, w_1) and (w_2, w_3),
-// w_q = s q + b in fp32 rounded once.
+// The table of one group of an affine pack: w_q = s q + b in fp32, rounded
+// once to bf16; lo gets the four low bytes (byte q of w_q) and hi the four
+// high bytes.
 __device__ __forceinline__ void affine_table(unsigned short s16, unsigned short b16, uint32_t& lo, uint32_t& hi) {
     const float sf = __half2float(__ushort_as_half(s16)), bf = __half2float(__ushort_as_half(b16));
-    const __nv_bfloat162 l = __floats2bfloat162_rn(bf, sf + bf);
-    const __nv_bfloat162 h = __floats2bfloat162_rn(fmaf(sf, 2.0f, bf), fmaf(sf, 3.0f, bf));
-    lo = *reinterpret_cast<const uint32_t*>(&l);
-    hi = *reinterpret_cast<const uint32_t*>(&h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(bf, sf + bf);                         // w_0, w_1
+    const __nv_bfloat162 h = __floats2bfloat162_rn(fmaf(sf, 2.0f, bf), fmaf(sf, 3.0f, bf)); // w_2, w_3
+    const uint32_t l32 = *reinterpret_cast<const uint32_t*>(&l), h32 = *reinterpret_cast<const uint32_t*>(&h);
+    lo = prmt(l32, h32, 0x6420u);
+    hi = prmt(l32, h32, 0x7531u);
 }
 
 // AFF: an affine pack (a compile-time switch, so that the other layouts'
