@@ -61,13 +61,29 @@ def src_hash(path: str) -> str:
 def load_traffic(kernel: str, src: str):
     """Per-launch DRAM bytes of `kernel` from a committed ncu summary, or None if
     the kernel source changed since the counters were taken."""
+    d = traffic_entry(kernel, src)
+    return d.get("dram_bytes_per_launch") if d else None
+
+
+def traffic_entry(kernel: str, src: str):
+    """The committed ncu summary entry of `kernel` (the captured launch, its DRAM
+    bytes and its algorithmic bytes), or None if the source changed since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(kernel)
     if not d or d.get("source_sha256_16") != src_hash(src):
         return None
-    return d.get("dram_bytes_per_launch")
+    return d
+
+
+def traffic_note(kernel: str, src: str) -> dict:
+    """What the roofline's `traffic` figure was taken on: the captured launch and
+    that launch's own algorithmic bytes (to compare the DRAM bytes against)."""
+    d = traffic_entry(kernel, src)
+    if not d:
+        return {"traffic_launch": None, "traffic_launch_alg_bytes": None}
+    return {"traffic_launch": d.get("workload"), "traffic_launch_alg_bytes": d.get("alg_bytes_per_launch")}
 
 
 # ---------------------------------------------------------------------------
@@ -618,7 +634,7 @@ def bench_prefill(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int, peaks:
         "roofline": {"bound": "tensor", "kernel": "tern_gemm (tcgen05)", "achieved": tf, "peak": peak,
                      "unit": "TFLOP/s", "frac": tf / peak,
                      "peak_source": f"{peaks['_source']} bf16_tflops_sustained (pass of {ms:.1f} ms)",
-                     "traffic": load_traffic("gemm_kernel", GEMM_SRC)},
+                     "traffic": load_traffic("gemm_kernel", GEMM_SRC), **traffic_note("gemm_kernel", GEMM_SRC)},
         "dominant": dom[0],
     }
 
@@ -765,7 +781,7 @@ def main() -> None:
         "roofline": {"bound": "hbm", "kernel": "gemv_kernel (one launch per tern_gemv_pair or tern_gemv call)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": f"{peaks['_source']} hbm_gbs",
-                     "traffic": load_traffic("gemv_kernel", GEMV_SRC)},
+                     "traffic": load_traffic("gemv_kernel", GEMV_SRC), **traffic_note("gemv_kernel", GEMV_SRC)},
         "clocks": dec["clocks"],
         "e2e": {"value": ws_count * dec["weight_bytes"] / (dec["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": dec["h2d"], "d2h_bytes_per_step": dec["d2h"]},
