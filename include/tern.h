@@ -26,6 +26,9 @@
  *   y       [M][N] row-major, y[m][n] = sum_k x[m][k] * (q[n][k] - 1) * s[n][k/128].
  *   signs   int8 [K], each +1 or -1.
  *   Packed size: N*K/4 bytes of codes + N*K/64 bytes of scales.
+ *   The 1-bit sibling format (tern_bin_*) keeps one bit per weight in uint32
+ *   words [N][K/32]; an affine pack (tern_affine_*) adds fp16 biases
+ *   [N][K/128] and allows code 3.  Their entry points describe them.
  *
  * Conventions:
  *   - Device entry points take device pointers owned by the caller, launch
@@ -40,11 +43,13 @@
  *     (a bounded wait that gave up) set a sticky device flag that
  *     tern_device_error() reads.
  *   - Pointers must be 16-byte aligned (TERN_ERR_ALIGN otherwise).
- *   - The kernels of tern_gemv, tern_fwht_gemm and tern_fwht use programmatic
- *     dependent launch: a tern_* kernel may begin reading `codes` and `scales`
- *     while the previous tern_* kernel on the stream is still running, so
- *     codes/scales must not be outputs of the immediately preceding tern_*
- *     call (tern_pack excepted: it never releases its dependents early).
+ *   - The product and rotation kernels use programmatic dependent launch.
+ *     Those of the *gemv* and *fwht* entry points may begin reading `codes`,
+ *     `scales` (and `biases`) while the previous tern_* kernel on the stream
+ *     is still running, so these must not be outputs of the immediately
+ *     preceding tern_* call (the packers and the scale conversion excepted:
+ *     they never release their dependents early).  The *gemm* kernels start
+ *     early too but read nothing before the previous kernel has finished.
  *     Activations, outputs and workspaces are always ordered.
  *   - Only sm_103 devices (GB300) are supported (TERN_ERR_ARCH otherwise).
  */
