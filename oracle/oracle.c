@@ -4,7 +4,7 @@
  *
  * TEST INFRASTRUCTURE ONLY.  This file is plain, slow, obviously correct C
  * that the tests, the smoke check and the benchmark's CPU-baseline leg use to
- * judge the CUDA library.  The library never links, loads or calls it, and it
+ * check the CUDA library.  The library never links, loads or calls it, and it
  * shares no code, header, table or helper with the library.
  *
  * Sources (the web pages this method is described on):
