@@ -97,6 +97,15 @@ def _stream(stream) -> int:
     return stream.cuda_stream
 
 
+def _covers(**need) -> None:
+    """name=(tensor, elements): each tensor must hold at least the elements the
+    call reads or writes through its pointer (the library sees only pointers
+    and sizes, so a short tensor would be read or written past its end)."""
+    for name, (t, n) in need.items():
+        if t is not None and t.numel() < n:
+            raise ValueError(f"{name} holds {t.numel()} elements; the call needs {n}")
+
+
 def _dev(t: torch.Tensor, dtype, name: str) -> int:
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
@@ -142,6 +151,7 @@ def pack(t: torch.Tensor, codes: torch.Tensor | None = None, bad_count: torch.Te
     N, K = t.shape
     if codes is None:
         codes = torch.empty((N, K // 16), dtype=torch.int32, device=t.device)
+    _covers(codes=(codes, N * (K // 16)), bad_count=(bad_count, 1))
     bp = _dev(bad_count, torch.int32, "bad_count") if bad_count is not None else None
     _check("tern_pack", lib().tern_pack(_dev(t, torch.int8, "t"), N, K, _dev(codes, torch.int32, "codes"),
                                         bp, _stream(stream)))
@@ -153,6 +163,7 @@ def scales_from_g64(s64: torch.Tensor, K: int, mismatch: torch.Tensor | None = N
     repeated) -> g128 scales fp16 [N, K/128]; differing halves are counted."""
     N = s64.shape[0]
     out = torch.empty((N, K // 128), dtype=torch.float16, device=s64.device)
+    _covers(s64=(s64, N * (K // 64)), mismatch=(mismatch, 1))
     mp = _dev(mismatch, torch.int32, "mismatch") if mismatch is not None else None
     _check("tern_scales_from_g64", lib().tern_scales_from_g64(_dev(s64, torch.float16, "s64"), N, K,
                                                               _dev(out, torch.float16, "s128"), mp, _stream(stream)))
@@ -176,6 +187,7 @@ def bin_pack(t: torch.Tensor, words: torch.Tensor | None = None, bad_count: torc
     N, K = t.shape
     if words is None:
         words = torch.empty((N, K // 32), dtype=torch.int32, device=t.device)
+    _covers(words=(words, N * (K // 32)), bad_count=(bad_count, 1))
     bp = _dev(bad_count, torch.int32, "bad_count") if bad_count is not None else None
     _check("tern_bin_pack", lib().tern_bin_pack(_dev(t, torch.int8, "t"), N, K, _dev(words, torch.int32, "words"),
                                                 bp, _stream(stream)))
@@ -236,6 +248,7 @@ def gemv(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y: torch.Te
     N = codes.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _covers(codes=(codes, N * (K // 16)), scales=(scales, N * (K // 128)), y=(y, M * N))
     if ws is None:
         ws = workspace(gemv_workspace_bytes(M, N, K), x.device)
     _check("tern_gemv", lib().tern_gemv(
@@ -252,6 +265,7 @@ def bin_gemv(x: torch.Tensor, words: torch.Tensor, scales: torch.Tensor, y: torc
     N = words.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _covers(words=(words, N * (K // 32)), scales=(scales, N * (K // 128)), y=(y, M * N))
     if ws is None:
         ws = workspace(gemv_workspace_bytes(M, N, K), x.device)
     _check("tern_bin_gemv", lib().tern_bin_gemv(
@@ -270,6 +284,8 @@ def gemv_pair(x: torch.Tensor, codes_a: torch.Tensor, scales_a: torch.Tensor, co
         y_a = torch.empty((M, Na), dtype=torch.float32, device=x.device)
     if y_b is None:
         y_b = torch.empty((M, Nb), dtype=torch.float32, device=x.device)
+    _covers(codes_a=(codes_a, Na * (K // 16)), scales_a=(scales_a, Na * (K // 128)), y_a=(y_a, M * Na),
+            codes_b=(codes_b, Nb * (K // 16)), scales_b=(scales_b, Nb * (K // 128)), y_b=(y_b, M * Nb))
     if ws is None:
         ws = workspace(int(lib().tern_gemv_pair_workspace_bytes(M, Na, Nb, K)), x.device)
     _check("tern_gemv_pair", lib().tern_gemv_pair(
@@ -287,6 +303,7 @@ def gemv_noalloc(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y: 
     N = codes.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _covers(codes=(codes, N * (K // 16)), scales=(scales, N * (K // 128)), y=(y, M * N))
     _check("tern_gemv_noalloc", lib().tern_gemv_noalloc(
         _dev(x, torch.bfloat16, "x"), _dev(codes, torch.int32, "codes"), _dev(scales, torch.float16, "scales"),
         _dev(y, torch.float32, "y"), M, N, K, _stream(stream)))
@@ -298,6 +315,7 @@ def fwht(x: torch.Tensor, signs: torch.Tensor, y: torch.Tensor | None = None, st
     M, K = x.shape
     if y is None:
         y = torch.empty_like(x)
+    _covers(signs=(signs, K), y=(y, M * K))
     _check("tern_fwht", lib().tern_fwht(_dev(x, torch.bfloat16, "x"), _dev(signs, torch.int8, "signs"),
                                         _dev(y, torch.bfloat16, "y"), M, K, _stream(stream)))
     return y
@@ -310,6 +328,7 @@ def fwht_gemm(x: torch.Tensor, signs: torch.Tensor, codes: torch.Tensor, scales:
     N = codes.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _covers(signs=(signs, K), codes=(codes, N * (K // 16)), scales=(scales, N * (K // 128)), y=(y, M * N))
     if ws is None:
         ws = workspace(gemv_workspace_bytes(M, N, K), x.device)
     _check("tern_fwht_gemm", lib().tern_fwht_gemm(
@@ -328,6 +347,7 @@ def gemm(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, y: torch.Te
         y = torch.empty((M, N), dtype=out_dtype, device=x.device)
     if y.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("y must be float32 or bfloat16")
+    _covers(codes=(codes, N * (K // 16)), scales=(scales, N * (K // 128)), y=(y, M * N))
     if ws is None:
         ws = workspace(gemm_workspace_bytes(M, N, K), x.device)
     _check("tern_gemm", lib().tern_gemm(
@@ -368,6 +388,7 @@ def bin_gemm(x: torch.Tensor, words: torch.Tensor, scales: torch.Tensor, y: torc
         y = torch.empty((M, N), dtype=out_dtype, device=x.device)
     if y.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("y must be float32 or bfloat16")
+    _covers(words=(words, N * (K // 32)), scales=(scales, N * (K // 128)), y=(y, M * N))
     if ws is None:
         ws = workspace(gemm_workspace_bytes(M, N, K), x.device)
     _check("tern_bin_gemm", lib().tern_bin_gemm(
@@ -386,6 +407,8 @@ def affine_gemv(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, bias
     N = codes.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _covers(codes=(codes, N * (K // 16)), scales=(scales, N * (K // 128)), biases=(biases, N * (K // 128)),
+            y=(y, M * N))
     if ws is None:
         ws = workspace(gemv_workspace_bytes(M, N, K), x.device)
     _check("tern_affine_gemv", lib().tern_affine_gemv(
@@ -406,6 +429,8 @@ def affine_gemm(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, bias
         y = torch.empty((M, N), dtype=out_dtype, device=x.device)
     if y.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("y must be float32 or bfloat16")
+    _covers(codes=(codes, N * (K // 16)), scales=(scales, N * (K // 128)), biases=(biases, N * (K // 128)),
+            y=(y, M * N))
     if ws is None:
         ws = workspace(gemm_workspace_bytes(M, N, K), x.device)
     _check("tern_affine_gemm", lib().tern_affine_gemm(
