@@ -44,8 +44,10 @@
  * Parity pins live in the "not gpu" tests: brute-force dense matmul from an
  * explicitly expanded W, exhaustive pack/unpack patterns, the explicit
  * Hadamard matrix for n <= 64, H*H = n*I, Parseval, closed forms on e_0 and
- * constant vectors, power-of-two linearity in the scales, one-hot columns, and
- * the bit-rate figures the card prints.
+ * constant vectors, power-of-two linearity in the scales, one-hot columns, the
+ * bit-rate figures the card prints, and for the 1-bit and affine forms their
+ * bit-exact agreement with the ternary product where the weights coincide
+ * (w = +-s; b = -s) and with the 1-bit product for the card's MLX pair.
  */
 #include <math.h>
 #include <stdint.h>
