@@ -244,3 +244,44 @@ def test_affine_argument_errors_never_launch(tern):
     need = tern.gemm_workspace_bytes(64, 256, 512)
     assert lib.tern_affine_gemm(P, P, P, P, P, 0, 64, 256, 512, P, need - 1, None) == 4
     assert tern.last_launch_count() == 0
+
+
+def test_header_is_plain_c_and_a_c_program_links_the_library(tern, tmp_path):
+    """The boundary needs no CUDA, torch or C++ headers: tern.h compiles as
+    C99 and C++17, and a plain C program links libtern.so and calls its
+    host-side entry points (no GPU needed for these)."""
+    import subprocess
+    inc = os.path.join(ROOT, "include")
+    hdr = os.path.join(inc, "tern.h")
+    for lang, std, cc in (("c", "-std=c99", "gcc"), ("c++", "-std=c++17", "g++")):
+        r = subprocess.run([cc, std, "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-x", lang, hdr],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+    src = tmp_path / "use_tern.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "tern.h"
+int main(void) {
+    int8_t t[2 * 32];
+    uint32_t codes[2 * 2];
+    int8_t back[2 * 32];
+    long long bad = -1;
+    for (int i = 0; i < 64; ++i) t[i] = (int8_t)((i % 3) - 1);
+    if (tern_pack_host(t, 2, 32, codes, &bad) != TERN_OK || bad != 0) return 1;
+    if (tern_unpack_host(codes, 2, 32, back, &bad) != TERN_OK || bad != 0) return 2;
+    if (memcmp(t, back, sizeof t) != 0) return 3;
+    if (tern_packed_bytes(17408, 5120) != 23674880u) return 4;
+    if (tern_gemv(NULL, NULL, NULL, NULL, 0, 1, 128, NULL, 0, NULL) != TERN_ERR_SHAPE) return 5;
+    printf("%s\n", tern_status_str(TERN_OK));
+    return 0;
+}
+''')
+    lib = tern.LIB_PATH
+    exe = tmp_path / "use_tern"
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", inc, str(src), lib, "-o", str(exe),
+                        f"-Wl,-rpath,{os.path.dirname(lib)}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.strip()
