@@ -659,7 +659,55 @@ def cpu_baseline(budget_s: float = 12.0) -> dict:
     gbps = calls * weight_bytes(N, K) / el / 1e9
     return {"value": gbps, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
             "sample": f"{calls} full M=1 products of one 5120->17408 matrix (23.7 MB packed) in {el:.1f} s "
-                      f"with the C oracle (fp64, OpenMP over outputs)"}
+                      f"with the C oracle (fp64, OpenMP over outputs)", "cpu": cpu_model()}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name, for the record (x86: /proc/cpuinfo; Arm: lscpu)."""
+    import platform
+    try:
+        for line in open("/proc/cpuinfo"):
+            k, _, v = line.partition(":")
+            if k.strip() == "model name" and v.strip():
+                return v.strip()
+    except OSError:
+        pass
+    try:
+        import subprocess
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() == "Model name" and v.strip():
+                return v.strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine() or "unknown"
+
+
+def cpu_baseline_pp512(budget_s: float = 5.0) -> dict:
+    """The oracle, as it stands, on a bounded sample of the pp512 workload: all
+    512 tokens against a growing number of rows of one gate-shaped (5120 ->
+    17408) matrix; the rate is extrapolated to the whole 64-layer pass."""
+    import oracle
+    import synth
+    oracle.build()
+    M, K, rows = synth.PREFILL_M, 5120, 64
+    p = synth.problem(5, M, rows, K, tag="cpu_pp")
+    codes, _ = oracle.pack(p.t)
+    oracle.matmul(p.x[:4], codes[:4], p.s[:4])                      # warm the library
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        oracle.matmul(p.x, codes, p.s)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or calls >= 50:
+            break
+    tflops = calls * 2.0 * M * rows * K / el / 1e12
+    total = sum(2.0 * M * N * K for (_, K, N) in synth.PREFILL_LAYER) * synth.PREFILL_LAYERS
+    return {"value": tflops, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{calls} products of 512 tokens x {rows} rows x K={K} (a slice of the gate matrix) in "
+                      f"{el:.1f} s with the C oracle (fp64, OpenMP over outputs)",
+            "extrapolated_pass_s": total / (tflops * 1e12)}
 
 
 def run_reference(args) -> None:
@@ -696,8 +744,9 @@ def run_reference(args) -> None:
         "config": {"workload": "decode GEMV M=1, 5120->17408 rows sample (CPU oracle)", "M": 1, "K": K,
                    "N_sampled": rows},
         "cpu_baseline": {"value": gbps, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
-                         "sample": f"{rows} rows x K={K} per step, {args.steps} steps"},
+                         "sample": f"{rows} rows x K={K} per step, {args.steps} steps", "cpu": cpu_model()},
         "e2e": {"value": gbps, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "rows": {"pp512": {"cpu_baseline": cpu_baseline_pp512(budget_s=3.0)}},
     }
     print(json.dumps(line), flush=True)
 
@@ -790,6 +839,8 @@ def main() -> None:
     }
     if rank == 0 and "cpu" not in skip:
         line["cpu_baseline"] = cpu_baseline()
+        if isinstance(rows.get("pp512"), dict) and "TFLOPs" in rows["pp512"]:
+            rows["pp512"]["cpu_baseline"] = cpu_baseline_pp512()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws_count > 1:
