@@ -617,3 +617,27 @@ def test_affine_matmul_sampled_equals_full(orc):
     ns = np.tile(np.arange(29), 3)
     ys, as_ = orc.affine_matmul_sampled(p.x, p.codes, p.s, p.b, ms, ns)
     assert np.array_equal(ys, y.reshape(-1)) and np.array_equal(as_, a.reshape(-1))
+
+
+# --------------------------------------------------------------------------
+# the rotation at its real block size against a library routine
+# --------------------------------------------------------------------------
+
+def test_rotation_at_4096_matches_scipy_sylvester_matrix(orc):
+    """scipy.linalg.hadamard builds Sylvester's construction (natural order)
+    independently; the oracle's 4096-point rotation is H_4096 (s x) / 64
+    against it, for two blocks of two tokens, and the explicit matrix agrees
+    with it entry for entry up to n = 1024."""
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    for n in (1, 2, 16, 256, 1024):
+        assert np.array_equal(orc.hadamard_explicit(n), scipy_linalg.hadamard(n).astype(np.float64))
+    K = 8192
+    H = scipy_linalg.hadamard(4096, dtype=np.int8).astype(np.float64)
+    x = synth.activations(16, "x4096", (2, K))
+    s = synth.signs(16, "s4096", K)
+    got = orc.rotate(x, s)
+    xs = bf16_bits_to_f64(x) * s
+    want = np.concatenate([xs[:, :4096] @ H.T, xs[:, 4096:] @ H.T], axis=1) / 64.0
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    v = synth.activations(17, "v", (1, 4096)).astype(np.float64)
+    assert np.allclose(orc.fwht(v[0]), H @ v[0], rtol=0, atol=1e-9)
