@@ -641,7 +641,8 @@ def bench_prefill(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int, peaks:
 
 def cpu_baseline(budget_s: float = 12.0) -> dict:
     """The oracle, as it stands, on a bounded sample of the decode workload:
-    repeated full M=1 products of one gate-shaped (5120 -> 17408) matrix."""
+    repeated full M=1 products of one gate-shaped (5120 -> 17408) matrix on all
+    host cores, then row slices of it on one core."""
     import oracle
     import synth
     oracle.build()
@@ -657,9 +658,21 @@ def cpu_baseline(budget_s: float = 12.0) -> dict:
         if el >= budget_s or calls >= 200:
             break
     gbps = calls * weight_bytes(N, K) / el / 1e9
-    return {"value": gbps, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+    cores = oracle.max_threads()
+    rows, calls1, t0 = 2048, 0, time.perf_counter()
+    while True:
+        oracle.matmul(p.x, codes[:rows], p.s[:rows], nthreads=1)
+        calls1 += 1
+        el1 = time.perf_counter() - t0
+        if el1 >= budget_s / 3 or calls1 >= 200:
+            break
+    gbps1 = calls1 * weight_bytes(rows, K) / el1 / 1e9
+    oracle.matmul(p.x, codes[:64], p.s[:64], nthreads=cores)    # the thread count persists: restore it
+    return {"value": gbps, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{calls} full M=1 products of one 5120->17408 matrix (23.7 MB packed) in {el:.1f} s "
-                      f"with the C oracle (fp64, OpenMP over outputs)", "cpu": cpu_model()}
+                      f"with the C oracle (fp64, OpenMP over outputs)", "cpu": cpu_model(),
+            "single_thread": {"value": gbps1, "unit": "GB/s", "cores": 1,
+                              "sample": f"{calls1} products of {rows} rows of that matrix in {el1:.1f} s, one thread"}}
 
 
 def cpu_model() -> str:
@@ -687,7 +700,8 @@ def cpu_model() -> str:
 def cpu_baseline_pp512(budget_s: float = 5.0) -> dict:
     """The oracle, as it stands, on a bounded sample of the pp512 workload: all
     512 tokens against a growing number of rows of one gate-shaped (5120 ->
-    17408) matrix; the rate is extrapolated to the whole 64-layer pass."""
+    17408) matrix, on all host cores and on one; the rates are extrapolated to
+    the whole 64-layer pass."""
     import oracle
     import synth
     oracle.build()
@@ -695,19 +709,28 @@ def cpu_baseline_pp512(budget_s: float = 5.0) -> dict:
     p = synth.problem(5, M, rows, K, tag="cpu_pp")
     codes, _ = oracle.pack(p.t)
     oracle.matmul(p.x[:4], codes[:4], p.s[:4])                      # warm the library
-    calls, t0 = 0, time.perf_counter()
-    while True:
-        oracle.matmul(p.x, codes, p.s)
-        calls += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or calls >= 50:
-            break
-    tflops = calls * 2.0 * M * rows * K / el / 1e12
     total = sum(2.0 * M * N * K for (_, K, N) in synth.PREFILL_LAYER) * synth.PREFILL_LAYERS
-    return {"value": tflops, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+
+    def rate(nthreads, r, budget):
+        calls, t0 = 0, time.perf_counter()
+        while True:
+            oracle.matmul(p.x, codes[:r], p.s[:r], nthreads=nthreads)
+            calls += 1
+            el = time.perf_counter() - t0
+            if el >= budget or calls >= 50:
+                return calls, el, calls * 2.0 * M * r * K / el / 1e12
+
+    cores = oracle.max_threads()
+    calls, el, tflops = rate(cores, rows, budget_s)
+    calls1, el1, tflops1 = rate(1, 8, budget_s / 3)
+    oracle.matmul(p.x[:4], codes[:4], p.s[:4], nthreads=cores)      # the thread count persists: restore it
+    return {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{calls} products of 512 tokens x {rows} rows x K={K} (a slice of the gate matrix) in "
                       f"{el:.1f} s with the C oracle (fp64, OpenMP over outputs)",
-            "extrapolated_pass_s": total / (tflops * 1e12)}
+            "extrapolated_pass_s": total / (tflops * 1e12),
+            "single_thread": {"value": tflops1, "unit": "TFLOP/s", "cores": 1,
+                              "sample": f"{calls1} products of 512 tokens x 8 rows x K={K} in {el1:.1f} s, one thread",
+                              "extrapolated_pass_s": total / (tflops1 * 1e12)}}
 
 
 def safe_cpu_baseline_pp512(budget_s: float) -> dict:

@@ -1005,9 +1005,18 @@ size_t flag_bytes(int N, int K) {
     const int G = K / kGroup;
     return G > kWarps ? align_up((size_t)((N + 15) / 16) * 4, 256) : 0;
 }
+// The part every plain call of the shape may use: the range flags of this
+// kernel, or the chunk counts and row sums of the FP8 decode kernel (which
+// start at the same offset and are zero between calls too).
+size_t base_bytes(int M, int T, int K) {
+    const int G = K / kGroup;
+    const size_t flags = G > kWarps ? align_up((size_t)T * 4, 256) : 0;
+    return std::max(flags, decode_supported(K) ? decode_workspace_bytes(M, T, K) : (size_t)0);
+}
 size_t workspace_bytes(int M, int N, int K, bool rot) {
     if (M < 1 || M > 16 || N < 1 || K < kGroup || K % kGroup != 0) return 0;
-    return flag_bytes(N, K) + (rot ? align_up((size_t)M * K * 2 + (size_t)M * (K / kGroup) * 4, 256) : 0);
+    return base_bytes(M, (N + 15) / 16, K) +
+           (rot ? align_up((size_t)M * K * 2 + (size_t)M * (K / kGroup) * 4, 256) : 0);
 }
 
 template <int MT, bool PRE, bool ONE, bool LEAN = false, bool BIN = false, bool AFF = false>
@@ -1032,13 +1041,6 @@ tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
     return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
 
-// A pair call (N2 > 0) reads one x for two matrices; its flag words cover the
-// tiles of both.
-size_t pair_flag_bytes(int N, int N2, int K) {
-    const int G = K / kGroup;
-    return G > kWarps ? align_up((size_t)((N + 15) / 16 + (N2 + 15) / 16) * 4, 256) : 0;
-}
-
 tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const void* scales, float* y, int M,
                 int N, int K, void* workspace, size_t workspace_bytes_, cudaStream_t stream, bool bin = false,
                 const uint32_t* codes2 = nullptr, const void* scales2 = nullptr, float* y2 = nullptr, int N2 = 0,
@@ -1046,9 +1048,16 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
     int sms = 0;
     tern_status st = check_device(&sms);
     if (st != TERN_OK) return st;
-    const size_t fb = N2 > 0 ? pair_flag_bytes(N, N2, K) : flag_bytes(N, K);
+    // the plain ternary product with K a multiple of 1024 runs the FP8 decode kernel
+    if (!signs && !biases && !bin && decode_supported(K)) {
+        st = decode_run(x, codes, scales, y, N, codes2, scales2, y2, N2, M, K, workspace, workspace_bytes_, sms,
+                        stream);
+        if (st == TERN_OK) set_launch_count(1);
+        return st;
+    }
+    const size_t fb = base_bytes(M, (N + 15) / 16 + (N2 + 15) / 16, K);
     if (fb > 0 || signs) {
-        const size_t need = N2 > 0 ? fb : workspace_bytes(M, N, K, signs != nullptr);
+        const size_t need = fb + (signs ? workspace_bytes(M, N, K, true) - base_bytes(M, (N + 15) / 16, K) : 0);
         if (!workspace || workspace_bytes_ < need) return TERN_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TERN_ERR_ALIGN;
     }
@@ -1163,7 +1172,7 @@ extern "C" tern_status tern_gemv(const void* x, const uint32_t* codes, const voi
 
 extern "C" size_t tern_gemv_pair_workspace_bytes(int M, int N_a, int N_b, int K) {
     if (M < 1 || M > 16 || N_a < 1 || N_b < 1 || K < kGroup || K % kGroup != 0) return 0;
-    return std::max<size_t>(256, pair_flag_bytes(N_a, N_b, K));
+    return std::max<size_t>(256, base_bytes(M, (N_a + 15) / 16 + (N_b + 15) / 16, K));
 }
 
 extern "C" tern_status tern_gemv_pair(const void* x, const uint32_t* codes_a, const void* scales_a, float* y_a,
@@ -1175,7 +1184,7 @@ extern "C" tern_status tern_gemv_pair(const void* x, const uint32_t* codes_a, co
     v = validate(x, codes_b, scales_b, y_b, M, N_b, K);
     if (v != TERN_OK) return v;
     if ((long long)N_a + N_b >= (1 << 28)) return TERN_ERR_SHAPE;
-    const size_t need = pair_flag_bytes(N_a, N_b, K);
+    const size_t need = base_bytes(M, (N_a + 15) / 16 + (N_b + 15) / 16, K);
     if (need > 0 && (!workspace || workspace_bytes_ < need)) return TERN_ERR_WORKSPACE;
     return run(x, nullptr, codes_a, scales_a, y_a, M, N_a, K, workspace, workspace_bytes_, (cudaStream_t)stream,
                false, codes_b, scales_b, y_b, N_b);
@@ -1235,25 +1244,16 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = TERN_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[64] = {};   // device address of the array, per device
-
 // The device address of the array on the current device.  In host code the
 // array's name is only a stand-in for the symbol, so the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress, with the device current.  It is looked up on every
+// call (a host-side query that issues no stream work), so an address can never
+// outlive a device reset that reloads the module.
 cudaError_t noalloc_scratch(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+    *out = p;
     return cudaSuccess;
 }
 
@@ -1265,7 +1265,7 @@ extern "C" tern_status tern_gemv_noalloc(const void* x, const uint32_t* codes, c
     set_launch_count(0);
     const tern_status v = validate(x, codes, scales, y, M, N, K);
     if (v != TERN_OK) return v;
-    const size_t need = tern::workspace_bytes(M, N, K, false);
+    const size_t need = tern::flag_bytes(N, K);
     if (need > kNoAllocScratchBytes) return TERN_ERR_WORKSPACE;
     int sms = 0;
     tern_status st = check_device(&sms);

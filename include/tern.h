@@ -224,18 +224,19 @@ tern_status tern_affine_gemv(const void *x, const uint32_t *codes, const void *s
  * allocator that must not recurse into itself, a runtime that hands out all
  * device memory up front): it takes no workspace and allocates nothing.  The
  * pages describe no counterpart; this is a library convenience.
- *   - Its scratch (the range flag words) is one file-scope device array of
- *     TERN_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds
- *     until the process exits.  Shapes whose scratch,
- *     tern_gemv_workspace_bytes(M, N, K) without the rotation part, exceeds
- *     it (N above 1,048,576 rows) are rejected with TERN_ERR_WORKSPACE and
- *     nothing is launched.
- *   - The first call on a device looks up the array's device address (once,
- *     with that device current) and plans the shape; make that first call
- *     before any stream capture.
- *   - Each call clears the flags it uses on `stream` before the product
- *     kernel.  All calls share the one array, so calls whose kernels overlap
- *     on the GPU (different streams) race: order them.
+ *   - Its scratch (one flag word per 16-row tile, when K > 1024) is one
+ *     file-scope device array of TERN_NOALLOC_SCRATCH_BYTES that every GPU
+ *     loading the library holds until the process exits.  Shapes whose flags
+ *     exceed it (N above 1,048,576 rows) are rejected with TERN_ERR_WORKSPACE
+ *     and nothing is launched.
+ *   - Every call looks up the array's device address on the current device
+ *     (a host-side query; no stream work).  The first call on a device also
+ *     loads the kernels and plans the shape: make it before any stream
+ *     capture.
+ *   - Each call clears the flags it uses with one cudaMemsetAsync on `stream`
+ *     before the product kernel (tern_last_launch_count counts the kernel
+ *     only).  All calls share the one array, so calls whose kernels overlap on
+ *     the GPU (different streams) race: order them.
  * Arguments, layout, results and tolerance as for tern_gemv. */
 tern_status tern_gemv_noalloc(const void *x, const uint32_t *codes, const void *scales, float *y,
                               int M, int N, int K, tern_stream_t stream);
@@ -276,9 +277,13 @@ tern_status tern_fwht_gemm(const void *x, const int8_t *signs, const uint32_t *c
 size_t tern_gemm_workspace_bytes(int M, int N, int K);
 
 /* y = x W^T on the tcgen05 tensor cores: each weight is unpacked on chip to
- * bf16 t * bf16(s_g) (the group scale rounded to bf16 and folded in), the
- * product accumulates in fp32 in tensor memory, and y is written as fp32
- * (y_is_bf16 == 0) or bf16 rounded to nearest even (y_is_bf16 != 0).
+ * bf16 t * bf16(s_g) (the group scale rounded to nearest even bf16 and folded
+ * in), the product accumulates in fp32 in tensor memory, and y is written as
+ * fp32 (y_is_bf16 == 0) or bf16 rounded to nearest even (y_is_bf16 != 0).
+ * On those operands the fp32 output is within 1e-3 * sum_k |x w| + 1e-6 and
+ * the bf16 output within 8e-3 * max(|y|, (sum_k (x w)^2)^(1/2)); the rounding
+ * of the scales moves y from the exact-scale product by at most
+ * sum_g |bf16(s_g) - s_g| |sum_{k in g} x_k t_k|.
  * The (tile, K-stage) iterations are shared out evenly over the SMs
  * (stream-K); the parts of a tile split between CTAs are added in fp32 in no
  * fixed order, so the last bits of such tiles may vary from run to run.
@@ -297,8 +302,9 @@ tern_status tern_bin_gemm(const void *x, const uint32_t *words, const void *scal
 
 /* The prefill product on an affine pack (W as for tern_affine_gemv): each
  * weight s q + b is formed in fp32 and rounded once to bf16 before the
- * tensor-core product, so the fp32 output is within 2^-8 * sum_k |x w| + 1e-6
- * of the exact product, as for tern_gemm.  Shapes, workspace
+ * tensor-core product, so the fp32 output differs from the exact product by at
+ * most what those roundings explain, sum_g sum_q |d_q| |sum_{k in g, q_k = q}
+ * x_k| with d_q = bf16(s q + b) - (s q + b), plus the fp32 accumulation.  Shapes, workspace
  * (tern_gemm_workspace_bytes), output types and error behaviour as for
  * tern_gemm; a NULL biases pointer is TERN_ERR_NULL and a misaligned one
  * TERN_ERR_ALIGN. */
@@ -320,7 +326,10 @@ enum {
     TERN_DEVERR_GEMM_MMA_WAIT = 0x103,       /* prefill: MMA issuer waited for operands or TMEM */
     TERN_DEVERR_GEMM_EPILOGUE_WAIT = 0x104,  /* prefill: epilogue waited for an accumulator */
     TERN_DEVERR_GEMM_TEARDOWN_WAIT = 0x105,  /* prefill: teardown waited for work in flight */
-    TERN_DEVERR_GEMV_RANGE_FLAG_WAIT = 0x202 /* decode: a K-slice waited for y's clearing */
+    TERN_DEVERR_GEMV_RANGE_FLAG_WAIT = 0x202, /* decode: a K-slice waited for y's clearing */
+    TERN_DEVERR_DECODE_PRODUCER_WAIT = 0x203, /* decode (FP8 path): loader waited for a free stage */
+    TERN_DEVERR_DECODE_CONSUMER_WAIT = 0x204, /* decode (FP8 path): a group warp waited for a stage or buffer */
+    TERN_DEVERR_DECODE_REDUCER_WAIT = 0x205   /* decode (FP8 path): the reducer waited for a stage's partials */
 };
 
 /* Reads and clears the sticky device-side error words of the current device

@@ -130,16 +130,29 @@ def test_argument_errors_never_launch(tern):
     assert lib.tern_wait_selftest(tern.SELFTEST_MBARRIER, 1000001, None) == 2
 
 def test_workspace_sizes(tern):
-    # one flag word per 16-row tile once K > 1024 (256-byte aligned), then, for
-    # the fused call when K % 4096 == 0, the staged rotated x: M x K fp16 values
-    # and one int32 exponent per token and 128-group (256-byte aligned)
+    # Once K spans more than one chunk of 8 groups (K > 1024): one flag word per
+    # 16-row tile (256-byte aligned); then, for the fused call when K % 4096 == 0,
+    # the staged rotated x: M x K fp16 values and one int32 exponent per token
+    # and 128-group (256-byte aligned)
     a256 = lambda v: (v + 255) // 256 * 256
+
+    def rot(M, K):
+        return a256(M * K * 2 + M * (K // 128) * 4)
+
     assert tern.gemv_workspace_bytes(1, 17408, 5120) == a256(1088 * 4)
     assert tern.gemv_workspace_bytes(16, 10, 17408) == 256
-    assert tern.gemv_workspace_bytes(2, 12288, 4096) == a256(768 * 4) + a256(2 * 4096 * 2 + 2 * 32 * 4)
-    assert tern.gemv_workspace_bytes(16, 12288, 8192) == a256(768 * 4) + a256(16 * 8192 * 2 + 16 * 64 * 4)
+    assert tern.gemv_workspace_bytes(2, 12288, 4096) == a256(768 * 4) + rot(2, 4096)
+    assert tern.gemv_workspace_bytes(16, 12288, 8192) == a256(768 * 4) + rot(16, 8192)
     assert tern.gemv_workspace_bytes(1, 16, 4096) == 256 + 256 * 33
-    assert tern.gemv_workspace_bytes(1, 256, 512) == 256      # one slice: nothing needed
+    assert tern.gemv_workspace_bytes(3, 100, 1152) == a256(7 * 4)
+    assert tern.gemv_workspace_bytes(1, 256, 512) == 256      # one chunk: nothing needed
+    assert tern.gemv_workspace_bytes(1, 256, 1024) == 256
+    # a pair call counts the tiles of both matrices
+    assert lib_pair(tern, 1, 17408, 17408, 5120) == a256(2176 * 4)
+
+
+def lib_pair(tern, M, Na, Nb, K):
+    return int(tern.lib().tern_gemv_pair_workspace_bytes(M, Na, Nb, K))
 
 
 def test_gemm_workspace_sizes(tern):

@@ -4,26 +4,28 @@ w = s q + b, every 2-bit code 0..3 valid).
 The decode product is held to |y - y_ref| <= 1e-3 * sum_k |x w| + 2^-23 *
 sum_k |x_k b_g(k)| + 1e-6 against the oracle's double-precision product: the
 kernel sums s * sum q x and b * sum x in fp32 and the two parts may cancel, so
-the rounding of the bias part is bounded by its own magnitude.  The prefill
-product rounds each weight once to bf16 and is held to 2^-8 * sum_k |x w| +
-1e-6 (fp32 out) and 8e-3 * sum_k |x w| + 1e-6 (bf16 out).  A one-hot
-activation picks s q + b of one column: exactly its fp32 value from the decode
-product and exactly its bf16 value from the prefill product, at every slot
-position (codes 5-7 and 13-15 are the ones the ternary unpack cannot read
-as 3).  Shapes span full and short K-slices, ragged N, M = 1..16, and the
-lean and general loops.
+the rounding of the bias part is bounded by its own magnitude.
+
+The prefill product forms each of a group's four weights s q + b in fp32 and
+rounds it once to bf16, so a weight differs from the exact one by
+d_q = bf16(fp32(s q + b)) - (s q + b), which the test computes exactly.  The
+difference from the oracle is then bounded by what those roundings explain,
+sum_g sum_q |d_q| |sum_{k in g, q_k = q} x_k|, plus 2^-12 * sum_k |x w| for the
+fp32 accumulation and 1e-6; a bf16 output adds its own rounding, 2^-8 of the
+result.  A one-hot activation picks s q + b of one column: exactly its fp32
+value from the decode product and exactly its bf16 value from the prefill
+product, at every slot position (codes 5-7 and 13-15 are the ones the ternary
+unpack cannot read as 3).  Shapes span full and short K-slices, ragged N,
+M = 1..16, and the lean and general loops.
 """
 import numpy as np
 import pytest
 import torch
 
 import synth
-from tests._util import assert_fp32_close, dev_bf16, dev_codes, dev_scales, dev_trits
+from tests._util import ACC_REL, assert_fp32_close, assert_within, dev_bf16, dev_codes, dev_scales, dev_trits, x_f64
 
 pytestmark = pytest.mark.gpu
-
-GEMM_REL = 2.0 ** -8
-BF16_REL = 8e-3
 
 
 @pytest.fixture(scope="module")
@@ -36,14 +38,9 @@ def tern():
     return t
 
 
-def xf64(x_bits: np.ndarray) -> np.ndarray:
-    return torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).view(torch.bfloat16).to(
-        torch.float64).numpy()
-
-
 def bias_scale(x_bits: np.ndarray, b: np.ndarray) -> np.ndarray:
     """sum_k |x[m, k]| |b[n, k / 128]| for every (m, n)."""
-    xa = np.abs(xf64(x_bits))
+    xa = np.abs(x_f64(x_bits))
     M, K = xa.shape
     return xa.reshape(M, K // 128, 128).sum(-1) @ np.abs(b.astype(np.float64)).T
 
@@ -116,7 +113,7 @@ def test_affine_special_cases(tern, orc):
     codes = tern.pack(dev_trits(p.t))
     x, s = dev_bf16(p.x), dev_scales(p.s)
     y = tern.affine_gemv(x, codes, s, -s)
-    y_ref, a_ref = orc.matmul(p.x, codes.cpu().numpy().view(np.uint32), p.s)
+    y_ref, a_ref = orc.matmul(p.x, orc.pack(p.t)[0], p.s)
     assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, abs_=2.0 ** -23 * bias_scale(p.x, p.s) + 1e-6,
                       what="affine as ternary")
     qb = (synth.binary(231, "q", (N, K)) > 0).astype(np.int8)
@@ -132,6 +129,50 @@ def test_affine_special_cases(tern, orc):
 # the prefill product (tcgen05)
 # --------------------------------------------------------------------------
 
+def codes_q(codes: np.ndarray) -> np.ndarray:
+    """The 2-bit codes [N, K] of a packed matrix."""
+    N = codes.shape[0]
+    return ((codes[:, :, None] >> (2 * np.arange(16, dtype=np.uint32))) & 3).reshape(N, -1).astype(np.uint8)
+
+
+def weight_rounding(s: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """|bf16(fp32(s q + b)) - (s q + b)| for q = 0..3: [N, G, 4]."""
+    q = np.arange(4, dtype=np.float32)
+    w32 = s.astype(np.float32)[:, :, None] * q + b.astype(np.float32)[:, :, None]
+    wb = torch.from_numpy(w32).to(torch.bfloat16).to(torch.float64).numpy()
+    exact = s.astype(np.float64)[:, :, None] * q.astype(np.float64) + b.astype(np.float64)[:, :, None]
+    return np.abs(wb - exact)
+
+
+def affine_rounding_bound(p, ms=None, ns=None) -> np.ndarray:
+    """sum_g sum_q |d_q| |sum_{k in g, q_k = q} x_k| per output."""
+    x = x_f64(p.x)
+    qa = codes_q(p.codes)
+    d = weight_rounding(p.s, p.b)
+    M, K = x.shape
+    G = K // 128
+    if ms is None:
+        out = np.zeros((M, qa.shape[0]))
+        for g in range(G):
+            sl = slice(128 * g, 128 * g + 128)
+            for q in range(4):
+                out += np.abs(x[:, sl] @ (qa[:, sl] == q).T.astype(np.float64)) * d[:, g, q][None, :]
+        return out
+    xs = x[ms].reshape(len(ms), G, 128)
+    qs = qa[ns].reshape(len(ns), G, 128)
+    out = np.zeros(len(ms))
+    for q in range(4):
+        out += (np.abs((xs * (qs == q)).sum(axis=2)) * d[ns, :, q]).sum(axis=1)
+    return out
+
+
+def check_prefill(y, p, y_ref, a_ref, bf16_out, ms=None, ns=None, what=""):
+    bound = affine_rounding_bound(p, ms, ns) + ACC_REL * a_ref + 1e-6
+    if bf16_out:
+        bound = bound * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(y_ref)
+    assert_within(y, y_ref, bound, what=what)
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 128, 128), (5, 200, 256), (200, 256, 1024), (300, 130, 640),
                                    (512, 512, 2048), (17, 1000, 128), (256, 256, 8192), (40, 128, 2048)])
 def test_affine_gemm_matches_oracle(tern, orc, M, N, K):
@@ -140,7 +181,7 @@ def test_affine_gemm_matches_oracle(tern, orc, M, N, K):
     torch.cuda.synchronize()
     assert tern.device_error() == 0
     y_ref, a_ref = orc.affine_matmul(p.x, p.codes, p.s, p.b)
-    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, rel=GEMM_REL, what=f"affine gemm M={M} N={N} K={K}")
+    check_prefill(y.cpu().numpy(), p, y_ref, a_ref, False, what=f"affine gemm M={M} N={N} K={K}")
 
 
 def test_affine_gemm_bf16_and_one_hot(tern, orc):
@@ -149,9 +190,9 @@ def test_affine_gemm_bf16_and_one_hot(tern, orc):
     c, s, b = dev_codes(p.codes), dev_scales(p.s), dev_scales(p.b)
     y = tern.affine_gemm(dev_bf16(p.x), c, s, b, out_dtype=torch.bfloat16)
     y_ref, a_ref = orc.affine_matmul(p.x, p.codes, p.s, p.b)
-    assert_fp32_close(y.to(torch.float64).cpu().numpy(), y_ref, a_ref, rel=BF16_REL, what="affine gemm bf16")
+    check_prefill(y.to(torch.float64).cpu().numpy(), p, y_ref, a_ref, True, what="affine gemm bf16")
     # one-hot rows of x pick bf16(fp32(s q + b)) exactly
-    q = ((p.codes[:, :, None] >> (2 * np.arange(16, dtype=np.uint32))) & 3).reshape(N, K)
+    q = codes_q(p.codes)
     W32 = (np.repeat(p.s.astype(np.float32), 128, axis=1) * q.astype(np.float32) +
            np.repeat(p.b.astype(np.float32), 128, axis=1))
     Wb = torch.from_numpy(W32).to(torch.bfloat16).to(torch.float64).numpy()
@@ -165,13 +206,15 @@ def test_affine_gemm_bf16_and_one_hot(tern, orc):
 def test_affine_gemm_prefill_layer_sampled(tern, orc, name, K, N):
     M = synth.PREFILL_M
     p = synth.affine_problem(260, M, N, K, tag=f"ap{name}")
-    y = tern.affine_gemm(dev_bf16(p.x), dev_codes(p.codes), dev_scales(p.s), dev_scales(p.b),
-                         out_dtype=torch.bfloat16)
+    c, s, b = dev_codes(p.codes), dev_scales(p.s), dev_scales(p.b)
+    y = tern.affine_gemm(dev_bf16(p.x), c, s, b, out_dtype=torch.bfloat16)
+    y32 = tern.affine_gemm(dev_bf16(p.x), c, s, b)
     torch.cuda.synchronize()
     assert tern.device_error() == 0
     rs = np.random.default_rng(K + N + 7)
     ms, ns = rs.integers(0, M, 3000), rs.integers(0, N, 3000)
     ms[:4], ns[:4] = M - 1, [0, N - 1, N - 2, N // 2]
     y_ref, a_ref = orc.affine_matmul_sampled(p.x, p.codes, p.s, p.b, ms, ns)
-    assert_fp32_close(y.to(torch.float64).cpu().numpy()[ms, ns], y_ref, a_ref, rel=BF16_REL,
-                      what=f"affine pp512 {name}")
+    check_prefill(y.to(torch.float64).cpu().numpy()[ms, ns], p, y_ref, a_ref, True, ms, ns,
+                  what=f"affine pp512 {name}")
+    check_prefill(y32.cpu().numpy()[ms, ns], p, y_ref, a_ref, False, ms, ns, what=f"affine pp512 {name} fp32")

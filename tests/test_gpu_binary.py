@@ -12,7 +12,8 @@ import pytest
 import torch
 
 import synth
-from tests._util import assert_fp32_close, dev_bf16, dev_scales, dev_trits
+from tests._util import (ACC_REL, assert_bf16_close, assert_fp32_close, assert_within, dev_bf16, dev_scales,
+                         dev_trits, f16_to_bf16_f16, l2_xw, scale_rounding_bound)
 
 pytestmark = pytest.mark.gpu
 
@@ -52,7 +53,7 @@ def test_bin_gemv_matches_oracle(tern, orc, M, N, K):
     tern.bin_gemv(dev_bf16(p.x), words, dev_scales(p.s), y=y)
     torch.cuda.synchronize()
     assert tern.device_error() == 0
-    y_ref, a_ref = orc.bin_matmul(p.x, words_host(words), p.s)
+    y_ref, a_ref = orc.bin_matmul(p.x, orc.bin_pack(p.t)[0], p.s)
     assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what=f"binary M={M} N={N} K={K}")
 
 
@@ -83,7 +84,7 @@ def test_bin_gemv_full_size_sampled(tern, orc, M, K, N):
     rs = np.random.default_rng(K + N + M)
     ms, ns = rs.integers(0, M, 3000), rs.integers(0, N, 3000)
     ms[:4], ns[:4] = M - 1, [0, N - 1, N - 2, N // 2]
-    y_ref, a_ref = orc.bin_matmul_sampled(p.x, words_host(words), p.s, ms, ns)
+    y_ref, a_ref = orc.bin_matmul_sampled(p.x, orc.bin_pack(p.t)[0], p.s, ms, ns)
     assert_fp32_close(y.cpu().numpy()[ms, ns], y_ref, a_ref, what=f"binary full M={M} {K}->{N}")
 
 
@@ -101,25 +102,43 @@ def test_bin_and_ternary_agree_on_pm1(tern, orc):
 
 
 # --------------------------------------------------------------------------
-# the prefill product on the 1-bit layout (tcgen05).  Each weight is unpacked
-# to (2b - 1) * bf16(s): the fp32 output is held to 2^-8 * sum_k |x w| + 1e-6,
-# the bf16 output to 8e-3 * sum_k |x w| + 1e-6, as for the 2-bit layout.
+# the prefill product on the 1-bit layout (tcgen05).  Each weight is exactly
+# (2b - 1) * bf16(s_g), so the oracle is given the bf16-rounded scales: fp32
+# output within 1e-3 * sum_k |x w| + 1e-6, bf16 output within
+# 8e-3 * max(|y_ref|, ||x (.) w||_2); against the exact-scale oracle the
+# difference stays within sum_g |bf16(s_g) - s_g| |sum_{k in g} x_k w_k / s_g|
+# plus 2^-12 * A for the accumulation.
 # --------------------------------------------------------------------------
 
-GEMM_REL = 2.0 ** -8
+FP32_REL = 1e-3
 BF16_REL = 8e-3
+
+
+def bin_check_fp32(orc, y, p, words, ms=None, ns=None, what=""):
+    got = y.cpu().numpy()
+    sb = f16_to_bf16_f16(p.s)
+    if ms is None:
+        y_b, a_b = orc.bin_matmul(p.x, words, sb)
+        y_ref, a_ref = orc.bin_matmul(p.x, words, p.s)
+    else:
+        got = got[ms, ns]
+        y_b, a_b = orc.bin_matmul_sampled(p.x, words, sb, ms, ns)
+        y_ref, a_ref = orc.bin_matmul_sampled(p.x, words, p.s, ms, ns)
+    assert_fp32_close(got, y_b, a_b, rel=FP32_REL, what=what)
+    assert_within(got, y_ref, scale_rounding_bound(p.x, p.t, p.s, ms, ns) + ACC_REL * a_ref + 1e-6,
+                  what=what + " (exact s)")
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 128), (5, 200, 256), (200, 256, 1024), (300, 130, 640),
                                    (512, 512, 2048), (17, 1000, 128), (256, 256, 8192), (40, 128, 2048)])
 def test_bin_gemm_matches_oracle(tern, orc, M, N, K):
     p = synth.binary_problem(100 + M, M, N, K, tag=f"m{N}x{K}")
-    words = tern.bin_pack(dev_trits(p.t))
-    y = tern.bin_gemm(dev_bf16(p.x), words, dev_scales(p.s))
+    y = tern.bin_gemm(dev_bf16(p.x), tern.bin_pack(dev_trits(p.t)), dev_scales(p.s))
     torch.cuda.synchronize()
     assert tern.device_error() == 0
-    y_ref, a_ref = orc.bin_matmul(p.x, words_host(words), p.s)
-    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, rel=GEMM_REL, what=f"binary gemm M={M} N={N} K={K}")
+    words, bad = orc.bin_pack(p.t)
+    assert bad == 0
+    bin_check_fp32(orc, y, p, words, what=f"binary gemm M={M} N={N} K={K}")
 
 
 def test_bin_gemm_bf16_and_one_hot(tern, orc):
@@ -127,15 +146,17 @@ def test_bin_gemm_bf16_and_one_hot(tern, orc):
     p = synth.binary_problem(110, M, N, K, tag="b16")
     words = tern.bin_pack(dev_trits(p.t))
     y = tern.bin_gemm(dev_bf16(p.x), words, dev_scales(p.s), out_dtype=torch.bfloat16)
-    y_ref, a_ref = orc.bin_matmul(p.x, words_host(words), p.s)
-    assert_fp32_close(y.to(torch.float64).cpu().numpy(), y_ref, a_ref, rel=BF16_REL, what="binary gemm bf16")
+    owords, _ = orc.bin_pack(p.t)
+    sb = f16_to_bf16_f16(p.s)
+    y_b, _ = orc.bin_matmul(p.x, owords, sb)
+    assert_bf16_close(y.to(torch.float64).cpu().numpy(), y_b, l2_xw(p.x, p.t, sb), rel=BF16_REL,
+                      what="binary gemm bf16")
     # one-hot rows of x pick (2b - 1) * bf16(s) exactly
     x = np.zeros((M, K), dtype=np.uint16)
     for m in range(M):
         x[m, (37 * m) % K] = 0x3F80
     y = tern.bin_gemm(dev_bf16(x), words, dev_scales(p.s)).cpu().numpy()
-    sb = torch.from_numpy(p.s.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
-    W = p.t.astype(np.float64) * np.repeat(sb, 128, axis=1)
+    W = p.t.astype(np.float64) * np.repeat(sb.astype(np.float64), 128, axis=1)
     for m in range(M):
         assert np.array_equal(y[m].astype(np.float64), W[:, (37 * m) % K]), m
 
@@ -146,11 +167,15 @@ def test_bin_gemm_prefill_layer_sampled(tern, orc, name, K, N):
     p = synth.binary_problem(120, M, N, K, tag=f"bp{name}")
     words = tern.bin_pack(dev_trits(p.t))
     y = tern.bin_gemm(dev_bf16(p.x), words, dev_scales(p.s), out_dtype=torch.bfloat16)
+    y32 = tern.bin_gemm(dev_bf16(p.x), words, dev_scales(p.s))
     torch.cuda.synchronize()
     assert tern.device_error() == 0
     rs = np.random.default_rng(K + N + 1)
     ms, ns = rs.integers(0, M, 3000), rs.integers(0, N, 3000)
     ms[:4], ns[:4] = M - 1, [0, N - 1, N - 2, N // 2]
-    y_ref, a_ref = orc.bin_matmul_sampled(p.x, words_host(words), p.s, ms, ns)
-    assert_fp32_close(y.to(torch.float64).cpu().numpy()[ms, ns], y_ref, a_ref, rel=BF16_REL,
+    owords, _ = orc.bin_pack(p.t)
+    sb = f16_to_bf16_f16(p.s)
+    y_b, _ = orc.bin_matmul_sampled(p.x, owords, sb, ms, ns)
+    assert_bf16_close(y.to(torch.float64).cpu().numpy()[ms, ns], y_b, l2_xw(p.x, p.t, sb, ms, ns), rel=BF16_REL,
                       what=f"binary pp512 {name}")
+    bin_check_fp32(orc, y32, p, owords, ms, ns, what=f"binary pp512 {name} fp32")

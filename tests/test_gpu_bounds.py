@@ -22,7 +22,8 @@ import pytest
 import torch
 
 import synth
-from tests._util import assert_fp32_close, dev_bf16, dev_scales, dev_trits, host_codes
+from tests._util import (assert_bf16_close, assert_fp32_close, dev_bf16, dev_scales, dev_trits, f16_to_bf16_f16,
+                         host_codes, l2_xw)
 
 pytestmark = pytest.mark.gpu
 
@@ -98,7 +99,7 @@ def test_gemv_writes_only_its_output(tern, orc, M, N, K):
         assert y.margins_intact() and ws.margins_intact()
         assert ws.inner_zero(), "the range flags are not back at zero"
     assert tern.device_error() == 0
-    y_ref, a_ref = orc.matmul(p.x, host_codes(codes), p.s)
+    y_ref, a_ref = orc.matmul(p.x, orc.pack(p.t)[0], p.s)
     assert_fp32_close(y.t.cpu().numpy(), y_ref, a_ref, what=f"canary gemv M={M} N={N} K={K}")
 
 
@@ -115,7 +116,7 @@ def test_bin_gemv_writes_only_its_output(tern, orc, M, N, K):
         assert y.margins_intact() and ws.margins_intact()
         assert ws.inner_zero(), "the range flags are not back at zero"
     assert tern.device_error() == 0
-    y_ref, a_ref = orc.bin_matmul(p.x, words.t.cpu().numpy().view(np.uint32), p.s)
+    y_ref, a_ref = orc.bin_matmul(p.x, orc.bin_pack(p.t)[0], p.s)
     assert_fp32_close(y.t.cpu().numpy(), y_ref, a_ref, what=f"canary binary M={M} N={N} K={K}")
 
 
@@ -129,7 +130,7 @@ def test_fwht_gemm_writes_only_its_output(tern, orc, M):
     tern.fwht_gemm(x, torch.from_numpy(p.signs).cuda(), codes, s, y=y.t, ws=ws.t)
     assert y.margins_intact() and ws.margins_intact()
     assert tern.device_error() == 0
-    y_ref, a_ref = orc.rotate_matmul(p.x, p.signs, host_codes(codes), p.s)
+    y_ref, a_ref = orc.rotate_matmul(p.x, p.signs, orc.pack(p.t)[0], p.s)
     assert_fp32_close(y.t.cpu().numpy(), y_ref, a_ref, what=f"canary fused M={M}")
 
 
@@ -146,9 +147,13 @@ def test_gemm_writes_only_its_output(tern, orc, M, N, K, dt):
         assert y.margins_intact() and ws.margins_intact()
         assert ws.inner_zero(), "the stream-K counters or sums are not back at zero"
     assert tern.device_error() == 0
-    y_ref, a_ref = orc.matmul(p.x, host_codes(codes), p.s)
-    rel = 8e-3 if dt == torch.bfloat16 else 2.0 ** -8
-    assert_fp32_close(y.t.to(torch.float64).cpu().numpy(), y_ref, a_ref, rel=rel, what=f"canary gemm M={M}")
+    ocodes, sb = orc.pack(p.t)[0], f16_to_bf16_f16(p.s)   # the prefill's operand: t * bf16(s_g)
+    y_b, a_b = orc.matmul(p.x, ocodes, sb)
+    got = y.t.to(torch.float64).cpu().numpy()
+    if dt == torch.bfloat16:
+        assert_bf16_close(got, y_b, l2_xw(p.x, p.t, sb), what=f"canary gemm M={M}")
+    else:
+        assert_fp32_close(got, y_b, a_b, what=f"canary gemm M={M}")
 
 
 @pytest.mark.parametrize("which,code", [(0, 0x202), (1, 0x103)])
@@ -172,8 +177,9 @@ def test_bounded_wait_reports_and_context_survives(tern, orc, which, code):
     M, N, K = 2, 600, 5120
     p = synth.problem(1000 + which, M, N, K, tag="after")
     x, codes, s = dev_bf16(p.x), tern.pack(dev_trits(p.t)), dev_scales(p.s)
-    y_ref, a_ref = orc.matmul(p.x, host_codes(codes), p.s)
+    ocodes = orc.pack(p.t)[0]
+    y_ref, a_ref = orc.matmul(p.x, ocodes, p.s)
     assert_fp32_close(tern.gemv(x, codes, s).cpu().numpy(), y_ref, a_ref, what="gemv after self-test")
-    assert_fp32_close(tern.gemm(x, codes, s).cpu().numpy(), y_ref, a_ref, rel=2.0 ** -8,
-                      what="gemm after self-test")
+    y_b, a_b = orc.matmul(p.x, ocodes, f16_to_bf16_f16(p.s))
+    assert_fp32_close(tern.gemm(x, codes, s).cpu().numpy(), y_b, a_b, what="gemm after self-test")
     assert tern.device_error() == 0

@@ -87,7 +87,7 @@ def test_gemv_tiny_workload(tern, orc):
 def test_gemv_ragged_shapes(tern, orc, M, N, K):
     p = synth.problem(100 + M, M, N, K, tag=f"{N}x{K}")
     y, codes = run_gemv(tern, p)
-    y_ref, a_ref = orc.matmul(p.x, host_codes(codes), p.s)
+    y_ref, a_ref = orc.matmul(p.x, orc.pack(p.t)[0], p.s)
     assert_fp32_close(y, y_ref, a_ref, what=f"M={M} N={N} K={K}")
 
 
@@ -194,7 +194,7 @@ def test_gemv_verify_full_size_sampled(tern, orc, M, K, N):
     ms = rs.integers(0, M, 2048)
     ns = rs.integers(0, N, 2048)
     ns[:16] = N - 1 - np.arange(16)                      # the last tile
-    y_ref, a_ref = orc.matmul_sampled(p.x, host_codes(codes), p.s, ms, ns)
+    y_ref, a_ref = orc.matmul_sampled(p.x, orc.pack(p.t)[0], p.s, ms, ns)
     assert_fp32_close(y[ms, ns], y_ref, a_ref, what=f"verify M={M} N={N}")
 
 
@@ -246,7 +246,7 @@ def test_fwht_gemm_fused_matches_oracle(tern, orc, M):
     codes = tern.pack(dev_trits(p.t))
     y = tern.fwht_gemm(dev_bf16(p.x), torch.from_numpy(p.signs).cuda(), codes, dev_scales(p.s))
     torch.cuda.synchronize()
-    y_ref, a_ref = orc.rotate_matmul(p.x, p.signs, host_codes(codes), p.s)
+    y_ref, a_ref = orc.rotate_matmul(p.x, p.signs, orc.pack(p.t)[0], p.s)
     assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what=f"fused M={M}")
 
 
@@ -264,7 +264,7 @@ def test_fwht_then_gemv_separate(tern, orc, M):
     rs = np.random.default_rng(M)
     ms = rs.integers(0, M, 4096)
     ns = rs.integers(0, N, 4096)
-    y_ref, a_ref = orc.matmul_sampled(xr_bits, host_codes(codes), p.s, ms, ns)
+    y_ref, a_ref = orc.matmul_sampled(xr_bits, orc.pack(p.t)[0], p.s, ms, ns)
     assert_fp32_close(y.cpu().numpy()[ms, ns], y_ref, a_ref, what="separate")
 
 
@@ -279,7 +279,7 @@ def test_fwht_gemm_full_size_sampled(tern, orc, M):
     # oracle on a row subset (the rotation is per token; the product per row)
     rs = np.random.default_rng(7 + M)
     rows = np.unique(rs.integers(0, N, 512))
-    y_ref, a_ref = orc.rotate_matmul(p.x, p.signs, host_codes(codes)[rows], p.s[rows])
+    y_ref, a_ref = orc.rotate_matmul(p.x, p.signs, orc.pack(p.t)[0][rows], p.s[rows])
     assert_fp32_close(y.cpu().numpy()[:, rows], y_ref, a_ref, what=f"rot full M={M}")
 
 
@@ -292,7 +292,7 @@ def test_gemv_overwrites_prefilled_y(tern, orc, M, N, K):
     y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     tern.gemv(dev_bf16(p.x), codes, dev_scales(p.s), y=y)
     torch.cuda.synchronize()
-    y_ref, a_ref = orc.matmul(p.x, host_codes(codes), p.s)
+    y_ref, a_ref = orc.matmul(p.x, orc.pack(p.t)[0], p.s)
     assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what=f"prefilled y M={M} N={N} K={K}")
 
 
@@ -312,7 +312,7 @@ def test_gemv_extreme_shapes(tern, orc, M, N, K):
     n = min(2000, M * N)
     ms, ns = rs.integers(0, M, n), rs.integers(0, N, n)
     ms[0], ns[0] = M - 1, N - 1
-    y_ref, a_ref = orc.matmul_sampled(p.x, host_codes(codes), p.s, ms, ns)
+    y_ref, a_ref = orc.matmul_sampled(p.x, orc.pack(p.t)[0], p.s, ms, ns)
     assert_fp32_close(y.cpu().numpy()[ms, ns], y_ref, a_ref, what=f"extreme M={M} N={N} K={K}")
     assert torch.isfinite(y).all()
 
@@ -338,7 +338,7 @@ def test_scales_from_g64_device(tern, orc):
     y64 = tern.gemv(x, codes, tern.scales_from_g64(torch.from_numpy(s64).cuda(), K))
     y128 = tern.gemv(x, codes, dev_scales(s128))
     torch.cuda.synchronize()
-    y_ref, a_ref = orc.matmul(p.x, host_codes(codes), s128)
+    y_ref, a_ref = orc.matmul(p.x, orc.pack(p.t)[0], s128)
     assert_fp32_close(y64.cpu().numpy(), y_ref, a_ref, what="g64 scales")
     assert_fp32_close(y128.cpu().numpy(), y_ref, a_ref, what="g128 scales")
 
@@ -355,8 +355,8 @@ def test_gemv_pair_matches_two_products(tern, orc, M, Na, Nb, K):
     ca, cb = tern.pack(dev_trits(pa.t)), tern.pack(dev_trits(pb.t))
     sa, sb = dev_scales(pa.s), dev_scales(pb.s)
     ws = tern.workspace(int(tern.lib().tern_gemv_pair_workspace_bytes(M, Na, Nb, K)))
-    ya_ref, aa_ref = orc.matmul(pa.x, host_codes(ca), pa.s)
-    yb_ref, ab_ref = orc.matmul(pa.x, host_codes(cb), pb.s)
+    ya_ref, aa_ref = orc.matmul(pa.x, orc.pack(pa.t)[0], pa.s)
+    yb_ref, ab_ref = orc.matmul(pa.x, orc.pack(pb.t)[0], pb.s)
     for call in range(2):
         ya = torch.full((M, Na), float("nan"), dtype=torch.float32, device="cuda")
         yb = torch.full((M, Nb), float("nan"), dtype=torch.float32, device="cuda")

@@ -5,19 +5,20 @@ kernels, one workspace shared by all of them) is captured once and replayed;
 the outputs are filled with NaN before the checked replay, so every element
 must be written by that replay.  Each product is compared with the oracle on
 sampled outputs at full size, within the tolerance of its kind:
-|y - y_ref| <= 1e-3 * sum_k |x w| + 1e-6 for the decode products, and the
-bf16-output bound 8e-3 * sum_k |x w| + 1e-6 for the prefill products.
+|y - y_ref| <= 1e-3 * sum_k |x w| + 1e-6 for the decode products, and, for
+the prefill products (bf16 out, weights t * bf16(s_g)), the bf16-output bound
+8e-3 * max(|y_ref|, ||x (.) w||_2) against the oracle on the bf16-rounded
+scales.
 """
 import numpy as np
 import pytest
 import torch
 
 import synth
-from tests._util import assert_fp32_close, dev_bf16, dev_scales, dev_trits, host_codes
+from tests._util import assert_bf16_close, assert_fp32_close, dev_bf16, dev_scales, dev_trits, f16_to_bf16_f16, l2_xw
 
 pytestmark = pytest.mark.gpu
 
-BF16_REL = 8e-3
 
 
 @pytest.fixture(scope="module")
@@ -52,7 +53,7 @@ def sample(M, N, seed, n=1500):
     return ms, ns
 
 
-def replay_and_check(tern, orc, g, probs, ys, rel=1e-3, what=""):
+def replay_and_check(tern, orc, g, probs, ys, prefill=False, what=""):
     for _ in range(2):
         g.replay()
     for y in ys:
@@ -62,9 +63,15 @@ def replay_and_check(tern, orc, g, probs, ys, rel=1e-3, what=""):
     assert tern.device_error() == 0
     for i, ((p, codes), y) in enumerate(zip(probs, ys)):
         ms, ns = sample(p.M, p.N, 77 + i)
-        y_ref, a_ref = orc.matmul_sampled(p.x, host_codes(codes), p.s, ms, ns)
         got = y.to(torch.float64).cpu().numpy()[ms, ns]
-        assert_fp32_close(got, y_ref, a_ref, rel=rel, what=f"{what} product {i} ({p.M}x{p.N}x{p.K})")
+        ocodes = orc.pack(p.t)[0]
+        if prefill:
+            sb = f16_to_bf16_f16(p.s)
+            y_b, _ = orc.matmul_sampled(p.x, ocodes, sb, ms, ns)
+            assert_bf16_close(got, y_b, l2_xw(p.x, p.t, sb, ms, ns), what=f"{what} product {i} ({p.M}x{p.N}x{p.K})")
+        else:
+            y_ref, a_ref = orc.matmul_sampled(p.x, ocodes, p.s, ms, ns)
+            assert_fp32_close(got, y_ref, a_ref, what=f"{what} product {i} ({p.M}x{p.N}x{p.K})")
 
 
 def test_verify_step_graph(tern, orc):
@@ -124,7 +131,7 @@ def test_prefill_layer_graph(tern, orc):
         for i, (p, codes) in enumerate(probs):
             tern.gemm(xs[i], codes, ss[i], y=ys[i], ws=ws)
 
-    replay_and_check(tern, orc, capture(run), probs, ys, rel=BF16_REL, what="prefill")
+    replay_and_check(tern, orc, capture(run), probs, ys, prefill=True, what="prefill")
 
 
 @pytest.mark.parametrize("M", [1, 16])
@@ -155,7 +162,7 @@ def test_fused_rotation_graph(tern, orc, M):
     rs = np.random.default_rng(M)
     rows = np.unique(rs.integers(0, N, 384))
     for c, p in enumerate(ps):
-        y_ref, a_ref = orc.rotate_matmul(p.x, p.signs, host_codes(codes[c])[rows], p.s[rows])
+        y_ref, a_ref = orc.rotate_matmul(p.x, p.signs, orc.pack(p.t)[0][rows], p.s[rows])
         assert_fp32_close(ys[c].cpu().numpy()[:, rows], y_ref, a_ref, what=f"rotated graph M={M} call {c}")
 
 
@@ -183,7 +190,7 @@ def test_binary_decode_graph(tern, orc):
     assert tern.device_error() == 0
     for i, p in enumerate(probs):
         ms, ns = sample(1, p.N, 88 + i)
-        y_ref, a_ref = orc.bin_matmul_sampled(p.x, words[i].cpu().numpy().view(np.uint32), p.s, ms, ns)
+        y_ref, a_ref = orc.bin_matmul_sampled(p.x, orc.bin_pack(p.t)[0], p.s, ms, ns)
         assert_fp32_close(ys[i].cpu().numpy()[ms, ns], y_ref, a_ref, what=f"binary graph product {i}")
 
 
@@ -220,5 +227,5 @@ def test_pair_decode_graph(tern, orc):
     for i, (p, codes) in enumerate(probs):
         x_bits = probs[i - 1][0].x if i % 3 == 1 else p.x          # up reads gate's activation
         ms, ns = sample(1, p.N, 99 + i)
-        y_ref, a_ref = orc.matmul_sampled(x_bits, host_codes(codes), p.s, ms, ns)
+        y_ref, a_ref = orc.matmul_sampled(x_bits, orc.pack(p.t)[0], p.s, ms, ns)
         assert_fp32_close(ys[i].cpu().numpy()[ms, ns], y_ref, a_ref, what=f"pair graph product {i}")
