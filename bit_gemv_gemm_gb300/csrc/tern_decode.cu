@@ -834,7 +834,7 @@ size_t decode_workspace_bytes(int M, int T, int K) {
     return dec_align((size_t)T * 4, 256);
 }
 
-bool decode_supported(int K) { return K % 1024 == 0; }
+bool decode_supported(int K) { (void)K; return false; }   // the f16 mma.sync kernel is faster on sm_103a
 
 // y1 = x W1^T (and y2 = x W2^T for a pair call, N2 > 0) with the FP8 decode
 // kernel.  Shapes and pointers are validated by the caller; K % 1024 == 0.
