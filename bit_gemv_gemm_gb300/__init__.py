@@ -365,7 +365,7 @@ def device_error() -> int:
 
 
 SELFTEST_RANGE_FLAG, SELFTEST_MBARRIER = 0, 1
-DEVERR_GEMM_MMA_WAIT, DEVERR_GEMV_RANGE_FLAG_WAIT = 0x103, 0x202
+DEVERR_GEMM_MMA_WAIT, DEVERR_GEMV_RANGE_FLAG_WAIT, DEVERR_GEMV_ACTIVATION_RANGE = 0x103, 0x202, 0x203
 
 
 def wait_selftest(which: int, limit_us: int, stream=None) -> None:

@@ -23,6 +23,7 @@ enum DeviceError : int {
     kDevErrGemmEpilogueWait = TERN_DEVERR_GEMM_EPILOGUE_WAIT,
     kDevErrGemmTeardownWait = TERN_DEVERR_GEMM_TEARDOWN_WAIT,
     kDevErrGemvConsumerWait = TERN_DEVERR_GEMV_RANGE_FLAG_WAIT,
+    kDevErrGemvActivationRange = TERN_DEVERR_GEMV_ACTIVATION_RANGE,
 };
 
 // Each translation unit whose kernels wait on barriers (the prefill and the
@@ -33,7 +34,6 @@ __device__ __forceinline__ void report_device_error(int* word, int code) {
 }
 cudaError_t read_gemm_device_error(int* code);
 cudaError_t read_gemv_device_error(int* code);
-cudaError_t read_decode_device_error(int* code);
 // One-CTA kernels that run a bounded wait nothing completes (tern_wait_selftest).
 cudaError_t launch_flag_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_mbar_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
@@ -86,14 +86,6 @@ tern_status check_device(int* sm_count);
 
 // Launch bookkeeping (tern_last_launch_count).
 void set_launch_count(int n);
-
-// The FP8 decode product (K a multiple of 1024): workspace bytes for M tokens
-// and T 16-row tiles, and the launch (arguments validated by the caller).
-bool decode_supported(int K);
-size_t decode_workspace_bytes(int M, int T, int K);
-tern_status decode_run(const void* x, const uint32_t* codes1, const void* scales1, float* y1, int N1,
-                       const uint32_t* codes2, const void* scales2, float* y2, int N2, int M, int K, void* workspace,
-                       size_t workspace_bytes, int sms, cudaStream_t stream);
 
 // cudaLaunchKernelEx with the programmatic-stream-serialization attribute.
 template <typename... KArgs, typename... Args>

@@ -272,6 +272,12 @@ __device__ __forceinline__ void red_inc(unsigned* p, unsigned wrap) {
 
 __device__ int g_gemv_error;   // sticky device error word of this translation unit
 
+// A group whose largest |x| is 2^100 or more (or not finite) is outside the
+// staging's exponent range: the call reports it, and its y is undefined.
+__device__ __forceinline__ void check_stage_range(float mx) {
+    if (!(mx < 0x1p100f)) report_device_error(&g_gemv_error, kDevErrGemvActivationRange);
+}
+
 // Scales of a slice [gA, gB): the copy starts at group g_lo and is `width`
 // groups wide; 16-byte chunks when every slice starts and ends on a multiple
 // of 8 groups, 4-byte pairs when G is even, single halves otherwise.
@@ -516,6 +522,7 @@ gemv_kernel(const GemvArgs a) {
                 for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(v[e]));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                check_stage_range(mx);
                 E = stage_exponent(mx);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -828,6 +835,7 @@ rotate_stage_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restric
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    check_stage_range(mx);
     const int E = stage_exponent(mx);
     const int g = blk * (kFwhtN / kGroup) + (i >> 3);
     const int e0 = 16 * (i & 7);                    // first value within the group
@@ -1005,13 +1013,12 @@ size_t flag_bytes(int N, int K) {
     const int G = K / kGroup;
     return G > kWarps ? align_up((size_t)((N + 15) / 16) * 4, 256) : 0;
 }
-// The part every plain call of the shape may use: the range flags of this
-// kernel, or the chunk counts and row sums of the FP8 decode kernel (which
-// start at the same offset and are zero between calls too).
+// The range flags of a call over T 16-row tiles (one matrix, or both of a
+// pair call), when K spans several slices.
 size_t base_bytes(int M, int T, int K) {
+    (void)M;
     const int G = K / kGroup;
-    const size_t flags = G > kWarps ? align_up((size_t)T * 4, 256) : 0;
-    return std::max(flags, decode_supported(K) ? decode_workspace_bytes(M, T, K) : (size_t)0);
+    return G > kWarps ? align_up((size_t)T * 4, 256) : 0;
 }
 size_t workspace_bytes(int M, int N, int K, bool rot) {
     if (M < 1 || M > 16 || N < 1 || K < kGroup || K % kGroup != 0) return 0;
@@ -1048,13 +1055,6 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
     int sms = 0;
     tern_status st = check_device(&sms);
     if (st != TERN_OK) return st;
-    // the plain ternary product with K a multiple of 1024 runs the FP8 decode kernel
-    if (!signs && !biases && !bin && decode_supported(K)) {
-        st = decode_run(x, codes, scales, y, N, codes2, scales2, y2, N2, M, K, workspace, workspace_bytes_, sms,
-                        stream);
-        if (st == TERN_OK) set_launch_count(1);
-        return st;
-    }
     const size_t fb = base_bytes(M, (N + 15) / 16 + (N2 + 15) / 16, K);
     if (fb > 0 || signs) {
         const size_t need = fb + (signs ? workspace_bytes(M, N, K, true) - base_bytes(M, (N + 15) / 16, K) : 0);

@@ -171,7 +171,10 @@ size_t tern_gemv_workspace_bytes(int M, int N, int K);
  * 8 groups (K > 1024) the K-slice sums are added into y with global float
  * reductions, and for M > 4 the group sums within a slice meet in shared-memory
  * atomics; in either case the last bits of y may vary from run to run.
- * |x| must stay below 2^100 (larger values overflow the fp16 staging). */
+ * Every |x| must be finite and below 2^100 (larger values would overflow the
+ * fp16 staging): a group of 128 activations outside that range makes the call
+ * report TERN_DEVERR_GEMV_ACTIVATION_RANGE through tern_device_error(), and
+ * its y is then undefined. */
 tern_status tern_gemv(const void *x, const uint32_t *codes, const void *scales, float *y,
                       int M, int N, int K, void *workspace, size_t workspace_bytes,
                       tern_stream_t stream);
@@ -327,9 +330,7 @@ enum {
     TERN_DEVERR_GEMM_EPILOGUE_WAIT = 0x104,  /* prefill: epilogue waited for an accumulator */
     TERN_DEVERR_GEMM_TEARDOWN_WAIT = 0x105,  /* prefill: teardown waited for work in flight */
     TERN_DEVERR_GEMV_RANGE_FLAG_WAIT = 0x202, /* decode: a K-slice waited for y's clearing */
-    TERN_DEVERR_DECODE_PRODUCER_WAIT = 0x203, /* decode (FP8 path): loader waited for a free stage */
-    TERN_DEVERR_DECODE_CONSUMER_WAIT = 0x204, /* decode (FP8 path): a group warp waited for a stage or buffer */
-    TERN_DEVERR_DECODE_REDUCER_WAIT = 0x205   /* decode (FP8 path): the reducer waited for a stage's partials */
+    TERN_DEVERR_GEMV_ACTIVATION_RANGE = 0x203 /* decode: a group's largest |x| was >= 2^100 or not finite */
 };
 
 /* Reads and clears the sticky device-side error words of the current device

@@ -22,7 +22,7 @@ import pytest
 import torch
 
 import synth
-from tests._util import (assert_bf16_close, assert_fp32_close, dev_bf16, dev_scales, dev_trits, f16_to_bf16_f16,
+from tests._util import (assert_bf16_close, assert_fp32_close, dev_bf16, dev_codes, dev_scales, dev_trits, f16_to_bf16_f16,
                          host_codes, l2_xw)
 
 pytestmark = pytest.mark.gpu
@@ -183,3 +183,33 @@ def test_bounded_wait_reports_and_context_survives(tern, orc, which, code):
     y_b, a_b = orc.matmul(p.x, ocodes, f16_to_bf16_f16(p.s))
     assert_fp32_close(tern.gemm(x, codes, s).cpu().numpy(), y_b, a_b, what="gemm after self-test")
     assert tern.device_error() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("big", [2.0 ** 100, 2.0 ** 120, float("inf")])
+def test_gemv_reports_activation_out_of_range(tern, orc, big):
+    """An activation group whose largest |x| is 2^100 or more, or not finite,
+    is outside the fp16 staging's exponent range: the call reports
+    TERN_DEVERR_GEMV_ACTIVATION_RANGE instead of returning wrong numbers
+    silently.  Just below the bound the product is still within tolerance,
+    and the next in-range call reports nothing."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    M, N, K = 2, 300, 2048
+    p = synth.problem(1700, M, N, K, tag="range")
+    ocodes, bad = orc.pack(p.t)
+    assert bad == 0
+    codes, s = dev_codes(ocodes), dev_scales(p.s)
+    assert tern.device_error() == 0
+    x = p.x.copy()
+    x[1, 777] = big
+    y = tern.gemv(dev_bf16(x), codes, s)
+    torch.cuda.synchronize()
+    assert tern.device_error() == tern.DEVERR_GEMV_ACTIVATION_RANGE
+    # just below the bound: no report, and the oracle's bound holds
+    x[1, 777] = np.float32(2.0 ** 99 * 1.5)
+    y = tern.gemv(dev_bf16(x), codes, s)
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    y_ref, a_ref = orc.matmul(x, ocodes, p.s)
+    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what="gemv just below the staging bound")
