@@ -167,8 +167,12 @@ size_t tern_gemv_workspace_bytes(int M, int N, int K);
  * For K <= 1024 the workspace may be NULL.  No pre-zeroing of y is needed (the
  * kernel clears what it adds into).
  * Results agree with the exact product to within 1e-3 * sum_k |x w| + 1e-6 per
- * element, and a row of zero weights gives exactly 0.  When K spans more than
- * 8 groups (K > 1024) the K-slice sums are added into y with global float
+ * element, plus 2^-22 * sum_g |s_g| * max_{k in g} |x_k|: the activation is
+ * staged in fp16 with one exponent per token and group, so values far below
+ * their group's largest lose bits (the term matters only when a group's
+ * largest |x| meets a zero weight and the rest of the group is some 2^12 or
+ * more below it).  A row of zero weights gives exactly 0.  When K spans more
+ * than 8 groups (K > 1024) the K-slice sums are added into y with global float
  * reductions, and for M > 4 the group sums within a slice meet in shared-memory
  * atomics; in either case the last bits of y may vary from run to run.
  * Every |x| must be finite and below 2^100 (larger values would overflow the

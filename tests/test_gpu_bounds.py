@@ -23,7 +23,7 @@ import torch
 
 import synth
 from tests._util import (assert_bf16_close, assert_fp32_close, dev_bf16, dev_codes, dev_scales, dev_trits, f16_to_bf16_f16,
-                         host_codes, l2_xw)
+                         host_codes, l2_xw, x_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -201,15 +201,36 @@ def test_gemv_reports_activation_out_of_range(tern, orc, big):
     assert bad == 0
     codes, s = dev_codes(ocodes), dev_scales(p.s)
     assert tern.device_error() == 0
-    x = p.x.copy()
-    x[1, 777] = big
+    def bf16_bits(v):   # the bf16 bit pattern of a value bf16 holds exactly
+        return np.uint16(np.array([v], dtype=np.float32).view(np.uint32)[0] >> 16)
+
+    x = p.x.copy()   # bf16 bit patterns
+    x[1, 777] = bf16_bits(big)
     y = tern.gemv(dev_bf16(x), codes, s)
     torch.cuda.synchronize()
     assert tern.device_error() == tern.DEVERR_GEMV_ACTIVATION_RANGE
-    # just below the bound: no report, and the oracle's bound holds
-    x[1, 777] = np.float32(2.0 ** 99 * 1.5)
+    # just below the bound: no report.  The other activations of that group
+    # are 2^99 below its largest and drop out of the fp16 staging, which the
+    # group term of the stated bound covers: |y - y_ref| <= 1e-3 sum_k |x w|
+    # + 2^-22 sum_g |s_g| max_{k in g} |x_k| + 1e-6
+    x[1, 777] = bf16_bits(2.0 ** 99 * 1.5)
     y = tern.gemv(dev_bf16(x), codes, s)
     torch.cuda.synchronize()
     assert tern.device_error() == 0
     y_ref, a_ref = orc.matmul(x, ocodes, p.s)
-    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what="gemv just below the staging bound")
+    xs = np.abs(x_f64(x)).reshape(M, K // 128, 128).max(axis=2)          # [M][G]
+    group_term = xs @ np.abs(p.s.astype(np.float64)).T                    # [M][N]
+    err = np.abs(y.cpu().numpy().astype(np.float64) - y_ref)
+    assert (err <= 1e-3 * a_ref + 2.0 ** -22 * group_term + 1e-6).all()
+    # the rows whose weight at the large activation is not zero meet the plain bound
+    rows = np.nonzero(p.t[:, 777] != 0)[0]
+    assert rows.size > 0
+    assert_fp32_close(y.cpu().numpy()[1, rows], y_ref[1, rows], a_ref[1, rows], what="gemv just below the bound")
+    # and with the whole group that large, every row does
+    x[1, 768:896] = bf16_bits(2.0 ** 98)
+    x[1, 777] = bf16_bits(2.0 ** 99 * 1.5)
+    y = tern.gemv(dev_bf16(x), codes, s)
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    y_ref, a_ref = orc.matmul(x, ocodes, p.s)
+    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what="gemv with a whole group near the bound")
