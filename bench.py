@@ -626,14 +626,20 @@ def bench_prefill(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int, peaks:
         ms = time_graph(g, max(2, steps // 20), max(1, warmup // 2))
     flops = layers * sum(2.0 * M * N * K for (_, K, N) in synth.PREFILL_LAYER)
     tf = flops / (ms * 1e-3) / 1e12
-    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    # a pass of ~16 ms timed over a few replays is a burst, not a seconds-long
+    # loop under the power cap: the burst peak is the denominator (the
+    # sustained one is kept beside it)
+    peak = peaks["bf16_tflops"]
+    peak_sus = peaks.get("bf16_tflops_sustained", peak)
+    for v in per_gemm.values():
+        v["frac"] = v["TFLOPs"] / peak
     dom = max(per_gemm.items(), key=lambda kv: kv[1]["us"])
     return {
         "M": M, "layers": layers, "ms_per_pass": ms, "TFLOPs": tf, "tokens_per_s": M / (ms * 1e-3),
         "per_gemm": per_gemm, "clocks": clk.summary(),
         "roofline": {"bound": "tensor", "kernel": "tern_gemm (tcgen05)", "achieved": tf, "peak": peak,
-                     "unit": "TFLOP/s", "frac": tf / peak,
-                     "peak_source": f"{peaks['_source']} bf16_tflops_sustained (pass of {ms:.1f} ms)",
+                     "unit": "TFLOP/s", "frac": tf / peak, "frac_of_sustained": tf / peak_sus,
+                     "peak_source": f"{peaks['_source']} bf16_tflops (burst; pass of {ms:.1f} ms)",
                      "traffic": load_traffic("gemm_kernel", GEMM_SRC), **traffic_note("gemm_kernel", GEMM_SRC)},
         "dominant": dom[0],
     }

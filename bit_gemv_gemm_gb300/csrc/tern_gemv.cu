@@ -173,23 +173,31 @@ __device__ __forceinline__ void slot_regs(int j, uint32_t w0, uint32_t w1, uint3
     }
 }
 
-// The chain of one (16-row, 128-weight) unit for one token tile.
+// The chains of one (16-row, 128-weight) unit for one token tile: the even
+// slots and the odd slots accumulate in two independent chains of four MMAs,
+// added at the end (acc = even + odd), so consecutive MMAs do not wait on one
+// another.  The all-ones pass runs the same two chains and the same addition,
+// so a row of zero weights still matches it bit for bit.
 template <bool Q3 = false>
 __device__ __forceinline__ void mma_chain1(float (&acc)[4], const uint32_t (&w)[4], const uint32_t (&b)[16]) {
+    float odd[4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         uint32_t r[4];
         slot_regs<Q3>(j, w[0], w[1], w[2], w[3], r);
-        mma16816(acc, r[0], r[1], r[2], r[3], b[2 * j], b[2 * j + 1], j > 0);
+        mma16816((j & 1) ? odd : acc, r[0], r[1], r[2], r[3], b[2 * j], b[2 * j + 1], j > 1);
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] += odd[e];
 }
 
-// Two units of the same group at once: 2 x MT independent MMA chains sharing
-// the B fragments, each in the slot order of mma_chain1 (so each keeps the
-// ones-pass rounding).
+// Two units of the same group at once: 2 x MT x 2 independent MMA chains
+// sharing the B fragments, each unit in the chain order of mma_chain1 (so each
+// keeps the ones-pass rounding).
 template <int MT, bool Q3 = false>
 __device__ __forceinline__ void pair_mmas(float (&acc)[2][MT][4], const uint32_t (&w)[2][4],
                                           const uint32_t (&b)[MT][16]) {
+    float odd[2][MT][4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         uint32_t r[2][4];
@@ -199,8 +207,15 @@ __device__ __forceinline__ void pair_mmas(float (&acc)[2][MT][4], const uint32_t
         for (int q = 0; q < 2; ++q)
 #pragma unroll
             for (int nt = 0; nt < MT; ++nt)
-                mma16816(acc[q][nt], r[q][0], r[q][1], r[q][2], r[q][3], b[nt][2 * j], b[nt][2 * j + 1], j > 0);
+                mma16816((j & 1) ? odd[q][nt] : acc[q][nt], r[q][0], r[q][1], r[q][2], r[q][3], b[nt][2 * j],
+                         b[nt][2 * j + 1], j > 1);
     }
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int nt = 0; nt < MT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[q][nt][e] += odd[q][nt][e];
 }
 
 // ---- the 1-bit sibling: bit k%32 of a word is weight k, w = (2b - 1) s ----
