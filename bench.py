@@ -541,7 +541,7 @@ def bench_affine(tern, steps: int, warmup: int, hbm: float, copies: int = 16):
     return out
 
 
-def bench_rotated(tern, steps: int, warmup: int, copies: int = 40):
+def bench_rotated(tern, steps: int, warmup: int, peaks: dict, copies: int = 40):
     import torch
     import synth
     K, N = synth.ROTATED["K"], synth.ROTATED["N"]
@@ -571,17 +571,43 @@ def bench_rotated(tern, steps: int, warmup: int, copies: int = 40):
             for c in range(copies):
                 tern.fwht(xs[c], signs, y=xr[c])
 
+        def product_only():
+            for c in range(copies):
+                tern.gemv(xr[c], mats[c][0], mats[c][1], y=ys[c], ws=ws)
+
         res = {"M": M, "K": K, "N": N}
-        for name, fn in (("fused", fused), ("separate", separate), ("fwht_only", rot_only)):
+        for name, fn in (("fused", fused), ("separate", separate), ("fwht_only", rot_only),
+                         ("product_only", product_only)):
             g = graph_of(fn)
             ms = time_graph(g, max(3, steps // 4), warmup)
             res[f"{name}_us"] = ms / copies * 1e3
         wb = weight_bytes(N, K)
         res["fused_weight_GBps"] = wb / (res["fused_us"] * 1e-6) / 1e9
         res["fwht_GBps"] = 4.0 * M * K / (res["fwht_only_us"] * 1e-6) / 1e9
+        res["fused_minus_product_us"] = res["fused_us"] - res["product_only_us"]
+        res["fused_hbm_frac"] = res["fused_weight_GBps"] / peaks["hbm_gbs"]
         out.append(res)
     del mats
-    return out
+    # the rotation alone where it is bandwidth-bound: many tokens, inputs and
+    # outputs larger than L2 (4 copies of 4096 x 4096 bf16 in and out)
+    Mb, nb = 4096, 4
+    xb = [synth.device_activations(5, f"RB{c}", (Mb, K)) for c in range(nb)]
+    yb = [torch.empty_like(x) for x in xb]
+
+    def big():
+        for c in range(nb):
+            tern.fwht(xb[c], signs, y=yb[c])
+
+    g = graph_of(big)
+    ms = time_graph(g, max(3, steps // 4), warmup)
+    us = ms / nb * 1e3
+    gbps = 4.0 * Mb * K / (us * 1e-6) / 1e9
+    bw = {"M": Mb, "K": K, "us": us, "GBps": gbps,
+          "roofline": {"bound": "hbm", "kernel": "fwht_kernel", "achieved": gbps, "peak": peaks["hbm_gbs"],
+                       "unit": "GB/s", "frac": gbps / peaks["hbm_gbs"], "peak_source": f"{peaks['_source']} hbm_gbs",
+                       "bytes": "bf16 in + bf16 out, 4 K bytes per token"}}
+    del xb, yb
+    return {"small_batch": out, "bandwidth": bw}
 
 
 def bench_prefill(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int, peaks: dict, dev_index: int):
@@ -837,7 +863,7 @@ def main() -> None:
         rows["verify"] = bench_verify(tern, sweep, qkv, args.steps, args.warmup)
         rows["verify_step"] = bench_verify_step(tern, sweep, qkv, args.steps, args.warmup)
     if "rotated" not in skip:
-        rows["rotated"] = bench_rotated(tern, args.steps, args.warmup)
+        rows["rotated"] = bench_rotated(tern, args.steps, args.warmup, peaks)
     if "binary" not in skip:
         rows["binary"] = bench_binary(tern, args.steps, args.warmup, hbm)
     if "affine" not in skip:

@@ -67,10 +67,17 @@
 // bits s and s + 16 (read as b * 2^(s' - 24)), MMA j takes slots j and j + 8,
 // and y = s F (2 acc - acc1).
 //
-// The rotation-fused call runs rotate_stage_kernel first: it rotates x, then
-// stages it exactly as the product would (exponent and scaled fp16 values, in
-// B-fragment order) into the workspace, and the product (PRE) loads the
-// fragments as they are.
+// The rotation-fused call.  For M <= 2 it is one launch (ROT): each CTA
+// rebuilds, in fp32 in shared memory, the 1024-wide slice of the rotated
+// activation that its K-slice reads, from H_4096 = H_4 (x) H_1024 (natural
+// order): the signed sum of the block's four 1024-wide parts picked by row a
+// of H_4 (a = the slice's place in its 4096-block), then a 1024-point
+// transform.  The warps stage their groups from it exactly as they stage a
+// bf16 x, so x' is never rounded to bf16.  Every row range of a slice repeats
+// that work, which is cheap for one or two tokens only; for more tokens
+// rotate_stage_kernel runs first: it rotates x once, stages it exactly as the
+// product would (exponent and scaled fp16 values, in B-fragment order) into
+// the workspace, and the product (PRE) loads the fragments as they are.
 #include <mutex>
 #include <type_traits>
 
@@ -98,6 +105,7 @@ template <> struct GemvCfg<2> { static constexpr int kCtasPerSm = 2; };
 struct GemvArgs {
     const void* x;              // bf16 [M][K], or the rotation's staged fragments (PRE)
     const int* xe;              // PRE: the staging exponent E of each (token, group)
+    const int8_t* signs;        // ROT: the rotation's sign pattern [K]
     const uint32_t* codes;      // [N][K/16]
     const __half* scales;       // [N][K/128]
     const __half* biases;       // [N][K/128], an affine pack (AFF) only
@@ -113,6 +121,7 @@ struct GemvArgs {
     int gpad;                   // scale row pitch in shared memory (halves)
     int boff;                   // AFF: the staged biases' offset from the scales (halves)
     uint32_t off_sc, off_part;  // shared-memory offsets (bytes)
+    uint32_t off_rot;           // ROT: the rotated slice, [M][kRotPitch] fp32
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -305,16 +314,91 @@ __host__ __device__ inline int scale_width(int G, int gA, int gB) {
     return scale_mode(G, gA, gB) == 4 ? ((gB + 1) & ~1) - (gA & ~1) : gB - gA;
 }
 
+// ---- the fused rotation's slice ----
+constexpr int kRotN = 1024;                      // a K-slice of 8 groups
+constexpr int kRotPitch = kRotN + kRotN / 16;    // floats per token, padded as fwht_pos pads
+// This CTA's slice sigma (8 groups) of x' = H_4096 (s (.) x) / 64 for every
+// token, into rot[m][fwht_pos(j)], j = 0..1023.  With the block b = sigma / 4
+// and the slice's place a = sigma % 4 in it, and H_4096 = H_4 (x) H_1024,
+//   x'[4096 b + 1024 a + j] = (H_1024 u)[j],
+//   u[j] = sum_{a'} (-1)^popcount(a & a') z[4096 b + 1024 a' + j] / 64,  z = s (.) x.
+// H_1024 = H_4 (x) H_16 (x) H_16 runs as three passes (index bits 0-3, 4-7,
+// 8-9).  Four tokens at a time, 64 threads each.  All threads of the CTA
+// call it; it ends with a barrier.
+__device__ __forceinline__ void rotate_slice(const __nv_bfloat16* __restrict__ x, const int8_t* __restrict__ signs,
+                                             int K, int M, int sigma, float* __restrict__ rot) {
+    const int blk = sigma >> 2, a = sigma & 3;
+    const int tq = threadIdx.x >> 6, tau = threadIdx.x & 63;
+    for (int m0 = 0; m0 < M; m0 += 4) {
+        const int m = m0 + tq;
+        float* u = rot + (size_t)m * kRotPitch;
+        float v[16];
+        if (m < M) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = 0.0f;
+#pragma unroll
+            for (int ap = 0; ap < 4; ++ap) {
+                const size_t k0 = (size_t)kFwhtN * blk + (size_t)kRotN * ap + 16 * tau;
+                const int4* xp = reinterpret_cast<const int4*>(x + (size_t)m * K + k0);
+                const int4 x0 = __ldg(xp), x1 = __ldg(xp + 1);
+                const int4 sg = __ldg(reinterpret_cast<const int4*>(signs + k0));
+                const uint32_t xw[8] = {(uint32_t)x0.x, (uint32_t)x0.y, (uint32_t)x0.z, (uint32_t)x0.w,
+                                        (uint32_t)x1.x, (uint32_t)x1.y, (uint32_t)x1.z, (uint32_t)x1.w};
+                const uint32_t sw[4] = {(uint32_t)sg.x, (uint32_t)sg.y, (uint32_t)sg.z, (uint32_t)sg.w};
+                const bool flip = (__popc(a & ap) & 1) != 0;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float xv = __uint_as_float(((xw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
+                    const int sv = (int)(int8_t)((sw[e >> 2] >> (8 * (e & 3))) & 0xFFu);
+                    v[e] += ((sv < 0) != flip) ? -xv : xv;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] *= 1.0f / 64.0f;
+            fwht16(v);   // index bits 0-3
+#pragma unroll
+            for (int e = 0; e < 16; ++e) u[fwht_pos(16 * tau + e)] = v[e];
+        }
+        __syncthreads();
+        if (m < M) {
+            // index bits 4-7: tau's bits 0-3 and 4-5 are bits 0-3 and 8-9
+            const int base = (tau & 15) | ((tau >> 4) << 8);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = u[fwht_pos(base | (e << 4))];
+            fwht16(v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) u[fwht_pos(base | (e << 4))] = v[e];
+        }
+        __syncthreads();
+        if (m < M) {
+            // index bits 8-9: four columns (bits 0-7) per thread
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const int c = 4 * tau + c4;
+                const float w0 = u[fwht_pos(c)], w1 = u[fwht_pos(c | 256)];
+                const float w2 = u[fwht_pos(c | 512)], w3 = u[fwht_pos(c | 768)];
+                const float p0 = w0 + w1, p1 = w0 - w1, p2 = w2 + w3, p3 = w2 - w3;
+                u[fwht_pos(c)] = p0 + p2;
+                u[fwht_pos(c | 256)] = p1 + p3;
+                u[fwht_pos(c | 512)] = p0 - p2;
+                u[fwht_pos(c | 768)] = p1 - p3;
+            }
+        }
+        __syncthreads();
+    }
+}
+
 // ONE: the single-token case (M = 1), whose epilogue keeps one value per row.
 // LEAN (when G is a multiple of 8): every warp has exactly one group over its
 // CTA's whole range, and only the lean loop is compiled.
 // BIN: the 1-bit sibling format (lean loop only): slice sigma is groups
 // 8 sigma .. 8 sigma + 7, and a warp whose group is past G has no units.
 // AFF: an affine pack, w = s q + b (one matrix, bf16 activations).
-template <int MT, bool PRE, bool ONE, bool LEAN = false, bool BIN = false, bool AFF = false>
+template <int MT, bool PRE, bool ONE, bool LEAN = false, bool BIN = false, bool AFF = false, bool ROT = false>
 __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kCtasPerSm)
 gemv_kernel(const GemvArgs a) {
     static_assert(!BIN || (LEAN && !PRE), "the 1-bit layout runs the lean loop on bf16 activations");
+    static_assert(!ROT || (LEAN && !PRE), "the in-kernel rotation's slices are whole 8-group slices");
     static_assert(!AFF || (!BIN && !PRE), "the affine pack has 2-bit codes and bf16 activations");
     constexpr int MP = 8 * MT;
     constexpr int SLOT = BIN ? kBinSlotBytes : kSlotBytes;
@@ -480,6 +564,12 @@ gemv_kernel(const GemvArgs a) {
     const int part_n = M <= kPrivateMaxM ? kWarps * rmax * 16 * M : rmax * 16 * MP;
     if (M > kPrivateMaxM || na == 0)
         for (int i = threadIdx.x; i < part_n; i += kThreads) part[i] = 0.0f;
+    // the in-kernel rotation: this CTA's slice of x' (after the PDL wait
+    // above: x may be the previous kernel's output), built while the first
+    // weight copies are still landing
+    if (ROT)
+        rotate_slice(reinterpret_cast<const __nv_bfloat16*>(a.x), a.signs, a.K, M, sigma,
+                     reinterpret_cast<float*>(smem + a.off_rot));
 
     // ---- stage one group's activation (read from global memory, possibly the
     // previous kernel's output): lane (gid, t) holds token nt*8+gid,
@@ -515,7 +605,13 @@ gemv_kernel(const GemvArgs a) {
                 }
             } else {
                 float v[32];
-                if (m < M) {
+                if (ROT && m < M) {
+                    // the rotated slice in shared memory (fp32)
+                    const float* u = reinterpret_cast<const float*>(smem + a.off_rot) + (size_t)m * kRotPitch;
+                    const int j0 = (g - gA) * kGroup + 32 * t;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = u[fwht_pos(j0 + e)];
+                } else if (m < M) {
                     const uint4* s4 = reinterpret_cast<const uint4*>(
                         reinterpret_cast<const __nv_bfloat16*>(a.x) + (size_t)m * a.K + (size_t)g * kGroup + 32 * t);
 #pragma unroll
@@ -884,8 +980,9 @@ struct Plan {
     int G, T, S, cps, ctas, rmax, MT, gpad, slot;
     int T2, cps1;   // a pair call: the second matrix's tiles (T counts both) and the first's ranges
     bool aff;       // an affine pack: biases staged after the scales, boff halves on
+    bool rot;       // the in-kernel rotation (ROT): the rotated slice after the partials
     int boff;
-    uint32_t off_sc, off_part;
+    uint32_t off_sc, off_part, off_rot;
     size_t smem;
 };
 
@@ -910,14 +1007,17 @@ void layout(Plan& p, int M, int cps) {
     off = align_up(off + (size_t)p.rmax * 16 * p.gpad * 2 * (p.aff ? 2 : 1), 16);
     p.off_part = (uint32_t)off;
     off += (M <= kPrivateMaxM ? (size_t)kWarps * p.rmax * 16 * M : (size_t)p.rmax * 16 * MP) * 4;
+    p.off_rot = (uint32_t)align_up(off, 16);
+    if (p.rot) off = p.off_rot + (size_t)M * kRotPitch * 4;
     p.smem = off;
 }
 
 // The device-independent part of the plan: slices and the scale pitch.  The
 // 1-bit layout's slices are groups 8 s .. 8 s + 7 (the last one may be short).
-Plan base_plan(int M, int N, int K, bool bin, int N2 = 0, bool aff = false) {
+Plan base_plan(int M, int N, int K, bool bin, int N2 = 0, bool aff = false, bool rot = false) {
     Plan p{};
     p.aff = aff;
+    p.rot = rot;
     p.G = K / kGroup;
     p.T2 = (N2 + 15) / 16;
     p.T = (N + 15) / 16 + p.T2;
@@ -936,7 +1036,7 @@ Plan base_plan(int M, int N, int K, bool bin, int N2 = 0, bool aff = false) {
 
 // Lets the kernel use the device's whole per-block shared memory; returns the
 // dynamic part it may take.
-template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN, bool AFF>
+template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN, bool AFF, bool ROT>
 cudaError_t kernel_smem_limit(int dev, int* limit) {
     static int optin_of[64] = {};
     if (!optin_of[dev]) {
@@ -944,10 +1044,10 @@ cudaError_t kernel_smem_limit(int dev, int* limit) {
         cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return e;
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, gemv_kernel<MT, PRE, ONE, LEAN, BIN, AFF>);
+        e = cudaFuncGetAttributes(&fa, gemv_kernel<MT, PRE, ONE, LEAN, BIN, AFF, ROT>);
         if (e != cudaSuccess) return e;
         optin -= (int)fa.sharedSizeBytes;   // the kernel's static shared memory comes first
-        e = cudaFuncSetAttribute(gemv_kernel<MT, PRE, ONE, LEAN, BIN, AFF>,
+        e = cudaFuncSetAttribute(gemv_kernel<MT, PRE, ONE, LEAN, BIN, AFF, ROT>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (e != cudaSuccess) return e;
         optin_of[dev] = optin;
@@ -958,11 +1058,11 @@ cudaError_t kernel_smem_limit(int dev, int* limit) {
 
 // One wave: as many CTAs as fit at once, by registers (the launch bound) and
 // by shared memory (which grows with the range length).
-template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN, bool AFF>
+template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN, bool AFF, bool ROT>
 tern_status make_plan(int M, int N, int K, int N2, int sms, int dev, Plan* out) {
     int limit = 0;
-    if (kernel_smem_limit<MT, PRE, ONE, LEAN, BIN, AFF>(dev, &limit) != cudaSuccess) return TERN_ERR_CUDA;
-    Plan p = base_plan(M, N, K, BIN, N2, AFF);
+    if (kernel_smem_limit<MT, PRE, ONE, LEAN, BIN, AFF, ROT>(dev, &limit) != cudaSuccess) return TERN_ERR_CUDA;
+    Plan p = base_plan(M, N, K, BIN, N2, AFF, ROT);
     const int need = (p.T + kMaxTiles - 1) / kMaxTiles;   // ranges short enough for the shared partials
     int cps = 1;
     for (int per_sm = GemvCfg<MT>::kCtasPerSm; per_sm >= 1; --per_sm) {
@@ -982,7 +1082,7 @@ tern_status make_plan(int M, int N, int K, int N2, int sms, int dev, Plan* out) 
 // Plans depend on the shape and the device only: keep the recent ones.
 struct PlanKey {
     int M, N, K, N2, dev;
-    bool pre, bin, aff;
+    bool pre, bin, aff, rot;
 };
 std::mutex g_plan_mu;
 constexpr int kPlanCache = 64;
@@ -990,7 +1090,7 @@ PlanKey g_plan_key[kPlanCache];
 Plan g_plan_val[kPlanCache];
 int g_plan_n = 0, g_plan_next = 0;
 
-template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN, bool AFF>
+template <int MT, bool PRE, bool ONE, bool LEAN, bool BIN, bool AFF, bool ROT>
 tern_status cached_plan(int M, int N, int K, int N2, int sms, Plan* out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TERN_ERR_CUDA;
@@ -999,15 +1099,15 @@ tern_status cached_plan(int M, int N, int K, int N2, int sms, Plan* out) {
     for (int i = 0; i < g_plan_n; ++i) {
         const PlanKey& k = g_plan_key[i];
         if (k.M == M && k.N == N && k.K == K && k.N2 == N2 && k.dev == dev && k.pre == PRE && k.bin == BIN &&
-            k.aff == AFF) {
+            k.aff == AFF && k.rot == ROT) {
             *out = g_plan_val[i];
             return TERN_OK;
         }
     }
-    const tern_status st = make_plan<MT, PRE, ONE, LEAN, BIN, AFF>(M, N, K, N2, sms, dev, out);
+    const tern_status st = make_plan<MT, PRE, ONE, LEAN, BIN, AFF, ROT>(M, N, K, N2, sms, dev, out);
     if (st != TERN_OK) return st;
     const int slot = g_plan_n < kPlanCache ? g_plan_n++ : (g_plan_next++ % kPlanCache);
-    g_plan_key[slot] = PlanKey{M, N, K, N2, dev, PRE, BIN, AFF};
+    g_plan_key[slot] = PlanKey{M, N, K, N2, dev, PRE, BIN, AFF, ROT};
     g_plan_val[slot] = *out;
     return TERN_OK;
 }
@@ -1035,16 +1135,19 @@ size_t base_bytes(int M, int T, int K) {
     const int G = K / kGroup;
     return G > kWarps ? align_up((size_t)T * 4, 256) : 0;
 }
+// The in-kernel rotation (ROT) serves M <= kRotMaxM; above that the fused call
+// stages the rotated x in the workspace.
+constexpr int kRotMaxM = 2;
 size_t workspace_bytes(int M, int N, int K, bool rot) {
     if (M < 1 || M > 16 || N < 1 || K < kGroup || K % kGroup != 0) return 0;
     return base_bytes(M, (N + 15) / 16, K) +
-           (rot ? align_up((size_t)M * K * 2 + (size_t)M * (K / kGroup) * 4, 256) : 0);
+           (rot && M > kRotMaxM ? align_up((size_t)M * K * 2 + (size_t)M * (K / kGroup) * 4, 256) : 0);
 }
 
-template <int MT, bool PRE, bool ONE, bool LEAN = false, bool BIN = false, bool AFF = false>
+template <int MT, bool PRE, bool ONE, bool LEAN = false, bool BIN = false, bool AFF = false, bool ROT = false>
 tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
     Plan p;
-    const tern_status st = cached_plan<MT, PRE, ONE, LEAN, BIN, AFF>(args.M, args.N, args.K, args.N2, sms, &p);
+    const tern_status st = cached_plan<MT, PRE, ONE, LEAN, BIN, AFF, ROT>(args.M, args.N, args.K, args.N2, sms, &p);
     if (st != TERN_OK) return st;
     args.G = p.G;
     args.T = p.T - p.T2;   // the first matrix's tiles
@@ -1057,8 +1160,9 @@ tern_status launch_gemv(GemvArgs args, int sms, cudaStream_t stream) {
     args.boff = p.boff;
     args.off_sc = p.off_sc;
     args.off_part = p.off_part;
+    args.off_rot = p.off_rot;
     const cudaError_t e =
-        launch_pdl(gemv_kernel<MT, PRE, ONE, LEAN, BIN, AFF>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true,
+        launch_pdl(gemv_kernel<MT, PRE, ONE, LEAN, BIN, AFF, ROT>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true,
                    args);
     return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
@@ -1073,7 +1177,7 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
     const size_t fb = base_bytes(M, (N + 15) / 16 + (N2 + 15) / 16, K);
     if (fb > 0 || signs) {
         const size_t need = fb + (signs ? workspace_bytes(M, N, K, true) - base_bytes(M, (N + 15) / 16, K) : 0);
-        if (!workspace || workspace_bytes_ < need) return TERN_ERR_WORKSPACE;
+        if (need > 0 && (!workspace || workspace_bytes_ < need)) return TERN_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TERN_ERR_ALIGN;
     }
     GemvArgs args{};
@@ -1094,7 +1198,12 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
     // K a multiple of 1024: slices of exactly 8 groups, one group per warp
     const bool lean = (K / kGroup) % kWarps == 0;
     int launches = 1;
-    if (signs) {
+    if (signs && M <= kRotMaxM) {
+        // the rotation inside the product (K % 4096 == 0: whole 8-group slices)
+        args.signs = signs;
+        st = M == 1 ? launch_gemv<1, false, true, true, false, false, true>(args, sms, stream)
+                    : launch_gemv<1, false, false, true, false, false, true>(args, sms, stream);
+    } else if (signs) {
         // staged x': M x K halves, then M x G exponents
         uint32_t* xs = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(workspace) + fb);
         int* xe = reinterpret_cast<int*>(xs + (size_t)M * K / 2);
@@ -1104,12 +1213,8 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
         args.x = xs;
         args.xe = xe;
         launches = 2;
-        st = M == 1 ? (lean ? launch_gemv<1, true, true, true>(args, sms, stream)
-                            : launch_gemv<1, true, true>(args, sms, stream))
-             : MT == 1 ? (lean ? launch_gemv<1, true, false, true>(args, sms, stream)
-                               : launch_gemv<1, true, false>(args, sms, stream))
-                       : (lean ? launch_gemv<2, true, false, true>(args, sms, stream)
-                               : launch_gemv<2, true, false>(args, sms, stream));
+        st = MT == 1 ? launch_gemv<1, true, false, true>(args, sms, stream)
+                     : launch_gemv<2, true, false, true>(args, sms, stream);
     } else if (biases) {
         st = M == 1 ? (lean ? launch_gemv<1, false, true, true, false, true>(args, sms, stream)
                             : launch_gemv<1, false, true, false, false, true>(args, sms, stream))

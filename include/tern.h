@@ -153,9 +153,10 @@ tern_status tern_bin_unpack_host(const uint32_t *words, int N, int K, int8_t *t)
 /* Workspace bytes tern_gemv and tern_fwht_gemm need for (M, N, K); 0 on bad
  * input.  The size covers both calls (at least 256).  It holds one 32-bit flag
  * word per 16-row tile when K > 1024 (the K-slice sums of a row range are
- * added into y, and the flag orders the range's clearing before the additions)
- * and, for tern_fwht_gemm, the rotated activation as the product stages it
- * (M * K fp16 values and one int32 exponent per token and 128-group).
+ * added into y, and the flag orders the range's clearing before the
+ * additions) and, for tern_fwht_gemm with M > 2, the rotated activation as the
+ * product stages it (M * K fp16 values and one int32 exponent per token and
+ * 128-group).
  * The workspace must be zero-filled once before its first use; every call
  * leaves its flags at zero again.  Calls that share a workspace must not run
  * concurrently (use one stream, or one workspace per stream).  After a device
@@ -259,12 +260,17 @@ tern_status tern_gemv_noalloc(const void *x, const uint32_t *codes, const void *
 tern_status tern_fwht(const void *x, const int8_t *signs, void *y, int M, int K,
                       tern_stream_t stream);
 
-/* Rotation fused into the product: y (fp32 [M][N]) = rot(x) W^T.  A rotation
- * prologue kernel computes the rotated activation in fp32 and stages it in the
- * workspace (L2-resident) as the product stages any activation: per token and
- * 128-group, fp16 values scaled by a power of two chosen from the group's
- * largest magnitude.  It is never rounded to bf16.
- * 1 <= M <= 16, K % 4096 == 0; workspace as for tern_gemv (required). */
+/* Rotation fused into the product: y (fp32 [M][N]) = rot(x) W^T.  The rotated
+ * activation is computed in fp32 and staged as the product stages any
+ * activation: per token and 128-group, fp16 values scaled by a power of two
+ * chosen from the group's largest magnitude; it is never rounded to bf16.
+ * For M <= 2 it is one kernel launch: each CTA of the product rebuilds the
+ * 1024-wide slice of x' its K-slice reads in shared memory (H_4096 =
+ * H_4 (x) H_1024: the signed sum of the 4096-block's four 1024-wide parts,
+ * then a 1024-point transform).  For M > 2 a prologue kernel rotates x once
+ * and stages it in the workspace (L2-resident) before the product (two
+ * launches).  1 <= M <= 16, K % 4096 == 0; workspace as for tern_gemv
+ * (required). */
 tern_status tern_fwht_gemm(const void *x, const int8_t *signs, const uint32_t *codes,
                            const void *scales, float *y, int M, int N, int K,
                            void *workspace, size_t workspace_bytes, tern_stream_t stream);

@@ -131,9 +131,10 @@ def test_argument_errors_never_launch(tern):
 
 def test_workspace_sizes(tern):
     # Once K spans more than one chunk of 8 groups (K > 1024): one flag word per
-    # 16-row tile (256-byte aligned); then, for the fused call when K % 4096 == 0,
-    # the staged rotated x: M x K fp16 values and one int32 exponent per token
-    # and 128-group (256-byte aligned)
+    # 16-row tile (256-byte aligned).  When K % 4096 == 0 the size also covers
+    # the fused call, which for M > 2 stages the rotated x there: M x K fp16
+    # values and one int32 exponent per token and 128-group (256-byte
+    # aligned); for M <= 2 the product rebuilds it in shared memory.
     a256 = lambda v: (v + 255) // 256 * 256
 
     def rot(M, K):
@@ -141,9 +142,10 @@ def test_workspace_sizes(tern):
 
     assert tern.gemv_workspace_bytes(1, 17408, 5120) == a256(1088 * 4)
     assert tern.gemv_workspace_bytes(16, 10, 17408) == 256
-    assert tern.gemv_workspace_bytes(2, 12288, 4096) == a256(768 * 4) + rot(2, 4096)
+    assert tern.gemv_workspace_bytes(2, 12288, 4096) == a256(768 * 4)
+    assert tern.gemv_workspace_bytes(3, 12288, 4096) == a256(768 * 4) + rot(3, 4096)
     assert tern.gemv_workspace_bytes(16, 12288, 8192) == a256(768 * 4) + rot(16, 8192)
-    assert tern.gemv_workspace_bytes(1, 16, 4096) == 256 + 256 * 33
+    assert tern.gemv_workspace_bytes(1, 16, 4096) == 256
     assert tern.gemv_workspace_bytes(3, 100, 1152) == a256(7 * 4)
     assert tern.gemv_workspace_bytes(1, 256, 512) == 256      # one chunk: nothing needed
     assert tern.gemv_workspace_bytes(1, 256, 1024) == 256

@@ -237,12 +237,14 @@ def test_fwht_roundtrip_and_norm(tern, orc):
     assert np.allclose(yn, np.linalg.norm(xf, axis=1), rtol=4e-3)
 
 
-@pytest.mark.parametrize("M", [1, 5, 16])
-def test_fwht_gemm_fused_matches_oracle(tern, orc, M):
+@pytest.mark.parametrize("M,K", [(1, 4096), (2, 4096), (5, 4096), (16, 4096), (1, 8192), (2, 12288), (3, 8192)])
+def test_fwht_gemm_fused_matches_oracle(tern, orc, M, K):
     """Fused rotation + product, rotated activation kept in fp32 on chip,
-    against the oracle with the rotation kept in double."""
-    K, N = 4096, 1000
-    p = synth.problem(60 + M, M, N, K, with_signs=True)
+    against the oracle with the rotation kept in double: the in-product
+    rotation (M <= 2) and the prologue kernel (M > 2), one and several
+    4096-blocks."""
+    N = 1000
+    p = synth.problem(60 + M, M, N, K, with_signs=True, tag=f"fz{K}")
     codes = tern.pack(dev_trits(p.t))
     y = tern.fwht_gemm(dev_bf16(p.x), torch.from_numpy(p.signs).cuda(), codes, dev_scales(p.s))
     torch.cuda.synchronize()
