@@ -815,6 +815,60 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+# Single cases for profiler captures: each runs its launch 3 times unprofiled
+# (warm-up) and then 2 more, with synthetic inputs of the bench's shapes.
+PROFILE_CASES = ("fwht_bw", "fused_m1", "fused_m16", "gemm_down", "gemm_qkv", "gemv_m1", "gemv_m16")
+
+
+def run_profile_case(name: str) -> None:
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import bit_gemv_gemm_gb300 as tern
+    import synth
+    K4, N4 = synth.ROTATED["K"], synth.ROTATED["N"]
+    if name == "fwht_bw":
+        # the rotation where it is bandwidth-bound: 4096 tokens x K = 4096
+        x = synth.device_activations(5, "PB.x", (4096, K4))
+        sg = synth.device_signs(5, "PB.s", K4)
+        y = torch.empty_like(x)
+        fn = lambda: tern.fwht(x, sg, y=y)
+    elif name in ("fused_m1", "fused_m16"):
+        M = 1 if name == "fused_m1" else 16
+        c = tern.pack(synth.device_trits(6, "PF.t", (N4, K4)))
+        sc = synth.device_scales(6, "PF.sc", (N4, K4 // 128))
+        x = synth.device_activations(6, f"PF.x{M}", (M, K4))
+        sg = synth.device_signs(6, "PF.s", K4)
+        y = torch.empty((M, N4), dtype=torch.float32, device="cuda")
+        ws = tern.workspace(tern.gemv_workspace_bytes(M, N4, K4))
+        fn = lambda: tern.fwht_gemm(x, sg, c, sc, y=y, ws=ws)
+    elif name in ("gemm_down", "gemm_qkv"):
+        K, N = (17408, 5120) if name == "gemm_down" else (5120, 6144)
+        M = 512
+        c = tern.pack(synth.device_trits(7, "PG.t", (N, K)))
+        sc = synth.device_scales(7, "PG.sc", (N, K // 128))
+        x = synth.device_activations(7, "PG.x", (M, K))
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        ws = tern.workspace(tern.gemm_workspace_bytes(M, N, K))
+        fn = lambda: tern.gemm(x, c, sc, y=y, ws=ws)
+    else:
+        M = 1 if name == "gemv_m1" else 16
+        K, N = 5120, 17408
+        c = tern.pack(synth.device_trits(8, "PV.t", (N, K)))
+        sc = synth.device_scales(8, "PV.sc", (N, K // 128))
+        x = synth.device_activations(8, f"PV.x{M}", (M, K))
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        ws = tern.workspace(tern.gemv_workspace_bytes(M, N, K))
+        fn = lambda: tern.gemv(x, c, sc, y=y, ws=ws)
+    for _ in range(5):
+        fn()
+    torch.cuda.synchronize()
+    err = tern.device_error()
+    if err:
+        raise SystemExit(f"device error {err:#x}")
+    print(f"profile case {name}: 5 launches done", flush=True)
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -823,7 +877,12 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=DECODE_LAYERS)
     ap.add_argument("--skip", default="", help="comma list of parts to skip: fused,verify,rotated,binary,affine,prefill,cpu")
+    ap.add_argument("--profile", default="", choices=["", *PROFILE_CASES],
+                    help="run one hot-path case a few times for a profiler capture and exit (no JSON line)")
     args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args.profile)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
