@@ -58,6 +58,9 @@ def _load():
                 "orc_matmul": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _I]),
                 "orc_matmul_sampled": (_I, [_P, _P, _P, _I, _P, _P, _I, _P, _P, _I]),
                 "orc_bin_pack": (ctypes.c_longlong, [_P, _I, _I, _P]),
+                "orc_f3_pack": (ctypes.c_longlong, [_P, _I, _I, _P]),
+                "orc_f3_unpack": (ctypes.c_longlong, [_P, _I, _I, _P]),
+                "orc_f3_matmul": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _I]),
                 "orc_bin_unpack": (_I, [_P, _I, _I, _P]),
                 "orc_bin_matmul": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _I]),
                 "orc_bin_matmul_sampled": (_I, [_P, _P, _P, _I, _P, _P, _I, _P, _P, _I]),
@@ -173,6 +176,47 @@ def bin_matmul_sampled(x_bf16: np.ndarray, words: np.ndarray, scales_f16: np.nda
     a = np.empty(len(ms), dtype=np.float64)
     if _load().orc_bin_matmul_sampled(_ptr(x), _ptr(words), _ptr(s), K, _ptr(ms), _ptr(ns), len(ms),
                                       _ptr(y), _ptr(a), nthreads) != 0:
+        raise ValueError("bad shape")
+    return y, a
+
+
+def f3_pack(t: np.ndarray) -> tuple[np.ndarray, int]:
+    """Native base-3 packing: t int8 [N, K] in {-1,0,1} -> (bytes uint8
+    [N, 26 K/128], count of entries outside {-1,0,1}).  Five trits per byte,
+    byte = q0 + 3 q1 + 9 q2 + 27 q3 + 81 q4 with q = t + 1; the 26th byte of a
+    group holds trits 125..127."""
+    t = _c(t, np.int8)
+    N, K = t.shape
+    out = np.empty((N, 26 * (K // 128)), dtype=np.uint8)
+    bad = _load().orc_f3_pack(_ptr(t), N, K, _ptr(out))
+    if bad < 0:
+        raise ValueError("K must be a multiple of 128")
+    return out, int(bad)
+
+
+def f3_unpack(packed: np.ndarray, K: int) -> tuple[np.ndarray, int]:
+    """bytes uint8 [N, 26 K/128] -> (t int8 [N, K], count of out-of-range bytes)."""
+    packed = _c(packed, np.uint8)
+    N = packed.shape[0]
+    t = np.empty((N, K), dtype=np.int8)
+    bad = _load().orc_f3_unpack(_ptr(packed), N, K, _ptr(t))
+    if bad < 0:
+        raise ValueError("K must be a multiple of 128")
+    return t, int(bad)
+
+
+def f3_matmul(x_bf16: np.ndarray, packed: np.ndarray, scales_f16: np.ndarray,
+              nthreads: int = 0) -> tuple[np.ndarray, np.ndarray]:
+    """y[m, n] = sum_k x[m, k] (q[n, k] - 1) s[n, k // 128] in double from the
+    base-3 bytes, and a = sum_k |x w|; returns (y, a)."""
+    x = _bits16(x_bf16)
+    s = _bits16(scales_f16)
+    packed = _c(packed, np.uint8)
+    M, K = x.shape
+    N = packed.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    a = np.empty((M, N), dtype=np.float64)
+    if _load().orc_f3_matmul(_ptr(x), _ptr(packed), _ptr(s), M, N, K, _ptr(y), _ptr(a), nthreads) != 0:
         raise ValueError("bad shape")
     return y, a
 

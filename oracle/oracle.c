@@ -41,6 +41,17 @@
  *     FP16 per 128 weights.  Reading for the unstated order and precision: the
  *     slot order of the ternary codes, and FP16 biases like the scales.
  *
+ *   - Native base-3 packing: the card gives the information content of a
+ *     trit (log2 3, about 1.585 bits) and the 1.71 bits/weight it implies with
+ *     the scale, and names packing at that density as future work ([card]
+ *     "Weight representation" and "Memory requirement").  It gives no layout.
+ *     Reading: five trits per byte, byte = q0 + 3 q1 + 9 q2 + 27 q3 + 81 q4
+ *     (values 0..242) with q = t + 1 and trit i of the byte at K position
+ *     5 j + i of its group; a 128-weight group is 25 such bytes and a 26th
+ *     holding trits 125..127 as q0 + 3 q1 + 9 q2 (values 0..26); rows are
+ *     [N][26 K/128] bytes.  That is 26 * 8 / 128 + 16 / 128 = 1.75 bits per
+ *     weight with the FP16 scale.
+ *
  * Parity pins live in the "not gpu" tests: brute-force dense matmul from an
  * explicitly expanded W, exhaustive pack/unpack patterns, the explicit
  * Hadamard matrix for n <= 64, H*H = n*I, Parseval, closed forms on e_0 and
@@ -574,3 +585,101 @@ int orc_max_threads(void)
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------ */
+/* Native base-3 packing (five trits per byte; see the header).              */
+/* ------------------------------------------------------------------------ */
+
+/* Trits per byte j of a group: 5, and 3 for the last one. */
+static int orc_f3_count(int j) { return j < 25 ? 5 : 3; }
+
+/* Packs t[N][K] in {-1,0,1} into out[N][26 K/128].  Returns the count of
+ * entries outside {-1,0,1} (packed as 0), or -1 if K is not a multiple of
+ * 128. */
+long long orc_f3_pack(const int8_t *t, int N, int K, uint8_t *out)
+{
+    if (N < 0 || K < 0 || K % 128 != 0)
+        return -1;
+    long long bad = 0;
+    int G = K / 128;
+    for (int n = 0; n < N; ++n)
+        for (int g = 0; g < G; ++g)
+            for (int j = 0; j < 26; ++j) {
+                int v = 0, p = 1;
+                for (int i = 0; i < orc_f3_count(j); ++i) {
+                    int tv = t[(size_t)n * K + (size_t)g * 128 + 5 * j + i];
+                    int q = tv + 1;
+                    if (q < 0 || q > 2) {
+                        ++bad;
+                        q = 0;
+                    }
+                    v += q * p;
+                    p *= 3;
+                }
+                out[(size_t)n * G * 26 + (size_t)g * 26 + j] = (uint8_t)v;
+            }
+    return bad;
+}
+
+/* Digit i of a byte in base 3, by repeated division. */
+static int orc_f3_digit(int v, int i)
+{
+    for (int r = 0; r < i; ++r)
+        v /= 3;
+    return v % 3;
+}
+
+/* Unpacks in[N][26 K/128] into t[N][K].  Returns the count of bytes out of
+ * range (above 242, or above 26 for a group's last byte), or -1 on a bad K. */
+long long orc_f3_unpack(const uint8_t *in, int N, int K, int8_t *t)
+{
+    if (N < 0 || K < 0 || K % 128 != 0)
+        return -1;
+    long long bad = 0;
+    int G = K / 128;
+    for (int n = 0; n < N; ++n)
+        for (int g = 0; g < G; ++g)
+            for (int j = 0; j < 26; ++j) {
+                int v = in[(size_t)n * G * 26 + (size_t)g * 26 + j];
+                if (v > (j < 25 ? 242 : 26))
+                    ++bad;
+                for (int i = 0; i < orc_f3_count(j); ++i)
+                    t[(size_t)n * K + (size_t)g * 128 + 5 * j + i] = (int8_t)(orc_f3_digit(v, i) - 1);
+            }
+    return bad;
+}
+
+/* y[m][n] = sum_k x[m][k] (q[n][k] - 1) s[n][k/128] from the base-3 bytes, in
+ * double, and a[m][n] = sum_k |x w| if a != NULL.  Returns 0, or -2 for a bad
+ * shape. */
+int orc_f3_matmul(const uint16_t *x, const uint8_t *packed, const uint16_t *scales, int M, int N, int K,
+                  double *y, double *a, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || K % 128 != 0)
+        return -2;
+    orc_set_threads(nthreads);
+    int G = K / 128;
+    long long total = (long long)M * N;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (long long i = 0; i < total; ++i) {
+        int m = (int)(i / N), n = (int)(i % N);
+        double acc = 0.0, mag = 0.0;
+        for (int g = 0; g < G; ++g) {
+            double sg = orc_f16_to_f64(scales[(size_t)n * G + g]);
+            for (int j = 0; j < 26; ++j) {
+                int v = packed[(size_t)n * G * 26 + (size_t)g * 26 + j];
+                for (int q = 0; q < orc_f3_count(j); ++q) {
+                    int k = g * 128 + 5 * j + q;
+                    double p = orc_bf16_to_f64(x[(size_t)m * K + k]) * (double)(orc_f3_digit(v, q) - 1) * sg;
+                    acc += p;
+                    mag += fabs(p);
+                }
+            }
+        }
+        y[i] = acc;
+        if (a)
+            a[i] = mag;
+    }
+    return 0;
+}
+
