@@ -441,6 +441,38 @@ def bench_verify_step(tern, sweep: DecodeSweep, qkv, steps: int, warmup: int):
             "weight_GBps": wb / (ms * 1e-3) / 1e9, "tokens_per_s": M / (ms * 1e-3)}
 
 
+def bench_f3(tern, steps: int, warmup: int, hbm: float, copies: int = 16):
+    """Native base-3 packing (five trits per byte): the decode product (M = 1,
+    and M = 5) per decode shape, `copies` distinct matrices (more bytes than
+    L2) back to back in one graph, beside the 2-bit product on the same shape."""
+    import torch
+    import synth
+    out = []
+    for (K, N) in synth.DECODE_SHAPES:
+        mats = []
+        for c in range(copies):
+            t = synth.device_trits(9, f"F{c}.{K}.t", (N, K))
+            mats.append((tern.f3_pack(t), synth.device_scales(9, f"F{c}.{K}.s", (N, K // 128))))
+            del t
+        wb = N * 26 * (K // 128) + N * (K // 128) * 2
+        for M in (1, 5):
+            xs = [synth.device_activations(9, f"F{c}.{K}.x{M}", (M, K)) for c in range(copies)]
+            y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+
+            def run(xs=xs, y=y):
+                for c in range(copies):
+                    tern.f3_gemv(xs[c], mats[c][0], mats[c][1], y=y)
+
+            g = graph_of(run)
+            ms = time_graph(g, max(3, steps // 4), warmup)
+            per = ms / copies * 1e-3
+            out.append({"M": M, "K": K, "N": N, "us": per * 1e6, "weight_bytes": wb,
+                        "weight_GBps": wb / per / 1e9, "hbm_frac": wb / per / 1e9 / hbm,
+                        "bits_per_weight": 8.0 * wb / (N * K)})
+        del mats
+    return out
+
+
 def bench_binary(tern, steps: int, warmup: int, hbm: float, copies: int = 16):
     """The 1-bit sibling format.  Decode (M = 1): per decode shape, `copies`
     distinct matrices (more bytes than L2) called back to back in one graph.
@@ -817,7 +849,7 @@ def run_reference(args) -> None:
 
 # Single cases for profiler captures: each runs its launch 3 times unprofiled
 # (warm-up) and then 2 more, with synthetic inputs of the bench's shapes.
-PROFILE_CASES = ("fwht_bw", "fused_m1", "fused_m16", "gemm_down", "gemm_qkv", "gemv_m1", "gemv_m16")
+PROFILE_CASES = ("fwht_bw", "fused_m1", "fused_m16", "gemm_down", "gemm_qkv", "gemv_m1", "gemv_m16", "f3_m1")
 
 
 def run_profile_case(name: str) -> None:
@@ -851,6 +883,13 @@ def run_profile_case(name: str) -> None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         ws = tern.workspace(tern.gemm_workspace_bytes(M, N, K))
         fn = lambda: tern.gemm(x, c, sc, y=y, ws=ws)
+    elif name == "f3_m1":
+        K, N = 5120, 17408
+        c = tern.f3_pack(synth.device_trits(8, "P3.t", (N, K)))
+        sc = synth.device_scales(8, "P3.sc", (N, K // 128))
+        x = synth.device_activations(8, "P3.x", (1, K))
+        y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+        fn = lambda: tern.f3_gemv(x, c, sc, y=y)
     else:
         M = 1 if name == "gemv_m1" else 16
         K, N = 5120, 17408
@@ -876,7 +915,7 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=DECODE_LAYERS)
-    ap.add_argument("--skip", default="", help="comma list of parts to skip: fused,verify,rotated,binary,affine,prefill,cpu")
+    ap.add_argument("--skip", default="", help="comma list of parts to skip: fused,verify,rotated,binary,f3,affine,prefill,cpu")
     ap.add_argument("--profile", default="", choices=["", *PROFILE_CASES],
                     help="run one hot-path case a few times for a profiler capture and exit (no JSON line)")
     args = ap.parse_args()
@@ -925,6 +964,8 @@ def main() -> None:
         rows["rotated"] = bench_rotated(tern, args.steps, args.warmup, peaks)
     if "binary" not in skip:
         rows["binary"] = bench_binary(tern, args.steps, args.warmup, hbm)
+    if "f3" not in skip:
+        rows["f3"] = bench_f3(tern, args.steps, args.warmup, hbm)
     if "affine" not in skip:
         rows["affine"] = bench_affine(tern, args.steps, args.warmup, hbm)
     if "prefill" not in skip:

@@ -60,6 +60,9 @@ EXPORTS = {
     "tern_bin_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
     "tern_affine_gemv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
     "tern_affine_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
+    "tern_f3_packed_bytes": (_SZ, [_I, _I]),
+    "tern_f3_pack": (_I, [_P, _I, _I, _P, _P, _P]),
+    "tern_f3_gemv": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
 }
 
 
@@ -192,6 +195,36 @@ def bin_pack(t: torch.Tensor, words: torch.Tensor | None = None, bad_count: torc
     _check("tern_bin_pack", lib().tern_bin_pack(_dev(t, torch.int8, "t"), N, K, _dev(words, torch.int32, "words"),
                                                 bp, _stream(stream)))
     return words
+
+
+def f3_pack(t: torch.Tensor, packed: torch.Tensor | None = None, bad_count: torch.Tensor | None = None,
+            stream=None) -> torch.Tensor:
+    """Device packer of the base-3 format: int8 [N, K] in {-1, 0, +1} -> uint8
+    [N, 26 K/128], five trits per byte (q0 + 3 q1 + 9 q2 + 27 q3 + 81 q4)."""
+    N, K = t.shape
+    nbytes = int(lib().tern_f3_packed_bytes(N, K))
+    if packed is None:
+        packed = torch.empty((N, 26 * (K // 128)), dtype=torch.uint8, device=t.device)
+    _covers(packed=(packed, nbytes), bad_count=(bad_count, 1))
+    bp = _dev(bad_count, torch.int32, "bad_count") if bad_count is not None else None
+    _check("tern_f3_pack", lib().tern_f3_pack(_dev(t, torch.int8, "t"), N, K, _dev(packed, torch.uint8, "packed"),
+                                              bp, _stream(stream)))
+    return packed
+
+
+def f3_gemv(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor, y: torch.Tensor | None = None,
+            stream=None) -> torch.Tensor:
+    """y (fp32 [M, N]) = x W^T on a base-3 pack, M = 1..16; x bf16 [M, K],
+    packed uint8 [N, 26 K/128], scales fp16 [N, K/128].  No workspace."""
+    M, K = x.shape
+    N = packed.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _covers(packed=(packed, N * 26 * (K // 128)), scales=(scales, N * (K // 128)), y=(y, M * N))
+    _check("tern_f3_gemv", lib().tern_f3_gemv(
+        _dev(x, torch.bfloat16, "x"), _dev(packed, torch.uint8, "packed"), _dev(scales, torch.float16, "scales"),
+        _dev(y, torch.float32, "y"), M, N, K, _stream(stream)))
+    return y
 
 
 def bin_pack_host(t: np.ndarray) -> tuple[np.ndarray, int]:

@@ -144,6 +144,40 @@ tern_status tern_bin_pack_host(const int8_t *t, int N, int K, uint32_t *words,
                                long long *bad_count);
 tern_status tern_bin_unpack_host(const uint32_t *words, int N, int K, int8_t *t);
 
+/* Native base-3 packing ("prism-ml/Ternary-Bonsai-27B-mlx-2bit" model card,
+ * "Weight representation: ternary g128" and "Memory requirement": a trit
+ * carries log2 3 bits, 1.71 bits/weight with the scale, named there as future
+ * work; the card gives no layout).  Five trits per byte: byte j < 25 of a
+ * 128-weight group holds trits 5 j .. 5 j + 4 of the group as
+ * q0 + 3 q1 + 9 q2 + 27 q3 + 81 q4 (q = t + 1, values 0..242); byte 25 holds
+ * trits 125..127 as q0 + 3 q1 + 9 q2 (values 0..26).  Rows are
+ * [N][26 K/128] bytes, so 1.75 bits per weight with the fp16 scales
+ * [N][K/128] of the 2-bit format (18 % fewer bytes than the 2-bit slots). */
+
+/* Bytes of a base-3 pack of an [N][K] matrix; 0 on bad input (K % 128 != 0). */
+size_t tern_f3_packed_bytes(int N, int K);
+
+/* Device packer.  t: int8 [N][K] in {-1,0,+1}; packed: uint8 [N][26 K/128],
+ * owned by the caller.  An entry outside {-1,0,+1} is packed as -1 and
+ * counted: if bad_count (device int, nullable) is given, the count is
+ * atomically ADDED to it.  K % 128 == 0, N >= 0 (TERN_ERR_SHAPE otherwise).
+ * One kernel launch (none for an empty matrix). */
+tern_status tern_f3_pack(const int8_t *t, int N, int K, uint8_t *packed, int *bad_count,
+                         tern_stream_t stream);
+
+/* The decode product on a base-3 pack: y (fp32 [M][N]) = x W^T,
+ * W[n][k] = (q[n][k] - 1) s[n][k/128].  x bf16 [M][K], packed as tern_f3_pack
+ * writes it, scales fp16 [N][K/128]; x, packed, scales and y 16-byte aligned,
+ * owned by the caller.  1 <= M <= 16, N >= 1, K >= 128 with K % 128 == 0.
+ * One kernel launch, no workspace; every element of y is written.  It runs on
+ * the CUDA cores (fp32 FMAs, a 243-entry table per byte): the five trits of a
+ * byte cannot be separated by masks the way the 2-bit slots are.  Results
+ * agree with the exact product to within 1e-3 * sum_k |x w| + 1e-6 per
+ * element.  A byte above 242 (above 26 for a group's last byte) is not a
+ * pack's; its weights are undefined. */
+tern_status tern_f3_gemv(const void *x, const uint8_t *packed, const void *scales, float *y,
+                         int M, int N, int K, tern_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* Decode / small-batch product, M = 1..16 (card, "Cross-platform          */
 /* throughput": tg128 is the memory-bandwidth-bound phase; "Speculative    */
