@@ -849,7 +849,7 @@ def run_reference(args) -> None:
 
 # Single cases for profiler captures: each runs its launch 3 times unprofiled
 # (warm-up) and then 2 more, with synthetic inputs of the bench's shapes.
-PROFILE_CASES = ("fwht_bw", "fused_m1", "fused_m16", "gemm_down", "gemm_qkv", "gemv_m1", "gemv_m16", "f3_m1")
+PROFILE_CASES = ("fwht_bw", "fused_m1", "fused_m16", "gemm_down", "gemm_qkv", "gemv_m1", "gemv_m8", "gemv_m16", "f3_m1")
 
 
 def run_profile_case(name: str) -> None:
@@ -891,7 +891,7 @@ def run_profile_case(name: str) -> None:
         y = torch.empty((1, N), dtype=torch.float32, device="cuda")
         fn = lambda: tern.f3_gemv(x, c, sc, y=y)
     else:
-        M = 1 if name == "gemv_m1" else 16
+        M = int(name.split("_m")[1])
         K, N = 5120, 17408
         c = tern.pack(synth.device_trits(8, "PV.t", (N, K)))
         sc = synth.device_scales(8, "PV.sc", (N, K // 128))

@@ -881,7 +881,7 @@ gemv_kernel(const GemvArgs a) {
     __syncthreads();
 
     // ---- the CTA's row sums ----
-    const int nv = R * 16 * M;
+    const int nr = R * 16;
     auto row_value = [&](int tl, int r, int m) -> float {
         if (M <= kPrivateMaxM) {
             float s = 0.0f;
@@ -891,17 +891,18 @@ gemv_kernel(const GemvArgs a) {
         return part[((size_t)tl * 16 + r) * MP + m];
     };
     if (S == 1) {
-        for (int i = threadIdx.x; i < nv; i += kThreads) {
-            const int m = i / (R * 16), rr = i - m * (R * 16);
-            const int r = tile_lo * 16 + rr;
-            if (r < N) yv[(size_t)m * N + r] = row_value(rr >> 4, rr & 15, m);
-        }
+        for (int m = 0; m < M; ++m)
+            for (int rr = threadIdx.x; rr < nr; rr += kThreads) {
+                const int r = tile_lo * 16 + rr;
+                if (r < N) yv[(size_t)m * N + r] = row_value(rr >> 4, rr & 15, m);
+            }
         return;
     }
     // ---- several slices: add the CTA's row sums into y.  A slice other than 0
     // first waits (bounded) until the slice-0 CTA has cleared the rows -- it
-    // did so right after the PDL wait, so by now the count is normally there --
-    // and counts itself; the S-th count returns the flag to 0. ----
+    // cleared them right after the PDL wait and counted a ring turn later at
+    // most, so by now the count has normally been seen -- and counts itself;
+    // the S-th count returns the flag to 0. ----
     __shared__ int go;
     if (sigma != 0) {
         if (threadIdx.x == 0) {
@@ -913,11 +914,11 @@ gemv_kernel(const GemvArgs a) {
         __syncthreads();
         if (!go) return;   // reported: y is left incomplete rather than wrong-ordered
     }
-    for (int i = threadIdx.x; i < nv; i += kThreads) {
-        const int m = i / (R * 16), rr = i - m * (R * 16);
-        const int r = tile_lo * 16 + rr;
-        if (r < N) atomicAdd(yv + (size_t)m * N + r, row_value(rr >> 4, rr & 15, m));
-    }
+    for (int m = 0; m < M; ++m)
+        for (int rr = threadIdx.x; rr < nr; rr += kThreads) {
+            const int r = tile_lo * 16 + rr;
+            if (r < N) atomicAdd(yv + (size_t)m * N + r, row_value(rr >> 4, rr & 15, m));
+        }
 }
 
 // Rotation prologue for the fused path: x' = H_4096 (s (.) x) / 64 in fp32,
@@ -974,6 +975,312 @@ rotate_stage_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restric
 }
 
 // ---------------------------------------------------------------------------
+// The product for 2 to 16 tokens, tile-major (2-bit codes, K a multiple of 512).
+//
+// Above, with several tokens every (tile, group) unit writes M partial row
+// sums per row to shared memory (with shared atomics past four tokens) and
+// eight warps' partials are summed at the end; that bookkeeping grows with M
+// while the MMAs do not.  Here a warp owns whole 16-row tiles and walks the
+// CTA's K-slice over them, four groups (one 2 KB stage of codes and the
+// tile's 16 x 4 scales) at a time, keeping each tile's 16 x M sums in
+// registers, so each output is written once.  The slice's staged activation
+// is computed once per CTA into shared memory, in the lanes' B-fragment order
+// (the same fp16 x 2^(E + 10 - 2j') values as above), with the all-ones
+// correction of each (group, token tile) and the tokens' F beside it.  The
+// MMA of a unit and of the ones pass compute each output from the same A row
+// and B column in the same order, so a row of zero weights gives exactly 0.
+// ---------------------------------------------------------------------------
+constexpr int kTQuad = 4;                                      // groups per stage
+constexpr int kTDepth = 4;                                     // stages in flight per warp (a power of 2)
+constexpr int kTCodeBytes = kTQuad * kSlotBytes;               // one stage's codes: four 16 x 32-byte units
+constexpr int kTStageBytes = kTCodeBytes + 16 * kTQuad * 2;    // and the tile's 16 x 4 scales
+constexpr int kTRingBytes = kWarps * kTDepth * kTStageBytes;
+constexpr int kTFragBytes = 4 * 32 * 16;                       // one (group, token tile): [4][32 lanes][16 B]
+constexpr int kTCorrBytes = 4 * 16;                            // (F, F acc1) of tokens 2t, 2t + 1: [4 t][float4]
+constexpr int kTCtasPerSm = 2;
+// From five tokens on (where the product above turns to shared atomics) the
+// tile-major loop is the faster one; below it, the product above.
+constexpr int kTileMinM = 5;
+
+// One unit's chain, slot j's MMA after slot j - 1's in one accumulator.
+__device__ __forceinline__ void unit_chain(float (&acc)[4], const uint32_t (&w)[4], const uint32_t (&b)[16]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t r[4];
+        slot_regs<false>(j, w[0], w[1], w[2], w[3], r);
+        mma16816(acc, r[0], r[1], r[2], r[3], b[2 * j], b[2 * j + 1], j > 0);
+    }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const GemvArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int M = a.M, G = a.G, S = a.S;
+    const int W = a.K / 16;   // code words per row
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, t = lane & 3;
+    const int sigma = blockIdx.x / a.cps, clu = blockIdx.x - sigma * a.cps;   // slice, range
+    const bool second = clu >= a.cps1;
+    const uint32_t* const codes = second ? a.codes2 : a.codes;
+    const __half* const scales = second ? a.scales2 : a.scales;
+    float* const yv = second ? a.y2 : a.y;
+    const int N = second ? a.N2 : a.N;
+    const int Tm = second ? a.T2 : a.T;
+    const int cpsm = second ? a.cps - a.cps1 : a.cps1;
+    const int clm = second ? clu - a.cps1 : clu;
+    // slice sigma: quads [qA, qA + nq) of the row's G / 4
+    const int Gq = G / kTQuad;
+    const int qA = (int)((long long)Gq * sigma / S);
+    const int nq = (int)((long long)Gq * (sigma + 1) / S) - qA;
+    const int gA = kTQuad * qA, Gs = kTQuad * nq;
+    // the range's tiles; warp w takes tiles w, w + 8, ... of it
+    const int tile_lo = (int)((long long)Tm * clm / cpsm);
+    const int R = (int)((long long)Tm * (clm + 1) / cpsm) - tile_lo;
+    const int n_items = warp < R ? (R - 1 - warp) / kWarps + 1 : 0;
+    const int n_st = n_items * nq;
+
+    unsigned char* const ring = smem + (size_t)warp * kTDepth * kTStageBytes;
+    unsigned char* const frag = smem + kTRingBytes;                                  // [Gs][MT][4][32][16 B]
+    unsigned char* const corr = frag + (size_t)Gs * MT * kTFragBytes;                // [Gs][MT][4][float4]
+
+    // ---- this warp's copies: stage s is quad s % nq of item s / nq.  Lane l
+    // copies 16-byte piece kk = l % 8 of the four groups' 128 bytes of rows
+    // l / 8 + 4 k (k = 0..3), and lanes 0-15 the 8 bytes of scales of row l.
+    // Rows past N read row N - 1; their sums are never written. ----
+    const int kk = lane & 7, r0 = lane >> 3;
+    const uint32_t ring_s = smem_addr(ring);
+    const uint32_t dst_c = (uint32_t)((kk >> 1) * kSlotBytes + r0 * 32 + (kk & 1) * 16);
+    const uint32_t dst_s = (uint32_t)(kTCodeBytes + (lane & 15) * 8);
+    const uint32_t* src_c[4];
+    const __half* src_s = scales;
+    int i_item = 0, i_q = 0, issued = 0;
+    auto item_src = [&](int it) {
+        const int row0 = (tile_lo + warp + kWarps * it) * 16;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            src_c[k] = codes + (size_t)min(row0 + r0 + 4 * k, N - 1) * W + (size_t)gA * 8 + kk * 4;
+        src_s = scales + (size_t)min(row0 + (lane & 15), N - 1) * G + gA;
+    };
+#pragma unroll
+    for (int k = 0; k < 4; ++k) src_c[k] = codes;
+    if (n_items > 0) item_src(0);
+    auto issue = [&](int slot) {
+        if (issued < n_st) {
+            const uint32_t base = ring_s + (uint32_t)(slot * kTStageBytes);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                cp_async16(base + dst_c + 128u * k, src_c[k], true);
+                src_c[k] += kTQuad * 8;
+            }
+            if (lane < 16) cp_async8(base + dst_s, src_s);
+            src_s += kTQuad;
+            ++issued;
+            if (++i_q == nq) {
+                i_q = 0;
+                if (++i_item < n_items) item_src(i_item);
+            }
+        }
+        cp_async_commit();   // one group per stage, empty past the end, so the waits count uniformly
+    };
+
+    pdl_launch_dependents();
+    // codes and scales are never the previous kernel's output: the first
+    // stages go out before the PDL wait
+#pragma unroll
+    for (int i = 0; i < kTDepth; ++i) issue(i);
+    pdl_wait();
+
+    // ---- several slices: the slice-0 CTA clears the range's rows of y (each
+    // warp the rows of its own tiles) and counts itself into the range's flag
+    // once every warp's zeros are visible; a CTA of another slice adds only
+    // after its warps have seen the flag non-zero, and counts itself once all
+    // of them have; the S-th count returns the flag to 0. ----
+    __shared__ unsigned cleared_warps, seen_warps;
+    const bool clearer = S > 1 && sigma == 0;
+    const bool adder = S > 1 && sigma != 0;
+    if (threadIdx.x == 0) {
+        cleared_warps = 0u;
+        seen_warps = 0u;
+    }
+    if (clearer)
+        for (int it = 0; it < n_items; ++it) {
+            const int row0 = (tile_lo + warp + kWarps * it) * 16;
+            for (int i = lane; i < 16 * M; i += 32) {
+                const int m = i >> 4, r = row0 + (i & 15);
+                if (r < N) yv[(size_t)m * N + r] = 0.0f;
+            }
+        }
+
+    // ---- stage the slice's activation: item (g, nt) of the Gs x MT, warp w
+    // taking items w, w + 8, ...; lane (gid, t) holds token 8 nt + gid,
+    // values 32 t .. 32 t + 31 of group gA + g, exactly as the product above
+    // stages a group ----
+    {
+        const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(a.x);
+        for (int item = warp; item < Gs * MT; item += kWarps) {
+            const int g = item / MT, nt = item - g * MT;
+            const int m = nt * 8 + gid;
+            float v[32];
+            if (m < M) {
+                const uint4* s4 =
+                    reinterpret_cast<const uint4*>(x + (size_t)m * a.K + (size_t)(gA + g) * kGroup + 32 * t);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 u = s4[q];
+                    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        v[8 * q + 2 * e] = __uint_as_float(uw[e] << 16);
+                        v[8 * q + 2 * e + 1] = __uint_as_float(uw[e] & 0xFFFF0000u);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+            }
+            float mx = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(v[e]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            check_stage_range(mx);
+            const int E = stage_exponent(mx);
+            uint32_t b[16];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float c = stage_multiplier(E, j);
+                const __half2 lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);        // k = 32t+j, +8
+                const __half2 hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c);  // k = 32t+16+j, +24
+                b[2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
+                b[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
+            unsigned char* fp = frag + (size_t)item * kTFragBytes + lane * 16;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(fp + q * 512) = make_uint4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+            // the all-ones pass: column n is token 8 nt + n; lane (., t) holds
+            // tokens 2t and 2t + 1, whose F the lanes of rows 2t and 2t + 1 hold
+            float acc1[4];
+            const uint32_t ones[4] = {0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u};
+            unit_chain(acc1, ones, b);
+            const float F = __uint_as_float((uint32_t)(14 - E + 127) << 23);   // 2^(14-E)
+            const float F0 = __shfl_sync(0xffffffffu, F, (2 * t) * 4);
+            const float F1 = __shfl_sync(0xffffffffu, F, (2 * t + 1) * 4);
+            if (gid == 0)
+                *reinterpret_cast<float4*>(corr + ((size_t)item * 4 + t) * 16) =
+                    make_float4(F0, F0 * acc1[0], F1, F1 * acc1[1]);
+        }
+    }
+    __syncthreads();
+
+    // a slice-0 warp: its clearing stores are visible; the eighth to say so
+    // counts the range's clearing into the flag
+    auto count_cleared = [&]() {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0 && atomicAdd(&cleared_warps, 1u) == (unsigned)(kWarps - 1))
+            red_inc(a.flag + clu, (unsigned)(S - 1));
+    };
+    auto count_seen = [&]() {
+        if (lane == 0 && atomicAdd(&seen_warps, 1u) == (unsigned)(kWarps - 1))
+            red_inc(a.flag + clu, (unsigned)(S - 1));
+    };
+    if (clearer && n_st == 0) count_cleared();
+    if (adder && n_st == 0) count_seen();   // a warp with tiles counts once it has seen the flag
+
+    // ---- the stages ----
+    const unsigned char* const rd = ring + gid * 32 + 8 * t;   // this lane's words of row gid in a stage's unit 0
+    unsigned flag_seen = 0u;
+    bool add_ok = true;
+    int s = 0;
+    for (int it = 0; it < n_items; ++it) {
+        // rows gid and gid + 8 of the tile, tokens 8 nt + 2t and 8 nt + 2t + 1
+        float y[MT][4];
+#pragma unroll
+        for (int nt = 0; nt < MT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) y[nt][e] = 0.0f;
+        for (int q = 0; q < nq; ++q, ++s) {
+            const int slot = s & (kTDepth - 1);
+            // stage s has landed (at most kTDepth - 1 newer groups pending)
+            cp_async_wait<kTDepth - 1>();
+            __syncwarp();
+            const unsigned char* st = rd + slot * kTStageBytes;
+            const unsigned char* scp = ring + slot * kTStageBytes + kTCodeBytes;
+            const uint2 sc0 = *reinterpret_cast<const uint2*>(scp + gid * 8);
+            const uint2 sc1 = *reinterpret_cast<const uint2*>(scp + (gid + 8) * 8);
+            const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sc0.x));
+            const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sc0.y));
+            const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&sc1.x));
+            const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&sc1.y));
+            const float s0[4] = {s01.x, s01.y, s23.x, s23.y};
+            const float s1[4] = {r01.x, r01.y, r23.x, r23.y};
+#pragma unroll
+            for (int u = 0; u < kTQuad; ++u) {
+                const uint2 v0 = *reinterpret_cast<const uint2*>(st + u * kSlotBytes);
+                const uint2 v1 = *reinterpret_cast<const uint2*>(st + u * kSlotBytes + 8 * 32);
+                // row gid word 2t, row gid + 8 word 2t, then words 2t + 1
+                const uint32_t w[4] = {v0.x, v1.x, v0.y, v1.y};
+                const int gl = kTQuad * q + u;
+#pragma unroll
+                for (int nt = 0; nt < MT; ++nt) {
+                    const unsigned char* fp = frag + (size_t)(gl * MT + nt) * kTFragBytes + lane * 16;
+                    uint32_t b[16];
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const uint4 z = *reinterpret_cast<const uint4*>(fp + qq * 512);
+                        b[4 * qq] = z.x;
+                        b[4 * qq + 1] = z.y;
+                        b[4 * qq + 2] = z.z;
+                        b[4 * qq + 3] = z.w;
+                    }
+                    float acc[4];
+                    unit_chain(acc, w, b);
+                    const float4 f = *reinterpret_cast<const float4*>(corr + ((size_t)(gl * MT + nt) * 4 + t) * 16);
+                    y[nt][0] = fmaf(s0[u], fmaf(f.x, acc[0], -f.y), y[nt][0]);   // row gid,     token 2t
+                    y[nt][1] = fmaf(s0[u], fmaf(f.z, acc[1], -f.w), y[nt][1]);   // row gid,     token 2t+1
+                    y[nt][2] = fmaf(s1[u], fmaf(f.x, acc[2], -f.y), y[nt][2]);   // row gid + 8, token 2t
+                    y[nt][3] = fmaf(s1[u], fmaf(f.z, acc[3], -f.w), y[nt][3]);   // row gid + 8, token 2t+1
+                }
+            }
+            // the stage is fully read by every lane: refill it kTDepth stages ahead
+            __syncwarp();
+            issue(slot);
+            if (s == 0) {
+                if (clearer) count_cleared();
+                // read ahead, so the load overlaps the loop
+                if (adder && lane == 0) flag_seen = ld_acquire_gpu(a.flag + clu);
+            }
+        }
+        // the tile's sums
+        const int row = (tile_lo + warp + kWarps * it) * 16 + gid;
+        if (adder && it == 0) {
+            int ok = 1;
+            if (lane == 0) {
+                ok = flag_seen != 0u || wait_flag_nonzero(a.flag + clu, kFlagWaitNs);
+                if (!ok) report_device_error(&g_gemv_error, kDevErrGemvConsumerWait);
+            }
+            add_ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+            if (add_ok) count_seen();
+        }
+        if (add_ok) {
+#pragma unroll
+            for (int nt = 0; nt < MT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = nt * 8 + 2 * t + (e & 1), r = row + 8 * (e >> 1);
+                    if (m < M && r < N) {
+                        float* p = yv + (size_t)m * N + r;
+                        if (S == 1) *p = y[nt][e];
+                        else atomicAdd(p, y[nt][e]);
+                    }
+                }
+        }
+    }
+    cp_async_wait<0>();
+}
+
+// ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
 struct Plan {
@@ -987,19 +1294,24 @@ struct Plan {
 };
 
 // Shared-memory layout for `cps` ranges (ring | scales | biases (AFF) | partials).
-void layout(Plan& p, int M, int cps) {
-    p.cps = cps;
-    if (p.T2 > 0) {
-        // a pair call: the ranges are shared out in proportion to the tiles,
-        // at least one each, so no range straddles the two matrices
-        const int T1 = p.T - p.T2;
-        p.cps = cps = std::max(cps, 2);
-        p.cps1 = std::min(cps - 1, std::max(1, (int)(((long long)cps * T1 + p.T / 2) / p.T)));
-        p.rmax = std::max((T1 + p.cps1 - 1) / p.cps1, (p.T2 + cps - p.cps1 - 1) / (cps - p.cps1));
-    } else {
-        p.cps1 = cps;
-        p.rmax = (p.T + cps - 1) / cps;
+// `cps` ranges over T tiles (the last T2 of them a pair call's second matrix):
+// returns the longest range, sets the first matrix's range count.  A pair
+// call's ranges are shared out in proportion to the tiles, at least one each,
+// so no range straddles the two matrices.
+int split_ranges(int T, int T2, int& cps, int& cps1) {
+    if (T2 > 0) {
+        const int T1 = T - T2;
+        cps = std::max(cps, 2);
+        cps1 = std::min(cps - 1, std::max(1, (int)(((long long)cps * T1 + T / 2) / T)));
+        return std::max((T1 + cps1 - 1) / cps1, (T2 + cps - cps1 - 1) / (cps - cps1));
     }
+    cps1 = cps;
+    return (T + cps - 1) / cps;
+}
+
+void layout(Plan& p, int M, int cps) {
+    p.rmax = split_ranges(p.T, p.T2, cps, p.cps1);
+    p.cps = cps;
     const int MP = 8 * p.MT;
     size_t off = (size_t)kWarps * kDepth * p.slot;
     p.off_sc = (uint32_t)off;
@@ -1110,6 +1422,104 @@ tern_status cached_plan(int M, int N, int K, int N2, int sms, Plan* out) {
     g_plan_key[slot] = PlanKey{M, N, K, N2, dev, PRE, BIN, AFF, ROT};
     g_plan_val[slot] = *out;
     return TERN_OK;
+}
+
+// ---- the tile-major product for 2 to 16 tokens: slices of whole quads,
+// ranges of tiles, one wave of CTAs when it fits ----
+struct PlanT {
+    int S, cps, cps1, ctas;
+    size_t smem;
+};
+size_t smem_t(int Gs, int MT) { return (size_t)kTRingBytes + (size_t)Gs * MT * (kTFragBytes + kTCorrBytes); }
+
+// The slice count trades the longest warp's stages (a warp's tiles times the
+// slice's quads) against the extra CTAs and the additions into y that more
+// slices bring, within the shared memory the slice's staged activation
+// needs; the range flags exist only when K spans more than one 1024-wide
+// slice, so shorter K keeps one slice.
+template <int MT>
+tern_status make_plan_t(int N, int K, int N2, int sms, int dev, PlanT* out) {
+    static int optin_of[64] = {};
+    if (!optin_of[dev]) {
+        int optin = 0;
+        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return TERN_ERR_CUDA;
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, gemvt_kernel<MT>) != cudaSuccess) return TERN_ERR_CUDA;
+        optin -= (int)fa.sharedSizeBytes;
+        if (cudaFuncSetAttribute(gemvt_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+            cudaSuccess)
+            return TERN_ERR_CUDA;
+        optin_of[dev] = optin;
+    }
+    const int G = K / kGroup, Gq = G / kTQuad;
+    const int T2 = (N2 + 15) / 16, T = (N + 15) / 16 + T2;
+    double best = 0.0;
+    PlanT bp{};
+    for (int S = 1; S <= Gq && S <= 64; ++S) {
+        if (S > 1 && G <= kWarps) break;
+        const int qmax = (Gq + S - 1) / S;
+        const size_t sm = smem_t(kTQuad * qmax, MT);
+        if (sm > (size_t)optin_of[dev]) continue;
+        const int per_sm = std::min(kTCtasPerSm, (int)(kSmemPerSm / (sm + kCtaSmemReserve)));
+        if (per_sm < 1) continue;
+        const int slots = sms * per_sm;
+        int cps = std::max(1, std::min(T, slots / S)), cps1 = 0;
+        const int rmax = split_ranges(T, T2, cps, cps1);
+        const int items = (rmax + kWarps - 1) / kWarps;
+        const long long waves = ((long long)S * cps + slots - 1) / slots;
+        const double cost = (double)waves * (items * (qmax + 0.5) + 1.0 + (S > 1 ? 0.5 : 0.0));
+        if (bp.ctas == 0 || cost < best) {
+            best = cost;
+            bp = PlanT{S, cps, cps1, S * cps, sm};
+        }
+    }
+    if (bp.ctas == 0) return TERN_ERR_SHAPE;
+    *out = bp;
+    return TERN_OK;
+}
+
+struct PlanTKey {
+    int MT, N, K, N2, dev;
+};
+PlanTKey g_plant_key[kPlanCache];
+PlanT g_plant_val[kPlanCache];
+int g_plant_n = 0, g_plant_next = 0;
+
+template <int MT>
+tern_status cached_plan_t(int N, int K, int N2, int sms, PlanT* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TERN_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return TERN_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    for (int i = 0; i < g_plant_n; ++i) {
+        const PlanTKey& k = g_plant_key[i];
+        if (k.MT == MT && k.N == N && k.K == K && k.N2 == N2 && k.dev == dev) {
+            *out = g_plant_val[i];
+            return TERN_OK;
+        }
+    }
+    const tern_status st = make_plan_t<MT>(N, K, N2, sms, dev, out);
+    if (st != TERN_OK) return st;
+    const int slot = g_plant_n < kPlanCache ? g_plant_n++ : (g_plant_next++ % kPlanCache);
+    g_plant_key[slot] = PlanTKey{MT, N, K, N2, dev};
+    g_plant_val[slot] = *out;
+    return TERN_OK;
+}
+
+template <int MT>
+tern_status launch_gemv_t(GemvArgs args, int sms, cudaStream_t stream) {
+    PlanT p;
+    const tern_status st = cached_plan_t<MT>(args.N, args.K, args.N2, sms, &p);
+    if (st != TERN_OK) return st;
+    args.G = args.K / kGroup;
+    args.T = (args.N + 15) / 16;
+    args.T2 = (args.N2 + 15) / 16;
+    args.S = p.S;
+    args.cps = p.cps;
+    args.cps1 = p.cps1;
+    const cudaError_t e = launch_pdl(gemvt_kernel<MT>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, args);
+    return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
 
 tern_status validate(const void* x, const uint32_t* codes, const void* scales, const float* y, int M, int N, int K) {
@@ -1227,6 +1637,8 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
         st = M == 1 ? launch_gemv<1, false, true, true, true>(args, sms, stream)
              : MT == 1 ? launch_gemv<1, false, false, true, true>(args, sms, stream)
                        : launch_gemv<2, false, false, true, true>(args, sms, stream);
+    } else if (M >= kTileMinM && K % (kTQuad * kGroup) == 0) {
+        st = MT == 1 ? launch_gemv_t<1>(args, sms, stream) : launch_gemv_t<2>(args, sms, stream);
     } else {
         st = M == 1 ? (lean ? launch_gemv<1, false, true, true>(args, sms, stream)
                             : launch_gemv<1, false, true>(args, sms, stream))

@@ -91,6 +91,44 @@ def test_gemv_ragged_shapes(tern, orc, M, N, K):
     assert_fp32_close(y, y_ref, a_ref, what=f"M={M} N={N} K={K}")
 
 
+@pytest.mark.parametrize("M", [5, 8, 9, 16])
+@pytest.mark.parametrize("N,K", [(37, 512), (300, 1536), (1000, 3072), (129, 17408)])
+def test_gemv_tile_major_shapes(tern, orc, M, N, K):
+    """Five tokens and more with K a multiple of 512 (the tile-major loop):
+    ragged N, one K-slice and several, every output against the oracle."""
+    p = synth.problem(120 + M, M, N, K, tag=f"tm{N}x{K}")
+    y, _ = run_gemv(tern, p)
+    assert tern.device_error() == 0
+    y_ref, a_ref = orc.matmul(p.x, orc.pack(p.t)[0], p.s)
+    assert_fp32_close(y, y_ref, a_ref, what=f"tile-major M={M} N={N} K={K}")
+
+
+def test_gemv_tile_major_exact(tern, orc):
+    """The tile-major loop on inputs with exact answers: zero trits give 0
+    (the all-ones correction cancels bit for bit), and x = 2 at one position
+    with trits +-1 gives 2 s exactly, for every position of a 512-wide row."""
+    N, K, M = 16, 512, 16
+    s = synth.scales(6, "tme", (N, K // 128), synth.SCALE_UNIFORM)
+    x = synth.activations(6, "tmx", (M, 1536))
+    z = tern.gemv(dev_bf16(x), tern.pack(dev_trits(np.zeros((N, 1536), dtype=np.int8))),
+                  dev_scales(synth.scales(6, "tmz", (N, 12))))
+    torch.cuda.synchronize()
+    assert (z.cpu().numpy() == 0).all()
+    t = np.ones((N, K), dtype=np.int8)
+    t[1::2] = -1
+    t[:, 300:310] *= -1
+    codes = tern.pack(dev_trits(t))
+    for k0 in range(0, K, M):
+        xe = np.zeros((M, K), dtype=np.uint16)
+        for i in range(M):
+            xe[i, k0 + i] = 0x4000                          # bf16 2.0
+        y = tern.gemv(dev_bf16(xe), codes, dev_scales(s)).cpu().numpy()
+        for i in range(M):
+            k = k0 + i
+            want = 2.0 * t[:, k].astype(np.float64) * s[:, k // 128].astype(np.float64)
+            assert np.array_equal(y[i].astype(np.float64), want), k
+
+
 def test_gemv_exact_cases(tern, orc):
     """Cases with an exact answer: all-zero trits give 0; one-hot x gives the
     column of W exactly (one nonzero product per output)."""
@@ -285,7 +323,7 @@ def test_fwht_gemm_full_size_sampled(tern, orc, M):
     assert_fp32_close(y.cpu().numpy()[:, rows], y_ref, a_ref, what=f"rot full M={M}")
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 300, 512), (1, 1000, 5120), (3, 777, 17408), (6, 129, 2176)])
+@pytest.mark.parametrize("M,N,K", [(1, 300, 512), (1, 1000, 5120), (3, 777, 17408), (6, 129, 2176), (9, 129, 2560)])
 def test_gemv_overwrites_prefilled_y(tern, orc, M, N, K):
     """y holding NaN before the call is fully overwritten, for one K-slice and
     for several (whose sums are added into a y the kernel clears first)."""
@@ -346,7 +384,8 @@ def test_scales_from_g64_device(tern, orc):
 
 
 @pytest.mark.parametrize("M,Na,Nb,K", [(1, 17408, 17408, 5120), (1, 300, 5000, 2048), (3, 777, 129, 17408),
-                                       (16, 64, 48, 1024), (5, 1000, 1000, 640), (1, 16, 16, 128)])
+                                       (16, 64, 48, 1024), (5, 1000, 1000, 640), (1, 16, 16, 128),
+                                       (8, 777, 300, 5120), (13, 33, 1000, 2560)])
 def test_gemv_pair_matches_two_products(tern, orc, M, Na, Nb, K):
     """Two matrices read with one activation in one launch: each output against
     the oracle, ragged row counts, one and several K-slices, twice on the same
