@@ -849,7 +849,8 @@ def run_reference(args) -> None:
 
 # Single cases for profiler captures: each runs its launch 3 times unprofiled
 # (warm-up) and then 2 more, with synthetic inputs of the bench's shapes.
-PROFILE_CASES = ("fwht_bw", "fused_m1", "fused_m16", "gemm_down", "gemm_qkv", "gemv_m1", "gemv_m8", "gemv_m16", "f3_m1")
+PROFILE_CASES = ("fwht_bw", "fused_m1", "fused_m16", "separate_m16", "gemm_down", "gemm_qkv", "gemv_m1", "gemv_m8",
+                 "gemv_m16", "f3_m1")
 
 
 def run_profile_case(name: str) -> None:
@@ -865,7 +866,7 @@ def run_profile_case(name: str) -> None:
         sg = synth.device_signs(5, "PB.s", K4)
         y = torch.empty_like(x)
         fn = lambda: tern.fwht(x, sg, y=y)
-    elif name in ("fused_m1", "fused_m16"):
+    elif name in ("fused_m1", "fused_m16", "separate_m16"):
         M = 1 if name == "fused_m1" else 16
         c = tern.pack(synth.device_trits(6, "PF.t", (N4, K4)))
         sc = synth.device_scales(6, "PF.sc", (N4, K4 // 128))
@@ -873,7 +874,11 @@ def run_profile_case(name: str) -> None:
         sg = synth.device_signs(6, "PF.s", K4)
         y = torch.empty((M, N4), dtype=torch.float32, device="cuda")
         ws = tern.workspace(tern.gemv_workspace_bytes(M, N4, K4))
-        fn = lambda: tern.fwht_gemm(x, sg, c, sc, y=y, ws=ws)
+        if name == "separate_m16":
+            xr = torch.empty_like(x)
+            fn = lambda: (tern.fwht(x, sg, y=xr), tern.gemv(xr, c, sc, y=y, ws=ws))
+        else:
+            fn = lambda: tern.fwht_gemm(x, sg, c, sc, y=y, ws=ws)
     elif name in ("gemm_down", "gemm_qkv"):
         K, N = (17408, 5120) if name == "gemm_down" else (5120, 6144)
         M = 512

@@ -998,6 +998,9 @@ constexpr int kTRingBytes = kWarps * kTDepth * kTStageBytes;
 constexpr int kTFragBytes = 4 * 32 * 16;                       // one (group, token tile): [4][32 lanes][16 B]
 constexpr int kTCorrBytes = 4 * 16;                            // (F, F acc1) of tokens 2t, 2t + 1: [4 t][float4]
 constexpr int kTCtasPerSm = 2;
+// staging items per warp whose loads go out together (one token tile; with
+// two, the extra registers spill)
+template <int MT> struct TStage { static constexpr int kBatch = MT == 1 ? 3 : 1; };
 // From five tokens on (where the product above turns to shared atomics) the
 // tile-major loop is the faster one; below it, the product above.
 constexpr int kTileMinM = 5;
@@ -1012,7 +1015,9 @@ __device__ __forceinline__ void unit_chain(float (&acc)[4], const uint32_t (&w)[
     }
 }
 
-template <int MT>
+// PRE: the activation comes staged by the rotation prologue (fragments and
+// exponents in the workspace), as for the product above.
+template <int MT, bool PRE>
 __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int M = a.M, G = a.G, S = a.S;
@@ -1116,27 +1121,58 @@ __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const Gemv
     // values 32 t .. 32 t + 31 of group gA + g, exactly as the product above
     // stages a group ----
     {
+        // a warp's items go kBatch at a time, their loads issued
+        // together so that one round trip serves them all
         const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(a.x);
-        for (int item = warp; item < Gs * MT; item += kWarps) {
+        const int n_items_x = Gs * MT;
+        for (int base = warp; base < n_items_x; base += kWarps * TStage<MT>::kBatch) {
+        uint4 raw[TStage<MT>::kBatch][4];
+        int raw_e[TStage<MT>::kBatch];
+#pragma unroll
+        for (int j = 0; j < TStage<MT>::kBatch; ++j) {
+            const int item = base + j * kWarps;
             const int g = item / MT, nt = item - g * MT;
             const int m = nt * 8 + gid;
-            float v[32];
-            if (m < M) {
+            raw_e[j] = 0;
+            if (PRE && item < n_items_x && m < M) raw_e[j] = a.xe[m * G + gA + g];
+            if (item < n_items_x && m < M) {
                 const uint4* s4 =
-                    reinterpret_cast<const uint4*>(x + (size_t)m * a.K + (size_t)(gA + g) * kGroup + 32 * t);
+                    PRE ? reinterpret_cast<const uint4*>(reinterpret_cast<const uint32_t*>(a.x) +
+                                                         ((size_t)(m * G + gA + g) * 4 + t) * 16)
+                        : reinterpret_cast<const uint4*>(x + (size_t)m * a.K + (size_t)(gA + g) * kGroup + 32 * t);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 u = s4[q];
-                    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        v[8 * q + 2 * e] = __uint_as_float(uw[e] << 16);
-                        v[8 * q + 2 * e + 1] = __uint_as_float(uw[e] & 0xFFFF0000u);
-                    }
-                }
+                for (int q = 0; q < 4; ++q) raw[j][q] = s4[q];
             } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+                for (int q = 0; q < 4; ++q) raw[j][q] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < TStage<MT>::kBatch; ++j) {
+            const int item = base + j * kWarps;
+            if (item >= n_items_x) break;
+            int E = 0;
+            uint32_t b[16];
+            if (PRE) {
+                // the fragments and exponent as the rotation prologue staged them
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    b[4 * q] = raw[j][q].x;
+                    b[4 * q + 1] = raw[j][q].y;
+                    b[4 * q + 2] = raw[j][q].z;
+                    b[4 * q + 3] = raw[j][q].w;
+                }
+                E = raw_e[j];
+            } else {
+            float v[32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t uw[4] = {raw[j][q].x, raw[j][q].y, raw[j][q].z, raw[j][q].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    v[8 * q + 2 * e] = __uint_as_float(uw[e] << 16);
+                    v[8 * q + 2 * e + 1] = __uint_as_float(uw[e] & 0xFFFF0000u);
+                }
             }
             float mx = 0.0f;
 #pragma unroll
@@ -1144,8 +1180,7 @@ __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const Gemv
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
             check_stage_range(mx);
-            const int E = stage_exponent(mx);
-            uint32_t b[16];
+            E = stage_exponent(mx);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const float c = stage_multiplier(E, j);
@@ -1153,6 +1188,7 @@ __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const Gemv
                 const __half2 hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c);  // k = 32t+16+j, +24
                 b[2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
                 b[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
             }
             unsigned char* fp = frag + (size_t)item * kTFragBytes + lane * 16;
 #pragma unroll
@@ -1169,6 +1205,7 @@ __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const Gemv
             if (gid == 0)
                 *reinterpret_cast<float4*>(corr + ((size_t)item * 4 + t) * 16) =
                     make_float4(F0, F0 * acc1[0], F1, F1 * acc1[1]);
+        }
         }
     }
     __syncthreads();
@@ -1437,7 +1474,7 @@ size_t smem_t(int Gs, int MT) { return (size_t)kTRingBytes + (size_t)Gs * MT * (
 // slices bring, within the shared memory the slice's staged activation
 // needs; the range flags exist only when K spans more than one 1024-wide
 // slice, so shorter K keeps one slice.
-template <int MT>
+template <int MT, bool PRE>
 tern_status make_plan_t(int N, int K, int N2, int sms, int dev, PlanT* out) {
     static int optin_of[64] = {};
     if (!optin_of[dev]) {
@@ -1445,9 +1482,9 @@ tern_status make_plan_t(int N, int K, int N2, int sms, int dev, PlanT* out) {
         if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return TERN_ERR_CUDA;
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, gemvt_kernel<MT>) != cudaSuccess) return TERN_ERR_CUDA;
+        if (cudaFuncGetAttributes(&fa, gemvt_kernel<MT, PRE>) != cudaSuccess) return TERN_ERR_CUDA;
         optin -= (int)fa.sharedSizeBytes;
-        if (cudaFuncSetAttribute(gemvt_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+        if (cudaFuncSetAttribute(gemvt_kernel<MT, PRE>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
             cudaSuccess)
             return TERN_ERR_CUDA;
         optin_of[dev] = optin;
@@ -1481,12 +1518,13 @@ tern_status make_plan_t(int N, int K, int N2, int sms, int dev, PlanT* out) {
 
 struct PlanTKey {
     int MT, N, K, N2, dev;
+    bool pre;
 };
 PlanTKey g_plant_key[kPlanCache];
 PlanT g_plant_val[kPlanCache];
 int g_plant_n = 0, g_plant_next = 0;
 
-template <int MT>
+template <int MT, bool PRE>
 tern_status cached_plan_t(int N, int K, int N2, int sms, PlanT* out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TERN_ERR_CUDA;
@@ -1494,23 +1532,23 @@ tern_status cached_plan_t(int N, int K, int N2, int sms, PlanT* out) {
     std::lock_guard<std::mutex> lk(g_plan_mu);
     for (int i = 0; i < g_plant_n; ++i) {
         const PlanTKey& k = g_plant_key[i];
-        if (k.MT == MT && k.N == N && k.K == K && k.N2 == N2 && k.dev == dev) {
+        if (k.MT == MT && k.N == N && k.K == K && k.N2 == N2 && k.dev == dev && k.pre == PRE) {
             *out = g_plant_val[i];
             return TERN_OK;
         }
     }
-    const tern_status st = make_plan_t<MT>(N, K, N2, sms, dev, out);
+    const tern_status st = make_plan_t<MT, PRE>(N, K, N2, sms, dev, out);
     if (st != TERN_OK) return st;
     const int slot = g_plant_n < kPlanCache ? g_plant_n++ : (g_plant_next++ % kPlanCache);
-    g_plant_key[slot] = PlanTKey{MT, N, K, N2, dev};
+    g_plant_key[slot] = PlanTKey{MT, N, K, N2, dev, PRE};
     g_plant_val[slot] = *out;
     return TERN_OK;
 }
 
-template <int MT>
+template <int MT, bool PRE = false>
 tern_status launch_gemv_t(GemvArgs args, int sms, cudaStream_t stream) {
     PlanT p;
-    const tern_status st = cached_plan_t<MT>(args.N, args.K, args.N2, sms, &p);
+    const tern_status st = cached_plan_t<MT, PRE>(args.N, args.K, args.N2, sms, &p);
     if (st != TERN_OK) return st;
     args.G = args.K / kGroup;
     args.T = (args.N + 15) / 16;
@@ -1518,7 +1556,8 @@ tern_status launch_gemv_t(GemvArgs args, int sms, cudaStream_t stream) {
     args.S = p.S;
     args.cps = p.cps;
     args.cps1 = p.cps1;
-    const cudaError_t e = launch_pdl(gemvt_kernel<MT>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, args);
+    const cudaError_t e =
+        launch_pdl(gemvt_kernel<MT, PRE>, dim3(p.ctas), dim3(kThreads), p.smem, stream, true, args);
     return e == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
 
@@ -1623,8 +1662,11 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
         args.x = xs;
         args.xe = xe;
         launches = 2;
-        st = MT == 1 ? launch_gemv<1, true, false, true>(args, sms, stream)
-                     : launch_gemv<2, true, false, true>(args, sms, stream);
+        if (M >= kTileMinM)
+            st = MT == 1 ? launch_gemv_t<1, true>(args, sms, stream) : launch_gemv_t<2, true>(args, sms, stream);
+        else
+            st = MT == 1 ? launch_gemv<1, true, false, true>(args, sms, stream)
+                         : launch_gemv<2, true, false, true>(args, sms, stream);
     } else if (biases) {
         st = M == 1 ? (lean ? launch_gemv<1, false, true, true, false, true>(args, sms, stream)
                             : launch_gemv<1, false, true, false, false, true>(args, sms, stream))
