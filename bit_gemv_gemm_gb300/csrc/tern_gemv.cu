@@ -1017,6 +1017,19 @@ __device__ __forceinline__ void unit_chain(float (&acc)[4], const uint32_t (&w)[
 
 // PRE: the activation comes staged by the rotation prologue (fragments and
 // exponents in the workspace), as for the product above.
+// A unit's chains for all MT token tiles, each slot unpacked once for all.
+template <int MT>
+__device__ __forceinline__ void unit_chains(float (&acc)[MT][4], const uint32_t (&w)[4], const uint32_t (&b)[MT][16]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t r[4];
+        slot_regs<false>(j, w[0], w[1], w[2], w[3], r);
+#pragma unroll
+        for (int nt = 0; nt < MT; ++nt)
+            mma16816(acc[nt], r[0], r[1], r[2], r[3], b[nt][2 * j], b[nt][2 * j + 1], j > 0);
+    }
+}
+
 template <int MT, bool PRE>
 __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -1259,25 +1272,28 @@ __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const Gemv
                 // row gid word 2t, row gid + 8 word 2t, then words 2t + 1
                 const uint32_t w[4] = {v0.x, v1.x, v0.y, v1.y};
                 const int gl = kTQuad * q + u;
+                uint32_t b[MT][16];
 #pragma unroll
                 for (int nt = 0; nt < MT; ++nt) {
                     const unsigned char* fp = frag + (size_t)(gl * MT + nt) * kTFragBytes + lane * 16;
-                    uint32_t b[16];
 #pragma unroll
                     for (int qq = 0; qq < 4; ++qq) {
                         const uint4 z = *reinterpret_cast<const uint4*>(fp + qq * 512);
-                        b[4 * qq] = z.x;
-                        b[4 * qq + 1] = z.y;
-                        b[4 * qq + 2] = z.z;
-                        b[4 * qq + 3] = z.w;
+                        b[nt][4 * qq] = z.x;
+                        b[nt][4 * qq + 1] = z.y;
+                        b[nt][4 * qq + 2] = z.z;
+                        b[nt][4 * qq + 3] = z.w;
                     }
-                    float acc[4];
-                    unit_chain(acc, w, b);
+                }
+                float acc[MT][4];
+                unit_chains<MT>(acc, w, b);
+#pragma unroll
+                for (int nt = 0; nt < MT; ++nt) {
                     const float4 f = *reinterpret_cast<const float4*>(corr + ((size_t)(gl * MT + nt) * 4 + t) * 16);
-                    y[nt][0] = fmaf(s0[u], fmaf(f.x, acc[0], -f.y), y[nt][0]);   // row gid,     token 2t
-                    y[nt][1] = fmaf(s0[u], fmaf(f.z, acc[1], -f.w), y[nt][1]);   // row gid,     token 2t+1
-                    y[nt][2] = fmaf(s1[u], fmaf(f.x, acc[2], -f.y), y[nt][2]);   // row gid + 8, token 2t
-                    y[nt][3] = fmaf(s1[u], fmaf(f.z, acc[3], -f.w), y[nt][3]);   // row gid + 8, token 2t+1
+                    y[nt][0] = fmaf(s0[u], fmaf(f.x, acc[nt][0], -f.y), y[nt][0]);   // row gid,     token 2t
+                    y[nt][1] = fmaf(s0[u], fmaf(f.z, acc[nt][1], -f.w), y[nt][1]);   // row gid,     token 2t+1
+                    y[nt][2] = fmaf(s1[u], fmaf(f.x, acc[nt][2], -f.y), y[nt][2]);   // row gid + 8, token 2t
+                    y[nt][3] = fmaf(s1[u], fmaf(f.z, acc[nt][3], -f.w), y[nt][3]);   // row gid + 8, token 2t+1
                 }
             }
             // the stage is fully read by every lane: refill it kTDepth stages ahead
