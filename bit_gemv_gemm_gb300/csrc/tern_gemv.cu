@@ -975,25 +975,26 @@ rotate_stage_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restric
 }
 
 // ---------------------------------------------------------------------------
-// The product for 2 to 16 tokens, tile-major (2-bit codes, K a multiple of 512).
+// The product for 5 to 16 tokens, tile-major (2-bit codes, K a multiple of 256).
 //
 // Above, with several tokens every (tile, group) unit writes M partial row
 // sums per row to shared memory (with shared atomics past four tokens) and
 // eight warps' partials are summed at the end; that bookkeeping grows with M
 // while the MMAs do not.  Here a warp owns whole 16-row tiles and walks the
-// CTA's K-slice over them, four groups (one 2 KB stage of codes and the
-// tile's 16 x 4 scales) at a time, keeping each tile's 16 x M sums in
-// registers, so each output is written once.  The slice's staged activation
+// CTA's K-slice over them, two tiles and two groups (one 2 KB stage of codes
+// and the tiles' 32 x 2 scales) at a time, keeping the tiles' 16 x M sums in
+// registers, so each output is written once; each group's staged activation
+// is read once for both tiles.  The slice's staged activation
 // is computed once per CTA into shared memory, in the lanes' B-fragment order
 // (the same fp16 x 2^(E + 10 - 2j') values as above), with the all-ones
 // correction of each (group, token tile) and the tokens' F beside it.  The
 // MMA of a unit and of the ones pass compute each output from the same A row
 // and B column in the same order, so a row of zero weights gives exactly 0.
 // ---------------------------------------------------------------------------
-constexpr int kTQuad = 4;                                      // groups per stage
+constexpr int kTDuo = 2;                                       // groups per stage
 constexpr int kTDepth = 4;                                     // stages in flight per warp (a power of 2)
-constexpr int kTCodeBytes = kTQuad * kSlotBytes;               // one stage's codes: four 16 x 32-byte units
-constexpr int kTStageBytes = kTCodeBytes + 16 * kTQuad * 2;    // and the tile's 16 x 4 scales
+constexpr int kTCodeBytes = 2 * kTDuo * kSlotBytes;            // one stage's codes: [group][tile] 16 x 32-byte units
+constexpr int kTStageBytes = kTCodeBytes + 32 * kTDuo * 2;     // and the two tiles' 32 x 2 scales
 constexpr int kTRingBytes = kWarps * kTDepth * kTStageBytes;
 constexpr int kTFragBytes = 4 * 32 * 16;                       // one (group, token tile): [4][32 lanes][16 B]
 constexpr int kTCorrBytes = 4 * 16;                            // (F, F acc1) of tokens 2t, 2t + 1: [4 t][float4]
@@ -1046,14 +1047,16 @@ __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const Gemv
     const int Tm = second ? a.T2 : a.T;
     const int cpsm = second ? a.cps - a.cps1 : a.cps1;
     const int clm = second ? clu - a.cps1 : clu;
-    // slice sigma: quads [qA, qA + nq) of the row's G / 4
-    const int Gq = G / kTQuad;
+    // slice sigma: duos [qA, qA + nq) of the row's G / 2 group pairs
+    const int Gq = G / kTDuo;
     const int qA = (int)((long long)Gq * sigma / S);
     const int nq = (int)((long long)Gq * (sigma + 1) / S) - qA;
-    const int gA = kTQuad * qA, Gs = kTQuad * nq;
-    // the range's tiles; warp w takes tiles w, w + 8, ... of it
-    const int tile_lo = (int)((long long)Tm * clm / cpsm);
-    const int R = (int)((long long)Tm * (clm + 1) / cpsm) - tile_lo;
+    const int gA = kTDuo * qA, Gs = kTDuo * nq;
+    // the range's tile pairs (tiles 2p and 2p + 1; a second tile past the
+    // matrix has rows past N); warp w takes pairs w, w + 8, ... of it
+    const int Pm = (Tm + 1) >> 1;
+    const int pair_lo = (int)((long long)Pm * clm / cpsm);
+    const int R = (int)((long long)Pm * (clm + 1) / cpsm) - pair_lo;
     const int n_items = warp < R ? (R - 1 - warp) / kWarps + 1 : 0;
     const int n_st = n_items * nq;
 
@@ -1061,37 +1064,37 @@ __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const Gemv
     unsigned char* const frag = smem + kTRingBytes;                                  // [Gs][MT][4][32][16 B]
     unsigned char* const corr = frag + (size_t)Gs * MT * kTFragBytes;                // [Gs][MT][4][float4]
 
-    // ---- this warp's copies: stage s is quad s % nq of item s / nq.  Lane l
-    // copies 16-byte piece kk = l % 8 of the four groups' 128 bytes of rows
-    // l / 8 + 4 k (k = 0..3), and lanes 0-15 the 8 bytes of scales of row l.
-    // Rows past N read row N - 1; their sums are never written. ----
-    const int kk = lane & 7, r0 = lane >> 3;
+    // ---- this warp's copies: stage s is duo s % nq of item s / nq.  Lane l
+    // copies 16-byte half l % 2 of row l / 2 of each (group, tile) unit, and
+    // the 4 bytes of scales of the pair's row l.  Rows past N read row N - 1;
+    // their sums are never written. ----
     const uint32_t ring_s = smem_addr(ring);
-    const uint32_t dst_c = (uint32_t)((kk >> 1) * kSlotBytes + r0 * 32 + (kk & 1) * 16);
-    const uint32_t dst_s = (uint32_t)(kTCodeBytes + (lane & 15) * 8);
-    const uint32_t* src_c[4];
+    const uint32_t dst_c = (uint32_t)((lane >> 1) * 32 + (lane & 1) * 16);
+    const uint32_t dst_s = (uint32_t)(kTCodeBytes + lane * 4);
+    const uint32_t* src_c[2];
     const __half* src_s = scales;
     int i_item = 0, i_q = 0, issued = 0;
     auto item_src = [&](int it) {
-        const int row0 = (tile_lo + warp + kWarps * it) * 16;
+        const int row0 = (pair_lo + warp + kWarps * it) * 32;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            src_c[k] = codes + (size_t)min(row0 + r0 + 4 * k, N - 1) * W + (size_t)gA * 8 + kk * 4;
-        src_s = scales + (size_t)min(row0 + (lane & 15), N - 1) * G + gA;
+        for (int tau = 0; tau < 2; ++tau)
+            src_c[tau] = codes + (size_t)min(row0 + 16 * tau + (lane >> 1), N - 1) * W + (size_t)gA * 8 + (lane & 1) * 4;
+        src_s = scales + (size_t)min(row0 + lane, N - 1) * G + gA;
     };
-#pragma unroll
-    for (int k = 0; k < 4; ++k) src_c[k] = codes;
+    src_c[0] = src_c[1] = codes;
     if (n_items > 0) item_src(0);
     auto issue = [&](int slot) {
         if (issued < n_st) {
             const uint32_t base = ring_s + (uint32_t)(slot * kTStageBytes);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                cp_async16(base + dst_c + 128u * k, src_c[k], true);
-                src_c[k] += kTQuad * 8;
-            }
-            if (lane < 16) cp_async8(base + dst_s, src_s);
-            src_s += kTQuad;
+            for (int g = 0; g < kTDuo; ++g)
+#pragma unroll
+                for (int tau = 0; tau < 2; ++tau)
+                    cp_async16(base + (uint32_t)((2 * g + tau) * kSlotBytes) + dst_c, src_c[tau] + 8 * g, true);
+            src_c[0] += kTDuo * 8;
+            src_c[1] += kTDuo * 8;
+            cp_async4(base + dst_s, src_s, true);
+            src_s += kTDuo;
             ++issued;
             if (++i_q == nq) {
                 i_q = 0;
@@ -1122,11 +1125,9 @@ __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const Gemv
     }
     if (clearer)
         for (int it = 0; it < n_items; ++it) {
-            const int row0 = (tile_lo + warp + kWarps * it) * 16;
-            for (int i = lane; i < 16 * M; i += 32) {
-                const int m = i >> 4, r = row0 + (i & 15);
-                if (r < N) yv[(size_t)m * N + r] = 0.0f;
-            }
+            const int r = (pair_lo + warp + kWarps * it) * 32 + lane;
+            if (r < N)
+                for (int m = 0; m < M; ++m) yv[(size_t)m * N + r] = 0.0f;
         }
 
     // ---- stage the slice's activation: item (g, nt) of the Gs x MT, warp w
@@ -1244,12 +1245,14 @@ __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const Gemv
     bool add_ok = true;
     int s = 0;
     for (int it = 0; it < n_items; ++it) {
-        // rows gid and gid + 8 of the tile, tokens 8 nt + 2t and 8 nt + 2t + 1
-        float y[MT][4];
+        // rows gid and gid + 8 of tiles 2p and 2p + 1, tokens 8 nt + 2t and 8 nt + 2t + 1
+        float y[2][MT][4];
 #pragma unroll
-        for (int nt = 0; nt < MT; ++nt)
+        for (int tau = 0; tau < 2; ++tau)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) y[nt][e] = 0.0f;
+            for (int nt = 0; nt < MT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) y[tau][nt][e] = 0.0f;
         for (int q = 0; q < nq; ++q, ++s) {
             const int slot = s & (kTDepth - 1);
             // stage s has landed (at most kTDepth - 1 newer groups pending)
@@ -1257,22 +1260,23 @@ __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const Gemv
             __syncwarp();
             const unsigned char* st = rd + slot * kTStageBytes;
             const unsigned char* scp = ring + slot * kTStageBytes + kTCodeBytes;
-            const uint2 sc0 = *reinterpret_cast<const uint2*>(scp + gid * 8);
-            const uint2 sc1 = *reinterpret_cast<const uint2*>(scp + (gid + 8) * 8);
-            const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sc0.x));
-            const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sc0.y));
-            const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&sc1.x));
-            const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&sc1.y));
-            const float s0[4] = {s01.x, s01.y, s23.x, s23.y};
-            const float s1[4] = {r01.x, r01.y, r23.x, r23.y};
+            // the scales of rows gid and gid + 8 of both tiles, both groups
+            float sv[2][2][kTDuo];
 #pragma unroll
-            for (int u = 0; u < kTQuad; ++u) {
-                const uint2 v0 = *reinterpret_cast<const uint2*>(st + u * kSlotBytes);
-                const uint2 v1 = *reinterpret_cast<const uint2*>(st + u * kSlotBytes + 8 * 32);
-                // row gid word 2t, row gid + 8 word 2t, then words 2t + 1
-                const uint32_t w[4] = {v0.x, v1.x, v0.y, v1.y};
-                const int gl = kTQuad * q + u;
+            for (int tau = 0; tau < 2; ++tau)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float2 f2 =
+                        __half22float2(*reinterpret_cast<const __half2*>(scp + (16 * tau + 8 * h + gid) * 4));
+                    sv[tau][h][0] = f2.x;
+                    sv[tau][h][1] = f2.y;
+                }
+#pragma unroll
+            for (int g = 0; g < kTDuo; ++g) {
+                const int gl = kTDuo * q + g;
+                // the group's staged activation, read once for both tiles
                 uint32_t b[MT][16];
+                float4 f[MT];
 #pragma unroll
                 for (int nt = 0; nt < MT; ++nt) {
                     const unsigned char* fp = frag + (size_t)(gl * MT + nt) * kTFragBytes + lane * 16;
@@ -1284,16 +1288,25 @@ __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const Gemv
                         b[nt][4 * qq + 2] = z.z;
                         b[nt][4 * qq + 3] = z.w;
                     }
+                    f[nt] = *reinterpret_cast<const float4*>(corr + ((size_t)(gl * MT + nt) * 4 + t) * 16);
                 }
-                float acc[MT][4];
-                unit_chains<MT>(acc, w, b);
 #pragma unroll
-                for (int nt = 0; nt < MT; ++nt) {
-                    const float4 f = *reinterpret_cast<const float4*>(corr + ((size_t)(gl * MT + nt) * 4 + t) * 16);
-                    y[nt][0] = fmaf(s0[u], fmaf(f.x, acc[nt][0], -f.y), y[nt][0]);   // row gid,     token 2t
-                    y[nt][1] = fmaf(s0[u], fmaf(f.z, acc[nt][1], -f.w), y[nt][1]);   // row gid,     token 2t+1
-                    y[nt][2] = fmaf(s1[u], fmaf(f.x, acc[nt][2], -f.y), y[nt][2]);   // row gid + 8, token 2t
-                    y[nt][3] = fmaf(s1[u], fmaf(f.z, acc[nt][3], -f.w), y[nt][3]);   // row gid + 8, token 2t+1
+                for (int tau = 0; tau < 2; ++tau) {
+                    const unsigned char* up = st + (2 * g + tau) * kSlotBytes;
+                    const uint2 v0 = *reinterpret_cast<const uint2*>(up);
+                    const uint2 v1 = *reinterpret_cast<const uint2*>(up + 8 * 32);
+                    // row gid word 2t, row gid + 8 word 2t, then words 2t + 1
+                    const uint32_t w[4] = {v0.x, v1.x, v0.y, v1.y};
+                    float acc[MT][4];
+                    unit_chains<MT>(acc, w, b);
+                    const float sa = sv[tau][0][g], sb = sv[tau][1][g];
+#pragma unroll
+                    for (int nt = 0; nt < MT; ++nt) {
+                        y[tau][nt][0] = fmaf(sa, fmaf(f[nt].x, acc[nt][0], -f[nt].y), y[tau][nt][0]);   // row gid,     token 2t
+                        y[tau][nt][1] = fmaf(sa, fmaf(f[nt].z, acc[nt][1], -f[nt].w), y[tau][nt][1]);   // row gid,     token 2t+1
+                        y[tau][nt][2] = fmaf(sb, fmaf(f[nt].x, acc[nt][2], -f[nt].y), y[tau][nt][2]);   // row gid + 8, token 2t
+                        y[tau][nt][3] = fmaf(sb, fmaf(f[nt].z, acc[nt][3], -f[nt].w), y[tau][nt][3]);   // row gid + 8, token 2t+1
+                    }
                 }
             }
             // the stage is fully read by every lane: refill it kTDepth stages ahead
@@ -1305,8 +1318,7 @@ __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const Gemv
                 if (adder && lane == 0) flag_seen = ld_acquire_gpu(a.flag + clu);
             }
         }
-        // the tile's sums
-        const int row = (tile_lo + warp + kWarps * it) * 16 + gid;
+        // the tiles' sums
         if (adder && it == 0) {
             int ok = 1;
             if (lane == 0) {
@@ -1317,17 +1329,20 @@ __global__ void __launch_bounds__(kThreads, kTCtasPerSm) gemvt_kernel(const Gemv
             if (add_ok) count_seen();
         }
         if (add_ok) {
+            const int row0 = (pair_lo + warp + kWarps * it) * 32 + gid;
 #pragma unroll
-            for (int nt = 0; nt < MT; ++nt)
+            for (int tau = 0; tau < 2; ++tau)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int m = nt * 8 + 2 * t + (e & 1), r = row + 8 * (e >> 1);
-                    if (m < M && r < N) {
-                        float* p = yv + (size_t)m * N + r;
-                        if (S == 1) *p = y[nt][e];
-                        else atomicAdd(p, y[nt][e]);
+                for (int nt = 0; nt < MT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int m = nt * 8 + 2 * t + (e & 1), r = row0 + 16 * tau + 8 * (e >> 1);
+                        if (m < M && r < N) {
+                            float* p = yv + (size_t)m * N + r;
+                            if (S == 1) *p = y[tau][nt][e];
+                            else atomicAdd(p, y[tau][nt][e]);
+                        }
                     }
-                }
         }
     }
     cp_async_wait<0>();
@@ -1505,14 +1520,15 @@ tern_status make_plan_t(int N, int K, int N2, int sms, int dev, PlanT* out) {
             return TERN_ERR_CUDA;
         optin_of[dev] = optin;
     }
-    const int G = K / kGroup, Gq = G / kTQuad;
-    const int T2 = (N2 + 15) / 16, T = (N + 15) / 16 + T2;
+    // ranges over tile pairs, slices over group pairs
+    const int G = K / kGroup, Gq = G / kTDuo;
+    const int T2 = ((N2 + 15) / 16 + 1) / 2, T = ((N + 15) / 16 + 1) / 2 + T2;
     double best = 0.0;
     PlanT bp{};
     for (int S = 1; S <= Gq && S <= 64; ++S) {
         if (S > 1 && G <= kWarps) break;
         const int qmax = (Gq + S - 1) / S;
-        const size_t sm = smem_t(kTQuad * qmax, MT);
+        const size_t sm = smem_t(kTDuo * qmax, MT);
         if (sm > (size_t)optin_of[dev]) continue;
         const int per_sm = std::min(kTCtasPerSm, (int)(kSmemPerSm / (sm + kCtaSmemReserve)));
         if (per_sm < 1) continue;
@@ -1521,7 +1537,7 @@ tern_status make_plan_t(int N, int K, int N2, int sms, int dev, PlanT* out) {
         const int rmax = split_ranges(T, T2, cps, cps1);
         const int items = (rmax + kWarps - 1) / kWarps;
         const long long waves = ((long long)S * cps + slots - 1) / slots;
-        const double cost = (double)waves * (items * (qmax + 0.5) + 1.0 + (S > 1 ? 0.5 : 0.0));
+        const double cost = (double)waves * (items * (qmax + 1.0) + 2.0 + (S > 1 ? 1.0 : 0.0));
         if (bp.ctas == 0 || cost < best) {
             best = cost;
             bp = PlanT{S, cps, cps1, S * cps, sm};
@@ -1695,7 +1711,7 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
         st = M == 1 ? launch_gemv<1, false, true, true, true>(args, sms, stream)
              : MT == 1 ? launch_gemv<1, false, false, true, true>(args, sms, stream)
                        : launch_gemv<2, false, false, true, true>(args, sms, stream);
-    } else if (M >= kTileMinM && K % (kTQuad * kGroup) == 0) {
+    } else if (M >= kTileMinM && K % (kTDuo * kGroup) == 0) {
         st = MT == 1 ? launch_gemv_t<1>(args, sms, stream) : launch_gemv_t<2>(args, sms, stream);
     } else {
         st = M == 1 ? (lean ? launch_gemv<1, false, true, true>(args, sms, stream)

@@ -92,10 +92,11 @@ def test_gemv_ragged_shapes(tern, orc, M, N, K):
 
 
 @pytest.mark.parametrize("M", [5, 8, 9, 16])
-@pytest.mark.parametrize("N,K", [(37, 512), (300, 1536), (1000, 3072), (129, 17408)])
+@pytest.mark.parametrize("N,K", [(37, 512), (300, 1536), (77, 2304), (1000, 3072), (129, 17408)])
 def test_gemv_tile_major_shapes(tern, orc, M, N, K):
-    """Five tokens and more with K a multiple of 512 (the tile-major loop):
-    ragged N, one K-slice and several, every output against the oracle."""
+    """Five tokens and more with K a multiple of 256 (the tile-major loop):
+    ragged N (an odd tile count leaves a pair's second tile past the matrix),
+    one K-slice and several, every output against the oracle."""
     p = synth.problem(120 + M, M, N, K, tag=f"tm{N}x{K}")
     y, _ = run_gemv(tern, p)
     assert tern.device_error() == 0
