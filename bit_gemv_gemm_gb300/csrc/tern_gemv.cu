@@ -921,22 +921,71 @@ gemv_kernel(const GemvArgs a) {
         }
 }
 
+// The 4-point transform in natural order, in registers.
+__device__ __forceinline__ void fwht4(float (&v)[4]) {
+    const float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+    v[0] = a0 + a2;
+    v[1] = a1 + a3;
+    v[2] = a0 - a2;
+    v[3] = a1 - a3;
+}
+
 // Rotation prologue for the fused path: x' = H_4096 (s (.) x) / 64 in fp32,
 // staged for the product exactly as the product stages a bf16 x (per token and
 // group, E from the largest |x'| and fp16 x' 2^(E + 10 - 2j')), so x' is never
-// rounded to bf16.  The fragments are stored in the order the product's lanes
-// hold them: xs[m][g][t][r] (uint32, two halves), lane t's B register r; xe[m][g]
-// = E.  Thread i owns the block's values 16 i .. 16 i + 15: one half of lane
-// t's registers of one group.
+// rounded to bf16.  One CTA per (token, 1024-wide slice sigma of a 4096-block
+// b = sigma / 4), with H_4096 = H_4 (x) H_1024 in natural order: the slice is
+// H_1024 u, u[j] = sum_{a'} (-1)^popcount(a & a') z[4096 b + 1024 a' + j] / 64
+// (a = sigma % 4, z = s (.) x), and H_1024 = H_4^(x)5 runs as five radix-4
+// passes over the index's base-4 digits, 256 threads x 4 values (the first in
+// registers, the others through shared memory).  The fragments are stored in
+// the order the product's lanes hold them: xs[m][g][t][r] (uint32, two
+// halves), lane t's B register r; xe[m][g] = E.  Threads 0-63 stage: thread i
+// owns the slice's values 16 i .. 16 i + 15, one half of lane t's registers of
+// one group.
 __global__ void __launch_bounds__(kFwhtThreads)
 rotate_stage_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restrict__ signs,
                     uint32_t* __restrict__ xs, int* __restrict__ xe, int K) {
-    __shared__ float sm[kFwhtSmemFloats];
+    __shared__ float sm[kRotN + kRotN / 16];
     pdl_launch_dependents();
     pdl_wait();
-    const int blk = blockIdx.x, m = blockIdx.y, G = K / kGroup;
-    fwht4096_block(x + (size_t)m * K + (size_t)blk * kFwhtN, signs + (size_t)blk * kFwhtN, sm);
+    const int sigma = blockIdx.x, m = blockIdx.y, G = K / kGroup;
+    const int blk = sigma >> 2, a = sigma & 3;
     const int i = threadIdx.x;
+    {
+        float u[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int ap = 0; ap < 4; ++ap) {
+            const size_t k0 = (size_t)kFwhtN * blk + (size_t)kRotN * ap + 4 * i;
+            const uint2 xw = *reinterpret_cast<const uint2*>(x + (size_t)m * K + k0);
+            const uint32_t sw = *reinterpret_cast<const uint32_t*>(signs + k0);
+            const bool neg = (__popc(a & ap) & 1) != 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t bits = ((e < 2 ? xw.x : xw.y) >> (16 * (e & 1))) & 0xFFFFu;
+                const float xv = __uint_as_float(bits << 16);
+                const int sg = (int)(int8_t)((sw >> (8 * e)) & 0xFFu);
+                u[e] += ((sg < 0) != neg) ? -xv : xv;
+            }
+        }
+        fwht4(u);   // digit 0 (bits 0-1): this thread's four consecutive values
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sm[fwht_pos(4 * i + e)] = u[e];
+        __syncthreads();
+#pragma unroll
+        for (int p = 1; p < 5; ++p) {
+            // digit p (bits 2p, 2p + 1): i with two zero bits inserted at 2p
+            const int base = ((i >> (2 * p)) << (2 * p + 2)) | (i & ((1 << (2 * p)) - 1));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) u[e] = sm[fwht_pos(base + (e << (2 * p)))];
+            fwht4(u);
+            const float sc = p == 4 ? 1.0f / 64.0f : 1.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sm[fwht_pos(base + (e << (2 * p)))] = u[e] * sc;
+            __syncthreads();
+        }
+    }
+    if (i >= 64) return;
     float v[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) v[e] = sm[fwht_pos(16 * i + e)];
@@ -949,7 +998,7 @@ rotate_stage_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restric
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
     check_stage_range(mx);
     const int E = stage_exponent(mx);
-    const int g = blk * (kFwhtN / kGroup) + (i >> 3);
+    const int g = sigma * (kRotN / kGroup) + (i >> 3);
     const int e0 = 16 * (i & 7);                    // first value within the group
     const int t = e0 >> 5, half = (e0 >> 4) & 1;    // lane t; this thread forms its registers 2j + half
     uint32_t r[8];
@@ -1688,7 +1737,7 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
         // staged x': M x K halves, then M x G exponents
         uint32_t* xs = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(workspace) + fb);
         int* xe = reinterpret_cast<int*>(xs + (size_t)M * K / 2);
-        const cudaError_t e = launch_pdl(rotate_stage_kernel, dim3(K / kFwhtN, M), dim3(kFwhtThreads), 0, stream,
+        const cudaError_t e = launch_pdl(rotate_stage_kernel, dim3(K / kRotN, M), dim3(kFwhtThreads), 0, stream,
                                          true, reinterpret_cast<const __nv_bfloat16*>(x), signs, xs, xe, K);
         if (e != cudaSuccess) return TERN_ERR_CUDA;
         args.x = xs;
