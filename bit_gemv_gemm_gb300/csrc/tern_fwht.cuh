@@ -87,4 +87,61 @@ __device__ __forceinline__ void fwht4096_block(const __nv_bfloat16* __restrict__
     __syncthreads();
 }
 
+// The 4-point transform in natural order, in registers.
+__device__ __forceinline__ void fwht4(float (&v)[4]) {
+    const float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+    v[0] = a0 + a2;
+    v[1] = a1 + a3;
+    v[2] = a0 - a2;
+    v[3] = a1 - a3;
+}
+
+constexpr int kFwhtSliceN = 1024;                                   // a quarter of a block
+constexpr int kFwhtSliceSmemFloats = kFwhtSliceN + kFwhtSliceN / 16;
+
+// Slice a (0..3) of one 4096 block of H_4096 (s (.) x) / 64, with H_4096 =
+// H_4 (x) H_1024 in natural order: the slice is H_1024 u / 64, u[j] =
+// sum_{a'} (-1)^popcount(a & a') z[1024 a' + j], z = s (.) x over the block.
+// H_1024 = H_4^(x)5 runs as five radix-4 passes over the index's base-4
+// digits, 256 threads x 4 values (the first in registers, the others through
+// shared memory).  x and signs point at the block (8- and 4-byte aligned);
+// the result is left in `sm` at fwht_pos(j).  Must be called by all 256
+// threads; ends with a __syncthreads().
+__device__ __forceinline__ void fwht1024_slice(const __nv_bfloat16* __restrict__ x,
+                                               const int8_t* __restrict__ signs, int a,
+                                               float* __restrict__ sm) {
+    const int i = threadIdx.x;
+    float u[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int ap = 0; ap < 4; ++ap) {
+        const int k0 = kFwhtSliceN * ap + 4 * i;
+        const uint2 xw = *reinterpret_cast<const uint2*>(x + k0);
+        const uint32_t sw = *reinterpret_cast<const uint32_t*>(signs + k0);
+        const bool neg = (__popc(a & ap) & 1) != 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t bits = ((e < 2 ? xw.x : xw.y) >> (16 * (e & 1))) & 0xFFFFu;
+            const float xv = __uint_as_float(bits << 16);
+            const int sg = (int)(int8_t)((sw >> (8 * e)) & 0xFFu);
+            u[e] += ((sg < 0) != neg) ? -xv : xv;
+        }
+    }
+    fwht4(u);   // digit 0 (bits 0-1): this thread's four consecutive values
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sm[fwht_pos(4 * i + e)] = u[e];
+    __syncthreads();
+#pragma unroll
+    for (int p = 1; p < 5; ++p) {
+        // digit p (bits 2p, 2p + 1): i with two zero bits inserted at 2p
+        const int base = ((i >> (2 * p)) << (2 * p + 2)) | (i & ((1 << (2 * p)) - 1));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) u[e] = sm[fwht_pos(base + (e << (2 * p)))];
+        fwht4(u);
+        const float sc = p == 4 ? 1.0f / 64.0f : 1.0f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sm[fwht_pos(base + (e << (2 * p)))] = u[e] * sc;
+        __syncthreads();
+    }
+}
+
 }  // namespace tern

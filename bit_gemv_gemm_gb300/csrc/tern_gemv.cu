@@ -921,24 +921,13 @@ gemv_kernel(const GemvArgs a) {
         }
 }
 
-// The 4-point transform in natural order, in registers.
-__device__ __forceinline__ void fwht4(float (&v)[4]) {
-    const float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
-    v[0] = a0 + a2;
-    v[1] = a1 + a3;
-    v[2] = a0 - a2;
-    v[3] = a1 - a3;
-}
-
 // Rotation prologue for the fused path: x' = H_4096 (s (.) x) / 64 in fp32,
 // staged for the product exactly as the product stages a bf16 x (per token and
 // group, E from the largest |x'| and fp16 x' 2^(E + 10 - 2j')), so x' is never
 // rounded to bf16.  One CTA per (token, 1024-wide slice sigma of a 4096-block
 // b = sigma / 4), with H_4096 = H_4 (x) H_1024 in natural order: the slice is
 // H_1024 u, u[j] = sum_{a'} (-1)^popcount(a & a') z[4096 b + 1024 a' + j] / 64
-// (a = sigma % 4, z = s (.) x), and H_1024 = H_4^(x)5 runs as five radix-4
-// passes over the index's base-4 digits, 256 threads x 4 values (the first in
-// registers, the others through shared memory).  The fragments are stored in
+// (a = sigma % 4, z = s (.) x).  The fragments are stored in
 // the order the product's lanes hold them: xs[m][g][t][r] (uint32, two
 // halves), lane t's B register r; xe[m][g] = E.  Threads 0-63 stage: thread i
 // owns the slice's values 16 i .. 16 i + 15, one half of lane t's registers of
@@ -946,45 +935,13 @@ __device__ __forceinline__ void fwht4(float (&v)[4]) {
 __global__ void __launch_bounds__(kFwhtThreads)
 rotate_stage_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restrict__ signs,
                     uint32_t* __restrict__ xs, int* __restrict__ xe, int K) {
-    __shared__ float sm[kRotN + kRotN / 16];
+    __shared__ float sm[kFwhtSliceSmemFloats];
     pdl_launch_dependents();
     pdl_wait();
     const int sigma = blockIdx.x, m = blockIdx.y, G = K / kGroup;
-    const int blk = sigma >> 2, a = sigma & 3;
+    const int blk = sigma >> 2;
     const int i = threadIdx.x;
-    {
-        float u[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int ap = 0; ap < 4; ++ap) {
-            const size_t k0 = (size_t)kFwhtN * blk + (size_t)kRotN * ap + 4 * i;
-            const uint2 xw = *reinterpret_cast<const uint2*>(x + (size_t)m * K + k0);
-            const uint32_t sw = *reinterpret_cast<const uint32_t*>(signs + k0);
-            const bool neg = (__popc(a & ap) & 1) != 0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t bits = ((e < 2 ? xw.x : xw.y) >> (16 * (e & 1))) & 0xFFFFu;
-                const float xv = __uint_as_float(bits << 16);
-                const int sg = (int)(int8_t)((sw >> (8 * e)) & 0xFFu);
-                u[e] += ((sg < 0) != neg) ? -xv : xv;
-            }
-        }
-        fwht4(u);   // digit 0 (bits 0-1): this thread's four consecutive values
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sm[fwht_pos(4 * i + e)] = u[e];
-        __syncthreads();
-#pragma unroll
-        for (int p = 1; p < 5; ++p) {
-            // digit p (bits 2p, 2p + 1): i with two zero bits inserted at 2p
-            const int base = ((i >> (2 * p)) << (2 * p + 2)) | (i & ((1 << (2 * p)) - 1));
-#pragma unroll
-            for (int e = 0; e < 4; ++e) u[e] = sm[fwht_pos(base + (e << (2 * p)))];
-            fwht4(u);
-            const float sc = p == 4 ? 1.0f / 64.0f : 1.0f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sm[fwht_pos(base + (e << (2 * p)))] = u[e] * sc;
-            __syncthreads();
-        }
-    }
+    fwht1024_slice(x + (size_t)m * K + (size_t)blk * kFwhtN, signs + (size_t)blk * kFwhtN, sigma & 3, sm);
     if (i >= 64) return;
     float v[16];
 #pragma unroll

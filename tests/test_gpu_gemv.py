@@ -241,8 +241,10 @@ def test_gemv_verify_full_size_sampled(tern, orc, M, K, N):
 # rotation
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("M,K", [(1, 4096), (16, 4096), (3, 8192), (2, 12288)])
+@pytest.mark.parametrize("M,K", [(1, 4096), (16, 4096), (3, 8192), (2, 12288), (200, 4096)])
 def test_fwht_matches_oracle(tern, orc, M, K):
+    """Small calls run one CTA per 1024-wide slice, calls with at least as
+    many 4096-blocks as SMs (200 tokens) one CTA per block."""
     x = synth.activations(40 + M, "x", (M, K))
     s = synth.signs(40 + M, "signs", K)
     y = tern.fwht(dev_bf16(x), torch.from_numpy(s).cuda())
