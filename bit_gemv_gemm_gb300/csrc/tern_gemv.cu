@@ -567,9 +567,15 @@ gemv_kernel(const GemvArgs a) {
     // the in-kernel rotation: this CTA's slice of x' (after the PDL wait
     // above: x may be the previous kernel's output), built while the first
     // weight copies are still landing
-    if (ROT)
-        rotate_slice(reinterpret_cast<const __nv_bfloat16*>(a.x), a.signs, a.K, M, sigma,
-                     reinterpret_cast<float*>(smem + a.off_rot));
+    // (one token: all 256 threads on its slice, five radix-4 passes)
+    if (ROT) {
+        float* rot = reinterpret_cast<float*>(smem + a.off_rot);
+        if (ONE)
+            fwht1024_slice(reinterpret_cast<const __nv_bfloat16*>(a.x) + (size_t)(sigma >> 2) * kFwhtN,
+                           a.signs + (size_t)(sigma >> 2) * kFwhtN, sigma & 3, rot);
+        else
+            rotate_slice(reinterpret_cast<const __nv_bfloat16*>(a.x), a.signs, a.K, M, sigma, rot);
+    }
 
     // ---- stage one group's activation (read from global memory, possibly the
     // previous kernel's output): lane (gid, t) holds token nt*8+gid,
