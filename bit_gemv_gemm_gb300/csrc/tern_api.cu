@@ -85,10 +85,11 @@ tern_status tern_device_error(int* code) {
     if (!code) return TERN_ERR_NULL;
     *code = 0;
     if (cudaDeviceSynchronize() != cudaSuccess) return TERN_ERR_CUDA;
-    int a = 0, b = 0;
+    int a = 0, b = 0, c = 0;
     if (read_gemm_device_error(&a) != cudaSuccess) return TERN_ERR_CUDA;
     if (read_gemv_device_error(&b) != cudaSuccess) return TERN_ERR_CUDA;
-    *code = a ? a : b;
+    if (read_f3_device_error(&c) != cudaSuccess) return TERN_ERR_CUDA;
+    *code = a ? a : (b ? b : c);
     return TERN_OK;
 }
 

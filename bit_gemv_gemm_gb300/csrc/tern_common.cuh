@@ -34,6 +34,7 @@ __device__ __forceinline__ void report_device_error(int* word, int code) {
 }
 cudaError_t read_gemm_device_error(int* code);
 cudaError_t read_gemv_device_error(int* code);
+cudaError_t read_f3_device_error(int* code);
 // One-CTA kernels that run a bounded wait nothing completes (tern_wait_selftest).
 cudaError_t launch_flag_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_mbar_wait_selftest(uint64_t limit_ns, cudaStream_t stream);

@@ -25,6 +25,7 @@
 #include <mutex>
 
 #include "tern_common.cuh"
+#include "tern_mma.cuh"
 
 namespace tern {
 namespace {
@@ -314,12 +315,372 @@ f3_gemv_table_kernel(const __nv_bfloat16* __restrict__ x, const uint8_t* __restr
     }
 }
 
+// ---------------------------------------------------------------------------
+// One token on the tensor pipe.
+//
+// A byte's five trits become five 2-bit codes through a 256-entry table
+// (q0 | q1 << 2 | ... | q4 << 8; bytes above 242 are not a pack's and give
+// undefined weights), the codes of a lane's 32 weights are assembled into the
+// two 2-bit code words the decode product reads (16 codes per word, code i at
+// bits 2i), and from there the unit is the decode product's: one AND per two
+// weights into fp16 A fragments, the `mma.sync` chain against the staged
+// activation, the all-ones correction, the group scale.  Lane (gid, t) takes
+// weights 32 t .. 32 t + 31 of a group: bytes from b0 = 32 t / 5 on, the first
+// 2 (32 t mod 5) bits of b0's codes dropped; seven bytes hold them, eight for
+// t = 2 (weights 64 .. 95 start at b0's last trit and end at byte 19's first).  The table has a copy
+// per lane ([v][lane] halfwords), so a warp's lookups never share a bank word
+// across different values.
+//
+// Work split (as the tile-major decode loop): K-slices of whole quads of
+// groups, ranges of 16-row tiles, a warp owning whole tiles and walking its
+// slice four groups (16 rows x 104 bytes and the 16 x 4 scales, 8-byte
+// copies) at a time, the row sums in registers.  The slices meet in y through
+// the range flags of the decode product, here in a file-scope array (the call
+// takes no workspace): the slice-0 CTA clears its rows and counts itself in;
+// the others add once they have seen the count; the S-th count returns the
+// word to 0, so the array is all zeros between calls.
+// ---------------------------------------------------------------------------
+constexpr int kF3mQuad = 4;                                    // groups per stage
+constexpr int kF3mDepth = 4;                                   // stages in flight per warp (a power of 2)
+constexpr int kF3mRowBytes = 26 * kF3mQuad;                    // a row's bytes per stage
+constexpr int kF3mCodeBytes = 16 * kF3mRowBytes;
+constexpr int kF3mStageBytes = kF3mCodeBytes + 16 * kF3mQuad * 2;   // and the tile's 16 x 4 scales
+constexpr int kF3mRingBytes = 8 * kF3mDepth * kF3mStageBytes;
+constexpr int kF3mLutBytes = 256 * 32 * 2;                    // [byte][lane] halfwords
+constexpr int kF3mGroupBytes = 256 + 8;                       // a group's staged fragments and (F, F acc1)
+constexpr int kF3mCtasPerSm = 2;
+constexpr int kF3mMaxRanges = 4096;                           // range flags in the file-scope array
+
+__device__ unsigned g_f3_flags[kF3mMaxRanges];   // zero between calls (see above)
+__device__ int g_f3_error;                       // sticky device error word of this translation unit
+
+struct F3mArgs {
+    const __nv_bfloat16* x;
+    const uint8_t* packed;
+    const __half* scales;
+    float* y;
+    int N, K, G, T, S, cps;
+};
+
+__device__ __forceinline__ void f3_check_stage_range(float mx) {
+    if (!(mx < 0x1p100f)) report_device_error(&g_f3_error, kDevErrGemvActivationRange);
+}
+
+__global__ void __launch_bounds__(kF3Threads, kF3mCtasPerSm) f3_mma_kernel(const F3mArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int G = a.G, S = a.S, N = a.N;
+    const size_t pitch = (size_t)26 * G;   // bytes per row
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, t = lane & 3;
+    const int sigma = blockIdx.x / a.cps, clu = blockIdx.x - sigma * a.cps;   // slice, range
+    const int Gq = G / kF3mQuad;
+    const int qA = (int)((long long)Gq * sigma / S);
+    const int nq = (int)((long long)Gq * (sigma + 1) / S) - qA;
+    const int gA = kF3mQuad * qA, Gs = kF3mQuad * nq;
+    const int tile_lo = (int)((long long)a.T * clu / a.cps);
+    const int R = (int)((long long)a.T * (clu + 1) / a.cps) - tile_lo;
+    const int n_items = warp < R ? (R - 1 - warp) / 8 + 1 : 0;
+    const int n_st = n_items * nq;
+
+    unsigned char* const ring = smem + (size_t)warp * kF3mDepth * kF3mStageBytes;
+    const unsigned short* const lut = reinterpret_cast<const unsigned short*>(smem + kF3mRingBytes);
+    uint32_t* const bfr = reinterpret_cast<uint32_t*>(smem + kF3mRingBytes + kF3mLutBytes);   // [Gs][4][t][4 words]
+    float2* const fcs = reinterpret_cast<float2*>(smem + kF3mRingBytes + kF3mLutBytes + (size_t)Gs * 256);
+
+    // ---- this warp's copies: lanes 0-25 take 8-byte piece l % 13 of rows
+    // 8 (l / 13) .. + 7, lanes 26-31 the scales of rows l - 26, + 6, + 12.
+    // Rows past N read row N - 1; their sums are never written. ----
+    const uint32_t ring_s = smem_addr(ring);
+    const int cpart = lane % 13, chalf = lane / 13;
+    int i_item = 0, i_q = 0, issued = 0, row0 = 0;
+    auto item_rows = [&](int it) { row0 = (tile_lo + warp + 8 * it) * 16; };
+    if (n_items > 0) item_rows(0);
+    auto issue = [&](int slot) {
+        if (issued < n_st) {
+            const uint32_t base = ring_s + (uint32_t)(slot * kF3mStageBytes);
+            const int g0 = gA + kF3mQuad * i_q;
+            if (lane < 26) {
+                const uint8_t* src = a.packed + (size_t)g0 * 26 + cpart * 8;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int rr = 8 * chalf + r;
+                    cp_async8(base + (uint32_t)(rr * kF3mRowBytes + cpart * 8),
+                              src + (size_t)min(row0 + rr, N - 1) * pitch);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 3; ++k) {
+                    const int rr = lane - 26 + 6 * k;
+                    if (rr < 16)
+                        cp_async8(base + (uint32_t)(kF3mCodeBytes + rr * 8),
+                                  a.scales + (size_t)min(row0 + rr, N - 1) * G + g0);
+                }
+            }
+            ++issued;
+            if (++i_q == nq) {
+                i_q = 0;
+                if (++i_item < n_items) item_rows(i_item);
+            }
+        }
+        cp_async_commit();   // one group per stage, empty past the end, so the waits count uniformly
+    };
+
+    pdl_launch_dependents();
+    // the weights are never the previous kernel's output: the first stages go
+    // out before the PDL wait
+#pragma unroll
+    for (int i = 0; i < kF3mDepth; ++i) issue(i);
+
+    // the byte table, a copy per lane: entry v holds v's five codes, two
+    // copies per 32-bit word
+    for (int v = threadIdx.x; v < 256; v += kF3Threads) {
+        int c = 0, r = v;
+#pragma unroll
+        for (int d = 0; d < 5; ++d) {
+            c |= ((r % 3) & 3) << (2 * d);
+            r /= 3;
+        }
+        if (v >= 243) c = v & 0x3FF;   // not a pack's byte: some codes, never out of bounds
+        uint32_t* row = reinterpret_cast<uint32_t*>(smem + kF3mRingBytes) + v * 16;
+        const uint32_t two = (uint32_t)c | ((uint32_t)c << 16);
+#pragma unroll
+        for (int l = 0; l < 16; ++l) row[l] = two;
+    }
+    pdl_wait();
+
+    __shared__ unsigned cleared_warps, seen_warps;
+    const bool clearer = S > 1 && sigma == 0;
+    const bool adder = S > 1 && sigma != 0;
+    unsigned* const flag = g_f3_flags + clu;
+    if (threadIdx.x == 0) {
+        cleared_warps = 0u;
+        seen_warps = 0u;
+    }
+    if (clearer)
+        for (int it = 0; it < n_items; ++it) {
+            const int r = (tile_lo + warp + 8 * it) * 16 + (lane & 15);
+            if (lane < 16 && r < N) a.y[r] = 0.0f;
+        }
+
+    // ---- the slice's activation, as the decode product stages it: lane
+    // (gid, t) of a warp takes group gA + 8 b + gid of block b ----
+    for (int blk = warp; blk * 8 < Gs; blk += 8) {
+        const int gl = blk * 8 + gid;
+        const bool ok = gl < Gs;
+        float v[32];
+        if (ok) {
+            const uint4* s4 = reinterpret_cast<const uint4*>(a.x + (size_t)(gA + gl) * 128 + 32 * t);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 u = s4[q];
+                const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    v[8 * q + 2 * e] = __uint_as_float(uw[e] << 16);
+                    v[8 * q + 2 * e + 1] = __uint_as_float(uw[e] & 0xFFFF0000u);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+        }
+        float mx = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(v[e]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        f3_check_stage_range(mx);
+        const int E = stage_exponent(mx);
+        uint32_t b[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float c = stage_multiplier(E, j);
+            const __half2 lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);
+            const __half2 hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c);
+            b[2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
+            b[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+        }
+        if (ok) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(bfr + gl * 64 + q * 16 + t * 4) =
+                    make_uint4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+        }
+        // the ones pass of the block's eight groups: column n is group 8 b + n
+        float acc1[4];
+        const uint32_t ones[4] = {0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u};
+        unit_chain(acc1, ones, b);
+        const float c_lo = __shfl_sync(0xffffffffu, acc1[0], gid >> 1);
+        const float c_hi = __shfl_sync(0xffffffffu, acc1[1], gid >> 1);
+        const float F = __uint_as_float((uint32_t)(14 - E + 127) << 23);   // 2^(14-E)
+        if (ok && t == 0) fcs[gl] = make_float2(F, F * ((gid & 1) ? c_hi : c_lo));
+    }
+    __syncthreads();
+
+    auto count_cleared = [&]() {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0 && atomicAdd(&cleared_warps, 1u) == 7u) red_inc(flag, (unsigned)(S - 1));
+    };
+    auto count_seen = [&]() {
+        if (lane == 0 && atomicAdd(&seen_warps, 1u) == 7u) red_inc(flag, (unsigned)(S - 1));
+    };
+    if (clearer && n_st == 0) count_cleared();
+    if (adder && n_st == 0) count_seen();
+
+    // ---- the stages ----
+    // this lane's 7 bytes of a group: b0 .. b0 + 6, the first r0 bits of b0's codes dropped
+    const int b0 = (32 * t) / 5, r0 = 2 * (32 * t - 5 * b0);
+    const unsigned short* const lut_l = lut + lane;
+    unsigned flag_seen = 0u;
+    bool add_ok = true;
+    int s = 0;
+    for (int it = 0; it < n_items; ++it) {
+        float y0 = 0.0f, y1 = 0.0f;   // rows gid and gid + 8
+        for (int q = 0; q < nq; ++q, ++s) {
+            const int slot = s & (kF3mDepth - 1);
+            cp_async_wait<kF3mDepth - 1>();
+            __syncwarp();
+            const unsigned char* st = ring + slot * kF3mStageBytes;
+            const uint2 sc0 = *reinterpret_cast<const uint2*>(st + kF3mCodeBytes + gid * 8);
+            const uint2 sc1 = *reinterpret_cast<const uint2*>(st + kF3mCodeBytes + (gid + 8) * 8);
+            const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sc0.x));
+            const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sc0.y));
+            const float2 r01 = __half22float2(*reinterpret_cast<const __half2*>(&sc1.x));
+            const float2 r23 = __half22float2(*reinterpret_cast<const __half2*>(&sc1.y));
+            const float s0[4] = {s01.x, s01.y, s23.x, s23.y};
+            const float s1[4] = {r01.x, r01.y, r23.x, r23.y};
+#pragma unroll
+            for (int u = 0; u < kF3mQuad; ++u) {
+                // the two code words of rows gid and gid + 8
+                uint32_t wd[2][2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int off = (gid + 8 * h) * kF3mRowBytes + 26 * u + b0;
+                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(st + (off & ~3));
+                    const uint32_t w0 = wp[0], w1 = wp[1], w2 = wp[2];
+                    const uint32_t sh = (uint32_t)(off & 3) * 8u;
+                    const uint32_t x0 = __funnelshift_r(w0, w1, sh), x1 = __funnelshift_r(w1, w2, sh);
+                    uint32_t L[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t byte = __byte_perm(i < 4 ? x0 : x1, 0u, 0x4440u | (uint32_t)(i & 3));
+                        L[i] = lut_l[byte * 32];
+                    }
+                    wd[h][0] = (L[0] >> r0) | (L[1] << (10 - r0)) | (L[2] << (20 - r0)) | (L[3] << (30 - r0));
+                    wd[h][1] = (L[3] >> (r0 + 2)) | (L[4] << (8 - r0)) | (L[5] << (18 - r0)) | (L[6] << (28 - r0)) |
+                               (r0 == 8 ? L[7] << 30 : 0u);
+                }
+                const uint32_t w[4] = {wd[0][0], wd[1][0], wd[0][1], wd[1][1]};
+                const int gl = kF3mQuad * q + u;
+                const uint4* bp = reinterpret_cast<const uint4*>(bfr + gl * 64 + t * 4);
+                uint32_t b[16];
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const uint4 z = bp[qq * 4];
+                    b[4 * qq] = z.x;
+                    b[4 * qq + 1] = z.y;
+                    b[4 * qq + 2] = z.z;
+                    b[4 * qq + 3] = z.w;
+                }
+                float acc[4];
+                unit_chain(acc, w, b);
+                const float2 fc = fcs[gl];
+                y0 = fmaf(s0[u], fmaf(fc.x, acc[0], -fc.y), y0);
+                y1 = fmaf(s1[u], fmaf(fc.x, acc[2], -fc.y), y1);
+            }
+            __syncwarp();
+            issue(slot);
+            if (s == 0) {
+                if (clearer) count_cleared();
+                if (adder && lane == 0) flag_seen = ld_acquire_gpu(flag);
+            }
+        }
+        const int row = (tile_lo + warp + 8 * it) * 16 + gid;
+        if (S == 1) {
+            if (t == 0) {
+                if (row < N) a.y[row] = y0;
+                if (row + 8 < N) a.y[row + 8] = y1;
+            }
+        } else {
+            if (adder && it == 0) {
+                int ok = 1;
+                if (lane == 0) {
+                    ok = flag_seen != 0u || wait_flag_nonzero(flag, kFlagWaitNs);
+                    if (!ok) report_device_error(&g_f3_error, kDevErrGemvConsumerWait);
+                }
+                add_ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+                if (add_ok) count_seen();
+            }
+            if (add_ok && t == 0) {
+                if (row < N) atomicAdd(a.y + row, y0);
+                if (row + 8 < N) atomicAdd(a.y + row + 8, y1);
+            }
+        }
+    }
+    cp_async_wait<0>();
+}
+
+
+size_t f3m_smem(int Gs) { return (size_t)kF3mRingBytes + kF3mLutBytes + (size_t)Gs * kF3mGroupBytes; }
+
+// The one-token plan: slices of whole quads and ranges of tiles, as the
+// tile-major decode loop plans them (the longest warp's stages against the
+// extra CTAs and additions of more slices), at most kF3mMaxRanges ranges;
+// several slices only when K spans more than one 1024-wide slice.
+struct F3mPlan {
+    int S, cps, ctas;
+    size_t smem;
+};
+bool f3m_plan(int N, int K, int sms, int optin, F3mPlan* out) {
+    const int G = K / 128, Gq = G / kF3mQuad, T = (N + 15) / 16;
+    double best = 0.0;
+    F3mPlan bp{};
+    for (int S = 1; S <= Gq && S <= 64; ++S) {
+        if (S > 1 && G <= 8) break;
+        const int qmax = (Gq + S - 1) / S;
+        const size_t sm = f3m_smem(kF3mQuad * qmax);
+        if (sm > (size_t)optin) continue;
+        const int per_sm = std::min(kF3mCtasPerSm, (int)((228 * 1024) / (sm + 1024)));
+        if (per_sm < 1) continue;
+        const int slots = sms * per_sm;
+        const int cps = std::max(1, std::min(std::min(T, kF3mMaxRanges), slots / S));
+        const int rmax = (T + cps - 1) / cps;
+        const int items = (rmax + 7) / 8;
+        const long long waves = ((long long)S * cps + slots - 1) / slots;
+        const double cost = (double)waves * (items * (qmax + 0.5) + 1.0 + (S > 1 ? 0.5 : 0.0));
+        if (bp.ctas == 0 || cost < best) {
+            best = cost;
+            bp = F3mPlan{S, cps, S * cps, sm};
+        }
+    }
+    if (bp.ctas == 0) return false;
+    *out = bp;
+    return true;
+}
+
 size_t f3_smem_bytes(int M) { return (size_t)(kF3Lut + M * kF3Chunk) * sizeof(float); }
 
 }  // namespace
 }  // namespace tern
 
 using namespace tern;
+
+namespace tern {
+// Reads and clears the base-3 product's device error word.
+cudaError_t read_f3_device_error(int* code) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_f3_error, sizeof(int));
+    if (e != cudaSuccess) return e;
+    if (v != 0) {
+        const int z = 0;
+        e = cudaMemcpyToSymbol(g_f3_error, &z, sizeof(int));
+        if (e != cudaSuccess) return e;
+    }
+    *code = v;
+    return cudaSuccess;
+}
+}  // namespace tern
 
 extern "C" size_t tern_f3_packed_bytes(int N, int K) {
     if (N < 0 || K < 0 || K % 128 != 0) return 0;
@@ -371,7 +732,45 @@ extern "C" tern_status tern_f3_gemv(const void* x, const uint8_t* packed, const 
         }
     }
     cudaError_t e;
-    if (M <= kF3TabMaxM) {
+    if (M == 1 && K % (kF3mQuad * 128) == 0) {
+        // one token on the tensor pipe
+        static int optin_of[64] = {};
+        static F3mPlan plan_of[64][8];
+        static int plan_key[64][8][2];
+        static int plan_n[64] = {};
+        F3mPlan p{};
+        bool have = false;
+        {
+            std::lock_guard<std::mutex> lk(mu);
+            if (!optin_of[dev]) {
+                int optin = 0;
+                cudaFuncAttributes fa;
+                if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+                    cudaFuncGetAttributes(&fa, f3_mma_kernel) != cudaSuccess)
+                    return TERN_ERR_CUDA;
+                optin -= (int)fa.sharedSizeBytes;
+                if (cudaFuncSetAttribute(f3_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+                    cudaSuccess)
+                    return TERN_ERR_CUDA;
+                optin_of[dev] = optin;
+            }
+            for (int i = 0; i < plan_n[dev]; ++i)
+                if (plan_key[dev][i][0] == N && plan_key[dev][i][1] == K) {
+                    p = plan_of[dev][i];
+                    have = true;
+                }
+            if (!have) {
+                if (!f3m_plan(N, K, sms, optin_of[dev], &p)) return TERN_ERR_SHAPE;
+                const int slot = plan_n[dev] < 8 ? plan_n[dev]++ : (N + K) % 8;
+                plan_key[dev][slot][0] = N;
+                plan_key[dev][slot][1] = K;
+                plan_of[dev][slot] = p;
+            }
+        }
+        F3mArgs args{reinterpret_cast<const __nv_bfloat16*>(x), packed, reinterpret_cast<const __half*>(scales), y,
+                     N, K, K / 128, (N + 15) / 16, p.S, p.cps};
+        e = launch_pdl(f3_mma_kernel, dim3(p.ctas), dim3(kF3Threads), p.smem, (cudaStream_t)stream, true, args);
+    } else if (M <= kF3TabMaxM) {
         // persistent: kF3TabCtasPerSm CTAs per SM, at most kF3TabRowsPerWarp rows per warp
         const int per_cta_cap = kF3Warps * kF3TabRowsPerWarp;
         const int ctas = std::max((N + per_cta_cap - 1) / per_cta_cap, std::min(N, kF3TabCtasPerSm * sms));

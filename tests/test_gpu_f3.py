@@ -86,3 +86,58 @@ def test_f3_zero_rows_and_scale_edges(tern, orc):
     assert (yh[:, 5] == 0).all() and (yh[:, 40] == 0).all() and (yh[:, 7] == 0).all()
     y_ref, a_ref = orc.f3_matmul(p.x, packed, s)
     assert_fp32_close(yh, y_ref, a_ref, what="f3 edges")
+
+
+@pytest.mark.parametrize("N,K", [(1, 512), (37, 512), (300, 1536), (1000, 3072), (129, 17408), (5, 65536)])
+def test_f3_gemv_one_token_tensor_pipe(tern, orc, N, K):
+    """One token with K a multiple of 512 runs the tensor-pipe product (the
+    five codes of a byte from a table, assembled into 2-bit words): ragged
+    N, one K-slice and many, every output against the oracle."""
+    p = synth.problem(95, 1, N, K, tag=f"f3m{N}x{K}")
+    packed, bad = orc.f3_pack(p.t)
+    assert bad == 0
+    y = torch.full((1, N), float("nan"), dtype=torch.float32, device="cuda")
+    tern.f3_gemv(dev_bf16(p.x), torch.from_numpy(packed).cuda(), dev_scales(p.s), y=y)
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    y_ref, a_ref = orc.f3_matmul(p.x, packed, p.s)
+    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what=f"f3 one token N={N} K={K}")
+
+
+def test_f3_one_token_exact_cases(tern, orc):
+    """Exact answers on the tensor-pipe product: zero trits give exactly 0;
+    trits +-1 with x = 2 at one position give 2 s exactly, at every position
+    of a 512-wide row (every byte, digit and lane of the assembly, the
+    three-trit last byte included)."""
+    N, K = 16, 512
+    s = synth.scales(96, "f3e", (N, K // 128), synth.SCALE_UNIFORM)
+    z, _ = orc.f3_pack(np.zeros((N, 1536), dtype=np.int8))
+    y = tern.f3_gemv(dev_bf16(synth.activations(96, "f3x", (1, 1536))), torch.from_numpy(z).cuda(),
+                     dev_scales(synth.scales(96, "f3z", (N, 12))))
+    torch.cuda.synchronize()
+    assert (y.cpu().numpy() == 0).all()
+    t = np.ones((N, K), dtype=np.int8)
+    t[1::2] = -1
+    t[:, 120:128] *= -1
+    packed, _ = orc.f3_pack(t)
+    dp = torch.from_numpy(packed).cuda()
+    ds = dev_scales(s)
+    for k in range(K):
+        x = np.zeros((1, K), dtype=np.uint16)
+        x[0, k] = 0x4000                                    # bf16 2.0
+        y = tern.f3_gemv(dev_bf16(x), dp, ds).cpu().numpy()
+        want = 2.0 * t[:, k].astype(np.float64) * s[:, k // 128].astype(np.float64)
+        assert np.array_equal(y[0].astype(np.float64), want), k
+
+
+def test_f3_one_token_bytes_outside_the_pack(tern, orc):
+    """Bytes above 242 are not a pack's (their weights are undefined), but a
+    call on them stays within its buffers and reports no device error."""
+    N, K = 40, 1024
+    rs = np.random.default_rng(97)
+    packed = rs.integers(0, 256, size=(N, 26 * (K // 128)), dtype=np.uint8)
+    y = tern.f3_gemv(dev_bf16(synth.activations(97, "f3o", (1, K))), torch.from_numpy(packed).cuda(),
+                     dev_scales(synth.scales(97, "f3os", (N, K // 128))))
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    assert torch.isfinite(y).all()
