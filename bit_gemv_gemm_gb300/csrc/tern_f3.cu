@@ -347,7 +347,6 @@ constexpr int kF3mCodeBytes = 16 * kF3mRowBytes;
 constexpr int kF3mStageBytes = kF3mCodeBytes + 16 * kF3mQuad * 2;   // and the tile's 16 x 4 scales
 constexpr int kF3mRingBytes = 8 * kF3mDepth * kF3mStageBytes;
 constexpr int kF3mLutBytes = 256 * 32 * 2;                    // [byte][lane] halfwords
-constexpr int kF3mGroupBytes = 256 + 8;                       // a group's staged fragments and (F, F acc1)
 constexpr int kF3mCtasPerSm = 2;
 constexpr int kF3mMaxRanges = 4096;                           // range flags in the file-scope array
 
@@ -359,16 +358,21 @@ struct F3mArgs {
     const uint8_t* packed;
     const __half* scales;
     float* y;
-    int N, K, G, T, S, cps;
+    int M, N, K, G, T, S, cps;
 };
 
 __device__ __forceinline__ void f3_check_stage_range(float mx) {
     if (!(mx < 0x1p100f)) report_device_error(&g_f3_error, kDevErrGemvActivationRange);
 }
 
+// ONE: a single token (the staged activation read by broadcast, 256 bytes a
+// group); otherwise MT token tiles of eight, each group's fragments per lane
+// (2 KB a group and token tile) with (F, F acc1) of the lane's two tokens.
+template <int MT, bool ONE>
 __global__ void __launch_bounds__(kF3Threads, kF3mCtasPerSm) f3_mma_kernel(const F3mArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
-    const int G = a.G, S = a.S, N = a.N;
+    const int G = a.G, S = a.S, N = a.N, M = ONE ? 1 : a.M;
+    constexpr int kFrag = ONE ? 256 : MT * 2048, kCorr = ONE ? 8 : MT * 64;   // per group
     const size_t pitch = (size_t)26 * G;   // bytes per row
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, t = lane & 3;
@@ -384,8 +388,11 @@ __global__ void __launch_bounds__(kF3Threads, kF3mCtasPerSm) f3_mma_kernel(const
 
     unsigned char* const ring = smem + (size_t)warp * kF3mDepth * kF3mStageBytes;
     const unsigned short* const lut = reinterpret_cast<const unsigned short*>(smem + kF3mRingBytes);
-    uint32_t* const bfr = reinterpret_cast<uint32_t*>(smem + kF3mRingBytes + kF3mLutBytes);   // [Gs][4][t][4 words]
-    float2* const fcs = reinterpret_cast<float2*>(smem + kF3mRingBytes + kF3mLutBytes + (size_t)Gs * 256);
+    // ONE: [Gs][4][t][4 words] and [Gs] (F, F acc1); else [Gs][MT][4][32 lanes][16 B] and [Gs][MT][t] float4
+    unsigned char* const frag = smem + kF3mRingBytes + kF3mLutBytes;
+    unsigned char* const corr = frag + (size_t)Gs * kFrag;
+    uint32_t* const bfr = reinterpret_cast<uint32_t*>(frag);
+    float2* const fcs = reinterpret_cast<float2*>(corr);
 
     // ---- this warp's copies: lanes 0-25 take 8-byte piece l % 13 of rows
     // 8 (l / 13) .. + 7, lanes 26-31 the scales of rows l - 26, + 6, + 12.
@@ -458,62 +465,123 @@ __global__ void __launch_bounds__(kF3Threads, kF3mCtasPerSm) f3_mma_kernel(const
     }
     if (clearer)
         for (int it = 0; it < n_items; ++it) {
-            const int r = (tile_lo + warp + 8 * it) * 16 + (lane & 15);
-            if (lane < 16 && r < N) a.y[r] = 0.0f;
+            const int row0c = (tile_lo + warp + 8 * it) * 16;
+            for (int i = lane; i < 16 * M; i += 32) {
+                const int m = i >> 4, r = row0c + (i & 15);
+                if (r < N) a.y[(size_t)m * N + r] = 0.0f;
+            }
         }
 
-    // ---- the slice's activation, as the decode product stages it: lane
-    // (gid, t) of a warp takes group gA + 8 b + gid of block b ----
-    for (int blk = warp; blk * 8 < Gs; blk += 8) {
-        const int gl = blk * 8 + gid;
-        const bool ok = gl < Gs;
-        float v[32];
-        if (ok) {
-            const uint4* s4 = reinterpret_cast<const uint4*>(a.x + (size_t)(gA + gl) * 128 + 32 * t);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 u = s4[q];
-                const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    v[8 * q + 2 * e] = __uint_as_float(uw[e] << 16);
-                    v[8 * q + 2 * e + 1] = __uint_as_float(uw[e] & 0xFFFF0000u);
+    // ---- the slice's activation, as the decode product stages it.  One
+    // token: lane (gid, t) of a warp takes group gA + 8 b + gid of block b.
+    // Several: item (g, nt) of the Gs x MT, warp w taking items w, w + 8, ...;
+    // lane (gid, t) holds token 8 nt + gid. ----
+    if constexpr (ONE) {
+        for (int blk = warp; blk * 8 < Gs; blk += 8) {
+            const int gl = blk * 8 + gid;
+            const bool ok = gl < Gs;
+            float v[32];
+            if (ok) {
+                const uint4* s4 = reinterpret_cast<const uint4*>(a.x + (size_t)(gA + gl) * 128 + 32 * t);
+    #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 u = s4[q];
+                    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        v[8 * q + 2 * e] = __uint_as_float(uw[e] << 16);
+                        v[8 * q + 2 * e + 1] = __uint_as_float(uw[e] & 0xFFFF0000u);
+                    }
                 }
+            } else {
+    #pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0.0f;
             }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+            float mx = 0.0f;
+    #pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(v[e]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            f3_check_stage_range(mx);
+            const int E = stage_exponent(mx);
+            uint32_t b[16];
+    #pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float c = stage_multiplier(E, j);
+                const __half2 lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);
+                const __half2 hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c);
+                b[2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
+                b[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
+            if (ok) {
+    #pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4*>(bfr + gl * 64 + q * 16 + t * 4) =
+                        make_uint4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+            }
+            // the ones pass of the block's eight groups: column n is group 8 b + n
+            float acc1[4];
+            const uint32_t ones[4] = {0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u};
+            unit_chain(acc1, ones, b);
+            const float c_lo = __shfl_sync(0xffffffffu, acc1[0], gid >> 1);
+            const float c_hi = __shfl_sync(0xffffffffu, acc1[1], gid >> 1);
+            const float F = __uint_as_float((uint32_t)(14 - E + 127) << 23);   // 2^(14-E)
+            if (ok && t == 0) fcs[gl] = make_float2(F, F * ((gid & 1) ? c_hi : c_lo));
         }
-        float mx = 0.0f;
+    } else {
+        for (int item = warp; item < Gs * MT; item += 8) {
+            const int g = item / MT, nt = item - g * MT;
+            const int m = nt * 8 + gid;
+            float v[32];
+            if (m < M) {
+                const uint4* s4 =
+                    reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + (size_t)(gA + g) * 128 + 32 * t);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(v[e]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        f3_check_stage_range(mx);
-        const int E = stage_exponent(mx);
-        uint32_t b[16];
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 u = s4[q];
+                    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float c = stage_multiplier(E, j);
-            const __half2 lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);
-            const __half2 hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c);
-            b[2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
-            b[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
-        }
-        if (ok) {
+                    for (int e = 0; e < 4; ++e) {
+                        v[8 * q + 2 * e] = __uint_as_float(uw[e] << 16);
+                        v[8 * q + 2 * e + 1] = __uint_as_float(uw[e] & 0xFFFF0000u);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+            }
+            float mx = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(v[e]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            f3_check_stage_range(mx);
+            const int E = stage_exponent(mx);
+            uint32_t b[16];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float c = stage_multiplier(E, j);
+                const __half2 lo = __floats2half2_rn(v[j] * c, v[j + 8] * c);
+                const __half2 hi = __floats2half2_rn(v[j + 16] * c, v[j + 24] * c);
+                b[2 * j] = *reinterpret_cast<const uint32_t*>(&lo);
+                b[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
+            unsigned char* fp = frag + (size_t)item * 2048 + lane * 16;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(bfr + gl * 64 + q * 16 + t * 4) =
-                    make_uint4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+                *reinterpret_cast<uint4*>(fp + q * 512) = make_uint4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+            // the all-ones pass: column n is token 8 nt + n; lane (., t) holds
+            // tokens 2t and 2t + 1, whose F the lanes of rows 2t and 2t + 1 hold
+            float acc1[4];
+            const uint32_t ones[4] = {0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u};
+            unit_chain(acc1, ones, b);
+            const float F = __uint_as_float((uint32_t)(14 - E + 127) << 23);
+            const float F0 = __shfl_sync(0xffffffffu, F, (2 * t) * 4);
+            const float F1 = __shfl_sync(0xffffffffu, F, (2 * t + 1) * 4);
+            if (gid == 0)
+                *reinterpret_cast<float4*>(corr + ((size_t)item * 4 + t) * 16) =
+                    make_float4(F0, F0 * acc1[0], F1, F1 * acc1[1]);
         }
-        // the ones pass of the block's eight groups: column n is group 8 b + n
-        float acc1[4];
-        const uint32_t ones[4] = {0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u};
-        unit_chain(acc1, ones, b);
-        const float c_lo = __shfl_sync(0xffffffffu, acc1[0], gid >> 1);
-        const float c_hi = __shfl_sync(0xffffffffu, acc1[1], gid >> 1);
-        const float F = __uint_as_float((uint32_t)(14 - E + 127) << 23);   // 2^(14-E)
-        if (ok && t == 0) fcs[gl] = make_float2(F, F * ((gid & 1) ? c_hi : c_lo));
     }
     __syncthreads();
 
@@ -536,7 +604,13 @@ __global__ void __launch_bounds__(kF3Threads, kF3mCtasPerSm) f3_mma_kernel(const
     bool add_ok = true;
     int s = 0;
     for (int it = 0; it < n_items; ++it) {
-        float y0 = 0.0f, y1 = 0.0f;   // rows gid and gid + 8
+        // rows gid and gid + 8; several tokens: tokens 8 nt + 2t and 8 nt + 2t + 1
+        float y0 = 0.0f, y1 = 0.0f;
+        float yt[MT][4];
+#pragma unroll
+        for (int nt = 0; nt < MT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) yt[nt][e] = 0.0f;
         for (int q = 0; q < nq; ++q, ++s) {
             const int slot = s & (kF3mDepth - 1);
             cp_async_wait<kF3mDepth - 1>();
@@ -573,21 +647,54 @@ __global__ void __launch_bounds__(kF3Threads, kF3mCtasPerSm) f3_mma_kernel(const
                 }
                 const uint32_t w[4] = {wd[0][0], wd[1][0], wd[0][1], wd[1][1]};
                 const int gl = kF3mQuad * q + u;
-                const uint4* bp = reinterpret_cast<const uint4*>(bfr + gl * 64 + t * 4);
-                uint32_t b[16];
+                if constexpr (ONE) {
+                    const uint4* bp = reinterpret_cast<const uint4*>(bfr + gl * 64 + t * 4);
+                    uint32_t b[16];
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    const uint4 z = bp[qq * 4];
-                    b[4 * qq] = z.x;
-                    b[4 * qq + 1] = z.y;
-                    b[4 * qq + 2] = z.z;
-                    b[4 * qq + 3] = z.w;
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const uint4 z = bp[qq * 4];
+                        b[4 * qq] = z.x;
+                        b[4 * qq + 1] = z.y;
+                        b[4 * qq + 2] = z.z;
+                        b[4 * qq + 3] = z.w;
+                    }
+                    float acc[4];
+                    unit_chain(acc, w, b);
+                    const float2 fc = fcs[gl];
+                    y0 = fmaf(s0[u], fmaf(fc.x, acc[0], -fc.y), y0);
+                    y1 = fmaf(s1[u], fmaf(fc.x, acc[2], -fc.y), y1);
+                } else {
+                    uint32_t b[MT][16];
+#pragma unroll
+                    for (int nt = 0; nt < MT; ++nt) {
+                        const unsigned char* fp = frag + (size_t)(gl * MT + nt) * 2048 + lane * 16;
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq) {
+                            const uint4 z = *reinterpret_cast<const uint4*>(fp + qq * 512);
+                            b[nt][4 * qq] = z.x;
+                            b[nt][4 * qq + 1] = z.y;
+                            b[nt][4 * qq + 2] = z.z;
+                            b[nt][4 * qq + 3] = z.w;
+                        }
+                    }
+                    float acc[MT][4];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t r[4];
+                        slot_regs<false>(j, w[0], w[1], w[2], w[3], r);
+#pragma unroll
+                        for (int nt = 0; nt < MT; ++nt)
+                            mma16816(acc[nt], r[0], r[1], r[2], r[3], b[nt][2 * j], b[nt][2 * j + 1], j > 0);
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < MT; ++nt) {
+                        const float4 f = *reinterpret_cast<const float4*>(corr + ((size_t)(gl * MT + nt) * 4 + t) * 16);
+                        yt[nt][0] = fmaf(s0[u], fmaf(f.x, acc[nt][0], -f.y), yt[nt][0]);   // row gid,     token 2t
+                        yt[nt][1] = fmaf(s0[u], fmaf(f.z, acc[nt][1], -f.w), yt[nt][1]);   // row gid,     token 2t+1
+                        yt[nt][2] = fmaf(s1[u], fmaf(f.x, acc[nt][2], -f.y), yt[nt][2]);   // row gid + 8, token 2t
+                        yt[nt][3] = fmaf(s1[u], fmaf(f.z, acc[nt][3], -f.w), yt[nt][3]);   // row gid + 8, token 2t+1
+                    }
                 }
-                float acc[4];
-                unit_chain(acc, w, b);
-                const float2 fc = fcs[gl];
-                y0 = fmaf(s0[u], fmaf(fc.x, acc[0], -fc.y), y0);
-                y1 = fmaf(s1[u], fmaf(fc.x, acc[2], -fc.y), y1);
             }
             __syncwarp();
             issue(slot);
@@ -597,24 +704,33 @@ __global__ void __launch_bounds__(kF3Threads, kF3mCtasPerSm) f3_mma_kernel(const
             }
         }
         const int row = (tile_lo + warp + 8 * it) * 16 + gid;
-        if (S == 1) {
-            if (t == 0) {
-                if (row < N) a.y[row] = y0;
-                if (row + 8 < N) a.y[row + 8] = y1;
+        if (adder && it == 0) {
+            int ok = 1;
+            if (lane == 0) {
+                ok = flag_seen != 0u || wait_flag_nonzero(flag, kFlagWaitNs);
+                if (!ok) report_device_error(&g_f3_error, kDevErrGemvConsumerWait);
             }
-        } else {
-            if (adder && it == 0) {
-                int ok = 1;
-                if (lane == 0) {
-                    ok = flag_seen != 0u || wait_flag_nonzero(flag, kFlagWaitNs);
-                    if (!ok) report_device_error(&g_f3_error, kDevErrGemvConsumerWait);
+            add_ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+            if (add_ok) count_seen();
+        }
+        auto put = [&](int m, int r, float v) {
+            if (m < M && r < N) {
+                float* p = a.y + (size_t)m * N + r;
+                if (S == 1) *p = v;
+                else atomicAdd(p, v);
+            }
+        };
+        if (add_ok) {
+            if constexpr (ONE) {
+                if (t == 0) {
+                    put(0, row, y0);
+                    put(0, row + 8, y1);
                 }
-                add_ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
-                if (add_ok) count_seen();
-            }
-            if (add_ok && t == 0) {
-                if (row < N) atomicAdd(a.y + row, y0);
-                if (row + 8 < N) atomicAdd(a.y + row + 8, y1);
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < MT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) put(nt * 8 + 2 * t + (e & 1), row + 8 * (e >> 1), yt[nt][e]);
             }
         }
     }
@@ -622,7 +738,9 @@ __global__ void __launch_bounds__(kF3Threads, kF3mCtasPerSm) f3_mma_kernel(const
 }
 
 
-size_t f3m_smem(int Gs) { return (size_t)kF3mRingBytes + kF3mLutBytes + (size_t)Gs * kF3mGroupBytes; }
+// per group: the staged activation and its correction (one token: 256 + 8
+// bytes; MT token tiles: MT x (2048 + 64))
+size_t f3m_smem(int Gs, int per_group) { return (size_t)kF3mRingBytes + kF3mLutBytes + (size_t)Gs * per_group; }
 
 // The one-token plan: slices of whole quads and ranges of tiles, as the
 // tile-major decode loop plans them (the longest warp's stages against the
@@ -632,14 +750,14 @@ struct F3mPlan {
     int S, cps, ctas;
     size_t smem;
 };
-bool f3m_plan(int N, int K, int sms, int optin, F3mPlan* out) {
+bool f3m_plan(int N, int K, int per_group, int sms, int optin, F3mPlan* out) {
     const int G = K / 128, Gq = G / kF3mQuad, T = (N + 15) / 16;
     double best = 0.0;
     F3mPlan bp{};
     for (int S = 1; S <= Gq && S <= 64; ++S) {
         if (S > 1 && G <= 8) break;
         const int qmax = (Gq + S - 1) / S;
-        const size_t sm = f3m_smem(kF3mQuad * qmax);
+        const size_t sm = f3m_smem(kF3mQuad * qmax, per_group);
         if (sm > (size_t)optin) continue;
         const int per_sm = std::min(kF3mCtasPerSm, (int)((228 * 1024) / (sm + 1024)));
         if (per_sm < 1) continue;
@@ -732,44 +850,47 @@ extern "C" tern_status tern_f3_gemv(const void* x, const uint8_t* packed, const 
         }
     }
     cudaError_t e;
-    if (M == 1 && K % (kF3mQuad * 128) == 0) {
-        // one token on the tensor pipe
-        static int optin_of[64] = {};
-        static F3mPlan plan_of[64][8];
-        static int plan_key[64][8][2];
+    if (K % (kF3mQuad * 128) == 0) {
+        // the tensor pipe: one token, one token tile (up to 8) or two
+        const int kind = M == 1 ? 0 : (M <= 8 ? 1 : 2);
+        const int per_group = kind == 0 ? 256 + 8 : (kind == 1 ? 2048 + 64 : 2 * (2048 + 64));
+        auto kern = kind == 0 ? f3_mma_kernel<1, true> : (kind == 1 ? f3_mma_kernel<1, false> : f3_mma_kernel<2, false>);
+        static int optin_of[64][3] = {};
+        static F3mPlan plan_of[64][16];
+        static int plan_key[64][16][3];
         static int plan_n[64] = {};
         F3mPlan p{};
         bool have = false;
         {
             std::lock_guard<std::mutex> lk(mu);
-            if (!optin_of[dev]) {
+            if (!optin_of[dev][kind]) {
                 int optin = 0;
                 cudaFuncAttributes fa;
                 if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-                    cudaFuncGetAttributes(&fa, f3_mma_kernel) != cudaSuccess)
+                    cudaFuncGetAttributes(&fa, kern) != cudaSuccess)
                     return TERN_ERR_CUDA;
                 optin -= (int)fa.sharedSizeBytes;
-                if (cudaFuncSetAttribute(f3_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
-                    cudaSuccess)
+                if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess)
                     return TERN_ERR_CUDA;
-                optin_of[dev] = optin;
+                optin_of[dev][kind] = optin;
             }
             for (int i = 0; i < plan_n[dev]; ++i)
-                if (plan_key[dev][i][0] == N && plan_key[dev][i][1] == K) {
+                if (plan_key[dev][i][0] == N && plan_key[dev][i][1] == K && plan_key[dev][i][2] == kind) {
                     p = plan_of[dev][i];
                     have = true;
                 }
             if (!have) {
-                if (!f3m_plan(N, K, sms, optin_of[dev], &p)) return TERN_ERR_SHAPE;
-                const int slot = plan_n[dev] < 8 ? plan_n[dev]++ : (N + K) % 8;
+                if (!f3m_plan(N, K, per_group, sms, optin_of[dev][kind], &p)) return TERN_ERR_SHAPE;
+                const int slot = plan_n[dev] < 16 ? plan_n[dev]++ : (N + K + kind) % 16;
                 plan_key[dev][slot][0] = N;
                 plan_key[dev][slot][1] = K;
+                plan_key[dev][slot][2] = kind;
                 plan_of[dev][slot] = p;
             }
         }
         F3mArgs args{reinterpret_cast<const __nv_bfloat16*>(x), packed, reinterpret_cast<const __half*>(scales), y,
-                     N, K, K / 128, (N + 15) / 16, p.S, p.cps};
-        e = launch_pdl(f3_mma_kernel, dim3(p.ctas), dim3(kF3Threads), p.smem, (cudaStream_t)stream, true, args);
+                     M, N, K, K / 128, (N + 15) / 16, p.S, p.cps};
+        e = launch_pdl(kern, dim3(p.ctas), dim3(kF3Threads), p.smem, (cudaStream_t)stream, true, args);
     } else if (M <= kF3TabMaxM) {
         // persistent: kF3TabCtasPerSm CTAs per SM, at most kF3TabRowsPerWarp rows per warp
         const int per_cta_cap = kF3Warps * kF3TabRowsPerWarp;

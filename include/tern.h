@@ -169,12 +169,18 @@ tern_status tern_f3_pack(const int8_t *t, int N, int K, uint8_t *packed, int *ba
  * W[n][k] = (q[n][k] - 1) s[n][k/128].  x bf16 [M][K], packed as tern_f3_pack
  * writes it, scales fp16 [N][K/128]; x, packed, scales and y 16-byte aligned,
  * owned by the caller.  1 <= M <= 16, N >= 1, K >= 128 with K % 128 == 0.
- * One kernel launch, no workspace; every element of y is written.  It runs on
- * the CUDA cores (fp32 FMAs, a 243-entry table per byte): the five trits of a
- * byte cannot be separated by masks the way the 2-bit slots are.  Results
- * agree with the exact product to within 1e-3 * sum_k |x w| + 1e-6 per
- * element.  A byte above 242 (above 26 for a group's last byte) is not a
- * pack's; its weights are undefined. */
+ * One kernel launch, no workspace; every element of y is written.  With K a
+ * multiple of 512 it runs on the tensor pipe: each byte's five trits become
+ * 2-bit codes through a table, and the product is tern_gemv's, with its
+ * accuracy statement (including the group term and the rule that a group
+ * whose largest |x| is 2^100 or more, or not finite, is reported as
+ * TERN_DEVERR_GEMV_ACTIVATION_RANGE through tern_device_error(), y then
+ * undefined); its K-slices meet through flag words in a file-scope array
+ * that every call on a device shares, so calls on different streams must be
+ * ordered by the caller.  Otherwise it runs on the CUDA cores (fp32 FMAs, a
+ * 243-entry table per byte) and agrees with the exact product to within
+ * 1e-3 * sum_k |x w| + 1e-6 per element.  A byte above 242 (above 26 for a
+ * group's last byte) is not a pack's; its weights are undefined. */
 tern_status tern_f3_gemv(const void *x, const uint8_t *packed, const void *scales, float *y,
                          int M, int N, int K, tern_stream_t stream);
 

@@ -141,3 +141,41 @@ def test_f3_one_token_bytes_outside_the_pack(tern, orc):
     torch.cuda.synchronize()
     assert tern.device_error() == 0
     assert torch.isfinite(y).all()
+
+
+@pytest.mark.parametrize("M", [2, 5, 9, 16])
+@pytest.mark.parametrize("N,K", [(37, 512), (300, 1536), (129, 17408)])
+def test_f3_gemv_tokens_tensor_pipe(tern, orc, M, N, K):
+    """Several tokens with K a multiple of 512 (one token tile up to eight
+    tokens, two up to sixteen): every output against the oracle."""
+    p = synth.problem(98 + M, M, N, K, tag=f"f3t{N}x{K}")
+    packed, bad = orc.f3_pack(p.t)
+    assert bad == 0
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    tern.f3_gemv(dev_bf16(p.x), torch.from_numpy(packed).cuda(), dev_scales(p.s), y=y)
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    y_ref, a_ref = orc.f3_matmul(p.x, packed, p.s)
+    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what=f"f3 M={M} N={N} K={K}")
+
+
+def test_f3_tokens_exact_cases(tern, orc):
+    """Sixteen tokens, x = 2 at a different position for each: 2 s exactly,
+    over every position of a 512-wide row."""
+    N, K, M = 16, 512, 16
+    s = synth.scales(99, "f3te", (N, K // 128), synth.SCALE_UNIFORM)
+    t = np.ones((N, K), dtype=np.int8)
+    t[1::2] = -1
+    t[:, 60:70] *= -1
+    packed, _ = orc.f3_pack(t)
+    dp = torch.from_numpy(packed).cuda()
+    ds = dev_scales(s)
+    for k0 in range(0, K, M):
+        x = np.zeros((M, K), dtype=np.uint16)
+        for i in range(M):
+            x[i, k0 + i] = 0x4000                           # bf16 2.0
+        y = tern.f3_gemv(dev_bf16(x), dp, ds).cpu().numpy()
+        for i in range(M):
+            k = k0 + i
+            want = 2.0 * t[:, k].astype(np.float64) * s[:, k // 128].astype(np.float64)
+            assert np.array_equal(y[i].astype(np.float64), want), k
