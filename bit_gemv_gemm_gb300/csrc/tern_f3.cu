@@ -327,9 +327,10 @@ f3_gemv_table_kernel(const __nv_bfloat16* __restrict__ x, const uint8_t* __restr
 // activation, the all-ones correction, the group scale.  Lane (gid, t) takes
 // weights 32 t .. 32 t + 31 of a group: bytes from b0 = 32 t / 5 on, the first
 // 2 (32 t mod 5) bits of b0's codes dropped; seven bytes hold them, eight for
-// t = 2 (weights 64 .. 95 start at b0's last trit and end at byte 19's first).  The table has a copy
-// per lane ([v][lane] halfwords), so a warp's lookups never share a bank word
-// across different values.
+// t = 2 (weights 64 .. 95 start at b0's last trit and end at byte 19's
+// first).  The table has a copy per lane ([v][lane] halfwords), so a warp's
+// lookups conflict at most two ways (the two lanes of a pair share each
+// word's bank).
 //
 // Work split (as the tile-major decode loop): K-slices of whole quads of
 // groups, ranges of 16-row tiles, a warp owning whole tiles and walking its
