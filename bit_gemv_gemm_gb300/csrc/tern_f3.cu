@@ -786,7 +786,10 @@ size_t f3_smem_bytes(int M) { return (size_t)(kF3Lut + M * kF3Chunk) * sizeof(fl
 using namespace tern;
 
 namespace tern {
-// Reads and clears the base-3 product's device error word.
+// Reads and clears the base-3 product's device error word.  A reported error
+// may have stopped a call before its range flags counted back to 0 (a slice
+// that gave up its wait never counts), so the flags are cleared with it: the
+// next call starts from zeros again.  The caller has synchronised the device.
 cudaError_t read_f3_device_error(int* code) {
     int v = 0;
     cudaError_t e = cudaMemcpyFromSymbol(&v, g_f3_error, sizeof(int));
@@ -794,6 +797,11 @@ cudaError_t read_f3_device_error(int* code) {
     if (v != 0) {
         const int z = 0;
         e = cudaMemcpyToSymbol(g_f3_error, &z, sizeof(int));
+        if (e != cudaSuccess) return e;
+        void* flags = nullptr;
+        e = cudaGetSymbolAddress(&flags, g_f3_flags);
+        if (e != cudaSuccess) return e;
+        e = cudaMemset(flags, 0, sizeof(g_f3_flags));
         if (e != cudaSuccess) return e;
     }
     *code = v;

@@ -177,7 +177,9 @@ tern_status tern_f3_pack(const int8_t *t, int N, int K, uint8_t *packed, int *ba
  * TERN_DEVERR_GEMV_ACTIVATION_RANGE through tern_device_error(), y then
  * undefined); its K-slices meet through flag words in a file-scope array
  * that every call on a device shares, so calls on different streams must be
- * ordered by the caller.  Otherwise it runs on the CUDA cores (fp32 FMAs, a
+ * ordered by the caller.  The words count back to 0 in every call; after a
+ * call that reported a device error, tern_device_error() clears them as it
+ * reads the error.  Otherwise it runs on the CUDA cores (fp32 FMAs, a
  * 243-entry table per byte) and agrees with the exact product to within
  * 1e-3 * sum_k |x w| + 1e-6 per element.  A byte above 242 (above 26 for a
  * group's last byte) is not a pack's; its weights are undefined. */
