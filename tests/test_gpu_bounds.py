@@ -88,7 +88,7 @@ def test_fwht_writes_only_its_output(tern, M, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 1000, 5120), (1, 17408, 5120), (3, 777, 17408), (6, 129, 2176),
-                                   (16, 200, 512), (5, 16, 128)])
+                                   (16, 200, 512), (5, 16, 128), (8, 300, 2560)])
 def test_gemv_writes_only_its_output(tern, orc, M, N, K):
     p = synth.problem(700 + M, M, N, K, tag=f"cv{N}x{K}")
     x, codes, s = dev_bf16(p.x), tern.pack(dev_trits(p.t)), dev_scales(p.s)
@@ -101,6 +101,47 @@ def test_gemv_writes_only_its_output(tern, orc, M, N, K):
     assert tern.device_error() == 0
     y_ref, a_ref = orc.matmul(p.x, orc.pack(p.t)[0], p.s)
     assert_fp32_close(y.t.cpu().numpy(), y_ref, a_ref, what=f"canary gemv M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 5120), (1, 129, 17408), (5, 77, 2048), (16, 33, 1024), (3, 40, 640)])
+def test_f3_gemv_writes_only_its_output(tern, orc, M, N, K):
+    """The base-3 product (no workspace: its range flags are file-scope) twice
+    into a guarded y: the margins intact, no device error, the second call
+    (after the first has returned its flags to zero) against the oracle."""
+    p = synth.problem(760 + M, M, N, K, tag=f"c3{N}x{K}")
+    packed, bad = orc.f3_pack(p.t)
+    assert bad == 0
+    y = Guarded((M, N), torch.float32)
+    for _ in range(2):
+        tern.f3_gemv(dev_bf16(p.x), torch.from_numpy(packed).cuda(), dev_scales(p.s), y=y.t)
+        assert y.margins_intact()
+    assert tern.device_error() == 0
+    y_ref, a_ref = orc.f3_matmul(p.x, packed, p.s)
+    assert_fp32_close(y.t.cpu().numpy(), y_ref, a_ref, what=f"canary f3 M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M", [1, 5])
+def test_f3_gemv_reports_activation_out_of_range(tern, orc, M):
+    """The base-3 tensor-pipe product stages the activation as the decode
+    product does: a group whose largest |x| is 2^100 or more is reported as
+    TERN_DEVERR_GEMV_ACTIVATION_RANGE, and the next in-range call (after the
+    report was read) matches the oracle."""
+    N, K = 300, 2048
+    p = synth.problem(1750 + M, M, N, K, tag="f3range")
+    packed, bad = orc.f3_pack(p.t)
+    assert bad == 0
+    dp, ds = torch.from_numpy(packed).cuda(), dev_scales(p.s)
+    assert tern.device_error() == 0
+    x = p.x.copy()
+    x[M - 1, 1500] = np.uint16(np.array([2.0 ** 101], dtype=np.float32).view(np.uint32)[0] >> 16)
+    tern.f3_gemv(dev_bf16(x), dp, ds)
+    torch.cuda.synchronize()
+    assert tern.device_error() == tern.DEVERR_GEMV_ACTIVATION_RANGE
+    y = tern.f3_gemv(dev_bf16(p.x), dp, ds)
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    y_ref, a_ref = orc.f3_matmul(p.x, packed, p.s)
+    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what=f"f3 after a range report M={M}")
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 1000, 5120), (3, 777, 17408), (6, 129, 2176), (16, 200, 640)])
