@@ -933,8 +933,11 @@ constexpr int kTCtasPerSm = 2;
 // two, the extra registers spill)
 template <int MT> struct TStage { static constexpr int kBatch = MT == 1 ? 3 : 1; };
 // From five tokens on (where the product above turns to shared atomics) the
-// tile-major loop is the faster one; below it, the product above.
+// tile-major loop is the faster one; from two, also for matrices of at most
+// kTileSmallN rows (measured on 5120 -> 6144: 6.54 / 6.56 us at two / four
+// tokens against 6.80 / 7.37; on 5120 -> 17408 the product above stays ahead).
 constexpr int kTileMinM = 5;
+constexpr int kTileSmallN = 8192;
 
 // A unit's chains for all MT token tiles, each slot unpacked once for all.
 template <int MT>
@@ -1612,7 +1615,7 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
         args.x = xs;
         args.xe = xe;
         launches = 2;
-        if (M >= kTileMinM)
+        if (M >= kTileMinM || N <= kTileSmallN)
             st = MT == 1 ? launch_gemv_t<1, true>(args, sms, stream) : launch_gemv_t<2, true>(args, sms, stream);
         else
             st = MT == 1 ? launch_gemv<1, true, false, true>(args, sms, stream)
@@ -1629,7 +1632,7 @@ tern_status run(const void* x, const int8_t* signs, const uint32_t* codes, const
         st = M == 1 ? launch_gemv<1, false, true, true, true>(args, sms, stream)
              : MT == 1 ? launch_gemv<1, false, false, true, true>(args, sms, stream)
                        : launch_gemv<2, false, false, true, true>(args, sms, stream);
-    } else if (M >= kTileMinM && K % (kTDuo * kGroup) == 0) {
+    } else if ((M >= kTileMinM || (M >= 2 && N + N2 <= kTileSmallN)) && K % (kTDuo * kGroup) == 0) {
         st = MT == 1 ? launch_gemv_t<1>(args, sms, stream) : launch_gemv_t<2>(args, sms, stream);
     } else {
         st = M == 1 ? (lean ? launch_gemv<1, false, true, true>(args, sms, stream)

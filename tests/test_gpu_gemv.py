@@ -91,10 +91,11 @@ def test_gemv_ragged_shapes(tern, orc, M, N, K):
     assert_fp32_close(y, y_ref, a_ref, what=f"M={M} N={N} K={K}")
 
 
-@pytest.mark.parametrize("M", [5, 8, 9, 16])
+@pytest.mark.parametrize("M", [2, 3, 5, 8, 9, 16])
 @pytest.mark.parametrize("N,K", [(37, 512), (300, 1536), (77, 2304), (1000, 3072), (129, 17408)])
 def test_gemv_tile_major_shapes(tern, orc, M, N, K):
-    """Five tokens and more with K a multiple of 256 (the tile-major loop):
+    """Five tokens and more, or two and more on at most 8192 rows, with K a
+    multiple of 256 (the tile-major loop):
     ragged N (an odd tile count leaves a pair's second tile past the matrix),
     one K-slice and several, every output against the oracle."""
     p = synth.problem(120 + M, M, N, K, tag=f"tm{N}x{K}")
@@ -291,6 +292,19 @@ def test_fwht_gemm_fused_matches_oracle(tern, orc, M, K):
     torch.cuda.synchronize()
     y_ref, a_ref = orc.rotate_matmul(p.x, p.signs, orc.pack(p.t)[0], p.s)
     assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what=f"fused M={M}")
+
+
+def test_fwht_gemm_fused_large_n(tern, orc):
+    """Three tokens on more than 8192 rows: the prologue's staged fragments
+    read by the per-group product (smaller matrices take the tile-major one)."""
+    M, N, K = 3, 9000, 4096
+    p = synth.problem(64, M, N, K, with_signs=True, tag="fzl")
+    codes = tern.pack(dev_trits(p.t))
+    y = tern.fwht_gemm(dev_bf16(p.x), torch.from_numpy(p.signs).cuda(), codes, dev_scales(p.s))
+    torch.cuda.synchronize()
+    assert tern.device_error() == 0
+    y_ref, a_ref = orc.rotate_matmul(p.x, p.signs, orc.pack(p.t)[0], p.s)
+    assert_fp32_close(y.cpu().numpy(), y_ref, a_ref, what="fused M=3 N=9000")
 
 
 @pytest.mark.parametrize("M", [1, 16])
