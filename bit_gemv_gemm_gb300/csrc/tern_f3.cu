@@ -328,9 +328,10 @@ f3_gemv_table_kernel(const __nv_bfloat16* __restrict__ x, const uint8_t* __restr
 // weights 32 t .. 32 t + 31 of a group: bytes from b0 = 32 t / 5 on, the first
 // 2 (32 t mod 5) bits of b0's codes dropped; seven bytes hold them, eight for
 // t = 2 (weights 64 .. 95 start at b0's last trit and end at byte 19's
-// first).  The table has a copy per lane ([v][lane] halfwords), so a warp's
-// lookups conflict at most two ways (the two lanes of a pair share each
-// word's bank).
+// first).  The table's 32-bit entries ([v][lane % 16]) hold the codes already
+// shifted for the lane's offset in b0, so the assembly takes fixed shifts;
+// lanes l and l + 16 share a copy, so a warp's lookups conflict at most two
+// ways.
 //
 // Work split (as the tile-major decode loop): K-slices of whole quads of
 // groups, ranges of 16-row tiles, a warp owning whole tiles and walking its
@@ -347,7 +348,7 @@ constexpr int kF3mRowBytes = 26 * kF3mQuad;                    // a row's bytes 
 constexpr int kF3mCodeBytes = 16 * kF3mRowBytes;
 constexpr int kF3mStageBytes = kF3mCodeBytes + 16 * kF3mQuad * 2;   // and the tile's 16 x 4 scales
 constexpr int kF3mRingBytes = 8 * kF3mDepth * kF3mStageBytes;
-constexpr int kF3mLutBytes = 256 * 32 * 2;                    // [byte][lane] halfwords
+constexpr int kF3mLutBytes = 256 * 16 * 4;                    // [byte][lane % 16] words
 constexpr int kF3mCtasPerSm = 2;
 constexpr int kF3mMaxRanges = 4096;                           // range flags in the file-scope array
 
@@ -373,7 +374,7 @@ template <int MT, bool ONE>
 __global__ void __launch_bounds__(kF3Threads, kF3mCtasPerSm) f3_mma_kernel(const F3mArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int G = a.G, S = a.S, N = a.N, M = ONE ? 1 : a.M;
-    constexpr int kFrag = ONE ? 256 : MT * 2048, kCorr = ONE ? 8 : MT * 64;   // per group
+    constexpr int kFrag = ONE ? 256 : MT * 2048;   // staged activation bytes per group
     const size_t pitch = (size_t)26 * G;   // bytes per row
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, t = lane & 3;
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(kF3Threads, kF3mCtasPerSm) f3_mma_kernel(const
     const int n_st = n_items * nq;
 
     unsigned char* const ring = smem + (size_t)warp * kF3mDepth * kF3mStageBytes;
-    const unsigned short* const lut = reinterpret_cast<const unsigned short*>(smem + kF3mRingBytes);
+    const uint32_t* const lut = reinterpret_cast<const uint32_t*>(smem + kF3mRingBytes);
     // ONE: [Gs][4][t][4 words] and [Gs] (F, F acc1); else [Gs][MT][4][32 lanes][16 B] and [Gs][MT][t] float4
     unsigned char* const frag = smem + kF3mRingBytes + kF3mLutBytes;
     unsigned char* const corr = frag + (size_t)Gs * kFrag;
@@ -439,8 +440,12 @@ __global__ void __launch_bounds__(kF3Threads, kF3mCtasPerSm) f3_mma_kernel(const
 #pragma unroll
     for (int i = 0; i < kF3mDepth; ++i) issue(i);
 
-    // the byte table, a copy per lane: entry v holds v's five codes, two
-    // copies per 32-bit word
+    // the byte table, a copy per lane l % 16 (lanes l and l + 16 share theirs):
+    // entry v of lane (gid, t) holds v's five codes shifted left by 8 - r0(t),
+    // where r0(t) = 2 (32 t mod 5) is the number of bits of the lane's first
+    // byte that belong to the lane before it (0, 4, 8, 2 for t = 0..3), so
+    // that the assembly below shifts by amounts that are the same for every
+    // lane
     for (int v = threadIdx.x; v < 256; v += kF3Threads) {
         int c = 0, r = v;
 #pragma unroll
@@ -450,9 +455,9 @@ __global__ void __launch_bounds__(kF3Threads, kF3mCtasPerSm) f3_mma_kernel(const
         }
         if (v >= 243) c = v & 0x3FF;   // not a pack's byte: some codes, never out of bounds
         uint32_t* row = reinterpret_cast<uint32_t*>(smem + kF3mRingBytes) + v * 16;
-        const uint32_t two = (uint32_t)c | ((uint32_t)c << 16);
+        const uint32_t sh4[4] = {(uint32_t)c << 8, (uint32_t)c << 4, (uint32_t)c, (uint32_t)c << 6};
 #pragma unroll
-        for (int l = 0; l < 16; ++l) row[l] = two;
+        for (int l = 0; l < 16; ++l) row[l] = sh4[l & 3];
     }
     pdl_wait();
 
@@ -598,9 +603,10 @@ __global__ void __launch_bounds__(kF3Threads, kF3mCtasPerSm) f3_mma_kernel(const
     if (adder && n_st == 0) count_seen();
 
     // ---- the stages ----
-    // this lane's 7 bytes of a group: b0 .. b0 + 6, the first r0 bits of b0's codes dropped
-    const int b0 = (32 * t) / 5, r0 = 2 * (32 * t - 5 * b0);
-    const unsigned short* const lut_l = lut + lane;
+    // this lane's bytes of a group: b0 .. b0 + 7, the first r0(t) bits of b0's
+    // codes dropped (the table's shift accounts for them)
+    const int b0 = (32 * t) / 5;
+    const uint32_t* const lut_l = lut + (lane & 15);
     unsigned flag_seen = 0u;
     bool add_ok = true;
     int s = 0;
@@ -640,11 +646,15 @@ __global__ void __launch_bounds__(kF3Threads, kF3mCtasPerSm) f3_mma_kernel(const
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const uint32_t byte = __byte_perm(i < 4 ? x0 : x1, 0u, 0x4440u | (uint32_t)(i & 3));
-                        L[i] = lut_l[byte * 32];
+                        L[i] = lut_l[byte * 16];
                     }
-                    wd[h][0] = (L[0] >> r0) | (L[1] << (10 - r0)) | (L[2] << (20 - r0)) | (L[3] << (30 - r0));
-                    wd[h][1] = (L[3] >> (r0 + 2)) | (L[4] << (8 - r0)) | (L[5] << (18 - r0)) | (L[6] << (28 - r0)) |
-                               (r0 == 8 ? L[7] << 30 : 0u);
+                    // L[i] = byte i's codes << (8 - r0): they sit at bits
+                    // 10 i - r0 of the lane's 64-bit code stream, so each
+                    // part lands by a fixed shift and the parts never overlap
+                    // (a sum is their OR); byte 7 reaches bits 30-31 of the
+                    // second word only when r0 = 8 and shifts out otherwise
+                    wd[h][0] = (L[0] >> 8) + (L[1] << 2) + (L[2] << 12) + (L[3] << 22);
+                    wd[h][1] = (L[3] >> 10) + L[4] + (L[5] << 10) + (L[6] << 20) + (L[7] << 30);
                 }
                 const uint32_t w[4] = {wd[0][0], wd[1][0], wd[0][1], wd[1][1]};
                 const int gl = kF3mQuad * q + u;

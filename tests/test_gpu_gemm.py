@@ -102,6 +102,28 @@ def test_gemm_exact_cases(tern):
         assert np.array_equal(y[m].astype(np.float64), W[:, m % K]), m
 
 
+def test_gemm_exact_cases_ragged_tokens(tern):
+    """Three token tiles, the last one ragged (M = 700): zero weights give
+    exactly 0, and one-hot x picks t * bf16(s) exactly at every (token, k)."""
+    M, N, K = 700, 136, 256
+    t = np.zeros((N, K), dtype=np.int8)
+    s = synth.scales(9, "ws", (N, K // 128))
+    x = synth.activations(9, "wx", (M, K))
+    y = tern.gemm(dev_bf16(x), tern.pack(dev_trits(t)), dev_scales(s))
+    torch.cuda.synchronize()
+    assert (y.cpu().numpy() == 0).all()
+    t = synth.trits(10, "wt", (N, K), synth.UNIFORM)
+    x = np.zeros((M, K), dtype=np.uint16)
+    for m in range(M):
+        x[m, (7 * m) % K] = 0x3F80
+    y = tern.gemm(dev_bf16(x), tern.pack(dev_trits(t)), dev_scales(s)).cpu().numpy()
+    assert tern.device_error() == 0
+    sb = torch.from_numpy(s.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    W = t.astype(np.float64) * np.repeat(sb, 128, axis=1)
+    for m in range(M):
+        assert np.array_equal(y[m].astype(np.float64), W[:, (7 * m) % K]), m
+
+
 @pytest.mark.parametrize("name,K,N", [(n, k, nn) for (n, k, nn) in synth.PREFILL_LAYER])
 def test_gemm_prefill_layer_sampled(tern, orc, name, K, N):
     """One pp512 layer's projection at full size (M=512), sampled outputs."""
