@@ -306,45 +306,87 @@ def bench_decode(tern, sweep: DecodeSweep, steps: int, warmup: int, ws_count: in
 
     # end to end through the same API: H2D of every projection's x, the sweep,
     # D2H of every y; pinned host buffers, copies inside the timed region.
+    # Two buffer sets: step i + 1's input copy and step i - 1's output copy run
+    # on a copy stream beside step i's sweep, and every step still copies its
+    # own inputs in and its own results out.
     xh = [x.cpu().pin_memory() for x in xs]
-    yh = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys]
-    xin = torch.cat([x.flatten() for x in xs])
     xhost = torch.cat([x.flatten() for x in xh]).pin_memory()
-    yout = torch.cat([y.flatten() for y in ys])
-    yhost = torch.empty_like(yout, device="cpu").pin_memory()
-    views, off = [], 0
-    for x in xs:
-        views.append(xin[off:off + x.numel()].view(x.shape))
-        off += x.numel()
-    yviews, off = [], 0
-    for y in ys:
-        yviews.append(yout[off:off + y.numel()].view(y.shape))
-        off += y.numel()
-    g2 = graph_of(lambda: sweep.run(views, yviews, ws, pair))
     st = torch.cuda.current_stream()
+    cp = torch.cuda.Stream()
+    sets = []
+    for _ in range(2):
+        xin = torch.empty(xhost.numel(), dtype=xhost.dtype, device="cuda")
+        yout = torch.empty(sum(y.numel() for y in ys), dtype=torch.float32, device="cuda")
+        views, off = [], 0
+        for x in xs:
+            views.append(xin[off:off + x.numel()].view(x.shape))
+            off += x.numel()
+        yviews, off = [], 0
+        for y in ys:
+            yviews.append(yout[off:off + y.numel()].view(y.shape))
+            off += y.numel()
+        g2 = graph_of(lambda v=views, yv=yviews: sweep.run(v, yv, ws, pair))
+        yhost = torch.empty(yout.numel(), dtype=torch.float32).pin_memory()
+        sets.append({"xin": xin, "yout": yout, "g": g2, "yhost": yhost,
+                     "h2d": torch.cuda.Event(), "comp": torch.cuda.Event()})
 
-    def e2e_step():
-        xin.copy_(xhost, non_blocking=True)
-        g2.replay()
-        yhost.copy_(yout, non_blocking=True)
+    def e2e_run(n):
+        """n pipelined steps; returns ms from the first input copy to the last output copy."""
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cp.wait_stream(st)
+        with torch.cuda.stream(cp):
+            a.record(cp)
+            sets[0]["xin"].copy_(xhost, non_blocking=True)
+            sets[0]["h2d"].record(cp)
+        for i in range(n):
+            cur, nxt = sets[i % 2], sets[(i + 1) % 2]
+            if i + 1 < n:
+                with torch.cuda.stream(cp):
+                    if i >= 1:
+                        cp.wait_event(nxt["comp"])       # step i - 1's sweep has read its x
+                    nxt["xin"].copy_(xhost, non_blocking=True)
+                    nxt["h2d"].record(cp)
+            st.wait_event(cur["h2d"])
+            cur["g"].replay()
+            cur["comp"].record(st)
+            with torch.cuda.stream(cp):
+                cp.wait_event(cur["comp"])
+                cur["yhost"].copy_(cur["yout"], non_blocking=True)
+        with torch.cuda.stream(cp):
+            b.record(cp)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    e2e_run(3)
+    e_steps = max(10, steps // 4)
+    barrier(ws_count)
+    e2e_ms = max_over_ranks(e2e_run(e_steps) / e_steps, ws_count)
+
+    # the same, one step after another on one stream (no overlap), for comparison
+    s0 = sets[0]
+
+    def serial_step():
+        s0["xin"].copy_(xhost, non_blocking=True)
+        s0["g"].replay()
+        s0["yhost"].copy_(s0["yout"], non_blocking=True)
 
     for _ in range(3):
-        e2e_step()
+        serial_step()
     torch.cuda.synchronize()
-    e_steps = max(10, steps // 4)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws_count)
     a.record(st)
     for _ in range(e_steps):
-        e2e_step()
+        serial_step()
     b.record(st)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(a.elapsed_time(b) / e_steps, ws_count)
-    del xh, yh
+    serial_ms = max_over_ranks(a.elapsed_time(b) / e_steps, ws_count)
+    yhost = s0["yhost"]
+    del xh
     return {
         "ms": ms, "clocks": clk.summary(), "launches_per_step": launches,
         "weight_bytes": sweep.weight_bytes(), "alg_bytes": sweep.alg_bytes(M, pair),
-        "e2e_ms": e2e_ms, "h2d": xhost.numel() * 2, "d2h": yhost.numel() * 4,
+        "e2e_ms": e2e_ms, "e2e_serial_ms": serial_ms, "h2d": xhost.numel() * 2, "d2h": yhost.numel() * 4,
     }
 
 
@@ -1002,7 +1044,9 @@ def main() -> None:
                      "traffic": load_traffic("gemv_kernel", GEMV_SRC), **traffic_note("gemv_kernel", GEMV_SRC)},
         "clocks": dec["clocks"],
         "e2e": {"value": ws_count * dec["weight_bytes"] / (dec["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": dec["h2d"], "d2h_bytes_per_step": dec["d2h"]},
+                "h2d_bytes_per_step": dec["h2d"], "d2h_bytes_per_step": dec["d2h"],
+                "copies": "copy stream beside the sweep, two buffer sets",
+                "serial_value": ws_count * dec["weight_bytes"] / (dec["e2e_serial_ms"] * 1e-3) / 1e9},
         "gpu_launches": dec["launches_per_step"] * args.steps,
         "rows": rows,
     }
