@@ -34,7 +34,7 @@ fwht_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restrict__ sign
 __global__ void __launch_bounds__(kFwhtThreads)
 fwht_slice_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restrict__ signs,
                   __nv_bfloat16* __restrict__ y, int K) {
-    __shared__ float sm[kFwhtSliceSmemFloats];
+    __shared__ __align__(16) float sm[kFwhtSliceSmemFloats];
     pdl_launch_dependents();
     pdl_wait();
     const int sigma = blockIdx.x, m = blockIdx.y, b = sigma >> 2;
@@ -42,8 +42,9 @@ fwht_slice_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restrict_
     fwht1024_slice(x + off, signs + (size_t)b * kFwhtN, sigma & 3, sm);
     // thread i writes values 4 i .. 4 i + 3 of the slice: 8-byte stores, coalesced
     const int i = threadIdx.x;
-    const __nv_bfloat162 p0 = __floats2bfloat162_rn(sm[fwht_pos(4 * i)], sm[fwht_pos(4 * i + 1)]);
-    const __nv_bfloat162 p1 = __floats2bfloat162_rn(sm[fwht_pos(4 * i + 2)], sm[fwht_pos(4 * i + 3)]);
+    const float4 q = *reinterpret_cast<const float4*>(sm + fwht_slice_pos(4 * i));
+    const __nv_bfloat162 p0 = __floats2bfloat162_rn(q.x, q.y);
+    const __nv_bfloat162 p1 = __floats2bfloat162_rn(q.z, q.w);
     uint2 o;
     o.x = *reinterpret_cast<const uint32_t*>(&p0);
     o.y = *reinterpret_cast<const uint32_t*>(&p1);

@@ -97,51 +97,72 @@ __device__ __forceinline__ void fwht4(float (&v)[4]) {
 }
 
 constexpr int kFwhtSliceN = 1024;                                   // a quarter of a block
-constexpr int kFwhtSliceSmemFloats = kFwhtSliceN + kFwhtSliceN / 16;
+constexpr int kFwhtSliceSmemFloats = kFwhtSliceN + kFwhtSliceN / 8;
+
+// Where value j of a slice sits in its shared buffer: a pad of four floats
+// per 32 keeps each phase below on distinct banks, and a reader of 32
+// consecutive values (one lane quarter of a group) gets them 16-byte aligned.
+__device__ __forceinline__ int fwht_slice_pos(int j) { return j + 4 * (j >> 5); }
 
 // Slice a (0..3) of one 4096 block of H_4096 (s (.) x) / 64, with H_4096 =
 // H_4 (x) H_1024 in natural order: the slice is H_1024 u / 64, u[j] =
 // sum_{a'} (-1)^popcount(a & a') z[1024 a' + j], z = s (.) x over the block.
-// H_1024 = H_4^(x)5 runs as five radix-4 passes over the index's base-4
-// digits, 256 threads x 4 values (the first in registers, the others through
-// shared memory).  x and signs point at the block (8- and 4-byte aligned);
-// the result is left in `sm` at fwht_pos(j).  Must be called by all 256
-// threads; ends with a __syncthreads().
+// Thread i sums u for j = 4 i .. 4 i + 3 (a sign is a flip of the bf16 sign
+// bit: its sign byte's bit 7, and row a of H_4 for the whole part), then
+// H_1024 = H_8 (x) H_128 runs as the index's bits 0-1 in registers, bits 2-6
+// across the lanes of the warp that holds those 128 values (j = 128 w + ...),
+// and bits 7-9 across the warps through shared memory: two barriers.  x and
+// signs point at the block (8- and 4-byte aligned); the result is left in
+// `sm` at fwht_slice_pos(j).  Must be called by all 256 threads; ends with a
+// __syncthreads().
 __device__ __forceinline__ void fwht1024_slice(const __nv_bfloat16* __restrict__ x,
                                                const int8_t* __restrict__ signs, int a,
                                                float* __restrict__ sm) {
-    const int i = threadIdx.x;
+    const int i = threadIdx.x, lane = i & 31;
     float u[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int ap = 0; ap < 4; ++ap) {
         const int k0 = kFwhtSliceN * ap + 4 * i;
         const uint2 xw = *reinterpret_cast<const uint2*>(x + k0);
         const uint32_t sw = *reinterpret_cast<const uint32_t*>(signs + k0);
-        const bool neg = (__popc(a & ap) & 1) != 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const uint32_t bits = ((e < 2 ? xw.x : xw.y) >> (16 * (e & 1))) & 0xFFFFu;
-            const float xv = __uint_as_float(bits << 16);
-            const int sg = (int)(int8_t)((sw >> (8 * e)) & 0xFFu);
-            u[e] += ((sg < 0) != neg) ? -xv : xv;
-        }
+        const uint32_t neg = (__popc(a & ap) & 1) ? 0x80008000u : 0u;
+        // sign bytes 0 and 1 (2 and 3) to bytes 1 and 3: their bit 7 onto
+        // the sign bits of the two bf16 values of a word
+        const uint32_t lo = xw.x ^ ((__byte_perm(sw, 0u, 0x1404u) & 0x80008000u) ^ neg);
+        const uint32_t hi = xw.y ^ ((__byte_perm(sw, 0u, 0x3424u) & 0x80008000u) ^ neg);
+        u[0] += __uint_as_float(lo << 16);
+        u[1] += __uint_as_float(lo & 0xFFFF0000u);
+        u[2] += __uint_as_float(hi << 16);
+        u[3] += __uint_as_float(hi & 0xFFFF0000u);
     }
-    fwht4(u);   // digit 0 (bits 0-1): this thread's four consecutive values
+    fwht4(u);   // index bits 0-1
 #pragma unroll
-    for (int e = 0; e < 4; ++e) sm[fwht_pos(4 * i + e)] = u[e];
+    for (int b = 0; b < 5; ++b) {   // index bits 2-6: lane bit b
+        const float sg = ((lane >> b) & 1) ? -1.0f : 1.0f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) u[e] = fmaf(u[e], sg, __shfl_xor_sync(0xffffffffu, u[e], 1 << b));
+    }
+    *reinterpret_cast<float4*>(sm + fwht_slice_pos(4 * i)) = make_float4(u[0], u[1], u[2], u[3]);
     __syncthreads();
+    if (i < 128) {   // index bits 7-9: thread i takes value i of each of the eight 128-wide parts
+        float v[8];
 #pragma unroll
-    for (int p = 1; p < 5; ++p) {
-        // digit p (bits 2p, 2p + 1): i with two zero bits inserted at 2p
-        const int base = ((i >> (2 * p)) << (2 * p + 2)) | (i & ((1 << (2 * p)) - 1));
+        for (int g = 0; g < 8; ++g) v[g] = sm[fwht_slice_pos(128 * g + i)];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) u[e] = sm[fwht_pos(base + (e << (2 * p)))];
-        fwht4(u);
-        const float sc = p == 4 ? 1.0f / 64.0f : 1.0f;
+        for (int h = 1; h < 8; h <<= 1) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sm[fwht_pos(base + (e << (2 * p)))] = u[e] * sc;
-        __syncthreads();
+            for (int g = 0; g < 8; ++g) {
+                if ((g & h) == 0) {
+                    const float p = v[g], q = v[g + h];
+                    v[g] = p + q;
+                    v[g + h] = p - q;
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < 8; ++g) sm[fwht_slice_pos(128 * g + i)] = v[g] * (1.0f / 64.0f);
     }
+    __syncthreads();
 }
 
 }  // namespace tern

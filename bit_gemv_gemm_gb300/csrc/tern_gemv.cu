@@ -530,11 +530,25 @@ gemv_kernel(const GemvArgs a) {
             } else {
                 float v[32];
                 if (ROT && m < M) {
-                    // the rotated slice in shared memory (fp32)
-                    const float* u = reinterpret_cast<const float*>(smem + a.off_rot) + (size_t)m * kRotPitch;
+                    // the rotated slice in shared memory (fp32): one token's
+                    // as fwht1024_slice leaves it, several tokens' at kRotPitch
                     const int j0 = (g - gA) * kGroup + 32 * t;
+                    if (ONE) {
+                        const float4* u4 = reinterpret_cast<const float4*>(
+                            reinterpret_cast<const float*>(smem + a.off_rot) + fwht_slice_pos(j0));
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = u[fwht_pos(j0 + e)];
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 z = u4[q];
+                            v[4 * q] = z.x;
+                            v[4 * q + 1] = z.y;
+                            v[4 * q + 2] = z.z;
+                            v[4 * q + 3] = z.w;
+                        }
+                    } else {
+                        const float* u = reinterpret_cast<const float*>(smem + a.off_rot) + (size_t)m * kRotPitch;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = u[fwht_pos(j0 + e)];
+                    }
                 } else if (m < M) {
                     const uint4* s4 = reinterpret_cast<const uint4*>(
                         reinterpret_cast<const __nv_bfloat16*>(a.x) + (size_t)m * a.K + (size_t)g * kGroup + 32 * t);
@@ -859,7 +873,7 @@ gemv_kernel(const GemvArgs a) {
 __global__ void __launch_bounds__(kFwhtThreads)
 rotate_stage_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restrict__ signs,
                     uint32_t* __restrict__ xs, int* __restrict__ xe, int K) {
-    __shared__ float sm[kFwhtSliceSmemFloats];
+    __shared__ __align__(16) float sm[kFwhtSliceSmemFloats];
     pdl_launch_dependents();
     pdl_wait();
     const int sigma = blockIdx.x, m = blockIdx.y, G = K / kGroup;
@@ -869,7 +883,7 @@ rotate_stage_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restric
     if (i >= 64) return;
     float v[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) v[e] = sm[fwht_pos(16 * i + e)];
+    for (int e = 0; e < 16; ++e) v[e] = sm[fwht_slice_pos(16 * i + e)];
     float mx = 0.0f;
 #pragma unroll
     for (int e = 0; e < 16; ++e) mx = fmaxf(mx, fabsf(v[e]));
@@ -1309,7 +1323,7 @@ void layout(Plan& p, int M, int cps) {
     p.off_part = (uint32_t)off;
     off += (M <= kPrivateMaxM ? (size_t)kWarps * p.rmax * 16 * M : (size_t)p.rmax * 16 * MP) * 4;
     p.off_rot = (uint32_t)align_up(off, 16);
-    if (p.rot) off = p.off_rot + (size_t)M * kRotPitch * 4;
+    if (p.rot) off = p.off_rot + (M == 1 ? (size_t)kFwhtSliceSmemFloats : (size_t)M * kRotPitch) * 4;
     p.smem = off;
 }
 
