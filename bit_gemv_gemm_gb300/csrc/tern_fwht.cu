@@ -65,9 +65,8 @@ extern "C" tern_status tern_fwht(const void* x, const int8_t* signs, void* y, in
     int sms = 0;
     tern_status st = check_device(&sms);
     if (st != TERN_OK) return st;
-    // fewer blocks than SMs: one CTA per 1024-wide slice instead (latency-bound
-    // sizes; for one token the block kernel measured faster ahead of a product)
-    const bool slices = (long long)(K / kFwhtN) * M < sms && M > 1;
+    // fewer blocks than SMs: one CTA per 1024-wide slice instead (latency-bound sizes)
+    const bool slices = (long long)(K / kFwhtN) * M < sms;
     const dim3 grid(slices ? K / kFwhtSliceN : K / kFwhtN, M);
     cudaError_t e = launch_pdl(slices ? fwht_slice_kernel : fwht_kernel, grid, dim3(kFwhtThreads), 0,
                                (cudaStream_t)stream, true, reinterpret_cast<const __nv_bfloat16*>(x), signs,
